@@ -1,0 +1,55 @@
+"""Tile-schedule rule -- TEST INFRASTRUCTURE ONLY (part of the oracle).
+
+The pages' kernel ("Varlen Flash Attention Implementation Plan", Task 1
+Step 1) maps a block to (q tile, head) from a global tile start and a linear
+scan over cu_seqlens_q; that mapping does not cover every token, so the
+schedule here is the plain rule the scheduler kernel must reproduce:
+
+  * one work item per (sequence b, local q tile i, head h) for every
+    sequence with Lq_b > 0, where tile i holds local query rows
+    [i*BQ, min(Lq_b, (i+1)*BQ));
+  * its cost is the number of BK-wide key tiles that hold at least one key
+    the tile's rows may see: ceil(Lk_b / BK) without a mask, and with the
+    top-left causal mask ceil(min(Lk_b, min(Lq_b, (i+1)*BQ)) / BK), because
+    the tile's last row min(Lq_b, (i+1)*BQ) - 1 sees keys 0 .. that row;
+  * items are ordered by cost, largest first (longest-processing-time
+    order), ties by (b, i, h) ascending.
+
+Each item is four int32: (b, i, h, cost).  Integer work: the scheduler kernel
+must match this bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def tile_cost(lq: int, lk: int, i: int, bq: int, bk: int, causal: bool) -> int:
+    """Number of key tiles that q tile i of a (lq, lk) sequence must visit."""
+    if not causal:
+        return _ceil_div(lk, bk)
+    last_row_plus_one = min(lq, (i + 1) * bq)
+    return _ceil_div(min(lk, last_row_plus_one), bk)
+
+
+def schedule(cu_seqlens_q, cu_seqlens_k, num_heads: int, bq: int, bk: int,
+             causal: bool) -> np.ndarray:
+    """The ordered work list, int32 [n_items, 4] of (b, i, h, cost)."""
+    cq = [int(x) for x in cu_seqlens_q]
+    ck = [int(x) for x in cu_seqlens_k]
+    items = []
+    for b in range(len(cq) - 1):
+        lq = cq[b + 1] - cq[b]
+        lk = ck[b + 1] - ck[b]
+        for i in range(_ceil_div(lq, bq)):
+            c = tile_cost(lq, lk, i, bq, bk, causal)
+            for h in range(num_heads):
+                items.append((c, b, i, h))
+    items.sort(key=lambda t: (-t[0], t[1], t[2], t[3]))
+    out = np.zeros((len(items), 4), dtype=np.int32)
+    for n, (c, b, i, h) in enumerate(items):
+        out[n] = (b, i, h, c)
+    return out

@@ -1,0 +1,475 @@
+/*
+ * vfa_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, fp64 CPU statement of what the variable-length attention
+ * path computes.  Only the test-suite, the package's smoke check and the
+ * bench's CPU-baseline leg may load this library; the product path never
+ * does.  It shares no code, header, table or helper with the CUDA library.
+ *
+ * Sources (the pages this follows):
+ *   - "Varlen Flash Attention Implementation Plan" (rustytorch), Task 1
+ *     Step 1 (the CUDA kernel: packed [total, heads, head_dim] layout,
+ *     cu_seqlens prefix sums, scaled scores, causal and boundary masks,
+ *     epilogue out = acc / l and lse = log(l) + m) and Task 2 Step 1
+ *     (varlen_attention_cpu: per-sequence masked softmax times V).
+ *   - "attention_ref.rs" (spark_storage): AttnState::new, step_tile_ref,
+ *     finalize_ref -- the paged GQA decode state (m, l, o), its update over
+ *     the tokens of the blocks listed for one tile, and the final o / l.
+ *
+ * All arithmetic is in double.  bf16 inputs are widened exactly.  Nothing is
+ * blocked, fused or reordered beyond the definition: each (sequence, head,
+ * query row) is computed on its own from the full set of keys it may see.
+ *
+ * Readings taken where the pages are silent or disagree (each is also listed
+ * in the design notes):
+ *   - causal alignment is top-left: local key j is visible to local query i
+ *     iff j <= i (the kernel compares local positions k_pos > q_pos);
+ *   - masked keys carry weight exactly zero (the kernel's -FLT_MAX sentinel
+ *     and the CPU reference's -inf sentinel both give that);
+ *   - an empty key set gives out = 0 and lse = -FLT_MAX (the kernel's
+ *     inv_l = 0 and lse epilogue);
+ *   - lse is the natural log of sum_j exp(scale * q.k_j);
+ *   - decode: every listed block contributes all block_size tokens; the
+ *     decode scale is 1/sqrt(head_dim).
+ *
+ * Parity pins (independent checks of this file) live in tests/: a numpy
+ * brute-force formulation, torch float64 scaled_dot_product_attention, the
+ * worked examples the plan's tests print, closed-form invariants, and the
+ * tile-fragmentation invariance that attention_ref.rs states as its purpose.
+ */
+#include <float.h>
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* Exact widening of a bfloat16 bit pattern to double. */
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Packed layout [tokens, heads, head_dim]: element (t, h, d). */
+static size_t packed_index(int64_t t, int h, int d, int num_heads, int head_dim)
+{
+    return ((size_t)t * (size_t)num_heads + (size_t)h) * (size_t)head_dim + (size_t)d;
+}
+
+int oracle_default_threads(void)
+{
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Varlen attention forward                                                  */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const uint16_t *q, *k, *v;
+    const int32_t *cu_q, *cu_k;
+    int batch, num_heads, head_dim;
+    double scale;
+    int causal;
+} varlen_problem;
+
+/*
+ * One query row: local row i of sequence b, head h.
+ *
+ *   K_set = { j : 0 <= j < Lk_b  and  (not causal or j <= i) }
+ *   s_j   = scale * sum_d q[tq, h, d] * k[cu_k[b] + j, h, d]
+ *   empty K_set: out = 0, lse = -FLT_MAX
+ *   else: M = max_j s_j, Z = sum_j exp(s_j - M),
+ *         out[d] = sum_j exp(s_j - M) * v[cu_k[b] + j, h, d] / Z,
+ *         lse = M + ln Z
+ *
+ * `s` and `w` are caller scratch of at least Lk_b doubles; `kidx` of Lk_b ints.
+ */
+static void varlen_row(const varlen_problem *p, int b, int i, int h,
+                       double *out_row, double *lse_out,
+                       double *s, double *w, int *kidx)
+{
+    const int D = p->head_dim, H = p->num_heads;
+    const int64_t tq = (int64_t)p->cu_q[b] + i;
+    const int64_t k0 = p->cu_k[b];
+    const int Lk = p->cu_k[b + 1] - p->cu_k[b];
+
+    int n = 0;
+    for (int j = 0; j < Lk; ++j) {
+        if (p->causal && j > i)
+            continue;                       /* masked: weight exactly zero */
+        kidx[n++] = j;
+    }
+    if (n == 0) {
+        for (int d = 0; d < D; ++d)
+            out_row[d] = 0.0;
+        *lse_out = -(double)FLT_MAX;
+        return;
+    }
+    for (int a = 0; a < n; ++a) {
+        const int64_t tk = k0 + kidx[a];
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += bf16_to_double(p->q[packed_index(tq, h, d, H, D)]) *
+                   bf16_to_double(p->k[packed_index(tk, h, d, H, D)]);
+        s[a] = p->scale * dot;
+    }
+    double M = s[0];
+    for (int a = 1; a < n; ++a)
+        if (s[a] > M)
+            M = s[a];
+    double Z = 0.0;
+    for (int a = 0; a < n; ++a) {
+        w[a] = exp(s[a] - M);
+        Z += w[a];
+    }
+    for (int d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int a = 0; a < n; ++a)
+            acc += w[a] * bf16_to_double(p->v[packed_index(k0 + kidx[a], h, d, H, D)]);
+        out_row[d] = acc / Z;
+    }
+    *lse_out = M + log(Z);
+}
+
+/* Work distribution: independent units handed out by an atomic counter. */
+typedef struct {
+    const varlen_problem *p;
+    /* full mode: unit = (b, h); rows mode: unit = one (token, head) row */
+    const int64_t *rows;   /* NULL in full mode; else pairs (token, head) */
+    int64_t n_units;
+    int64_t next;          /* shared counter */
+    int max_lk;
+    double *out, *lse;     /* full mode: packed [Tq,H,D] and [Tq,H]; rows mode: [n,D], [n] */
+    int status;
+} varlen_job;
+
+/* Sequence that owns packed query token t: cu_q[b] <= t < cu_q[b+1]. */
+static int owner_sequence(const int32_t *cu, int batch, int64_t t)
+{
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {              /* first b with cu[b+1] > t */
+        int mid = (lo + hi) / 2;
+        if (cu[mid + 1] > t)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return lo;
+}
+
+static void *varlen_worker(void *arg)
+{
+    varlen_job *job = (varlen_job *)arg;
+    const varlen_problem *p = job->p;
+    const int D = p->head_dim, H = p->num_heads;
+    size_t nscratch = (size_t)(job->max_lk > 0 ? job->max_lk : 1);
+    double *s = (double *)malloc(nscratch * sizeof(double));
+    double *w = (double *)malloc(nscratch * sizeof(double));
+    int *kidx = (int *)malloc(nscratch * sizeof(int));
+    if (!s || !w || !kidx) {
+        __atomic_store_n(&job->status, -1, __ATOMIC_SEQ_CST);
+        free(s); free(w); free(kidx);
+        return NULL;
+    }
+    for (;;) {
+        int64_t u = __atomic_fetch_add(&job->next, 1, __ATOMIC_RELAXED);
+        if (u >= job->n_units)
+            break;
+        if (job->rows == NULL) {
+            const int b = (int)(u / H), h = (int)(u % H);
+            const int Lq = p->cu_q[b + 1] - p->cu_q[b];
+            for (int i = 0; i < Lq; ++i) {
+                const int64_t tq = (int64_t)p->cu_q[b] + i;
+                varlen_row(p, b, i, h, job->out + packed_index(tq, h, 0, H, D),
+                           job->lse + (size_t)tq * H + h, s, w, kidx);
+            }
+        } else {
+            const int64_t tq = job->rows[2 * u];
+            const int h = (int)job->rows[2 * u + 1];
+            const int b = owner_sequence(p->cu_q, p->batch, tq);
+            varlen_row(p, b, (int)(tq - p->cu_q[b]), h, job->out + (size_t)u * D,
+                       job->lse + u, s, w, kidx);
+        }
+    }
+    free(s); free(w); free(kidx);
+    return NULL;
+}
+
+static int run_varlen_job(varlen_job *job, int nthreads)
+{
+    if (nthreads <= 0)
+        nthreads = oracle_default_threads();
+    if ((int64_t)nthreads > job->n_units)
+        nthreads = job->n_units > 0 ? (int)job->n_units : 1;
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!tid)
+        return -1;
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (pthread_create(&tid[t], NULL, varlen_worker, job) != 0)
+            break;
+        ++started;
+    }
+    if (started == 0)
+        varlen_worker(job);
+    for (int t = 0; t < started; ++t)
+        pthread_join(tid[t], NULL);
+    free(tid);
+    if (job->status != 0)
+        return -1;
+    return started > 0 ? started : 1;
+}
+
+static int check_cu(const int32_t *cu, int batch)
+{
+    if (cu[0] != 0)
+        return -2;
+    for (int b = 0; b < batch; ++b)
+        if (cu[b + 1] < cu[b])
+            return -2;
+    return 0;
+}
+
+static int max_len(const int32_t *cu, int batch)
+{
+    int m = 0;
+    for (int b = 0; b < batch; ++b)
+        if (cu[b + 1] - cu[b] > m)
+            m = cu[b + 1] - cu[b];
+    return m;
+}
+
+/*
+ * Full varlen forward.  q: [cu_q[B], H, D], k/v: [cu_k[B], H, D] (bf16 bits).
+ * out: double [cu_q[B], H, D]; lse: double [cu_q[B], H].
+ * Returns the number of threads used (> 0), or < 0 on bad arguments.
+ */
+int oracle_varlen_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const int32_t *cu_q, const int32_t *cu_k, int batch,
+                      int num_heads, int head_dim, double scale, int causal,
+                      double *out, double *lse, int nthreads)
+{
+    if (batch < 1 || num_heads < 1 || head_dim < 1)
+        return -1;
+    if (check_cu(cu_q, batch) || check_cu(cu_k, batch))
+        return -2;
+    varlen_problem p = {q, k, v, cu_q, cu_k, batch, num_heads, head_dim, scale, causal != 0};
+    varlen_job job;
+    memset(&job, 0, sizeof job);
+    job.p = &p;
+    job.rows = NULL;
+    job.n_units = (int64_t)batch * num_heads;
+    job.max_lk = max_len(cu_k, batch);
+    job.out = out;
+    job.lse = lse;
+    return run_varlen_job(&job, nthreads);
+}
+
+/*
+ * Sampled rows of the same forward.  rows: int64 pairs (packed token, head),
+ * n_rows of them.  out_rows: double [n_rows, D]; lse_rows: double [n_rows].
+ */
+int oracle_varlen_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                           const int32_t *cu_q, const int32_t *cu_k, int batch,
+                           int num_heads, int head_dim, double scale, int causal,
+                           const int64_t *rows, int64_t n_rows,
+                           double *out_rows, double *lse_rows, int nthreads)
+{
+    if (batch < 1 || num_heads < 1 || head_dim < 1 || n_rows < 0)
+        return -1;
+    if (check_cu(cu_q, batch) || check_cu(cu_k, batch))
+        return -2;
+    for (int64_t r = 0; r < n_rows; ++r)
+        if (rows[2 * r] < 0 || rows[2 * r] >= cu_q[batch] ||
+            rows[2 * r + 1] < 0 || rows[2 * r + 1] >= num_heads)
+            return -3;
+    varlen_problem p = {q, k, v, cu_q, cu_k, batch, num_heads, head_dim, scale, causal != 0};
+    varlen_job job;
+    memset(&job, 0, sizeof job);
+    job.p = &p;
+    job.rows = rows;
+    job.n_units = n_rows;
+    job.max_lk = max_len(cu_k, batch);
+    job.out = out_rows;
+    job.lse = lse_rows;
+    return run_varlen_job(&job, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Paged GQA decode (state m, l, o)                                          */
+/* ------------------------------------------------------------------------ */
+
+/* AttnState::new: m = -inf, l = 0, o = 0. */
+void oracle_decode_init(double *m, double *l, double *o, int num_seqs,
+                        int num_q_heads, int head_dim)
+{
+    const size_t n = (size_t)num_seqs * (size_t)num_q_heads;
+    for (size_t i = 0; i < n; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.0;
+    }
+    memset(o, 0, n * (size_t)head_dim * sizeof(double));
+}
+
+typedef struct {
+    const uint16_t *q, *k_pool, *v_pool;
+    const int32_t *tile_blocks, *tile_block_counts;
+    int tile_capacity, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
+    int64_t num_blocks;
+    double *m, *l, *o;
+    int64_t next;
+    int status;
+} decode_job;
+
+/*
+ * One (sequence, q head) of one tile step.  The tokens of this step are all
+ * block_size tokens of every block id tile_blocks[seq, 0:count].  With x
+ * their logits (q . k) / sqrt(D), the state that describes every token seen
+ * so far is m = max x, l = sum exp(x - m), o = sum exp(x - m) v; merging the
+ * old state with this step's set re-expresses both sums at the new max.
+ */
+static void decode_unit(decode_job *job, int seq, int qh, double *x, int64_t *tok)
+{
+    const int D = job->head_dim, Hq = job->num_q_heads, Hkv = job->num_kv_heads;
+    const int group = Hq / Hkv;
+    const int kh = qh / group;
+    const int count = job->tile_block_counts[seq];
+    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+    const size_t sidx = (size_t)seq * Hq + qh;
+    const uint16_t *qrow = job->q + sidx * D;
+
+    int64_t n = 0;
+    for (int b = 0; b < count; ++b) {
+        const int64_t blk = job->tile_blocks[(size_t)seq * job->tile_capacity + b];
+        for (int t = 0; t < job->block_size; ++t) {
+            /* pool layout [num_blocks, block_size, num_kv_heads, head_dim] */
+            const int64_t base = ((blk * job->block_size + t) * Hkv + kh) * (int64_t)D;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += bf16_to_double(qrow[d]) * bf16_to_double(job->k_pool[base + d]);
+            x[n] = dot * inv_sqrt_d;
+            tok[n] = base;
+            ++n;
+        }
+    }
+    if (n == 0)
+        return;                                   /* an empty tile leaves the state as it was */
+
+    const double m_old = job->m[sidx];
+    double m_new = m_old;
+    for (int64_t a = 0; a < n; ++a)
+        if (x[a] > m_new)
+            m_new = x[a];
+    const double carry = exp(m_old - m_new);      /* 0 when m_old = -inf */
+    double l_new = job->l[sidx] * carry;
+    double *orow = job->o + sidx * D;
+    for (int d = 0; d < D; ++d)
+        orow[d] *= carry;
+    for (int64_t a = 0; a < n; ++a) {
+        const double e = exp(x[a] - m_new);
+        l_new += e;
+        for (int d = 0; d < D; ++d)
+            orow[d] += e * bf16_to_double(job->v_pool[tok[a] + d]);
+    }
+    job->m[sidx] = m_new;
+    job->l[sidx] = l_new;
+}
+
+static void *decode_worker(void *arg)
+{
+    decode_job *job = (decode_job *)arg;
+    const size_t cap_tokens = (size_t)(job->tile_capacity > 0 ? job->tile_capacity : 1) *
+                              (size_t)job->block_size;
+    double *x = (double *)malloc(cap_tokens * sizeof(double));
+    int64_t *tok = (int64_t *)malloc(cap_tokens * sizeof(int64_t));
+    if (!x || !tok) {
+        __atomic_store_n(&job->status, -1, __ATOMIC_SEQ_CST);
+        free(x); free(tok);
+        return NULL;
+    }
+    const int64_t n_units = (int64_t)job->num_seqs * job->num_q_heads;
+    for (;;) {
+        int64_t u = __atomic_fetch_add(&job->next, 1, __ATOMIC_RELAXED);
+        if (u >= n_units)
+            break;
+        decode_unit(job, (int)(u / job->num_q_heads), (int)(u % job->num_q_heads), x, tok);
+    }
+    free(x); free(tok);
+    return NULL;
+}
+
+/*
+ * One tile step over every sequence.  q: [S, Hq, D]; pools: [num_blocks,
+ * block_size, Hkv, D] (bf16 bits); tile_blocks: [S, tile_capacity];
+ * tile_block_counts: [S].  m, l: double [S, Hq]; o: double [S, Hq, D] (in/out).
+ * Returns threads used (> 0) or < 0 on bad arguments (nothing is changed).
+ */
+int oracle_decode_step(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                       int64_t num_blocks, const int32_t *tile_blocks,
+                       const int32_t *tile_block_counts, int tile_capacity, int num_seqs,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       double *m, double *l, double *o, int nthreads)
+{
+    if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 ||
+        block_size < 1 || tile_capacity < 0 || num_q_heads % num_kv_heads != 0)
+        return -1;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int c = tile_block_counts[s];
+        if (c < 0 || c > tile_capacity)
+            return -2;
+        for (int b = 0; b < c; ++b) {
+            const int32_t blk = tile_blocks[(size_t)s * tile_capacity + b];
+            if (blk < 0 || blk >= num_blocks)
+                return -3;
+        }
+    }
+    decode_job job;
+    memset(&job, 0, sizeof job);
+    job.q = q; job.k_pool = k_pool; job.v_pool = v_pool;
+    job.tile_blocks = tile_blocks; job.tile_block_counts = tile_block_counts;
+    job.tile_capacity = tile_capacity; job.num_seqs = num_seqs;
+    job.num_q_heads = num_q_heads; job.num_kv_heads = num_kv_heads;
+    job.head_dim = head_dim; job.block_size = block_size; job.num_blocks = num_blocks;
+    job.m = m; job.l = l; job.o = o;
+
+    const int64_t n_units = (int64_t)num_seqs * num_q_heads;
+    if (nthreads <= 0)
+        nthreads = oracle_default_threads();
+    if ((int64_t)nthreads > n_units)
+        nthreads = (int)n_units;
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!tid)
+        return -1;
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (pthread_create(&tid[t], NULL, decode_worker, &job) != 0)
+            break;
+        ++started;
+    }
+    if (started == 0)
+        decode_worker(&job);
+    for (int t = 0; t < started; ++t)
+        pthread_join(tid[t], NULL);
+    free(tid);
+    if (job.status != 0)
+        return -1;
+    return started > 0 ? started : 1;
+}
+
+/* finalize_ref: out = o * (l > 0 ? 1 / l : 0), kept in double here. */
+void oracle_decode_finalize(const double *l, const double *o, int num_seqs,
+                            int num_q_heads, int head_dim, double *out)
+{
+    const size_t n = (size_t)num_seqs * (size_t)num_q_heads;
+    for (size_t i = 0; i < n; ++i) {
+        const double inv_l = l[i] > 0.0 ? 1.0 / l[i] : 0.0;
+        for (int d = 0; d < head_dim; ++d)
+            out[i * head_dim + d] = o[i * head_dim + d] * inv_l;
+    }
+}

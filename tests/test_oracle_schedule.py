@@ -1,0 +1,63 @@
+"""Pins for the tile-schedule rule (CPU only, integers).
+
+  * brute force: an item's cost equals the number of key tiles holding at
+    least one (row, key) pair the mask lets through, found by enumeration;
+  * coverage: every (sequence, q tile, head) appears exactly once and the
+    tiles cover every query row of every head once;
+  * order: costs never increase along the list, ties in (b, i, h) order.
+"""
+import numpy as np
+import pytest
+
+from variable_length_flashattention_gb300 import workloads as W
+
+
+def _brute_cost(lq, lk, i, bq, bk, causal):
+    rows = range(i * bq, min(lq, (i + 1) * bq))
+    n = 0
+    for j in range(-(-lk // bk)):
+        keys = range(j * bk, min(lk, (j + 1) * bk))
+        if any((not causal) or c <= r for r in rows for c in keys):
+            n += 1
+    return n
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("bq,bk", [(128, 128), (128, 64), (64, 128)])
+def test_cost_matches_enumeration(oracle_mod, causal, bq, bk):
+    rng = np.random.default_rng(0)
+    lq = [int(x) for x in rng.integers(0, 400, 12)] + [1, 128, 129, 256, 0, 300]
+    lk = [int(x) for x in rng.integers(0, 400, 12)] + [1, 128, 129, 255, 7, 0]
+    cq, ck = W.cu_seqlens(lq), W.cu_seqlens(lk)
+    items = oracle_mod.schedule(cq, ck, 2, bq, bk, causal)
+    for b, i, h, c in items:
+        assert c == _brute_cost(lq[b], lk[b], i, bq, bk, causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_coverage_and_order(oracle_mod, causal):
+    lq, lk = W.cross_lengths(3)
+    H = 5
+    cq, ck = W.cu_seqlens(lq), W.cu_seqlens(lk)
+    items = oracle_mod.schedule(cq, ck, H, 128, 128, causal)
+    seen = set()
+    rows = 0
+    for b, i, h, c in items:
+        key = (int(b), int(i), int(h))
+        assert key not in seen
+        seen.add(key)
+        assert 0 <= i * 128 < lq[b]
+        rows += min(lq[b], (i + 1) * 128) - i * 128
+    assert rows == sum(lq) * H
+    assert len(seen) == H * sum(-(-x // 128) for x in lq)
+    keys = [(-int(c), int(b), int(i), int(h)) for b, i, h, c in items]
+    assert keys == sorted(keys)
+
+
+def test_tiny_workload_list():
+    import oracle
+    items = oracle.schedule(W.cu_seqlens([1, 7, 64, 129]), W.cu_seqlens([1, 7, 64, 129]),
+                            2, 128, 128, True)
+    # five q tiles (one per short sequence, two for the 129-token one) times two heads
+    assert len(items) == 10
+    assert [tuple(x) for x in items[:2]] == [(3, 1, 0, 2), (3, 1, 1, 2)]
