@@ -1,0 +1,226 @@
+/*
+ * vfa.h -- C ABI of libvfa: variable-length FlashAttention forward and paged
+ * GQA decode for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument named as a device buffer is a CUDA device
+ *     address on the current device, allocated and owned by the caller.  The
+ *     library never allocates, frees or retains caller memory, and keeps no
+ *     pointer after a call returns.
+ *   - Calls are asynchronous: they enqueue work on `stream` (NULL means the
+ *     legacy default stream) and return.  Results are ready when the stream
+ *     has reached that point.
+ *   - Host-detected errors (null or misaligned pointers, unsupported sizes,
+ *     a too-small workspace, a device that is not compute capability 10.3)
+ *     return a non-zero vfa_status immediately and enqueue nothing.
+ *     vfa_last_error() then describes the problem.
+ *   - Data errors that only the device can see (cu_seqlens that are not a
+ *     valid prefix sum, a block id outside the pool, a tile count above the
+ *     tile capacity) never fault or trap: the kernels record a status code
+ *     in a device status word, skip the offending work and leave its outputs
+ *     untouched.  vfa_read_status() fetches that word.
+ *   - bf16 means IEEE bfloat16 (1-8-7); f32 is IEEE binary32.
+ */
+#ifndef VFA_H
+#define VFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same object as cudaStream_t / CUstream). */
+typedef struct CUstream_st *vfa_stream_t;
+
+typedef enum {
+    VFA_OK = 0,
+    VFA_ERR_INVALID_ARG = 1,   /* host: null/misaligned pointer, bad size        */
+    VFA_ERR_UNSUPPORTED = 2,   /* host: a size this build does not implement     */
+    VFA_ERR_ARCH = 3,          /* host: the current device is not sm_103         */
+    VFA_ERR_CUDA = 4,          /* host: a CUDA runtime call failed               */
+    VFA_ERR_BAD_SEQLENS = 5,   /* device: cu_seqlens not a valid prefix sum      */
+    VFA_ERR_BAD_BLOCK = 6,     /* device: block id or tile count out of range    */
+    VFA_ERR_TIMEOUT = 7,       /* device: a bounded wait inside a kernel expired */
+    VFA_ERR_WORKSPACE = 8      /* device: the work list does not fit the workspace */
+} vfa_status;
+
+/* Message for the last non-OK status returned on the calling host thread. */
+const char *vfa_last_error(void);
+
+/* Library version string, e.g. "vfa 0.1 sm_103a". */
+const char *vfa_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Variable-length attention forward                                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Workspace bytes vfa_varlen_fwd needs for these sizes (an upper bound that
+ * holds for any cu_seqlens with these totals).  The first int32 of the
+ * workspace is the call's device status word (see vfa_read_status).
+ */
+size_t vfa_varlen_fwd_workspace_bytes(int batch, int total_q, int total_k, int num_heads,
+                                      int head_dim);
+
+/*
+ * Tile shape the forward uses for `head_dim`: q tile rows (*block_q) and key
+ * tile rows (*block_k).  The work list is built over these tiles.
+ * Returns VFA_ERR_UNSUPPORTED for a head_dim this build does not implement.
+ */
+vfa_status vfa_varlen_fwd_tile_shape(int head_dim, int *block_q, int *block_k);
+
+/*
+ * Exact softmax(scale * Q K^T, optional causal mask) V over packed
+ * variable-length sequences, plus the per-(token, head) log-sum-exp.
+ *
+ * Defined by "Varlen Flash Attention Implementation Plan" (rustytorch),
+ * Task 1 Step 1 (kernel preconditions, packed layout, masks, online-softmax
+ * recurrence and the out / lse epilogue) and Task 2 Step 1 (the CPU
+ * reference it must agree with).  The plan's kernel takes one block per
+ * (global q tile, head); this library instead builds a per-sequence q-tile
+ * work list on the device and covers every query row.
+ *
+ * q            device bf16 [total_q, num_heads, head_dim], packed row-major.
+ * k, v         device bf16 [total_k, num_heads, head_dim].
+ * cu_seqlens_q device int32 [batch + 1]: 0, running sums of the q lengths;
+ *              cu_seqlens_q[batch] == total_q.  Sequence b owns q rows
+ *              [cu_seqlens_q[b], cu_seqlens_q[b+1]).
+ * cu_seqlens_k device int32 [batch + 1], the same for keys/values.
+ * total_q, total_k  the tensors' first extents (needed on the host to describe
+ *              the tensors to the TMA engine).
+ * max_seqlen_q an upper bound on every q length (checked on the device).
+ * softmax_scale the factor applied to q.k before the softmax.
+ * causal       non-zero: top-left causal mask in local positions -- local key
+ *              j is visible to local query i iff j <= i.
+ * out          device bf16 [total_q, num_heads, head_dim]: out = sum_j p_j v_j /
+ *              sum_j p_j, rounded to nearest even; 0 for a query with no
+ *              visible key.
+ * lse          device f32 [total_q, num_heads]: natural-log sum of
+ *              exp(scale * q.k_j) over visible keys; -FLT_MAX when there is
+ *              none.
+ * workspace    device scratch of at least vfa_varlen_fwd_workspace_bytes()
+ *              bytes, 256-byte aligned; reused across calls; calls that share
+ *              one workspace must be stream-ordered.
+ *
+ * Supported: head_dim in {64, 128, 256}; num_heads >= 1; batch >= 1; q, k,
+ * v, out 16-byte aligned.  Sequences of length 0 are allowed (no rows, or no
+ * keys).  Device-detected: cu_seqlens not starting at 0, decreasing, not
+ * ending at total_q / total_k, or a q length above max_seqlen_q
+ * -> VFA_ERR_BAD_SEQLENS, nothing written to out / lse.
+ */
+vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
+                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                          int total_q, int total_k, int max_seqlen_q, int batch,
+                          int num_heads, int head_dim, float softmax_scale, int causal,
+                          void *out, float *lse, void *workspace, size_t workspace_bytes,
+                          vfa_stream_t stream);
+
+/*
+ * The device tile scheduler alone (the first kernel vfa_varlen_fwd runs),
+ * writing into caller buffers so the work list can be inspected.
+ *
+ * Items are int32 quadruples (b, i, h, cost): q tile i (local rows
+ * [i*block_q, min(Lq_b, (i+1)*block_q))) of sequence b, head h, and cost =
+ * the number of key tiles it visits (ceil(Lk_b / block_k); causal:
+ * ceil(min(Lk_b, min(Lq_b, (i+1)*block_q)) / block_k)).  Order: cost
+ * descending, ties by (b, i, h) ascending.  Sequences with Lq_b == 0 give no
+ * items.
+ *
+ * items        device int32 [items_capacity, 4] (output).
+ * n_items      device int32 [1] (output): number of items written.
+ * status       device int32 [1] (output): VFA_OK or a device-detected code.
+ * scratch      device scratch of vfa_varlen_fwd_workspace_bytes() bytes.
+ */
+vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                               int total_q, int total_k, int max_seqlen_q, int batch,
+                               int num_heads, int block_q, int block_k, int causal,
+                               int32_t *items, int items_capacity, int32_t *n_items,
+                               int32_t *status, void *scratch, size_t scratch_bytes,
+                               vfa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Paged GQA decode                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * AttnState::new of "attention_ref.rs" (spark_storage): m = -inf, l = 0,
+ * o = 0.
+ *
+ * m, l   device f32 [num_seqs, num_q_heads]; o device f32 [num_seqs,
+ *        num_q_heads, head_dim].  device_status (nullable) device int32 [1] is
+ *        set to VFA_OK.
+ */
+vfa_status vfa_paged_decode_init(float *m, float *l, float *o, int num_seqs, int num_q_heads,
+                                 int head_dim, int32_t *device_status, vfa_stream_t stream);
+
+/*
+ * One tile update, step_tile_ref of "attention_ref.rs": for every sequence s
+ * and q head qh (kv head kh = qh / (num_q_heads / num_kv_heads)) the state
+ * (m, l, o) absorbs every one of the block_size tokens of every block id
+ * tile_blocks[s, 0:tile_block_counts[s]]; logits are (q . k) / sqrt(head_dim).
+ * After any sequence of steps the state satisfies m = max logit, l = sum
+ * exp(logit - m), o = sum exp(logit - m) v over all tokens absorbed so far
+ * (m is in natural-log units).  Each KV block is read once per kv head group.
+ *
+ * q                 device bf16 [num_seqs, num_q_heads, head_dim].
+ * k_pool, v_pool    device bf16 [num_blocks, block_size, num_kv_heads, head_dim].
+ * tile_blocks       device int32 [num_seqs, tile_capacity]: physical block ids.
+ * tile_block_counts device int32 [num_seqs]: entries used per row (0 = no-op).
+ * m, l, o           the state (in/out), as in vfa_paged_decode_init.
+ * device_status     nullable device int32 [1]: a count outside
+ *                   [0, tile_capacity] or a block id outside [0, num_blocks)
+ *                   stores VFA_ERR_BAD_BLOCK here (first error wins) and that
+ *                   sequence's state is left unchanged for this step.
+ *
+ * Supported: head_dim in {64, 128, 256}; block_size == 16;
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ */
+vfa_status vfa_paged_decode_step(const void *q, const void *k_pool, const void *v_pool,
+                                 int num_blocks, const int32_t *tile_blocks,
+                                 const int32_t *tile_block_counts, int tile_capacity,
+                                 int num_seqs, int num_q_heads, int num_kv_heads,
+                                 int head_dim, int block_size, float *m, float *l, float *o,
+                                 int32_t *device_status, vfa_stream_t stream);
+
+/*
+ * finalize_ref of "attention_ref.rs": out = bf16(o * (l > 0 ? 1 / l : 0)),
+ * round to nearest even.  l: device f32 [num_seqs, num_q_heads]; o: device
+ * f32 [num_seqs, num_q_heads, head_dim]; out: device bf16, same shape as o.
+ */
+vfa_status vfa_paged_decode_finalize(const float *l, const float *o, int num_seqs,
+                                     int num_q_heads, int head_dim, void *out,
+                                     vfa_stream_t stream);
+
+/*
+ * Test hook for the block-table gather of vfa_paged_decode_step: runs the
+ * same device address computation and writes, for every sequence s, listed
+ * block b < count_s, token t and kv head kh, the K and V rows it reads into
+ * k_out / v_out (device bf16 [num_seqs, tile_capacity, block_size,
+ * num_kv_heads, head_dim]); unlisted slots are left untouched.  Errors as in
+ * vfa_paged_decode_step.
+ */
+vfa_status vfa_debug_paged_gather(const void *k_pool, const void *v_pool, int num_blocks,
+                                  const int32_t *tile_blocks, const int32_t *tile_block_counts,
+                                  int tile_capacity, int num_seqs, int num_kv_heads,
+                                  int head_dim, int block_size, void *k_out, void *v_out,
+                                  int32_t *device_status, vfa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Waits for `stream`, then copies the device int32 at `device_status_word`
+ * (the first word of a vfa_varlen_fwd workspace, or a decode device_status)
+ * to *host_status.
+ */
+vfa_status vfa_read_status(const void *device_status_word, vfa_stream_t stream,
+                           int32_t *host_status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VFA_H */

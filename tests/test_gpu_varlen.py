@@ -1,0 +1,165 @@
+"""GPU parity of vfa_varlen_fwd against the fp64 oracle (through the C ABI).
+
+Full elementwise comparison where the oracle finishes in seconds (tiny,
+packed, cross-attention at D=64 and D=256, edge cases); sampled rows for the
+32768-token long-tail workload, in the same launch configuration the bench
+times.  Outputs start as NaN canaries, so a row the kernel never wrote fails.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import FLT_MAX, assert_lse_close, assert_out_close, run_varlen, to_dev
+from variable_length_flashattention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vfa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from variable_length_flashattention_gb300 import build, vfa as binding
+    build.build()
+    return binding
+
+
+def _oracle_full(oracle_mod, case):
+    out, lse, _ = oracle_mod.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens_q,
+                                        case.cu_seqlens_k, case.num_heads, case.head_dim,
+                                        case.softmax_scale, case.causal)
+    return out, lse
+
+
+def _check_full(vfa, oracle_mod, case):
+    out, lse, status = run_varlen(vfa, case)
+    assert status == 0, f"device status {status}"
+    ref_out, ref_lse = _oracle_full(oracle_mod, case)
+    assert_out_close(out, ref_out, case.name)
+    assert_lse_close(lse, ref_lse, case.name)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny(vfa, oracle_mod, causal, seed):
+    _check_full(vfa, oracle_mod, W.tiny(causal, seed))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_packed_training_batch(vfa, oracle_mod, seed):
+    _check_full(vfa, oracle_mod, W.packed(seed))
+
+
+@pytest.mark.parametrize("head_dim", [64, 256])
+def test_cross_attention(vfa, oracle_mod, head_dim):
+    case = W.cross(head_dim, 0)
+    assert sum(1 for x in case.lengths_k if x == 1) >= 4
+    _check_full(vfa, oracle_mod, case)
+
+
+def test_longtail_sampled(vfa, oracle_mod):
+    case = W.longtail(0)
+    assert case.total_q == 32768 and max(case.lengths_q) == 8192
+    out, lse, status = run_varlen(vfa, case)
+    assert status == 0
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))     # every row written
+    rng = np.random.default_rng(123)
+    H = case.num_heads
+    rows = [np.stack([rng.integers(0, case.total_q, 1500), rng.integers(0, H, 1500)], 1)]
+    for b in range(case.batch):            # first and last row of every sequence, random head
+        q0, q1 = int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1])
+        if q1 > q0:
+            rows.append(np.array([[q0, rng.integers(0, H)], [q1 - 1, rng.integers(0, H)]]))
+    b8 = case.lengths_q.index(8192)        # the last q tile of the longest sequence, all heads 0/31
+    q1 = int(case.cu_seqlens_q[b8 + 1])
+    rows.append(np.stack([np.arange(q1 - 128, q1), np.zeros(128, int)], 1))
+    rows.append(np.stack([np.arange(q1 - 128, q1), np.full(128, H - 1)], 1))
+    rows = np.concatenate(rows).astype(np.int64)
+    ref_out, ref_lse, _ = oracle_mod.varlen_fwd_rows(case.q, case.k, case.v, case.cu_seqlens_q,
+                                                     case.cu_seqlens_k, H, case.head_dim,
+                                                     case.softmax_scale, True, rows)
+    assert_out_close(out[rows[:, 0], rows[:, 1]], ref_out, "longtail")
+    assert_lse_close(lse[rows[:, 0], rows[:, 1]], ref_lse, "longtail")
+
+
+EDGE = [
+    # (lengths_q, lengths_k, H, D, causal)
+    ([0, 5, 0, 130], [3, 0, 0, 130], 2, 128, False),       # empty q rows, empty key sets
+    ([0, 5, 0, 130], [3, 0, 0, 130], 2, 128, True),
+    ([1, 127, 128, 129, 256, 257], [1, 127, 128, 129, 256, 257], 3, 64, True),
+    ([1, 127, 128, 129, 256, 257], [1, 127, 128, 129, 256, 257], 3, 256, True),
+    ([300, 7, 1], [40, 300, 1], 2, 128, True),             # Lq > Lk and Lq < Lk, top-left causal
+    ([300, 7, 1], [40, 300, 1], 2, 256, True),
+    ([200, 64], [65, 500], 1, 256, False),
+    ([1] * 40, [1] * 40, 4, 64, True),                       # many one-token sequences
+]
+
+
+@pytest.mark.parametrize("lq,lk,H,D,causal", EDGE)
+def test_edge_shapes(vfa, oracle_mod, lq, lk, H, D, causal):
+    case = W.make_varlen("edge", lq, lk, H, D, causal, 1.0, value_seed=sum(lq) + D)
+    _check_full(vfa, oracle_mod, case)
+
+
+def test_large_logits_rescale_path(vfa, oracle_mod):
+    # sigma 3: scaled logits span tens of units, so the running max jumps by more
+    # than the lazy-rescale threshold many times along a row
+    case = W.make_varlen("wide", [700, 300], [700, 900], 2, 128, True, 3.0, value_seed=9)
+    _check_full(vfa, oracle_mod, case)
+
+
+def test_single_long_sequence_sampled(vfa, oracle_mod):
+    case = W.make_varlen("long", [16384], [16384], 1, 128, True, 1.0, value_seed=4)
+    out, lse, status = run_varlen(vfa, case)
+    assert status == 0
+    rows = np.stack([np.r_[0:64, 8000:8064, 16320:16384], np.zeros(192, int)], 1).astype(np.int64)
+    ref_out, ref_lse, _ = oracle_mod.varlen_fwd_rows(case.q, case.k, case.v, case.cu_seqlens_q,
+                                                     case.cu_seqlens_k, 1, 128,
+                                                     case.softmax_scale, True, rows)
+    assert_out_close(out[rows[:, 0], rows[:, 1]], ref_out, "long")
+    assert_lse_close(lse[rows[:, 0], rows[:, 1]], ref_lse, "long")
+
+
+def test_deterministic(vfa):
+    case = W.packed(2)
+    a = run_varlen(vfa, case)
+    b = run_varlen(vfa, case)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("bad", ["start", "decreasing", "end", "max_seqlen"])
+def test_bad_cu_seqlens_sets_status_and_writes_nothing(vfa, bad):
+    case = W.tiny(True, 0)
+    d = to_dev(case)
+    cu_q = d["cu_q"].clone()
+    max_q = case.max_seqlen_q
+    if bad == "start":
+        cu_q[0] = 1
+    elif bad == "decreasing":
+        cu_q[2] = cu_q[1] - 1
+    elif bad == "end":
+        cu_q[-1] = cu_q[-1] - 1
+    else:
+        max_q = 100
+    out = torch.full_like(d["q"], 7.0)
+    lse = torch.full((case.total_q, 2), 7.0, device="cuda")
+    ws = vfa.alloc_workspace(case.batch, case.total_q, case.total_k, 2, 64)
+    vfa.varlen_fwd(d["q"], d["k"], d["v"], cu_q, d["cu_k"], max_q, case.softmax_scale, True,
+                   out=out, lse=lse, workspace=ws)
+    assert vfa.read_status(ws) == vfa.VFA_ERR_BAD_SEQLENS
+    assert torch.all(out == 7.0) and torch.all(lse == 7.0)
+    # the same workspace is usable again afterwards
+    out2, lse2, status = run_varlen(vfa, case, workspace=ws)
+    assert status == 0 and np.all(np.isfinite(out2))
+
+
+def test_scale_and_plan_example(vfa):
+    # the plan's two-independent-sequences example, through the GPU path
+    H, D = 1, 64
+    cu = torch.tensor([0, 3, 7], dtype=torch.int32, device="cuda")
+    vals = torch.tensor([1.0] * 3 + [100.0] * 4)[:, None, None].expand(-1, H, D)
+    x = vals.contiguous().to(torch.bfloat16).cuda()
+    out, lse = vfa.varlen_fwd(x, x, x, cu, cu, 4, 0.5, False)
+    o = out.float().cpu()
+    assert torch.allclose(o[:3], torch.ones(3, H, D)) and torch.allclose(o[3:], torch.full((4, H, D), 100.0))

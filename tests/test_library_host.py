@@ -1,0 +1,110 @@
+"""Host-side checks of libvfa (no GPU): it builds, loads, exports every symbol
+that include/vfa.h declares, and rejects bad arguments before touching a
+device.  No call here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def vfa():
+    from variable_length_flashattention_gb300 import build, vfa as binding
+    build.build()
+    binding.lib()
+    return binding
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "vfa.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = set(re.findall(r"\b(vfa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(vfa):
+    declared = _declared_symbols()
+    assert len(declared) >= 10
+    L = vfa.lib()
+    for name in declared:
+        assert hasattr(L, name), f"{name} declared in vfa.h but not exported"
+    bound = {n for n, _, _ in vfa.SIGNATURES}
+    assert bound == set(declared), "binding and header disagree"
+
+
+def test_version_and_tile_shape(vfa):
+    assert "sm_103a" in vfa.version()
+    assert vfa.tile_shape(64) == (128, 128)
+    assert vfa.tile_shape(128) == (128, 128)
+    assert vfa.tile_shape(256) == (128, 64)
+    with pytest.raises(vfa.VfaError) as e:
+        vfa.tile_shape(96)
+    assert e.value.status == vfa.VFA_ERR_UNSUPPORTED
+
+
+def test_workspace_bound_covers_worst_case(vfa):
+    # one item per (q tile, head); the bound must hold for any split of total_q
+    import oracle
+    from variable_length_flashattention_gb300 import workloads as W
+    for lengths in ([1] * 50, [129] * 7, [128, 1, 0, 255, 3], [5000]):
+        cu = W.cu_seqlens(lengths)
+        n_items = len(oracle.schedule(cu, cu, 3, 128, 128, True))
+        total = int(cu[-1])
+        ws = vfa.workspace_bytes(len(lengths), total, total, 3, 128)
+        assert ws >= 256 + 16 * n_items
+    assert vfa.lib().vfa_varlen_fwd_workspace_bytes(0, 10, 10, 1, 128) == 0
+    assert vfa.lib().vfa_varlen_fwd_workspace_bytes(1, 10, 10, 1, 80) == 0
+
+
+def test_host_rejects_null_and_unsupported(vfa):
+    L = vfa.lib()
+    nul = None
+    st = L.vfa_varlen_fwd(nul, nul, nul, nul, nul, 1, 1, 1, 1, 1, 128, 1.0, 0, nul, nul, nul, 0, nul)
+    assert st == vfa.VFA_ERR_INVALID_ARG
+    assert b"null" in L.vfa_last_error()
+    fake = ctypes.c_void_p(0x100000)   # never dereferenced: rejected before any device work
+    st = L.vfa_varlen_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 1, 1, 96, 1.0, 0, fake, fake,
+                          fake, 1 << 20, nul)
+    assert st == vfa.VFA_ERR_UNSUPPORTED
+    st = L.vfa_varlen_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 1, 1, 128, 1.0, 0, fake, fake,
+                          fake, 16, nul)
+    assert st == vfa.VFA_ERR_INVALID_ARG and b"workspace too small" in L.vfa_last_error()
+    odd = ctypes.c_void_p(0x100002)
+    st = L.vfa_varlen_fwd(odd, fake, fake, fake, fake, 1, 1, 1, 1, 1, 128, 1.0, 0, fake, fake,
+                          fake, 1 << 20, nul)
+    assert st == vfa.VFA_ERR_INVALID_ARG and b"aligned" in L.vfa_last_error()
+    # decode: unsupported group size / block size / head_dim
+    st = L.vfa_paged_decode_step(fake, fake, fake, 4, fake, fake, 2, 1, 12, 4, 128, 16, fake,
+                                 fake, fake, nul, nul)
+    assert st == vfa.VFA_ERR_UNSUPPORTED
+    st = L.vfa_paged_decode_step(fake, fake, fake, 4, fake, fake, 2, 1, 8, 2, 128, 32, fake,
+                                 fake, fake, nul, nul)
+    assert st == vfa.VFA_ERR_UNSUPPORTED
+    st = L.vfa_paged_decode_step(fake, fake, fake, 4, fake, fake, 2, 1, 9, 2, 128, 16, fake,
+                                 fake, fake, nul, nul)
+    assert st == vfa.VFA_ERR_INVALID_ARG
+    st = L.vfa_paged_decode_finalize(fake, fake, 1, 1, 12, fake, nul)
+    assert st == vfa.VFA_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(vfa):
+    import torch
+    x = torch.zeros(4, 1, 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 4], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        vfa.varlen_fwd(x, x, x, cu, cu, 4, 0.125, False)
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "variable_length_flashattention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                with open(os.path.join(dirpath, fn)) as f:
+                    src = f.read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), fn
+                assert "vfa_oracle" not in src, fn

@@ -1,0 +1,438 @@
+// api.cu -- the C ABI declared in include/vfa.h: argument checks, TMA tensor
+// map encoding, workspace carve-up and launches.  Nothing here allocates or
+// frees device memory.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+vfa_status fail(vfa_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+vfa_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(VFA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+    bool ok = false;
+    int sm_count = 0;
+    int major = 0, minor = 0;
+};
+
+// The current device must be compute capability 10.3 (the only one built for).
+vfa_status current_device(DeviceInfo *out)
+{
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64)
+        return fail(VFA_ERR_CUDA, "device ordinal %d out of range", dev);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!cache[dev].ok) {
+            DeviceInfo d;
+            if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+                (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
+                (e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)))
+                return cuda_fail(e, "cudaDeviceGetAttribute");
+            d.ok = true;
+            cache[dev] = d;
+        }
+        *out = cache[dev];
+    }
+    if (out->major != 10 || out->minor != 3)
+        return fail(VFA_ERR_ARCH, "device is sm_%d%d; this library is built for sm_103a only",
+                    out->major, out->minor);
+    return VFA_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+vfa_status get_encoder(EncodeTiledFn *fn)
+{
+    static std::once_flag once;
+    static EncodeTiledFn f = nullptr;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                               cudaEnableDefault, &q);
+        if (err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            f = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    if (!f)
+        return fail(VFA_ERR_CUDA, "cuTensorMapEncodeTiled is not available (%s)",
+                    cudaGetErrorName(err));
+    *fn = f;
+    return VFA_OK;
+}
+
+// [rows, heads, head_dim] bf16 tensor as a 3-D TMA map (innermost first:
+// dim, head, row); box = 64 columns x 1 head x box_rows rows, 128-byte swizzle.
+vfa_status encode_packed_map(CUtensorMap *map, const void *base, int rows, int heads,
+                             int head_dim, int box_rows)
+{
+    EncodeTiledFn enc;
+    vfa_status st = get_encoder(&enc);
+    if (st)
+        return st;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(heads),
+                                static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                   static_cast<cuuint64_t>(heads) * head_dim * 2};
+    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(VFA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return VFA_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
+
+}  // namespace
+
+extern "C" {
+
+const char *vfa_last_error(void) { return g_err; }
+
+const char *vfa_version(void) { return "vfa 0.1 sm_103a"; }
+
+size_t vfa_varlen_fwd_workspace_bytes(int batch, int total_q, int total_k, int num_heads,
+                                      int head_dim)
+{
+    if (batch < 1 || total_q < 0 || total_k < 0 || num_heads < 1 || !supported_head_dim(head_dim))
+        return 0;
+    return vfa::workspace_layout(batch, total_q, total_k, num_heads, vfa::kBlockQ,
+                                 vfa::block_k_for(head_dim))
+        .total_bytes;
+}
+
+vfa_status vfa_varlen_fwd_tile_shape(int head_dim, int *block_q, int *block_k)
+{
+    if (!supported_head_dim(head_dim))
+        return fail(VFA_ERR_UNSUPPORTED, "head_dim %d not supported (64, 128, 256)", head_dim);
+    if (!block_q || !block_k)
+        return fail(VFA_ERR_INVALID_ARG, "null output pointer");
+    *block_q = vfa::kBlockQ;
+    *block_k = vfa::block_k_for(head_dim);
+    return VFA_OK;
+}
+
+vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                               int total_q, int total_k, int max_seqlen_q, int batch,
+                               int num_heads, int block_q, int block_k, int causal,
+                               int32_t *items, int items_capacity, int32_t *n_items,
+                               int32_t *status, void *scratch, size_t scratch_bytes,
+                               vfa_stream_t stream)
+{
+    if (!cu_seqlens_q || !cu_seqlens_k || !items || !n_items || !status || !scratch)
+        return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
+    if (batch < 1 || num_heads < 1 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
+        block_q < 1 || block_k < 1 || items_capacity < 0)
+        return fail(VFA_ERR_INVALID_ARG, "bad size argument");
+    if (!aligned(items, 16) || !aligned(scratch, 4))
+        return fail(VFA_ERR_INVALID_ARG, "items must be 16-byte aligned");
+    const int need = vfa::schedule_scratch_ints(batch, total_q, total_k, block_q, block_k);
+    if (scratch_bytes < static_cast<size_t>(need) * sizeof(int))
+        return fail(VFA_ERR_INVALID_ARG, "scratch too small: %zu < %zu bytes", scratch_bytes,
+                    static_cast<size_t>(need) * sizeof(int));
+    DeviceInfo dev;
+    vfa_status st = current_device(&dev);
+    if (st)
+        return st;
+    vfa::SchedArgs a;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.batch = batch;
+    a.total_q = total_q;
+    a.total_k = total_k;
+    a.max_seqlen_q = max_seqlen_q;
+    a.num_heads = num_heads;
+    a.block_q = block_q;
+    a.block_k = block_k;
+    a.causal = causal != 0;
+    a.items = reinterpret_cast<int4 *>(items);
+    a.item_capacity = items_capacity;
+    a.n_items = n_items;
+    a.status = status;
+    a.scratch = static_cast<int32_t *>(scratch);
+    a.scratch_ints = static_cast<int>(scratch_bytes / sizeof(int));
+    cudaError_t e = vfa::launch_schedule(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "scheduler launch");
+    return VFA_OK;
+}
+
+vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
+                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int total_q,
+                          int total_k, int max_seqlen_q, int batch, int num_heads, int head_dim,
+                          float softmax_scale, int causal, void *out, float *lse, void *workspace,
+                          size_t workspace_bytes, vfa_stream_t stream)
+{
+    if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out || !lse || !workspace)
+        return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
+    if (batch < 1 || num_heads < 1 || total_q < 0 || total_k < 0 || max_seqlen_q < 0)
+        return fail(VFA_ERR_INVALID_ARG, "bad size argument (batch %d, heads %d, totals %d/%d)",
+                    batch, num_heads, total_q, total_k);
+    if (!supported_head_dim(head_dim))
+        return fail(VFA_ERR_UNSUPPORTED, "head_dim %d not supported (64, 128, 256)", head_dim);
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+        !aligned(lse, 4) || !aligned(workspace, 256))
+        return fail(VFA_ERR_INVALID_ARG,
+                    "q, k, v, out must be 16-byte aligned, lse 4-byte, workspace 256-byte");
+    if (static_cast<long long>(num_heads) * head_dim * 2 > (1LL << 40) ||
+        static_cast<long long>(total_q) * num_heads > (1LL << 31) ||
+        static_cast<long long>(total_k) * num_heads > (1LL << 31))
+        return fail(VFA_ERR_UNSUPPORTED, "tensor too large");
+    const int bq = vfa::kBlockQ, bk = vfa::block_k_for(head_dim);
+    const vfa::WorkspaceLayout wl =
+        vfa::workspace_layout(batch, total_q, total_k, num_heads, bq, bk);
+    if (workspace_bytes < wl.total_bytes)
+        return fail(VFA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
+                    wl.total_bytes);
+    DeviceInfo dev;
+    vfa_status st = current_device(&dev);
+    if (st)
+        return st;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *status = reinterpret_cast<int32_t *>(ws);
+    int32_t *n_items = reinterpret_cast<int32_t *>(ws + 4);
+    int4 *items = reinterpret_cast<int4 *>(ws + wl.items_offset);
+
+    vfa::SchedArgs sa;
+    sa.cu_q = cu_seqlens_q;
+    sa.cu_k = cu_seqlens_k;
+    sa.batch = batch;
+    sa.total_q = total_q;
+    sa.total_k = total_k;
+    sa.max_seqlen_q = max_seqlen_q;
+    sa.num_heads = num_heads;
+    sa.block_q = bq;
+    sa.block_k = bk;
+    sa.causal = causal != 0;
+    sa.items = items;
+    sa.item_capacity = wl.item_capacity;
+    sa.n_items = n_items;
+    sa.status = status;
+    sa.scratch = reinterpret_cast<int32_t *>(ws + wl.scratch_offset);
+    sa.scratch_ints = wl.scratch_ints;
+    cudaError_t e = vfa::launch_schedule(sa, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "scheduler launch");
+
+    if (wl.item_capacity == 0)
+        return VFA_OK;                       // no query rows at all
+
+    vfa::PrefillArgs pa;
+    memset(&pa, 0, sizeof pa);
+    if ((st = encode_packed_map(&pa.tm_q, q, total_q, num_heads, head_dim, bq)) ||
+        (st = encode_packed_map(&pa.tm_k, k, total_k, num_heads, head_dim, bk)) ||
+        (st = encode_packed_map(&pa.tm_v, v, total_k, num_heads, head_dim, bk)))
+        return st;
+    pa.cu_q = cu_seqlens_q;
+    pa.cu_k = cu_seqlens_k;
+    pa.items = items;
+    pa.n_items = n_items;
+    pa.status = status;
+    pa.out = out;
+    pa.lse = lse;
+    pa.num_heads = num_heads;
+    pa.scale_log2 = softmax_scale * 1.4426950408889634f;
+    pa.causal = causal != 0;
+    const int grid = wl.item_capacity < dev.sm_count ? wl.item_capacity : dev.sm_count;
+    e = vfa::launch_prefill(head_dim, pa, grid, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "prefill launch");
+    return VFA_OK;
+}
+
+vfa_status vfa_paged_decode_init(float *m, float *l, float *o, int num_seqs, int num_q_heads,
+                                 int head_dim, int32_t *device_status, vfa_stream_t stream)
+{
+    if (!m || !l || !o)
+        return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
+    if (num_seqs < 1 || num_q_heads < 1 || head_dim < 1)
+        return fail(VFA_ERR_INVALID_ARG, "bad size argument");
+    DeviceInfo dev;
+    vfa_status st = current_device(&dev);
+    if (st)
+        return st;
+    cudaError_t e = vfa::launch_decode_init(m, l, o, num_seqs, num_q_heads, head_dim,
+                                            device_status, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode init launch");
+    return VFA_OK;
+}
+
+static vfa_status check_decode_args(const void *q, const void *k_pool, const void *v_pool,
+                                    int num_blocks, const int32_t *tile_blocks,
+                                    const int32_t *counts, int tile_capacity, int num_seqs,
+                                    int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size)
+{
+    if (!k_pool || !v_pool || !tile_blocks || !counts || (q == nullptr && num_q_heads < 0))
+        return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
+    if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || num_blocks < 0 ||
+        tile_capacity < 0)
+        return fail(VFA_ERR_INVALID_ARG, "bad size argument");
+    if (num_q_heads % num_kv_heads != 0)
+        return fail(VFA_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
+                    num_q_heads, num_kv_heads);
+    const int g = num_q_heads / num_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8)
+        return fail(VFA_ERR_UNSUPPORTED, "q heads per kv head %d not supported (1, 2, 4, 8)", g);
+    if (!supported_head_dim(head_dim))
+        return fail(VFA_ERR_UNSUPPORTED, "head_dim %d not supported (64, 128, 256)", head_dim);
+    if (block_size != 16)
+        return fail(VFA_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || (q && !aligned(q, 16)) ||
+        !aligned(tile_blocks, 4) || !aligned(counts, 4))
+        return fail(VFA_ERR_INVALID_ARG, "pools and q must be 16-byte aligned");
+    return VFA_OK;
+}
+
+vfa_status vfa_paged_decode_step(const void *q, const void *k_pool, const void *v_pool,
+                                 int num_blocks, const int32_t *tile_blocks,
+                                 const int32_t *tile_block_counts, int tile_capacity,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, float *m, float *l, float *o,
+                                 int32_t *device_status, vfa_stream_t stream)
+{
+    if (!q || !m || !l || !o)
+        return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
+    vfa_status st = check_decode_args(q, k_pool, v_pool, num_blocks, tile_blocks,
+                                      tile_block_counts, tile_capacity, num_seqs, num_q_heads,
+                                      num_kv_heads, head_dim, block_size);
+    if (st)
+        return st;
+    if (!aligned(o, 16) || !aligned(m, 4) || !aligned(l, 4))
+        return fail(VFA_ERR_INVALID_ARG, "o must be 16-byte aligned");
+    DeviceInfo dev;
+    if ((st = current_device(&dev)))
+        return st;
+    vfa::DecodeStepArgs a;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.tile_blocks = tile_blocks;
+    a.tile_block_counts = tile_block_counts;
+    a.num_blocks = num_blocks;
+    a.tile_capacity = tile_capacity;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.m = m;
+    a.l = l;
+    a.o = o;
+    a.status = device_status;
+    cudaError_t e = vfa::launch_decode_step(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode step launch");
+    return VFA_OK;
+}
+
+vfa_status vfa_paged_decode_finalize(const float *l, const float *o, int num_seqs,
+                                     int num_q_heads, int head_dim, void *out,
+                                     vfa_stream_t stream)
+{
+    if (!l || !o || !out)
+        return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
+    if (num_seqs < 1 || num_q_heads < 1 || head_dim < 8 || head_dim % 8 != 0)
+        return fail(VFA_ERR_INVALID_ARG, "bad size argument (head_dim must be a multiple of 8)");
+    if (!aligned(o, 16) || !aligned(out, 16))
+        return fail(VFA_ERR_INVALID_ARG, "o and out must be 16-byte aligned");
+    DeviceInfo dev;
+    vfa_status st = current_device(&dev);
+    if (st)
+        return st;
+    cudaError_t e = vfa::launch_decode_finalize(l, o, num_seqs, num_q_heads, head_dim, out,
+                                                reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode finalize launch");
+    return VFA_OK;
+}
+
+vfa_status vfa_debug_paged_gather(const void *k_pool, const void *v_pool, int num_blocks,
+                                  const int32_t *tile_blocks, const int32_t *tile_block_counts,
+                                  int tile_capacity, int num_seqs, int num_kv_heads, int head_dim,
+                                  int block_size, void *k_out, void *v_out,
+                                  int32_t *device_status, vfa_stream_t stream)
+{
+    if (!k_out || !v_out)
+        return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
+    vfa_status st = check_decode_args(nullptr, k_pool, v_pool, num_blocks, tile_blocks,
+                                      tile_block_counts, tile_capacity, num_seqs, num_kv_heads,
+                                      num_kv_heads, head_dim, block_size);
+    if (st)
+        return st;
+    if (!aligned(k_out, 16) || !aligned(v_out, 16))
+        return fail(VFA_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
+    DeviceInfo dev;
+    if ((st = current_device(&dev)))
+        return st;
+    vfa::DecodeStepArgs a;
+    memset(&a, 0, sizeof a);
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.tile_blocks = tile_blocks;
+    a.tile_block_counts = tile_block_counts;
+    a.num_blocks = num_blocks;
+    a.tile_capacity = tile_capacity;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_kv_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.status = device_status;
+    cudaError_t e =
+        vfa::launch_decode_gather(a, k_out, v_out, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "decode gather launch");
+    return VFA_OK;
+}
+
+vfa_status vfa_read_status(const void *device_status_word, vfa_stream_t stream,
+                           int32_t *host_status)
+{
+    if (!device_status_word || !host_status)
+        return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    e = cudaMemcpy(host_status, device_status_word, sizeof(int32_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy (status)");
+    return VFA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+// internal.h -- declarations shared by the host API and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/vfa.h"
+
+namespace vfa {
+
+// ------------------------------------------------------------ tile shapes
+
+// Query rows per tile: one tcgen05 M=128 accumulator, one TMEM lane per row.
+constexpr int kBlockQ = 128;
+
+__host__ __device__ constexpr int block_k_for(int head_dim)
+{
+    return head_dim == 256 ? 64 : 128;
+}
+
+// ------------------------------------------------------------ workspace
+
+// Layout of the varlen forward workspace (all offsets in bytes):
+//   [0]   int32 status word
+//   [4]   int32 number of work items
+//   [8]   int32 reserved
+//   [256] int4 items[item_capacity]
+//   then  int32 scheduler scratch
+struct WorkspaceLayout {
+    size_t items_offset;
+    int item_capacity;
+    size_t scratch_offset;
+    int scratch_ints;
+    size_t total_bytes;
+};
+
+WorkspaceLayout workspace_layout(int batch, int total_q, int total_k, int num_heads,
+                                 int block_q, int block_k);
+
+// ------------------------------------------------------------ scheduler
+
+struct SchedArgs {
+    const int32_t *cu_q;
+    const int32_t *cu_k;
+    int batch, total_q, total_k, max_seqlen_q, num_heads, block_q, block_k, causal;
+    int4 *items;
+    int item_capacity;
+    int32_t *n_items;
+    int32_t *status;
+    int32_t *scratch;
+    int scratch_ints;
+};
+
+cudaError_t launch_schedule(const SchedArgs &a, cudaStream_t stream);
+
+// Number of scheduler scratch ints for these sizes.
+int schedule_scratch_ints(int batch, int total_q, int total_k, int block_q, int block_k);
+
+// ------------------------------------------------------------ prefill
+
+struct PrefillArgs {
+    CUtensorMap tm_q, tm_k, tm_v;
+    const int32_t *cu_q;
+    const int32_t *cu_k;
+    const int4 *items;
+    const int32_t *n_items;
+    int32_t *status;
+    void *out;
+    float *lse;
+    int num_heads;
+    float scale_log2;     // softmax_scale * log2(e)
+    int causal;
+};
+
+cudaError_t launch_prefill(int head_dim, const PrefillArgs &a, int grid, cudaStream_t stream);
+size_t prefill_smem_bytes(int head_dim);
+
+// ------------------------------------------------------------ decode
+
+struct DecodeStepArgs {
+    const void *q, *k_pool, *v_pool;
+    const int32_t *tile_blocks, *tile_block_counts;
+    int num_blocks, tile_capacity, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
+    float *m, *l, *o;
+    int32_t *status;      // nullable
+};
+
+cudaError_t launch_decode_init(float *m, float *l, float *o, int num_seqs, int num_q_heads,
+                               int head_dim, int32_t *status, cudaStream_t stream);
+cudaError_t launch_decode_step(const DecodeStepArgs &a, cudaStream_t stream);
+cudaError_t launch_decode_finalize(const float *l, const float *o, int num_seqs,
+                                   int num_q_heads, int head_dim, void *out,
+                                   cudaStream_t stream);
+cudaError_t launch_decode_gather(const DecodeStepArgs &a, void *k_out, void *v_out,
+                                 cudaStream_t stream);
+
+}  // namespace vfa

@@ -1,0 +1,491 @@
+// prefill.cu -- variable-length attention forward on sm_103a.
+//
+// Computes, per packed query row, softmax(scale * q K^T, masks) V and the
+// natural-log log-sum-exp, by the tiled online-softmax recurrence of
+// "Varlen Flash Attention Implementation Plan", Task 1 Step 1 (running row
+// max m, running denominator l, accumulator rescaled when m grows, final
+// out = acc / l, lse = m + log l; causal and sequence-boundary masks on local
+// positions).  The plan's tile sizes, thread layout and sequence lookup are
+// not kept; this kernel is built for Blackwell:
+//
+//   * persistent CTAs walk a device-built work list (sched.cu) of
+//     (sequence, 128-row q tile, head) items in longest-first order;
+//   * warp 0 moves Q, K and V tiles with TMA (128-byte swizzle) into a
+//     shared-memory ring guarded by mbarriers;
+//   * warp 1 issues tcgen05.mma: S = Q K^T into one of two TMEM buffers, and
+//     O += P V with P read straight from TMEM (P overwrites its S buffer as
+//     bf16) and V as an MN-major shared-memory operand;
+//   * warps 2-5 own one query row per thread: they read S rows from TMEM,
+//     apply scale and masks, keep m and l, write P back to TMEM, rescale O
+//     in TMEM when the row max has grown by more than 2^8 (exact after the
+//     final division because l and O always share one reference max), and
+//     run the epilogue (O / l -> bf16, lse).
+// Every wait is bounded: on expiry the kernel records VFA_ERR_TIMEOUT,
+// drains its own in-flight copies and MMAs, frees TMEM and returns.
+#include <cfloat>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace vfa {
+
+namespace {
+
+template <int D>
+struct Cfg {
+    static constexpr int BQ = kBlockQ;
+    static constexpr int BK = block_k_for(D);
+    static constexpr int NS = 2;                          // K/V ring stages
+    static constexpr int NQ = D == 256 ? 1 : 2;           // Q buffers
+    static constexpr int DB = D / 64;                     // 128-byte column blocks per row
+    static constexpr uint32_t Q_BYTES = BQ * D * 2;
+    static constexpr uint32_t KV_BYTES = BK * D * 2;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t O_COL = 0;                  // O: columns [0, D)
+    static constexpr uint32_t S_COL = D;                  // S buffers: [D, D+BK), [D+BK, D+2BK)
+    static constexpr int NUM_BARS = 2 * NQ + 4 * NS + 7;
+    static constexpr size_t SMEM = 1024 /*alignment slack*/ + NQ * Q_BYTES + 2 * NS * KV_BYTES +
+                                   NUM_BARS * 8 + 64;
+    static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BQ, BK, false, false);
+    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BQ, D, false, true);
+    static_assert(S_COL + 2 * BK <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+constexpr int kThreads = 192;      // 6 warps: TMA, MMA, 4 x softmax/epilogue
+
+__device__ __forceinline__ int item_slot(int k, int cta, int grid)
+{
+    // Snake order over the longest-first list: even rounds left to right,
+    // odd rounds right to left, so each CTA's total cost stays even.
+    return k * grid + ((k & 1) ? (grid - 1 - cta) : cta);
+}
+
+__device__ __forceinline__ void record_error(int32_t *status, int code)
+{
+    atomicCAS(status, 0, code);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs p)
+{
+    using C = Cfg<D>;
+    constexpr int BQ = C::BQ, BK = C::BK, NS = C::NS, NQ = C::NQ, DB = C::DB;
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem_base;
+    __shared__ int s_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // 1024-byte aligned carve-up (128-byte swizzle atoms need it).
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t sQ = base;
+    const uint32_t sK = sQ + NQ * C::Q_BYTES;
+    const uint32_t sV = sK + NS * C::KV_BYTES;
+    const uint32_t bars = sV + NS * C::KV_BYTES;
+    auto q_full = [&](int i) { return bars + 8u * i; };
+    auto q_empty = [&](int i) { return bars + 8u * (NQ + i); };
+    auto k_full = [&](int i) { return bars + 8u * (2 * NQ + i); };
+    auto k_empty = [&](int i) { return bars + 8u * (2 * NQ + NS + i); };
+    auto v_full = [&](int i) { return bars + 8u * (2 * NQ + 2 * NS + i); };
+    auto v_empty = [&](int i) { return bars + 8u * (2 * NQ + 3 * NS + i); };
+    auto s_full = [&](int x) { return bars + 8u * (2 * NQ + 4 * NS + x); };
+    auto s_free = [&](int x) { return bars + 8u * (2 * NQ + 4 * NS + 2 + x); };
+    auto p_full = [&](int x) { return bars + 8u * (2 * NQ + 4 * NS + 4 + x); };
+    const uint32_t drain_bar = bars + 8u * (2 * NQ + 4 * NS + 6);
+    volatile int *abort = &s_abort;
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int i = 0; i < NQ; ++i) {
+            mbar_init(q_full(i), 1);
+            mbar_init(q_empty(i), 1);
+        }
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(k_full(i), 1);
+            mbar_init(k_empty(i), 1);
+            mbar_init(v_full(i), 1);
+            mbar_init(v_empty(i), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(s_full(x), 1);
+            mbar_init(s_free(x), 1);
+            mbar_init(p_full(x), 128);
+        }
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&s_tmem_base), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem_base;
+
+    const int n_items = (*p.status == 0) ? *p.n_items : 0;
+    const int grid = gridDim.x, cta = blockIdx.x;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_map(&p.tm_q);
+            tma_prefetch_map(&p.tm_k);
+            tma_prefetch_map(&p.tm_v);
+            uint32_t qit = 0, kfills = 0, vfills = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int idx = item_slot(k, cta, grid);
+                if (idx >= n_items)
+                    break;
+                const int4 it = p.items[idx];
+                const int b = it.x, i = it.y, h = it.z, nk = it.w;
+                if (nk == 0)
+                    continue;
+                const int q_row0 = p.cu_q[b] + i * BQ;
+                const int k_row0 = p.cu_k[b];
+                const int qb = qit % NQ;
+                if (!mbar_wait(q_empty(qb), ((qit / NQ) & 1u) ^ 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(q_full(qb), C::Q_BYTES);
+                for (int db = 0; db < DB; ++db)
+                    tma_load_3d(sQ + qb * C::Q_BYTES + db * (BQ * 128), &p.tm_q, q_full(qb),
+                                db * 64, h, q_row0);
+                ++qit;
+                for (int j = 0; j < nk; ++j) {
+                    const int st = kfills % NS;
+                    if (!mbar_wait(k_empty(st), ((kfills / NS) & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(k_full(st), C::KV_BYTES);
+                    for (int db = 0; db < DB; ++db)
+                        tma_load_3d(sK + st * C::KV_BYTES + db * (BK * 128), &p.tm_k, k_full(st),
+                                    db * 64, h, k_row0 + j * BK);
+                    ++kfills;
+                    if (!mbar_wait(v_empty(st), ((vfills / NS) & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(v_full(st), C::KV_BYTES);
+                    for (int db = 0; db < DB; ++db)
+                        tma_load_3d(sV + st * C::KV_BYTES + db * (BK * 128), &p.tm_v, v_full(st),
+                                    db * 64, h, k_row0 + j * BK);
+                    ++vfills;
+                }
+            }
+            if (*abort) {
+                // Drain: the last fill of each stage / Q buffer may still be in flight.
+                auto last_fill_wait = [&](uint32_t fills, int nslots, int slot, uint32_t bar) {
+                    const uint32_t n = fills / nslots + (static_cast<uint32_t>(slot) < fills % nslots ? 1u : 0u);
+                    if (n > 0)
+                        mbar_wait_drain(bar, (n - 1) & 1u);
+                };
+                for (int st = 0; st < NS; ++st) {
+                    last_fill_wait(kfills, NS, st, k_full(st));
+                    last_fill_wait(vfills, NS, st, v_full(st));
+                }
+                for (int qb = 0; qb < NQ; ++qb)
+                    last_fill_wait(qit, NQ, qb, q_full(qb));
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t qit = 0, kv = 0, g = 0;
+            bool ok = true;
+            // O += P V for the key tile with global index gp held in ring slot kvp.
+            auto issue_pv = [&](uint32_t gp, uint32_t kvp, bool acc) -> bool {
+                const int xp = gp & 1;
+                const int stp = kvp % NS;
+                if (!mbar_wait(p_full(xp), (gp >> 1) & 1u, abort))
+                    return false;
+                if (!mbar_wait(v_full(stp), (kvp / NS) & 1u, abort))
+                    return false;
+                tc_fence_after();
+                const uint32_t v_base = sV + stp * C::KV_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t bdesc = sdesc_sw128(v_base + kk * (16 * 128), BK * 128, 1024);
+                    mma_ts(tmem + C::O_COL, tmem + C::S_COL + xp * BK + kk * 8, bdesc,
+                           C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(s_free(xp));
+                mma_commit(v_empty(stp));
+                return true;
+            };
+            for (int k = 0; ok; ++k) {
+                const int idx = item_slot(k, cta, grid);
+                if (idx >= n_items)
+                    break;
+                const int nk = p.items[idx].w;
+                if (nk == 0)
+                    continue;
+                const int qb = qit % NQ;
+                if (!mbar_wait(q_full(qb), (qit / NQ) & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t q_base = sQ + qb * C::Q_BYTES;
+                for (int j = 0; j < nk; ++j) {
+                    const int st = kv % NS;
+                    const int x = g & 1;
+                    if (!mbar_wait(k_full(st), (kv / NS) & 1u, abort) ||
+                        !mbar_wait(s_free(x), ((g >> 1) & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t k_base = sK + st * C::KV_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off_q = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+                        const uint32_t off_k = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+                        mma_ss(tmem + C::S_COL + x * BK, sdesc_sw128(q_base + off_q, 16, 1024),
+                               sdesc_sw128(k_base + off_k, 16, 1024), C::IDESC_QK,
+                               kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(s_full(x));
+                    mma_commit(k_empty(st));
+                    if (j == nk - 1)
+                        mma_commit(q_empty(qb));
+                    if (j > 0 && !issue_pv(g - 1, kv - 1, j - 1 > 0)) {
+                        ok = false;
+                        break;
+                    }
+                    ++g;
+                    ++kv;
+                }
+                if (!ok)
+                    break;
+                if (!issue_pv(g - 1, kv - 1, nk - 1 > 0)) {
+                    ok = false;
+                    break;
+                }
+                ++qit;
+            }
+            if (*abort) {
+                // Every MMA this thread issued must finish before TMEM is freed.
+                mma_commit(drain_bar);
+                mbar_wait_drain(drain_bar, 0);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax / epilogue
+        const int quarter = warp & 3;                 // TMEM lanes [32*quarter, 32*quarter+32)
+        const int r = quarter * 32 + lane;            // this thread's row in the q tile
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const float scale_log2 = p.scale_log2;
+        const int H = p.num_heads;
+        uint32_t g = 0;
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+
+        for (int k = 0;; ++k) {
+            const int idx = item_slot(k, cta, grid);
+            if (idx >= n_items || *abort)
+                break;
+            const int4 it = p.items[idx];
+            const int b = it.x, i = it.y, h = it.z, nk = it.w;
+            const int q0 = p.cu_q[b];
+            const int lq = p.cu_q[b + 1] - q0;
+            const int lk = p.cu_k[b + 1] - p.cu_k[b];
+            const int q_local = i * BQ + r;
+            const bool row_valid = q_local < lq;
+            const long long tok = static_cast<long long>(q0) + q_local;
+
+            if (nk == 0) {
+                if (row_valid) {
+                    uint4 z = make_uint4(0, 0, 0, 0);
+                    uint4 *dst = reinterpret_cast<uint4 *>(out + (tok * H + h) * D);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c)
+                        dst[c] = z;
+                    p.lse[tok * H + h] = -FLT_MAX;
+                }
+                continue;
+            }
+
+            float m_used = -INFINITY;     // reference max, log2 units of the scaled score
+            float l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < nk; ++j) {
+                const int x = g & 1;
+                if (!mbar_wait(s_full(x), (g >> 1) & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t s_addr = tmem + lane_addr + C::S_COL + x * BK;
+                float s[BK];
+                {
+                    uint32_t sr[BK];
+#pragma unroll
+                    for (int c = 0; c < BK / 32; ++c)
+                        tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < BK; ++c)
+                        s[c] = __uint_as_float(sr[c]);
+                }
+                const int k_base = j * BK;
+                const bool need_mask = (k_base + BK > lk) || (p.causal && k_base + BK - 1 > i * BQ);
+                float mt = -INFINITY;
+                if (need_mask) {
+                    const int lim = p.causal ? min(lk, q_local + 1) : lk;   // keys < lim visible
+#pragma unroll
+                    for (int c = 0; c < BK; ++c) {
+                        const float t = (k_base + c < lim) ? s[c] * scale_log2 : -INFINITY;
+                        s[c] = t;
+                        mt = fmaxf(mt, t);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BK; ++c) {
+                        s[c] *= scale_log2;
+                        mt = fmaxf(mt, s[c]);
+                    }
+                }
+                const float m_new = fmaxf(m_used, mt);
+                const bool grow = m_new > m_used + 8.0f;    // also true for m_used = -inf
+                if (j == 0) {
+                    m_used = m_new;
+                } else if (__any_sync(0xffffffffu, grow)) {
+                    // O must hold the previous tile's product before it is rescaled.
+                    const uint32_t gp = g - 1;
+                    if (!mbar_wait(s_free(gp & 1), (gp >> 1) & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const float f = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
+                    const uint32_t o_addr = tmem + lane_addr + C::O_COL;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t rr[32];
+                        tmem_ld32(o_addr + c * 32, rr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            rr[e] = __float_as_uint(__uint_as_float(rr[e]) * f);
+                        tmem_st32(o_addr + c * 32, rr);
+                    }
+                    tmem_wait_st();
+                    l *= f;
+                    m_used = m_new;
+                }
+                const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+                float ls = 0.f;
+#pragma unroll
+                for (int c = 0; c < BK / 64; ++c) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float p0 = ex2_approx(s[c * 64 + 2 * e] - mref);
+                        const float p1 = ex2_approx(s[c * 64 + 2 * e + 1] - mref);
+                        ls += p0 + p1;
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(s_addr + c * 32, pk);
+                }
+                l += ls;
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(p_full(x));
+                ++g;
+            }
+            if (!ok)
+                break;
+
+            // Epilogue: wait for the item's last O += P V, then O / l -> bf16 and lse.
+            const uint32_t gl = g - 1;
+            if (!mbar_wait(s_free(gl & 1), (gl >> 1) & 1u, abort))
+                break;
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const uint32_t o_addr = tmem + lane_addr + C::O_COL;
+            uint4 *dst = reinterpret_cast<uint4 *>(out + (tok * H + h) * D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(o_addr + c * 32, rr);
+                tmem_wait_ld();
+                if (row_valid) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(rr[8 * e + 0]) * inv_l,
+                                          __uint_as_float(rr[8 * e + 1]) * inv_l);
+                        v.y = pack_bf16x2(__uint_as_float(rr[8 * e + 2]) * inv_l,
+                                          __uint_as_float(rr[8 * e + 3]) * inv_l);
+                        v.z = pack_bf16x2(__uint_as_float(rr[8 * e + 4]) * inv_l,
+                                          __uint_as_float(rr[8 * e + 5]) * inv_l);
+                        v.w = pack_bf16x2(__uint_as_float(rr[8 * e + 6]) * inv_l,
+                                          __uint_as_float(rr[8 * e + 7]) * inv_l);
+                        dst[c * 4 + e] = v;
+                    }
+                }
+            }
+            if (row_valid)
+                p.lse[tok * H + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -FLT_MAX;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort && threadIdx.x == 0)
+        record_error(p.status, VFA_ERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const PrefillArgs &a, int grid, cudaStream_t stream)
+{
+    static int attr_done[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 64 && !attr_done[dev]) {
+        e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(Cfg<D>::SMEM));
+        if (e != cudaSuccess)
+            return e;
+        attr_done[dev] = 1;
+    }
+    prefill_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t prefill_smem_bytes(int head_dim)
+{
+    switch (head_dim) {
+    case 64: return Cfg<64>::SMEM;
+    case 128: return Cfg<128>::SMEM;
+    case 256: return Cfg<256>::SMEM;
+    default: return 0;
+    }
+}
+
+cudaError_t launch_prefill(int head_dim, const PrefillArgs &a, int grid, cudaStream_t stream)
+{
+    switch (head_dim) {
+    case 64: return launch_d<64>(a, grid, stream);
+    case 128: return launch_d<128>(a, grid, stream);
+    case 256: return launch_d<256>(a, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace vfa

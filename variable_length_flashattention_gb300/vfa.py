@@ -1,0 +1,241 @@
+"""Python binding of libvfa (include/vfa.h): argument marshalling only.
+
+Every function takes torch tensors that already live on the current CUDA
+device, passes their data pointers and the current torch stream to the C ABI,
+and raises ``VfaError`` on a non-OK status.  All computation happens in the
+library's kernels; there is no fallback of any kind: if ``libvfa.so`` has not
+been built (``python -m variable_length_flashattention_gb300.build``) the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libvfa.so")
+_lock = threading.Lock()
+_lib = None
+
+STATUS_NAMES = {
+    0: "VFA_OK",
+    1: "VFA_ERR_INVALID_ARG",
+    2: "VFA_ERR_UNSUPPORTED",
+    3: "VFA_ERR_ARCH",
+    4: "VFA_ERR_CUDA",
+    5: "VFA_ERR_BAD_SEQLENS",
+    6: "VFA_ERR_BAD_BLOCK",
+    7: "VFA_ERR_TIMEOUT",
+    8: "VFA_ERR_WORKSPACE",
+}
+VFA_OK, VFA_ERR_INVALID_ARG, VFA_ERR_UNSUPPORTED, VFA_ERR_ARCH, VFA_ERR_CUDA = 0, 1, 2, 3, 4
+VFA_ERR_BAD_SEQLENS, VFA_ERR_BAD_BLOCK, VFA_ERR_TIMEOUT, VFA_ERR_WORKSPACE = 5, 6, 7, 8
+
+# Every symbol include/vfa.h declares: (name, restype, argtypes).
+_P, _I, _F, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = [
+    ("vfa_last_error", ctypes.c_char_p, []),
+    ("vfa_version", ctypes.c_char_p, []),
+    ("vfa_varlen_fwd_workspace_bytes", _S, [_I, _I, _I, _I, _I]),
+    ("vfa_varlen_fwd_tile_shape", _I, [_I, _P, _P]),
+    ("vfa_varlen_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _S, _P]),
+    ("vfa_varlen_schedule", _I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _S, _P]),
+    ("vfa_paged_decode_init", _I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    ("vfa_paged_decode_step", _I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    ("vfa_paged_decode_finalize", _I, [_P, _P, _I, _I, _I, _P, _P]),
+    ("vfa_debug_paged_gather", _I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    ("vfa_read_status", _I, [_P, _P, _P]),
+]
+
+
+class VfaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"libvfa.so is not built ({_LIB_PATH}); run "
+                "`python -m variable_length_flashattention_gb300.build` first")
+        L = ctypes.CDLL(_LIB_PATH)
+        for name, res, args in SIGNATURES:
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+        return L
+
+
+def _check(st: int):
+    if st != VFA_OK:
+        raise VfaError(st, lib().vfa_last_error().decode(errors="replace"))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def version() -> str:
+    return lib().vfa_version().decode()
+
+
+# ----------------------------------------------------------------- varlen forward
+
+def tile_shape(head_dim: int) -> Tuple[int, int]:
+    bq, bk = ctypes.c_int(), ctypes.c_int()
+    _check(lib().vfa_varlen_fwd_tile_shape(head_dim, ctypes.byref(bq), ctypes.byref(bk)))
+    return bq.value, bk.value
+
+
+def workspace_bytes(batch: int, total_q: int, total_k: int, num_heads: int, head_dim: int) -> int:
+    n = lib().vfa_varlen_fwd_workspace_bytes(batch, total_q, total_k, num_heads, head_dim)
+    if n == 0:
+        raise VfaError(VFA_ERR_INVALID_ARG, "no workspace size for these arguments")
+    return int(n)
+
+
+def alloc_workspace(batch: int, total_q: int, total_k: int, num_heads: int, head_dim: int,
+                    device=None) -> torch.Tensor:
+    n = workspace_bytes(batch, total_q, total_k, num_heads, head_dim)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def varlen_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+               cu_seqlens_k: torch.Tensor, max_seqlen_q: int, softmax_scale: float,
+               causal: bool, out: Optional[torch.Tensor] = None,
+               lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+               stream=None):
+    """out bf16 [Tq, H, D], lse f32 [Tq, H] = varlen attention forward (vfa_varlen_fwd)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _need(cu_seqlens_k, torch.int32, "cu_seqlens_k")
+    if q.dim() != 3 or k.shape != v.shape or k.dim() != 3 or q.shape[1:] != k.shape[1:]:
+        raise ValueError("q, k, v must be [tokens, heads, head_dim] with matching heads/head_dim")
+    total_q, H, D = q.shape
+    total_k = k.shape[0]
+    batch = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != batch + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((total_q, H), dtype=torch.float32, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    if workspace is None:
+        workspace = alloc_workspace(batch, total_q, total_k, H, D, device=q.device)
+    st = lib().vfa_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                              total_q, total_k, int(max_seqlen_q), batch, H, D,
+                              float(softmax_scale), int(bool(causal)), _ptr(out), _ptr(lse),
+                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _stream(stream))
+    _check(st)
+    return out, lse
+
+
+def schedule(cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, total_q: int, total_k: int,
+             max_seqlen_q: int, num_heads: int, block_q: int, block_k: int, causal: bool,
+             stream=None):
+    """Runs the device tile scheduler alone; returns (items int32 [n, 4] on device, status)."""
+    batch = cu_seqlens_q.numel() - 1
+    cap = num_heads * (total_q // block_q + batch)
+    dev = cu_seqlens_q.device
+    items = torch.full((max(cap, 1), 4), -1, dtype=torch.int32, device=dev)
+    n_items = torch.zeros(1, dtype=torch.int32, device=dev)
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    ints = (batch + 1) + 3 * (total_q // block_q + batch) + (total_k + block_k - 1) // block_k + 1
+    scratch = torch.empty(ints, dtype=torch.int32, device=dev)
+    st = lib().vfa_varlen_schedule(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), total_q, total_k,
+                                   int(max_seqlen_q), batch, num_heads, block_q, block_k,
+                                   int(bool(causal)), _ptr(items), cap, _ptr(n_items),
+                                   _ptr(status), _ptr(scratch), scratch.numel() * 4,
+                                   _stream(stream))
+    _check(st)
+    n = int(n_items.item())
+    return items[:n], int(status.item())
+
+
+def read_status(word: torch.Tensor, stream=None) -> int:
+    """The int32 at word.data_ptr() (workspace status word or decode status)."""
+    out = ctypes.c_int32()
+    _check(lib().vfa_read_status(_ptr(word), _stream(stream), ctypes.byref(out)))
+    return int(out.value)
+
+
+# ----------------------------------------------------------------- paged decode
+
+def decode_init(m: torch.Tensor, l: torch.Tensor, o: torch.Tensor,
+                status: Optional[torch.Tensor] = None, stream=None):
+    S, Hq, D = o.shape
+    for t, n in ((m, "m"), (l, "l"), (o, "o")):
+        _need(t, torch.float32, n)
+    _check(lib().vfa_paged_decode_init(_ptr(m), _ptr(l), _ptr(o), S, Hq, D, _ptr(status),
+                                       _stream(stream)))
+
+
+def decode_step(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                tile_blocks: torch.Tensor, tile_block_counts: torch.Tensor,
+                m: torch.Tensor, l: torch.Tensor, o: torch.Tensor,
+                status: Optional[torch.Tensor] = None, stream=None):
+    _need(q, torch.bfloat16, "q")
+    _need(k_pool, torch.bfloat16, "k_pool")
+    _need(v_pool, torch.bfloat16, "v_pool")
+    _need(tile_blocks, torch.int32, "tile_blocks")
+    _need(tile_block_counts, torch.int32, "tile_block_counts")
+    S, Hq, D = q.shape
+    nb, bs, Hkv, D2 = k_pool.shape
+    if D2 != D or v_pool.shape != k_pool.shape or tile_blocks.shape[0] != S:
+        raise ValueError("inconsistent decode shapes")
+    _check(lib().vfa_paged_decode_step(_ptr(q), _ptr(k_pool), _ptr(v_pool), nb, _ptr(tile_blocks),
+                                       _ptr(tile_block_counts), tile_blocks.shape[1], S, Hq, Hkv,
+                                       D, bs, _ptr(m), _ptr(l), _ptr(o), _ptr(status),
+                                       _stream(stream)))
+
+
+def decode_finalize(l: torch.Tensor, o: torch.Tensor, out: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    S, Hq, D = o.shape
+    if out is None:
+        out = torch.empty((S, Hq, D), dtype=torch.bfloat16, device=o.device)
+    _check(lib().vfa_paged_decode_finalize(_ptr(l), _ptr(o), S, Hq, D, _ptr(out),
+                                           _stream(stream)))
+    return out
+
+
+def debug_paged_gather(k_pool: torch.Tensor, v_pool: torch.Tensor, tile_blocks: torch.Tensor,
+                       tile_block_counts: torch.Tensor, k_out: torch.Tensor, v_out: torch.Tensor,
+                       status: Optional[torch.Tensor] = None, stream=None):
+    nb, bs, Hkv, D = k_pool.shape
+    S, cap = tile_blocks.shape
+    _check(lib().vfa_debug_paged_gather(_ptr(k_pool), _ptr(v_pool), nb, _ptr(tile_blocks),
+                                        _ptr(tile_block_counts), cap, S, Hkv, D, bs,
+                                        _ptr(k_out), _ptr(v_out), _ptr(status), _stream(stream)))
