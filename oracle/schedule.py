@@ -12,8 +12,12 @@ schedule here is the plain rule the scheduler kernel must reproduce:
     the tile's rows may see: ceil(Lk_b / BK) without a mask, and with the
     top-left causal mask ceil(min(Lk_b, min(Lq_b, (i+1)*BQ)) / BK), because
     the tile's last row min(Lq_b, (i+1)*BQ) - 1 sees keys 0 .. that row;
-  * items are ordered by cost, largest first (longest-processing-time
-    order), ties by (b, i, h) ascending.
+  * the items of one (b, h) form a group and stay next to each other, so
+    the q tiles that share a sequence's keys and values run at the same time;
+  * groups are ordered by their largest item cost, then their total cost,
+    both descending, then by (b, h) ascending (longest work first keeps the
+    tail short when CTAs take items in list order);
+  * inside a group, items are ordered by cost descending, then i ascending.
 
 Each item is four int32: (b, i, h, cost).  Integer work: the scheduler kernel
 must match this bit for bit.
@@ -40,16 +44,21 @@ def schedule(cu_seqlens_q, cu_seqlens_k, num_heads: int, bq: int, bk: int,
     """The ordered work list, int32 [n_items, 4] of (b, i, h, cost)."""
     cq = [int(x) for x in cu_seqlens_q]
     ck = [int(x) for x in cu_seqlens_k]
-    items = []
+    groups = []
     for b in range(len(cq) - 1):
         lq = cq[b + 1] - cq[b]
         lk = ck[b + 1] - ck[b]
-        for i in range(_ceil_div(lq, bq)):
-            c = tile_cost(lq, lk, i, bq, bk, causal)
-            for h in range(num_heads):
-                items.append((c, b, i, h))
-    items.sort(key=lambda t: (-t[0], t[1], t[2], t[3]))
+        tiles = [(tile_cost(lq, lk, i, bq, bk, causal), i) for i in range(_ceil_div(lq, bq))]
+        if not tiles:
+            continue
+        tiles.sort(key=lambda t: (-t[0], t[1]))
+        biggest = max(c for c, _ in tiles)
+        total = sum(c for c, _ in tiles)
+        for h in range(num_heads):
+            groups.append(((-biggest, -total, b, h), [(b, i, h, c) for c, i in tiles]))
+    groups.sort(key=lambda g: g[0])
+    items = [it for _, members in groups for it in members]
     out = np.zeros((len(items), 4), dtype=np.int32)
-    for n, (c, b, i, h) in enumerate(items):
-        out[n] = (b, i, h, c)
+    for n, it in enumerate(items):
+        out[n] = it
     return out

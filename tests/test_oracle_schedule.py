@@ -4,7 +4,9 @@
     least one (row, key) pair the mask lets through, found by enumeration;
   * coverage: every (sequence, q tile, head) appears exactly once and the
     tiles cover every query row of every head once;
-  * order: costs never increase along the list, ties in (b, i, h) order.
+  * order: the items of one (sequence, head) are contiguous; groups come in
+    non-increasing order of their largest cost, then total cost; costs never
+    increase inside a group.
 """
 import numpy as np
 import pytest
@@ -50,8 +52,17 @@ def test_coverage_and_order(oracle_mod, causal):
         rows += min(lq[b], (i + 1) * 128) - i * 128
     assert rows == sum(lq) * H
     assert len(seen) == H * sum(-(-x // 128) for x in lq)
-    keys = [(-int(c), int(b), int(i), int(h)) for b, i, h, c in items]
+    # groups contiguous, keyed by (largest cost, total cost) non-increasing
+    runs = []
+    for b, i, h, c in items:
+        if not runs or runs[-1][0] != (int(b), int(h)):
+            runs.append(((int(b), int(h)), []))
+        runs[-1][1].append((int(c), int(i)))
+    assert len({r[0] for r in runs}) == len(runs), "a group is split"
+    keys = [(-max(c for c, _ in m), -sum(c for c, _ in m), g) for g, m in runs]
     assert keys == sorted(keys)
+    for _, m in runs:
+        assert [(-c, i) for c, i in m] == sorted((-c, i) for c, i in m)
 
 
 def test_tiny_workload_list():
@@ -60,4 +71,4 @@ def test_tiny_workload_list():
                             2, 128, 128, True)
     # five q tiles (one per short sequence, two for the 129-token one) times two heads
     assert len(items) == 10
-    assert [tuple(x) for x in items[:2]] == [(3, 1, 0, 2), (3, 1, 1, 2)]
+    assert [tuple(x) for x in items[:4]] == [(3, 1, 0, 2), (3, 0, 0, 1), (3, 1, 1, 2), (3, 0, 1, 1)]

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/vfa.h: argument checks, TMA tensor
 // map encoding, workspace carve-up and launches.  Nothing here allocates or
 // frees device memory.
+#include <cfloat>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -180,6 +181,7 @@ vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_se
     a.item_capacity = items_capacity;
     a.n_items = n_items;
     a.status = status;
+    a.next_item = nullptr;
     a.scratch = static_cast<int32_t *>(scratch);
     a.scratch_ints = static_cast<int>(scratch_bytes / sizeof(int));
     cudaError_t e = vfa::launch_schedule(a, reinterpret_cast<cudaStream_t>(stream));
@@ -201,6 +203,9 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
                     batch, num_heads, total_q, total_k);
     if (!supported_head_dim(head_dim))
         return fail(VFA_ERR_UNSUPPORTED, "head_dim %d not supported (64, 128, 256)", head_dim);
+    if (!(softmax_scale >= 0.f) || softmax_scale > FLT_MAX)
+        return fail(VFA_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0 (got %g)",
+                    static_cast<double>(softmax_scale));
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
         !aligned(lse, 4) || !aligned(workspace, 256))
         return fail(VFA_ERR_INVALID_ARG,
@@ -224,6 +229,7 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     int32_t *n_items = reinterpret_cast<int32_t *>(ws + 4);
+    int32_t *next_item = reinterpret_cast<int32_t *>(ws + 8);
     int4 *items = reinterpret_cast<int4 *>(ws + wl.items_offset);
 
     vfa::SchedArgs sa;
@@ -241,6 +247,7 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     sa.item_capacity = wl.item_capacity;
     sa.n_items = n_items;
     sa.status = status;
+    sa.next_item = next_item;
     sa.scratch = reinterpret_cast<int32_t *>(ws + wl.scratch_offset);
     sa.scratch_ints = wl.scratch_ints;
     cudaError_t e = vfa::launch_schedule(sa, s);
@@ -260,11 +267,15 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     pa.cu_k = cu_seqlens_k;
     pa.items = items;
     pa.n_items = n_items;
+    pa.next_item = next_item;
     pa.status = status;
     pa.out = out;
     pa.lse = lse;
     pa.num_heads = num_heads;
-    pa.scale_log2 = softmax_scale * 1.4426950408889634f;
+    // The kernel takes row maxima on raw scores, which needs a positive scale;
+    // a zero scale (uniform weights) becomes the smallest normal float, which
+    // gives the same weights for every finite score.
+    pa.scale_log2 = softmax_scale > 0.f ? softmax_scale * 1.4426950408889634f : FLT_MIN;
     pa.causal = causal != 0;
     const int grid = wl.item_capacity < dev.sm_count ? wl.item_capacity : dev.sm_count;
     e = vfa::launch_prefill(head_dim, pa, grid, s);

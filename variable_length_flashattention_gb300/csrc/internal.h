@@ -49,6 +49,7 @@ struct SchedArgs {
     int item_capacity;
     int32_t *n_items;
     int32_t *status;
+    int32_t *next_item;   // nullable: the prefill's dynamic-fetch counter, reset to 0
     int32_t *scratch;
     int scratch_ints;
 };
@@ -66,11 +67,12 @@ struct PrefillArgs {
     const int32_t *cu_k;
     const int4 *items;
     const int32_t *n_items;
+    int32_t *next_item;   // atomic counter CTAs take items from (reset by the scheduler)
     int32_t *status;
     void *out;
     float *lse;
     int num_heads;
-    float scale_log2;     // softmax_scale * log2(e)
+    float scale_log2;     // softmax_scale * log2(e), > 0
     int causal;
 };
 

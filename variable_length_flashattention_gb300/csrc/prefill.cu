@@ -8,18 +8,21 @@
 // positions).  The plan's tile sizes, thread layout and sequence lookup are
 // not kept; this kernel is built for Blackwell:
 //
-//   * persistent CTAs walk a device-built work list (sched.cu) of
-//     (sequence, 128-row q tile, head) items in longest-first order;
+//   * persistent CTAs take (sequence, 128-row q tile, head) items from the
+//     device-built work list (sched.cu) through an atomic counter; the
+//     producer warp fetches and hands each item to the other warps through a
+//     two-slot shared-memory ring;
 //   * warp 0 moves Q, K and V tiles with TMA (128-byte swizzle) into a
 //     shared-memory ring guarded by mbarriers;
-//   * warp 1 issues tcgen05.mma: S = Q K^T into one of two TMEM buffers, and
+//   * warp 1 issues tcgen05.mma: S = Q K^T into one of three TMEM buffers, and
 //     O += P V with P read straight from TMEM (P overwrites its S buffer as
 //     bf16) and V as an MN-major shared-memory operand;
 //   * warps 2-5 own one query row per thread: they read S rows from TMEM,
-//     apply scale and masks, keep m and l, write P back to TMEM, rescale O
-//     in TMEM when the row max has grown by more than 2^8 (exact after the
-//     final division because l and O always share one reference max), and
-//     run the epilogue (O / l -> bf16, lse).
+//     take the row max on the raw scores (the scale is positive), fold scale
+//     and max into one FMA before exp2, keep m and l, write P back to TMEM,
+//     rescale O in TMEM only when the row max has grown by more than 2^8
+//     (exact after the final division because l and O always share one
+//     reference max), and run the epilogue (O / l -> bf16, lse).
 // Every wait is bounded: on expiry the kernel records VFA_ERR_TIMEOUT,
 // drains its own in-flight copies and MMAs, frees TMEM and returns.
 #include <cfloat>
@@ -42,25 +45,20 @@ struct Cfg {
     static constexpr uint32_t Q_BYTES = BQ * D * 2;
     static constexpr uint32_t KV_BYTES = BK * D * 2;
     static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int NSB = 3;                         // S/P buffers in TMEM
     static constexpr uint32_t O_COL = 0;                  // O: columns [0, D)
-    static constexpr uint32_t S_COL = D;                  // S buffers: [D, D+BK), [D+BK, D+2BK)
-    static constexpr int NUM_BARS = 2 * NQ + 4 * NS + 7;
+    static constexpr uint32_t S_COL = D;                  // S buffer x: [D + x*BK, D + (x+1)*BK)
+    static constexpr int NUM_BARS = 2 * NQ + 4 * NS + 3 * NSB + 1 + 4;
     static constexpr size_t SMEM = 1024 /*alignment slack*/ + NQ * Q_BYTES + 2 * NS * KV_BYTES +
                                    NUM_BARS * 8 + 64;
     static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BQ, BK, false, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BQ, D, false, true);
-    static_assert(S_COL + 2 * BK <= TMEM_COLS, "TMEM budget");
+    static_assert(S_COL + NSB * BK <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 constexpr int kThreads = 192;      // 6 warps: TMA, MMA, 4 x softmax/epilogue
-
-__device__ __forceinline__ int item_slot(int k, int cta, int grid)
-{
-    // Snake order over the longest-first list: even rounds left to right,
-    // odd rounds right to left, so each CTA's total cost stays even.
-    return k * grid + ((k & 1) ? (grid - 1 - cta) : cta);
-}
+constexpr int kItemConsumers = 5;  // MMA lane + one arrival per softmax warp
 
 __device__ __forceinline__ void record_error(int32_t *status, int code)
 {
@@ -76,6 +74,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
+    __shared__ int4 s_item[2][2];     // (b, i, h, cost), (q row 0 of b, Lq, Lk, k row 0 of b)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -93,10 +92,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     auto k_empty = [&](int i) { return bars + 8u * (2 * NQ + NS + i); };
     auto v_full = [&](int i) { return bars + 8u * (2 * NQ + 2 * NS + i); };
     auto v_empty = [&](int i) { return bars + 8u * (2 * NQ + 3 * NS + i); };
+    constexpr int NSB = C::NSB;
     auto s_full = [&](int x) { return bars + 8u * (2 * NQ + 4 * NS + x); };
-    auto s_free = [&](int x) { return bars + 8u * (2 * NQ + 4 * NS + 2 + x); };
-    auto p_full = [&](int x) { return bars + 8u * (2 * NQ + 4 * NS + 4 + x); };
-    const uint32_t drain_bar = bars + 8u * (2 * NQ + 4 * NS + 6);
+    auto s_free = [&](int x) { return bars + 8u * (2 * NQ + 4 * NS + NSB + x); };
+    auto p_full = [&](int x) { return bars + 8u * (2 * NQ + 4 * NS + 2 * NSB + x); };
+    const uint32_t drain_bar = bars + 8u * (2 * NQ + 4 * NS + 3 * NSB);
+    auto item_full = [&](int x) { return bars + 8u * (2 * NQ + 4 * NS + 3 * NSB + 1 + x); };
+    auto item_empty = [&](int x) { return bars + 8u * (2 * NQ + 4 * NS + 3 * NSB + 3 + x); };
     volatile int *abort = &s_abort;
 
     if (threadIdx.x == 0) {
@@ -111,10 +113,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             mbar_init(v_full(i), 1);
             mbar_init(v_empty(i), 1);
         }
-        for (int x = 0; x < 2; ++x) {
+        for (int x = 0; x < NSB; ++x) {
             mbar_init(s_full(x), 1);
             mbar_init(s_free(x), 1);
             mbar_init(p_full(x), 128);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(item_full(x), 1);
+            mbar_init(item_empty(x), kItemConsumers);
         }
         mbar_init(drain_bar, 1);
         fence_barrier_init();
@@ -123,32 +129,58 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         tmem_alloc(smem_u32(&s_tmem_base), C::TMEM_COLS);
         tmem_relinquish();
     }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&p.tm_q);
+        tma_prefetch_map(&p.tm_k);
+        tma_prefetch_map(&p.tm_v);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem_base;
 
-    const int n_items = (*p.status == 0) ? *p.n_items : 0;
-    const int grid = gridDim.x, cta = blockIdx.x;
+    // The work list is written by the scheduler grid launched just before.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // Take the next item from the ring (consumer side); false at the end.
+    auto next_item = [&](uint32_t n, int4 &it, int4 &seq) -> bool {
+        const int slot = n & 1;
+        if (!mbar_wait(item_full(slot), (n >> 1) & 1u, abort))
+            return false;
+        it = s_item[slot][0];
+        seq = s_item[slot][1];
+        return it.x >= 0;
+    };
 
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ producer
         if (lane == 0) {
-            tma_prefetch_map(&p.tm_q);
-            tma_prefetch_map(&p.tm_k);
-            tma_prefetch_map(&p.tm_v);
-            uint32_t qit = 0, kfills = 0, vfills = 0;
+            const int n_items = (*p.status == 0) ? *p.n_items : 0;
+            uint32_t n = 0, qit = 0, kfills = 0, vfills = 0;
             bool ok = true;
-            for (int k = 0; ok; ++k) {
-                const int idx = item_slot(k, cta, grid);
-                if (idx >= n_items)
+            for (;; ++n) {
+                const int slot = n & 1;
+                if (!mbar_wait(item_empty(slot), ((n >> 1) & 1u) ^ 1u, abort)) {
+                    ok = false;
                     break;
-                const int4 it = p.items[idx];
-                const int b = it.x, i = it.y, h = it.z, nk = it.w;
+                }
+                const int idx = atomicAdd(p.next_item, 1);
+                const int4 it = idx < n_items ? p.items[idx] : make_int4(-1, 0, 0, 0);
+                int4 seq = make_int4(0, 0, 0, 0);
+                if (it.x >= 0) {
+                    const int q0 = p.cu_q[it.x], k0 = p.cu_k[it.x];
+                    seq = make_int4(q0, p.cu_q[it.x + 1] - q0, p.cu_k[it.x + 1] - k0, k0);
+                }
+                s_item[slot][0] = it;
+                s_item[slot][1] = seq;
+                mbar_arrive(item_full(slot));
+                if (it.x < 0)
+                    break;
+                const int i = it.y, h = it.z, nk = it.w;
                 if (nk == 0)
                     continue;
-                const int q_row0 = p.cu_q[b] + i * BQ;
-                const int k_row0 = p.cu_k[b];
+                const int q_row0 = seq.x + i * BQ;
+                const int k_row0 = seq.w;
                 const int qb = qit % NQ;
                 if (!mbar_wait(q_empty(qb), ((qit / NQ) & 1u) ^ 1u, abort)) {
                     ok = false;
@@ -180,13 +212,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                                     db * 64, h, k_row0 + j * BK);
                     ++vfills;
                 }
+                if (!ok)
+                    break;
             }
-            if (*abort) {
+            if (!ok || *abort) {
                 // Drain: the last fill of each stage / Q buffer may still be in flight.
                 auto last_fill_wait = [&](uint32_t fills, int nslots, int slot, uint32_t bar) {
-                    const uint32_t n = fills / nslots + (static_cast<uint32_t>(slot) < fills % nslots ? 1u : 0u);
-                    if (n > 0)
-                        mbar_wait_drain(bar, (n - 1) & 1u);
+                    const uint32_t k = fills / nslots + (static_cast<uint32_t>(slot) < fills % nslots ? 1u : 0u);
+                    if (k > 0)
+                        mbar_wait_drain(bar, (k - 1) & 1u);
                 };
                 for (int st = 0; st < NS; ++st) {
                     last_fill_wait(kfills, NS, st, k_full(st));
@@ -199,33 +233,45 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t qit = 0, kv = 0, g = 0;
+            // Descriptors of every buffer, built once; a k-step only adds a
+            // compile-time offset (in 16-byte units) to the start-address field.
+            // (The start-address field is the low 14 bits, address / 16; shared
+            // addresses stay below 256 KiB, so descriptors are linear in it.)
+            const uint64_t q_desc0 = sdesc_sw128(sQ, 16, 1024);
+            const uint64_t k_desc0 = sdesc_sw128(sK, 16, 1024);
+            const uint64_t v_desc0 = sdesc_sw128(sV, BK * 128, 1024);
+            uint32_t n = 0, qit = 0, kv = 0, g = 0;
             bool ok = true;
             // O += P V for the key tile with global index gp held in ring slot kvp.
             auto issue_pv = [&](uint32_t gp, uint32_t kvp, bool acc) -> bool {
-                const int xp = gp & 1;
+                const int xp = gp % NSB;
                 const int stp = kvp % NS;
-                if (!mbar_wait(p_full(xp), (gp >> 1) & 1u, abort))
+                if (!mbar_wait(p_full(xp), (gp / NSB) & 1u, abort))
                     return false;
                 if (!mbar_wait(v_full(stp), (kvp / NS) & 1u, abort))
                     return false;
                 tc_fence_after();
-                const uint32_t v_base = sV + stp * C::KV_BYTES;
+                const uint64_t vd = v_desc0 + stp * (C::KV_BYTES >> 4);
+                const uint32_t a_tm = tmem + C::S_COL + xp * BK;
+                if (acc)
+                    mma_ts_c<1>(tmem + C::O_COL, a_tm, vd, C::IDESC_PV);
+                else
+                    mma_ts_c<0>(tmem + C::O_COL, a_tm, vd, C::IDESC_PV);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint64_t bdesc = sdesc_sw128(v_base + kk * (16 * 128), BK * 128, 1024);
-                    mma_ts(tmem + C::O_COL, tmem + C::S_COL + xp * BK + kk * 8, bdesc,
-                           C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 1; kk < BK / 16; ++kk)
+                    mma_ts_c<1>(tmem + C::O_COL, a_tm + kk * 8, vd + kk * (16 * 128 / 16),
+                                C::IDESC_PV);
                 mma_commit(s_free(xp));
                 mma_commit(v_empty(stp));
                 return true;
             };
-            for (int k = 0; ok; ++k) {
-                const int idx = item_slot(k, cta, grid);
-                if (idx >= n_items)
+            for (;; ++n) {
+                int4 it, seq;
+                const bool more = next_item(n, it, seq);
+                mbar_arrive(item_empty(n & 1));
+                if (!more)
                     break;
-                const int nk = p.items[idx].w;
+                const int nk = it.w;
                 if (nk == 0)
                     continue;
                 const int qb = qit % NQ;
@@ -233,25 +279,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     ok = false;
                     break;
                 }
-                const uint32_t q_base = sQ + qb * C::Q_BYTES;
+                const uint64_t qd = q_desc0 + qb * (C::Q_BYTES >> 4);
                 for (int j = 0; j < nk; ++j) {
                     const int st = kv % NS;
-                    const int x = g & 1;
+                    const int x = g % NSB;
                     if (!mbar_wait(k_full(st), (kv / NS) & 1u, abort) ||
-                        !mbar_wait(s_free(x), ((g >> 1) & 1u) ^ 1u, abort)) {
+                        !mbar_wait(s_free(x), ((g / NSB) & 1u) ^ 1u, abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t k_base = sK + st * C::KV_BYTES;
+                    const uint64_t kd = k_desc0 + st * (C::KV_BYTES >> 4);
+                    const uint32_t s_tm = tmem + C::S_COL + x * BK;
+                    mma_ss_c<0>(s_tm, qd, kd, C::IDESC_QK);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off_q = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-                        const uint32_t off_k = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-                        mma_ss(tmem + C::S_COL + x * BK, sdesc_sw128(q_base + off_q, 16, 1024),
-                               sdesc_sw128(k_base + off_k, 16, 1024), C::IDESC_QK,
-                               kk > 0 ? 1u : 0u);
-                    }
+                    for (int kk = 1; kk < D / 16; ++kk)
+                        mma_ss_c<1>(s_tm, qd + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4),
+                                    kd + (((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4),
+                                    C::IDESC_QK);
                     mma_commit(s_full(x));
                     mma_commit(k_empty(st));
                     if (j == nk - 1)
@@ -271,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 }
                 ++qit;
             }
-            if (*abort) {
+            if (!ok || *abort) {
                 // Every MMA this thread issued must finish before TMEM is freed.
                 mma_commit(drain_bar);
                 mbar_wait_drain(drain_bar, 0);
@@ -287,15 +332,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         uint32_t g = 0;
         __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
 
-        for (int k = 0;; ++k) {
-            const int idx = item_slot(k, cta, grid);
-            if (idx >= n_items || *abort)
+        const float2 scale2 = make_float2(scale_log2, scale_log2);
+        for (uint32_t n = 0;; ++n) {
+            int4 it, seq;
+            const bool more = next_item(n, it, seq);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(item_empty(n & 1));
+            if (!more)
                 break;
-            const int4 it = p.items[idx];
-            const int b = it.x, i = it.y, h = it.z, nk = it.w;
-            const int q0 = p.cu_q[b];
-            const int lq = p.cu_q[b + 1] - q0;
-            const int lk = p.cu_k[b + 1] - p.cu_k[b];
+            const int i = it.y, h = it.z, nk = it.w;
+            const int q0 = seq.x, lq = seq.y, lk = seq.z;
             const int q_local = i * BQ + r;
             const bool row_valid = q_local < lq;
             const long long tok = static_cast<long long>(q0) + q_local;
@@ -316,8 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             float l = 0.f;
             bool ok = true;
             for (int j = 0; j < nk; ++j) {
-                const int x = g & 1;
-                if (!mbar_wait(s_full(x), (g >> 1) & 1u, abort)) {
+                const int x = g % NSB;
+                if (!mbar_wait(s_full(x), (g / NSB) & 1u, abort)) {
                     ok = false;
                     break;
                 }
@@ -334,32 +381,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     for (int c = 0; c < BK; ++c)
                         s[c] = __uint_as_float(sr[c]);
                 }
+                // Row max of the raw scores (the scale is positive): eight
+                // independent three-input max chains.
                 const int k_base = j * BK;
                 const bool need_mask = (k_base + BK > lk) || (p.causal && k_base + BK - 1 > i * BQ);
-                float mt = -INFINITY;
                 if (need_mask) {
-                    const int lim = p.causal ? min(lk, q_local + 1) : lk;   // keys < lim visible
+                    const int lim = (p.causal ? min(lk, q_local + 1) : lk) - k_base;   // keys < lim visible
 #pragma unroll
-                    for (int c = 0; c < BK; ++c) {
-                        const float t = (k_base + c < lim) ? s[c] * scale_log2 : -INFINITY;
-                        s[c] = t;
-                        mt = fmaxf(mt, t);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < BK; ++c) {
-                        s[c] *= scale_log2;
-                        mt = fmaxf(mt, s[c]);
-                    }
+                    for (int c = 0; c < BK; ++c)
+                        s[c] = c < lim ? s[c] : -INFINITY;
                 }
-                const float m_new = fmaxf(m_used, mt);
+                float mx[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    mx[e] = fmaxf(s[e], s[e + 8]);
+#pragma unroll
+                for (int c = 16; c < BK; c += 16)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        mx[e] = fmax3(mx[e], s[c + e], s[c + 8 + e]);
+                const float mt_raw = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                           fmaxf(mx[6], mx[7]));
+                const float m_tile = mt_raw == -INFINITY ? -INFINITY : mt_raw * scale_log2;
+                const float m_new = fmaxf(m_used, m_tile);
                 const bool grow = m_new > m_used + 8.0f;    // also true for m_used = -inf
                 if (j == 0) {
                     m_used = m_new;
                 } else if (__any_sync(0xffffffffu, grow)) {
                     // O must hold the previous tile's product before it is rescaled.
                     const uint32_t gp = g - 1;
-                    if (!mbar_wait(s_free(gp & 1), (gp >> 1) & 1u, abort)) {
+                    if (!mbar_wait(s_free(gp % NSB), (gp / NSB) & 1u, abort)) {
                         ok = false;
                         break;
                     }
@@ -380,21 +431,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     l *= f;
                     m_used = m_new;
                 }
-                const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-                float ls = 0.f;
+                // p = 2^(s * scale_log2 - m): packed FMA pairs, one exp2 per score,
+                // packed sums into four pair accumulators.
+                const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+                const float2 negm2 = make_float2(neg_m, neg_m);
+                float2 ls[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    ls[e] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int c = 0; c < BK / 64; ++c) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        const float p0 = ex2_approx(s[c * 64 + 2 * e] - mref);
-                        const float p1 = ex2_approx(s[c * 64 + 2 * e + 1] - mref);
-                        ls += p0 + p1;
-                        pk[e] = pack_bf16x2(p0, p1);
+                        const float2 t = __ffma2_rn(make_float2(s[c * 64 + 2 * e], s[c * 64 + 2 * e + 1]),
+                                                    scale2, negm2);
+                        const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+                        ls[e & 3] = __fadd2_rn(ls[e & 3], pp);
+                        pk[e] = pack_bf16x2(pp.x, pp.y);
                     }
                     tmem_st32(s_addr + c * 32, pk);
                 }
-                l += ls;
+                const float2 l2 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
+                l += l2.x + l2.y;
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(p_full(x));
@@ -405,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
             // Epilogue: wait for the item's last O += P V, then O / l -> bf16 and lse.
             const uint32_t gl = g - 1;
-            if (!mbar_wait(s_free(gl & 1), (gl >> 1) & 1u, abort))
+            if (!mbar_wait(s_free(gl % NSB), (gl / NSB) & 1u, abort))
                 break;
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -462,7 +521,20 @@ cudaError_t launch_d(const PrefillArgs &a, int grid, cudaStream_t stream)
             return e;
         attr_done[dev] = 1;
     }
-    prefill_kernel<D><<<grid, kThreads, Cfg<D>::SMEM, stream>>>(a);
+    // Programmatic dependent launch: the prologue overlaps the scheduler grid.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, prefill_kernel<D>, a);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 

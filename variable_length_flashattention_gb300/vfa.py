@@ -172,8 +172,9 @@ def schedule(cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, total_q: in
     items = torch.full((max(cap, 1), 4), -1, dtype=torch.int32, device=dev)
     n_items = torch.zeros(1, dtype=torch.int32, device=dev)
     status = torch.full((1,), -1, dtype=torch.int32, device=dev)
-    ints = (batch + 1) + 3 * (total_q // block_q + batch) + (total_k + block_k - 1) // block_k + 1
-    scratch = torch.empty(ints, dtype=torch.int32, device=dev)
+    # scratch of vfa_varlen_fwd_workspace_bytes() bytes covers any tile shape
+    nbytes = workspace_bytes(batch, total_q, total_k, num_heads, 128)
+    scratch = torch.empty((nbytes + 3) // 4, dtype=torch.int32, device=dev)
     st = lib().vfa_varlen_schedule(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), total_q, total_k,
                                    int(max_seqlen_q), batch, num_heads, block_q, block_k,
                                    int(bool(causal)), _ptr(items), cap, _ptr(n_items),
