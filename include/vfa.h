@@ -118,6 +118,40 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
                           vfa_stream_t stream);
 
 /*
+ * vfa_varlen_fwd without a caller workspace.  The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory --
+ * code on a real-time or callback thread that must not enter the allocator,
+ * runtimes that give kernels a fixed memory plan and forbid other
+ * allocations, plugins that only receive their inputs' and outputs' pointers.
+ *
+ * Same arguments, results and device checks as vfa_varlen_fwd, minus the
+ * workspace: the scratch (status word, work list, scheduler records) lives
+ * in one 1 MiB array inside the library, which every GPU that loads the
+ * library keeps reserved until the process exits.  It allocates nothing and
+ * frees nothing.
+ *
+ * device_status  nullable device int32 [1]: receives the call's status word
+ *                (VFA_OK or VFA_ERR_BAD_SEQLENS ...), copied on `stream`.
+ *
+ * Limits and rules:
+ *   - a problem whose vfa_varlen_fwd_workspace_bytes() exceeds 1 MiB
+ *     (roughly num_heads * (total_q / 128 + batch) > 60000) returns
+ *     VFA_ERR_UNSUPPORTED and enqueues nothing;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture;
+ *   - all calls share the one array: calls whose work can overlap on the GPU
+ *     (different streams without ordering) race and give undefined results.
+ *     Each call rewrites every scratch word it reads, so stream-ordered calls
+ *     are independent.
+ */
+vfa_status vfa_varlen_fwd_noalloc(const void *q, const void *k, const void *v,
+                                  const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                  int total_q, int total_k, int max_seqlen_q, int batch,
+                                  int num_heads, int head_dim, float softmax_scale, int causal,
+                                  void *out, float *lse, int32_t *device_status,
+                                  vfa_stream_t stream);
+
+/*
  * The device tile scheduler alone (the first kernel vfa_varlen_fwd runs),
  * writing into caller buffers so the work list can be inspected.
  *

@@ -117,6 +117,11 @@ bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 
 }  // namespace
 
+vfa_status vfa::set_error(vfa_status st, const char *message)
+{
+    return fail(st, "%s", message);
+}
+
 extern "C" {
 
 const char *vfa_last_error(void) { return g_err; }

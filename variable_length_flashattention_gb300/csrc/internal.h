@@ -10,6 +10,9 @@
 
 namespace vfa {
 
+// Records `message` as the calling thread's vfa_last_error() text; returns st.
+vfa_status set_error(vfa_status st, const char *message);
+
 // ------------------------------------------------------------ tile shapes
 
 // Query rows per tile: one tcgen05 M=128 accumulator, one TMEM lane per row.

@@ -42,6 +42,7 @@ SIGNATURES = [
     ("vfa_varlen_fwd_workspace_bytes", _S, [_I, _I, _I, _I, _I]),
     ("vfa_varlen_fwd_tile_shape", _I, [_I, _P, _P]),
     ("vfa_varlen_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _S, _P]),
+    ("vfa_varlen_fwd_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
     ("vfa_varlen_schedule", _I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _S, _P]),
     ("vfa_paged_decode_init", _I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     ("vfa_paged_decode_step", _I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
@@ -158,6 +159,31 @@ def varlen_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: 
                               float(softmax_scale), int(bool(causal)), _ptr(out), _ptr(lse),
                               _ptr(workspace), workspace.numel() * workspace.element_size(),
                               _stream(stream))
+    _check(st)
+    return out, lse
+
+
+def varlen_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                       cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, max_seqlen_q: int,
+                       softmax_scale: float, causal: bool, out: torch.Tensor, lse: torch.Tensor,
+                       device_status: Optional[torch.Tensor] = None, stream=None):
+    """vfa_varlen_fwd_noalloc: the forward with the library's static scratch.
+
+    For callers that cannot allocate device memory: the caller passes only
+    inputs and outputs (allocated however it likes); the library allocates
+    nothing.  Calls that can overlap on the GPU must not use it concurrently.
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _need(cu_seqlens_k, torch.int32, "cu_seqlens_k")
+    total_q, H, D = q.shape
+    st = lib().vfa_varlen_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q),
+                                      _ptr(cu_seqlens_k), total_q, k.shape[0], int(max_seqlen_q),
+                                      cu_seqlens_q.numel() - 1, H, D, float(softmax_scale),
+                                      int(bool(causal)), _ptr(out), _ptr(lse), _ptr(device_status),
+                                      _stream(stream))
     _check(st)
     return out, lse
 
