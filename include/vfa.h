@@ -65,11 +65,12 @@ size_t vfa_varlen_fwd_workspace_bytes(int batch, int total_q, int total_k, int n
                                       int head_dim);
 
 /*
- * Tile shape the forward uses for `head_dim`: q tile rows (*block_q) and key
- * tile rows (*block_k).  The work list is built over these tiles.
+ * Tile shape the forward uses for `head_dim`: q tile rows (*block_q), key
+ * tile rows (*block_k), and whether one work item holds two q tiles
+ * (*pair_tiles, 0 or 1).  The work list is built over these tiles.
  * Returns VFA_ERR_UNSUPPORTED for a head_dim this build does not implement.
  */
-vfa_status vfa_varlen_fwd_tile_shape(int head_dim, int *block_q, int *block_k);
+vfa_status vfa_varlen_fwd_tile_shape(int head_dim, int *block_q, int *block_k, int *pair_tiles);
 
 /*
  * Exact softmax(scale * Q K^T, optional causal mask) V over packed
@@ -135,7 +136,7 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
  *
  * Limits and rules:
  *   - a problem whose vfa_varlen_fwd_workspace_bytes() exceeds 1 MiB
- *     (roughly num_heads * (total_q / 128 + batch) > 60000) returns
+ *     (roughly num_heads * (total_q / 128 + batch) > 30000) returns
  *     VFA_ERR_UNSUPPORTED and enqueues nothing;
  *   - the first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture;
@@ -155,24 +156,33 @@ vfa_status vfa_varlen_fwd_noalloc(const void *q, const void *k, const void *v,
  * The device tile scheduler alone (the first kernel vfa_varlen_fwd runs),
  * writing into caller buffers so the work list can be inspected.
  *
- * Items are int32 quadruples (b, i, h, cost): q tile i (local rows
- * [i*block_q, min(Lq_b, (i+1)*block_q))) of sequence b, head h, and cost =
- * the number of key tiles it visits (ceil(Lk_b / block_k); causal:
- * ceil(min(Lk_b, min(Lq_b, (i+1)*block_q)) / block_k)).  Order: cost
- * descending, ties by (b, i, h) ascending.  Sequences with Lq_b == 0 give no
- * items.
+ * A tile is q tile i (local rows [i*block_q, min(Lq_b, (i+1)*block_q))) of
+ * sequence b and head h; its cost is the number of key tiles it visits
+ * (ceil(Lk_b / block_k); causal: ceil(min(Lk_b, min(Lq_b, (i+1)*block_q)) /
+ * block_k)).  The tiles of one (b, h) stay together; groups are ordered by
+ * their largest cost, then total cost (descending), then (b, h); inside a
+ * group by cost descending, then i.  With pair_tiles != 0 two consecutive
+ * tiles of a group form one item (what vfa_varlen_fwd uses for head_dim <=
+ * 128); otherwise each tile is one item.  Each item is eight int32:
+ * (b, i_a, h, cost_a, i_b, cost_b, 0, 0), with i_b = -1 and cost_b = 0 when
+ * the second slot is empty.  Sequences with Lq_b == 0 give no items.
  *
- * items        device int32 [items_capacity, 4] (output).
+ * block_k must be a power of two and block_q a multiple of block_k
+ * (VFA_ERR_UNSUPPORTED otherwise); vfa_varlen_fwd_tile_shape() only returns
+ * such shapes.
+ *
+ * items        device int32 [items_capacity, 8] (output).
  * n_items      device int32 [1] (output): number of items written.
  * status       device int32 [1] (output): VFA_OK or a device-detected code.
- * scratch      device scratch of vfa_varlen_fwd_workspace_bytes() bytes.
+ * scratch      device scratch of vfa_varlen_fwd_workspace_bytes() bytes,
+ *              8-byte aligned.
  */
 vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                                int total_q, int total_k, int max_seqlen_q, int batch,
                                int num_heads, int block_q, int block_k, int causal,
-                               int32_t *items, int items_capacity, int32_t *n_items,
-                               int32_t *status, void *scratch, size_t scratch_bytes,
-                               vfa_stream_t stream);
+                               int pair_tiles, int32_t *items, int items_capacity,
+                               int32_t *n_items, int32_t *status, void *scratch,
+                               size_t scratch_bytes, vfa_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Paged GQA decode                                                          */

@@ -17,10 +17,14 @@ schedule here is the plain rule the scheduler kernel must reproduce:
   * groups are ordered by their largest item cost, then their total cost,
     both descending, then by (b, h) ascending (longest work first keeps the
     tail short when CTAs take items in list order);
-  * inside a group, items are ordered by cost descending, then i ascending.
+  * inside a group, tiles are ordered by cost descending, then i ascending;
+  * when the kernel processes two q tiles per work item (`pair`), consecutive
+    tiles of a group form one item (the second slot is empty for the last
+    tile of a group with an odd count); otherwise each tile is one item.
 
-Each item is four int32: (b, i, h, cost).  Integer work: the scheduler kernel
-must match this bit for bit.
+Each item is eight int32: (b, i_a, h, cost_a, i_b, cost_b, 0, 0), with
+i_b = -1 and cost_b = 0 when the second slot is empty.  Integer work: the
+scheduler kernel must match this bit for bit.
 """
 from __future__ import annotations
 
@@ -40,8 +44,8 @@ def tile_cost(lq: int, lk: int, i: int, bq: int, bk: int, causal: bool) -> int:
 
 
 def schedule(cu_seqlens_q, cu_seqlens_k, num_heads: int, bq: int, bk: int,
-             causal: bool) -> np.ndarray:
-    """The ordered work list, int32 [n_items, 4] of (b, i, h, cost)."""
+             causal: bool, pair: bool = False) -> np.ndarray:
+    """The ordered work list, int32 [n_items, 8] of (b, i_a, h, cost_a, i_b, cost_b, 0, 0)."""
     cq = [int(x) for x in cu_seqlens_q]
     ck = [int(x) for x in cu_seqlens_k]
     groups = []
@@ -54,11 +58,17 @@ def schedule(cu_seqlens_q, cu_seqlens_k, num_heads: int, bq: int, bk: int,
         tiles.sort(key=lambda t: (-t[0], t[1]))
         biggest = max(c for c, _ in tiles)
         total = sum(c for c, _ in tiles)
+        step = 2 if pair else 1
         for h in range(num_heads):
-            groups.append(((-biggest, -total, b, h), [(b, i, h, c) for c, i in tiles]))
+            members = []
+            for k in range(0, len(tiles), step):
+                ca, ia = tiles[k]
+                cb, ib = tiles[k + 1] if step == 2 and k + 1 < len(tiles) else (0, -1)
+                members.append((b, ia, h, ca, ib, cb, 0, 0))
+            groups.append(((-biggest, -total, b, h), members))
     groups.sort(key=lambda g: g[0])
     items = [it for _, members in groups for it in members]
-    out = np.zeros((len(items), 4), dtype=np.int32)
+    out = np.zeros((len(items), 8), dtype=np.int32)
     for n, it in enumerate(items):
         out[n] = it
     return out

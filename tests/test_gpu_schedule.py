@@ -18,12 +18,12 @@ def vfa():
     return binding
 
 
-def _check(vfa, oracle_mod, lq, lk, H, bq, bk, causal):
+def _check(vfa, oracle_mod, lq, lk, H, bq, bk, causal, pair=False):
     cq, ck = W.cu_seqlens(lq), W.cu_seqlens(lk)
     items, status = vfa.schedule(torch.from_numpy(cq).cuda(), torch.from_numpy(ck).cuda(),
-                                 int(cq[-1]), int(ck[-1]), max(lq), H, bq, bk, causal)
+                                 int(cq[-1]), int(ck[-1]), max(lq), H, bq, bk, causal, pair)
     assert status == 0
-    ref = oracle_mod.schedule(cq, ck, H, bq, bk, causal)
+    ref = oracle_mod.schedule(cq, ck, H, bq, bk, causal, pair)
     got = items.cpu().numpy()
     assert got.shape == ref.shape
     np.testing.assert_array_equal(got, ref)
@@ -33,8 +33,9 @@ def _check(vfa, oracle_mod, lq, lk, H, bq, bk, causal):
                                   "cross-d256"])
 def test_workload_schedules(vfa, oracle_mod, name):
     case = W.VARLEN_WORKLOADS[name](0)
-    bq, bk = vfa.tile_shape(case.head_dim)
-    _check(vfa, oracle_mod, case.lengths_q, case.lengths_k, case.num_heads, bq, bk, case.causal)
+    bq, bk, pair = vfa.tile_shape(case.head_dim)
+    _check(vfa, oracle_mod, case.lengths_q, case.lengths_k, case.num_heads, bq, bk, case.causal,
+           pair)
 
 
 @pytest.mark.parametrize("seed", range(6))
@@ -46,7 +47,8 @@ def test_random_mixes(vfa, oracle_mod, seed, causal):
     lk = [int(x) for x in rng.integers(0, 1500, B)]
     lq[0] = max(lq[0], 1)
     for bq, bk in ((128, 128), (128, 64)):
-        _check(vfa, oracle_mod, lq, lk, int(rng.integers(1, 5)), bq, bk, causal)
+        for pair in (False, True):
+            _check(vfa, oracle_mod, lq, lk, int(rng.integers(1, 5)), bq, bk, causal, pair)
 
 
 def test_many_tiles_use_global_scratch(vfa, oracle_mod):
@@ -54,6 +56,7 @@ def test_many_tiles_use_global_scratch(vfa, oracle_mod):
     lq = [128] * 4200 + [700000]
     lk = [1] * 4200 + [700000]
     _check(vfa, oracle_mod, lq, lk, 1, 128, 128, True)
+    _check(vfa, oracle_mod, lq, lk, 1, 128, 128, True, pair=True)
 
 
 def test_bad_seqlens_status(vfa):

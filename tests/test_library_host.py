@@ -38,9 +38,9 @@ def test_exports_every_declared_symbol(vfa):
 
 def test_version_and_tile_shape(vfa):
     assert "sm_103a" in vfa.version()
-    assert vfa.tile_shape(64) == (128, 128)
-    assert vfa.tile_shape(128) == (128, 128)
-    assert vfa.tile_shape(256) == (128, 64)
+    assert vfa.tile_shape(64) == (128, 128, True)
+    assert vfa.tile_shape(128) == (128, 128, True)
+    assert vfa.tile_shape(256) == (128, 64, False)
     with pytest.raises(vfa.VfaError) as e:
         vfa.tile_shape(96)
     assert e.value.status == vfa.VFA_ERR_UNSUPPORTED
@@ -55,7 +55,7 @@ def test_workspace_bound_covers_worst_case(vfa):
         n_items = len(oracle.schedule(cu, cu, 3, 128, 128, True))
         total = int(cu[-1])
         ws = vfa.workspace_bytes(len(lengths), total, total, 3, 128)
-        assert ws >= 256 + 16 * n_items
+        assert ws >= 256 + 32 * n_items
     assert vfa.lib().vfa_varlen_fwd_workspace_bytes(0, 10, 10, 1, 128) == 0
     assert vfa.lib().vfa_varlen_fwd_workspace_bytes(1, 10, 10, 1, 80) == 0
 

@@ -138,31 +138,36 @@ size_t vfa_varlen_fwd_workspace_bytes(int batch, int total_q, int total_k, int n
         .total_bytes;
 }
 
-vfa_status vfa_varlen_fwd_tile_shape(int head_dim, int *block_q, int *block_k)
+vfa_status vfa_varlen_fwd_tile_shape(int head_dim, int *block_q, int *block_k, int *pair_tiles)
 {
     if (!supported_head_dim(head_dim))
         return fail(VFA_ERR_UNSUPPORTED, "head_dim %d not supported (64, 128, 256)", head_dim);
-    if (!block_q || !block_k)
+    if (!block_q || !block_k || !pair_tiles)
         return fail(VFA_ERR_INVALID_ARG, "null output pointer");
     *block_q = vfa::kBlockQ;
     *block_k = vfa::block_k_for(head_dim);
+    *pair_tiles = vfa::pairs_for(head_dim) ? 1 : 0;
     return VFA_OK;
 }
 
 vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                                int total_q, int total_k, int max_seqlen_q, int batch,
                                int num_heads, int block_q, int block_k, int causal,
-                               int32_t *items, int items_capacity, int32_t *n_items,
-                               int32_t *status, void *scratch, size_t scratch_bytes,
-                               vfa_stream_t stream)
+                               int pair_tiles, int32_t *items, int items_capacity,
+                               int32_t *n_items, int32_t *status, void *scratch,
+                               size_t scratch_bytes, vfa_stream_t stream)
 {
     if (!cu_seqlens_q || !cu_seqlens_k || !items || !n_items || !status || !scratch)
         return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
     if (batch < 1 || num_heads < 1 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
         block_q < 1 || block_k < 1 || items_capacity < 0)
         return fail(VFA_ERR_INVALID_ARG, "bad size argument");
-    if (!aligned(items, 16) || !aligned(scratch, 4))
-        return fail(VFA_ERR_INVALID_ARG, "items must be 16-byte aligned");
+    if (!aligned(items, 16) || !aligned(scratch, 8))
+        return fail(VFA_ERR_INVALID_ARG, "items must be 16-byte and scratch 8-byte aligned");
+    if ((block_k & (block_k - 1)) != 0 || block_q % block_k != 0)
+        return fail(VFA_ERR_UNSUPPORTED,
+                    "block_k must be a power of two and block_q a multiple of it (%d, %d)",
+                    block_q, block_k);
     const int need = vfa::schedule_scratch_ints(batch, total_q, total_k, block_q, block_k);
     if (scratch_bytes < static_cast<size_t>(need) * sizeof(int))
         return fail(VFA_ERR_INVALID_ARG, "scratch too small: %zu < %zu bytes", scratch_bytes,
@@ -182,6 +187,7 @@ vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_se
     a.block_q = block_q;
     a.block_k = block_k;
     a.causal = causal != 0;
+    a.pair = pair_tiles != 0;
     a.items = reinterpret_cast<int4 *>(items);
     a.item_capacity = items_capacity;
     a.n_items = n_items;
@@ -248,6 +254,7 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     sa.block_q = bq;
     sa.block_k = bk;
     sa.causal = causal != 0;
+    sa.pair = vfa::pairs_for(head_dim) ? 1 : 0;
     sa.items = items;
     sa.item_capacity = wl.item_capacity;
     sa.n_items = n_items;
@@ -266,7 +273,8 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     memset(&pa, 0, sizeof pa);
     if ((st = encode_packed_map(&pa.tm_q, q, total_q, num_heads, head_dim, bq)) ||
         (st = encode_packed_map(&pa.tm_k, k, total_k, num_heads, head_dim, bk)) ||
-        (st = encode_packed_map(&pa.tm_v, v, total_k, num_heads, head_dim, bk)))
+        (st = encode_packed_map(&pa.tm_v, v, total_k, num_heads, head_dim, bk)) ||
+        (st = encode_packed_map(&pa.tm_o, out, total_q, num_heads, head_dim, bq)))
         return st;
     pa.cu_q = cu_seqlens_q;
     pa.cu_k = cu_seqlens_k;

@@ -28,8 +28,9 @@ __host__ __device__ constexpr int block_k_for(int head_dim)
 // Layout of the varlen forward workspace (all offsets in bytes):
 //   [0]   int32 status word
 //   [4]   int32 number of work items
-//   [8]   int32 reserved
-//   [256] int4 items[item_capacity]
+//   [8]   int32 next item to take (the prefill's atomic counter)
+//   [256] items[item_capacity], 32 bytes each: int4 (b, i_a, h, cost_a),
+//         int4 (i_b, cost_b, 0, 0) with i_b = -1 when the second slot is empty
 //   then  int32 scheduler scratch
 struct WorkspaceLayout {
     size_t items_offset;
@@ -48,7 +49,8 @@ struct SchedArgs {
     const int32_t *cu_q;
     const int32_t *cu_k;
     int batch, total_q, total_k, max_seqlen_q, num_heads, block_q, block_k, causal;
-    int4 *items;
+    int pair;             // non-zero: two consecutive tiles of a group per item
+    int4 *items;          // two int4 per item
     int item_capacity;
     int32_t *n_items;
     int32_t *status;
@@ -65,10 +67,10 @@ int schedule_scratch_ints(int batch, int total_q, int total_k, int block_q, int 
 // ------------------------------------------------------------ prefill
 
 struct PrefillArgs {
-    CUtensorMap tm_q, tm_k, tm_v;
+    CUtensorMap tm_q, tm_k, tm_v, tm_o;   // tm_o: the output, for tile stores
     const int32_t *cu_q;
     const int32_t *cu_k;
-    const int4 *items;
+    const int4 *items;    // two int4 per item
     const int32_t *n_items;
     int32_t *next_item;   // atomic counter CTAs take items from (reset by the scheduler)
     int32_t *status;
@@ -79,8 +81,17 @@ struct PrefillArgs {
     int causal;
 };
 
+// Whether the forward for `head_dim` runs two q tiles per work item.
+__host__ __device__ constexpr bool pairs_for(int head_dim)
+{
+    return head_dim <= 128;
+}
+
+// Dispatches by head_dim: two-q-tile kernel (prefill_pair.cu) for 64 and 128,
+// single-tile kernel (prefill.cu) for 256.
 cudaError_t launch_prefill(int head_dim, const PrefillArgs &a, int grid, cudaStream_t stream);
-size_t prefill_smem_bytes(int head_dim);
+cudaError_t launch_prefill_pair(int head_dim, const PrefillArgs &a, int grid,
+                                cudaStream_t stream);
 
 // ------------------------------------------------------------ decode
 

@@ -19,7 +19,7 @@ namespace {
 
 // 1 MiB of scratch, reserved on every GPU that loads the library until the
 // process exits.  It holds the forward's status word, work-list header and
-// work list (16 bytes per (q tile, head)) plus the scheduler's per-sequence
+// work list (32 bytes per item) plus the scheduler's per-sequence
 // records; vfa_varlen_fwd_workspace_bytes() gives the size a problem needs.
 constexpr size_t kStaticScratchBytes = 1u << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];

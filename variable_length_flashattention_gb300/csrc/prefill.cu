@@ -1,4 +1,6 @@
-// prefill.cu -- variable-length attention forward on sm_103a.
+// prefill.cu -- variable-length attention forward on sm_103a, one q tile per
+// CTA work item (used for head_dim 256, whose O accumulator alone fills half
+// of TMEM; head_dim 64 and 128 use prefill_pair.cu).
 //
 // Computes, per packed query row, softmax(scale * q K^T, masks) V and the
 // natural-log log-sum-exp, by the tiled online-softmax recurrence of
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     break;
                 }
                 const int idx = atomicAdd(p.next_item, 1);
-                const int4 it = idx < n_items ? p.items[idx] : make_int4(-1, 0, 0, 0);
+                const int4 it = idx < n_items ? p.items[2 * idx] : make_int4(-1, 0, 0, 0);
                 int4 seq = make_int4(0, 0, 0, 0);
                 if (it.x >= 0) {
                     const int q0 = p.cu_q[it.x], k0 = p.cu_k[it.x];
@@ -540,24 +542,13 @@ cudaError_t launch_d(const PrefillArgs &a, int grid, cudaStream_t stream)
 
 }  // namespace
 
-size_t prefill_smem_bytes(int head_dim)
-{
-    switch (head_dim) {
-    case 64: return Cfg<64>::SMEM;
-    case 128: return Cfg<128>::SMEM;
-    case 256: return Cfg<256>::SMEM;
-    default: return 0;
-    }
-}
-
 cudaError_t launch_prefill(int head_dim, const PrefillArgs &a, int grid, cudaStream_t stream)
 {
-    switch (head_dim) {
-    case 64: return launch_d<64>(a, grid, stream);
-    case 128: return launch_d<128>(a, grid, stream);
-    case 256: return launch_d<256>(a, grid, stream);
-    default: return cudaErrorInvalidValue;
-    }
+    if (pairs_for(head_dim))
+        return launch_prefill_pair(head_dim, a, grid, stream);
+    if (head_dim == 256)
+        return launch_d<256>(a, grid, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace vfa

@@ -1,0 +1,679 @@
+// prefill_pair.cu -- variable-length attention forward on sm_103a, two q
+// tiles per CTA work item (head_dim 64 and 128).
+//
+// Same definition as prefill.cu ("Varlen Flash Attention Implementation
+// Plan", Task 1 Step 1: scaled scores, causal and key-boundary masks on local
+// positions, online softmax with running max m and denominator l, out =
+// acc / l, lse = m + log l).  What changes is how the work is laid out on
+// the SM:
+//
+//   * a work item holds two q tiles (a, b) of the same (sequence, head); each
+//     K/V tile is loaded once by TMA and used by both;
+//   * warp 0 loads Q and K, warp 10 loads V, each with its own ring;
+//   * warp 1 issues, per key tile j:  S_a = Q_a K_j^T,  O_b += P_b V_{j-1},
+//     S_b = Q_b K_j^T,  O_a += P_a V_j  -- while one softmax warpgroup works
+//     on its scores the tensor core runs the other tile's products.  P_x
+//     lives in S_x's TMEM columns; the next S_x is issued right after the
+//     O_x += P_x V that reads it: tcgen05.mma instructions of one thread run
+//     in issue order, so the product has read P_x before S_x is rewritten
+//     (and waiting for its completion instead would idle the tensor core);
+//   * warps 2-5 own tile a's 128 rows, warps 6-9 tile b's, one row per
+//     thread (TMEM lane = row).  After a tile's first key block, scores are
+//     exponentiated against the current reference max in the same pass that
+//     finds the block's max; only if the max grew by more than 2^8 is the
+//     block redone at the new max (and O, l rescaled); P stays in registers
+//     until that is decided, so S is still intact for a redo;
+//   * full output tiles leave through a swizzled shared-memory stage and a
+//     TMA tensor store; a sequence's last, partial tile is stored row by row;
+//   * TMEM: O_a, O_b (D columns each), S/P_a, S/P_b (128 columns each).
+// Everything else (item ring fed by an atomic counter, bounded waits with
+// drain-and-report on expiry) is as in prefill.cu.
+#include <cfloat>
+#include <type_traits>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace vfa {
+
+namespace {
+
+template <int D>
+struct PairCfg {
+    static constexpr int BQ = kBlockQ;
+    static constexpr int BK = 128;
+    static constexpr int NS = D == 64 ? 4 : 2;            // K and V ring stages
+    static constexpr int DB = D / 64;                     // 128-byte column blocks per row
+    static constexpr uint32_t Q_BYTES = BQ * D * 2;
+    static constexpr uint32_t KV_BYTES = BK * D * 2;
+    static constexpr uint32_t STAGE_BYTES = BQ * 128;     // one 64-column block of an O tile
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t S_COL = 2 * D;              // S_x at S_COL + x * BK; O_x at x * D
+    static constexpr int NUM_BARS = 4 + 4 * NS + 6 + 4 + 1 + 4;
+    static constexpr size_t SMEM = 1024 + 2 * Q_BYTES + 2 * NS * KV_BYTES + 2 * STAGE_BYTES +
+                                   NUM_BARS * 8 + 64;
+    static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BQ, BK, false, false);
+    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BQ, D, false, true);
+    static_assert(S_COL + 2 * BK <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+constexpr int kThreads = 352;       // 11 warps: Q/K loads, MMA, 2 x 4 softmax, V loads
+constexpr int kVWarp = 10;
+constexpr int kItemConsumers = 10;  // MMA + V loader + one arrival per softmax warp
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale when the max grows by > 2^8
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ PrefillArgs p)
+{
+    using C = PairCfg<D>;
+    constexpr int BQ = C::BQ, BK = C::BK, NS = C::NS, DB = C::DB;
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem_base;
+    __shared__ int s_abort;
+    __shared__ int4 s_item[2][3];     // (b, i_a, h, cost_a), (i_b, cost_b, -, -), (q0, Lq, Lk, k0)
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t sQ = base;                           // Q_a, Q_b
+    const uint32_t sK = sQ + 2 * C::Q_BYTES;
+    const uint32_t sV = sK + NS * C::KV_BYTES;
+    const uint32_t sO = sV + NS * C::KV_BYTES;          // output staging, one block per q slot
+    const uint32_t bars = sO + 2 * C::STAGE_BYTES;
+    auto q_full = [&](int x) { return bars + 8u * x; };
+    auto q_empty = [&](int x) { return bars + 8u * (2 + x); };
+    auto k_full = [&](int i) { return bars + 8u * (4 + i); };
+    auto k_empty = [&](int i) { return bars + 8u * (4 + NS + i); };
+    auto v_full = [&](int i) { return bars + 8u * (4 + 2 * NS + i); };
+    auto v_empty = [&](int i) { return bars + 8u * (4 + 3 * NS + i); };
+    auto s_full = [&](int x) { return bars + 8u * (4 + 4 * NS + x); };
+    auto o_done = [&](int x) { return bars + 8u * (4 + 4 * NS + 2 + x); };   // an O_x += P_x V finished
+    auto p_full = [&](int x) { return bars + 8u * (4 + 4 * NS + 4 + x); };
+    auto item_full = [&](int x) { return bars + 8u * (4 + 4 * NS + 6 + x); };
+    auto item_empty = [&](int x) { return bars + 8u * (4 + 4 * NS + 8 + x); };
+    const uint32_t drain_bar = bars + 8u * (4 + 4 * NS + 10);
+    auto stage_ready = [&](int x) { return bars + 8u * (4 + 4 * NS + 11 + x); };
+    auto stage_free = [&](int x) { return bars + 8u * (4 + 4 * NS + 13 + x); };
+    volatile int *abort = &s_abort;
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(q_full(x), 1);
+            mbar_init(q_empty(x), 1);
+            mbar_init(s_full(x), 1);
+            mbar_init(o_done(x), 1);
+            mbar_init(p_full(x), 128);
+            mbar_init(item_full(x), 1);
+            mbar_init(item_empty(x), kItemConsumers);
+            mbar_init(stage_ready(x), 128);
+            mbar_init(stage_free(x), 1);
+        }
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(k_full(i), 1);
+            mbar_init(k_empty(i), 1);
+            mbar_init(v_full(i), 1);
+            mbar_init(v_empty(i), 1);
+        }
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&s_tmem_base), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&p.tm_q);
+        tma_prefetch_map(&p.tm_k);
+        tma_prefetch_map(&p.tm_v);
+        tma_prefetch_map(&p.tm_o);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem_base;
+
+    // The work list is written by the scheduler grid launched just before.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    auto next_item = [&](uint32_t n, int4 &it, int4 &itb, int4 &seq) -> bool {
+        const int slot = n & 1;
+        if (!mbar_wait(item_full(slot), (n >> 1) & 1u, abort))
+            return false;
+        it = s_item[slot][0];
+        itb = s_item[slot][1];
+        seq = s_item[slot][2];
+        return it.x >= 0;
+    };
+    // Drain after an abort: the last fill of each ring slot may still be in flight.
+    auto last_fill_wait = [&](uint32_t fills, int nslots, int slot, uint32_t bar) {
+        const uint32_t k = fills / nslots + (static_cast<uint32_t>(slot) < fills % nslots ? 1u : 0u);
+        if (k > 0)
+            mbar_wait_drain(bar, (k - 1) & 1u);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ items, Q and K
+        if (lane == 0) {
+            const int n_items = (*p.status == 0) ? *p.n_items : 0;
+            uint32_t n = 0, qloads[2] = {0, 0}, kfills = 0;
+            bool ok = true;
+            for (;; ++n) {
+                const int slot = n & 1;
+                if (!mbar_wait(item_empty(slot), ((n >> 1) & 1u) ^ 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                const int idx = atomicAdd(p.next_item, 1);
+                int4 it = make_int4(-1, 0, 0, 0), itb = make_int4(-1, 0, 0, 0);
+                int4 seq = make_int4(0, 0, 0, 0);
+                if (idx < n_items) {
+                    it = p.items[2 * idx];
+                    itb = p.items[2 * idx + 1];
+                    const int q0 = p.cu_q[it.x], k0 = p.cu_k[it.x];
+                    seq = make_int4(q0, p.cu_q[it.x + 1] - q0, p.cu_k[it.x + 1] - k0, k0);
+                }
+                s_item[slot][0] = it;
+                s_item[slot][1] = itb;
+                s_item[slot][2] = seq;
+                mbar_arrive(item_full(slot));
+                if (it.x < 0)
+                    break;
+                const int h = it.z, nk_a = it.w;
+                const int nk_b = itb.x >= 0 ? itb.y : 0;
+                if (nk_a == 0)
+                    continue;
+                for (int x = 0; x < 2 && ok; ++x) {
+                    if (x == 1 && nk_b == 0)
+                        break;
+                    const int i = x == 0 ? it.y : itb.x;
+                    if (!mbar_wait(q_empty(x), (qloads[x] & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(q_full(x), C::Q_BYTES);
+                    for (int db = 0; db < DB; ++db)
+                        tma_load_3d(sQ + x * C::Q_BYTES + db * (BQ * 128), &p.tm_q, q_full(x),
+                                    db * 64, h, seq.x + i * BQ);
+                    ++qloads[x];
+                }
+                for (int j = 0; j < nk_a && ok; ++j) {
+                    const int st = kfills % NS;
+                    if (!mbar_wait(k_empty(st), ((kfills / NS) & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(k_full(st), C::KV_BYTES);
+                    for (int db = 0; db < DB; ++db)
+                        tma_load_3d(sK + st * C::KV_BYTES + db * (BK * 128), &p.tm_k, k_full(st),
+                                    db * 64, h, seq.w + j * BK);
+                    ++kfills;
+                }
+                if (!ok)
+                    break;
+            }
+            if (!ok || *abort) {
+                for (int st = 0; st < NS; ++st)
+                    last_fill_wait(kfills, NS, st, k_full(st));
+                for (int x = 0; x < 2; ++x)
+                    if (qloads[x] > 0)
+                        mbar_wait_drain(q_full(x), (qloads[x] - 1) & 1u);
+            }
+        }
+    } else if (warp == kVWarp) {
+        // ------------------------------------------------------------ V
+        if (lane == 0) {
+            uint32_t vfills = 0;
+            bool ok = true;
+            for (uint32_t n = 0;; ++n) {
+                int4 it, itb, seq;
+                const bool more = next_item(n, it, itb, seq);
+                mbar_arrive(item_empty(n & 1));
+                if (!more)
+                    break;
+                const int h = it.z, nk_a = it.w;
+                for (int j = 0; j < nk_a; ++j) {
+                    const int st = vfills % NS;
+                    if (!mbar_wait(v_empty(st), ((vfills / NS) & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(v_full(st), C::KV_BYTES);
+                    for (int db = 0; db < DB; ++db)
+                        tma_load_3d(sV + st * C::KV_BYTES + db * (BK * 128), &p.tm_v, v_full(st),
+                                    db * 64, h, seq.w + j * BK);
+                    ++vfills;
+                }
+                if (!ok)
+                    break;
+            }
+            if (!ok || *abort)
+                for (int st = 0; st < NS; ++st)
+                    last_fill_wait(vfills, NS, st, v_full(st));
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint64_t q_desc0 = sdesc_sw128(sQ, 16, 1024);
+            const uint64_t k_desc0 = sdesc_sw128(sK, 16, 1024);
+            const uint64_t v_desc0 = sdesc_sw128(sV, BK * 128, 1024);
+            uint32_t n = 0, kv = 0, qloads[2] = {0, 0}, gt[2] = {0, 0};   // tiles per q slot
+            bool ok = true;
+            // S_x = Q_x K^T for q slot x, K in ring slot st (issue order after the
+            // previous O_x += P_x V protects P_x; see the file comment).
+            auto issue_qk = [&](int x, int st) {
+                const uint64_t qd = q_desc0 + x * (C::Q_BYTES >> 4);
+                const uint64_t kd = k_desc0 + st * (C::KV_BYTES >> 4);
+                const uint32_t s_tm = tmem + C::S_COL + x * BK;
+                mma_ss_c<0>(s_tm, qd, kd, C::IDESC_QK);
+#pragma unroll
+                for (int kk = 1; kk < D / 16; ++kk)
+                    mma_ss_c<1>(s_tm, qd + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4),
+                                kd + (((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4), C::IDESC_QK);
+                mma_commit(s_full(x));
+            };
+            // O_x += P_x V for q slot x (its tile number gt[x]), V in ring slot st.
+            auto issue_pv = [&](int x, int st, uint32_t v_fill, bool acc) -> bool {
+                if (!mbar_wait(p_full(x), gt[x] & 1u, abort) ||
+                    !mbar_wait(v_full(st), (v_fill / NS) & 1u, abort))
+                    return false;
+                tc_fence_after();
+                const uint64_t vd = v_desc0 + st * (C::KV_BYTES >> 4);
+                const uint32_t a_tm = tmem + C::S_COL + x * BK;
+                const uint32_t o_tm = tmem + x * D;
+                if (acc)
+                    mma_ts_c<1>(o_tm, a_tm, vd, C::IDESC_PV);
+                else
+                    mma_ts_c<0>(o_tm, a_tm, vd, C::IDESC_PV);
+#pragma unroll
+                for (int kk = 1; kk < BK / 16; ++kk)
+                    mma_ts_c<1>(o_tm, a_tm + kk * 8, vd + kk * (16 * 128 / 16), C::IDESC_PV);
+                mma_commit(o_done(x));
+                ++gt[x];
+                return true;
+            };
+            for (;; ++n) {
+                int4 it, itb, seq;
+                const bool more = next_item(n, it, itb, seq);
+                mbar_arrive(item_empty(n & 1));
+                if (!more)
+                    break;
+                const int nk_a = it.w;
+                const int nk_b = itb.x >= 0 ? itb.y : 0;
+                if (nk_a == 0)
+                    continue;
+                if (!mbar_wait(q_full(0), qloads[0] & 1u, abort) ||
+                    (nk_b > 0 && !mbar_wait(q_full(1), qloads[1] & 1u, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int j = 0; j < nk_a && ok; ++j) {
+                    const int st = kv % NS;
+                    const int st_prev = (kv + NS - 1) % NS;
+                    if (!mbar_wait(k_full(st), (kv / NS) & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_qk(0, st);                              // S_a(j)
+                    if (j == nk_a - 1)
+                        mma_commit(q_empty(0));
+                    if (j >= 1 && j - 1 < nk_b) {
+                        // O_b += P_b(j-1) V(j-1); V(j-1) is then free
+                        if (!issue_pv(1, st_prev, kv - 1, j - 1 > 0)) {
+                            ok = false;
+                            break;
+                        }
+                        mma_commit(v_empty(st_prev));
+                    }
+                    if (j < nk_b) {
+                        issue_qk(1, st);                          // S_b(j)
+                        if (j == nk_b - 1)
+                            mma_commit(q_empty(1));
+                    }
+                    mma_commit(k_empty(st));
+                    if (!issue_pv(0, st, kv, j > 0)) {            // O_a += P_a(j) V(j)
+                        ok = false;
+                        break;
+                    }
+                    if (j >= nk_b)
+                        mma_commit(v_empty(st));                  // tile b does not use V(j)
+                    ++kv;
+                }
+                if (!ok)
+                    break;
+                if (nk_b == nk_a) {
+                    const int st_last = (kv + NS - 1) % NS;
+                    if (!issue_pv(1, st_last, kv - 1, nk_a - 1 > 0)) {
+                        ok = false;
+                        break;
+                    }
+                    mma_commit(v_empty(st_last));
+                }
+                ++qloads[0];
+                if (nk_b > 0)
+                    ++qloads[1];
+            }
+            if (!ok || *abort) {
+                mma_commit(drain_bar);
+                mbar_wait_drain(drain_bar, 0);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax / epilogue
+        const int x = (warp - 2) >> 2;                // q slot: 0 = tile a (warps 2-5), 1 = tile b
+        const int quarter = warp & 3;                 // TMEM lanes [32*quarter, +32)
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t s_addr = tmem + lane_addr + C::S_COL + x * BK;
+        const uint32_t o_addr = tmem + lane_addr + x * D;
+        const uint32_t stage = sO + x * C::STAGE_BYTES;
+        const bool leader = (warp & 3) == 2 && lane == 0;   // first warp of the warpgroup
+        const float scale_log2 = p.scale_log2;
+        const float2 scale2 = make_float2(scale_log2, scale_log2);
+        const int H = p.num_heads;
+        uint32_t g = 0;                               // this slot's tiles so far
+        uint32_t stage_uses = 0;                      // output blocks staged so far
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+        using Masked = std::integral_constant<bool, true>;
+        using Plain = std::integral_constant<bool, false>;
+
+        for (uint32_t n = 0;; ++n) {
+            int4 it, itb, seq;
+            const bool more = next_item(n, it, itb, seq);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(item_empty(n & 1));
+            if (!more)
+                break;
+            const int i = x == 0 ? it.y : itb.x;
+            if (i < 0)
+                continue;                             // no second tile in this item
+            const int h = it.z;
+            const int nk = x == 0 ? it.w : itb.y;
+            const int q0 = seq.x, lq = seq.y, lk = seq.z;
+            const int q_local = i * BQ + r;
+            const bool row_valid = q_local < lq;
+            const long long tok = static_cast<long long>(q0) + q_local;
+
+            if (nk == 0) {
+                if (row_valid) {
+                    uint4 z = make_uint4(0, 0, 0, 0);
+                    uint4 *dst = reinterpret_cast<uint4 *>(out + (tok * H + h) * D);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c)
+                        dst[c] = z;
+                    p.lse[tok * H + h] = -FLT_MAX;
+                }
+                continue;
+            }
+
+            float m_used = -INFINITY;
+            float l = 0.f;
+            bool ok = true;
+            for (int j = 0; j < nk; ++j) {
+                if (!mbar_wait(s_full(x), g & 1u, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int k_base = j * BK;
+                const bool need_mask = (k_base + BK > lk) || (p.causal && k_base + BK - 1 > i * BQ);
+                const int lim = need_mask ? (p.causal ? min(lk, q_local + 1) : lk) - k_base : BK;
+
+                // Row max of the raw scores of this block (scale > 0), 32 columns at a time.
+                auto block_max = [&](auto masked) -> float {
+                    constexpr bool MASK = decltype(masked)::value;
+                    float mx[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        mx[e] = -INFINITY;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t sr[32];
+                        tmem_ld32(s_addr + cc * 32, sr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; c += 16)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                float s0 = __uint_as_float(sr[c + e]);
+                                float s1 = __uint_as_float(sr[c + 8 + e]);
+                                if (MASK) {
+                                    s0 = cc * 32 + c + e < lim ? s0 : -INFINITY;
+                                    s1 = cc * 32 + c + 8 + e < lim ? s1 : -INFINITY;
+                                }
+                                mx[e] = fmax3(mx[e], s0, s1);
+                            }
+                    }
+                    return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7]));
+                };
+                // p = 2^(s * scale_log2 - m) packed to bf16 pairs in pk (not yet stored:
+                // S must stay intact in TMEM in case the block is redone); returns the
+                // block's sum of p and (through mt_raw) its raw row max.
+                uint32_t pk[64];
+                auto exp_block = [&](auto masked, float m_ref, float &mt_raw) -> float {
+                    constexpr bool MASK = decltype(masked)::value;
+                    const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                    const float2 negm2 = make_float2(neg_m, neg_m);
+                    float2 ls[4];
+                    float mx[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        ls[e] = make_float2(0.f, 0.f);
+                        mx[e] = -INFINITY;
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t sr[32];
+                        tmem_ld32(s_addr + cc * 32, sr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            float s0 = __uint_as_float(sr[2 * e]);
+                            float s1 = __uint_as_float(sr[2 * e + 1]);
+                            if (MASK) {
+                                // a masked score becomes -inf: it drops out of the max and
+                                // 2^(-inf) = 0 (the scale is > 0, so no -inf * 0)
+                                s0 = cc * 32 + 2 * e < lim ? s0 : -INFINITY;
+                                s1 = cc * 32 + 2 * e + 1 < lim ? s1 : -INFINITY;
+                            }
+                            mx[e & 3] = fmax3(mx[e & 3], s0, s1);
+                            const float2 t = __ffma2_rn(make_float2(s0, s1), scale2, negm2);
+                            const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+                            ls[e & 3] = __fadd2_rn(ls[e & 3], pp);
+                            pk[cc * 16 + e] = pack_bf16x2(pp.x, pp.y);
+                        }
+                    }
+                    mt_raw = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
+                    const float2 l2 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
+                    return l2.x + l2.y;
+                };
+                auto do_exp = [&](float m_ref, float &mt) {
+                    return need_mask ? exp_block(Masked{}, m_ref, mt) : exp_block(Plain{}, m_ref, mt);
+                };
+                auto to_log2 = [&](float raw_max) {
+                    return raw_max == -INFINITY ? -INFINITY : raw_max * scale_log2;
+                };
+                float ls_blk, mt_raw;
+                if (j == 0) {
+                    m_used = to_log2(need_mask ? block_max(Masked{}) : block_max(Plain{}));
+                    ls_blk = do_exp(m_used, mt_raw);
+                } else {
+                    // Speculate that the reference max still holds.
+                    ls_blk = do_exp(m_used, mt_raw);
+                    const float m_new = fmaxf(m_used, to_log2(mt_raw));
+                    const bool grow = m_new > m_used + kRescaleThreshold;   // true for m_used = -inf
+                    if (__any_sync(0xffffffffu, grow)) {
+                        // O_x must hold the previous block's product before it is rescaled.
+                        if (!mbar_wait(o_done(x), (g - 1) & 1u, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const float f = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t rr[32];
+                            tmem_ld32(o_addr + c * 32, rr);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                rr[e] = __float_as_uint(__uint_as_float(rr[e]) * f);
+                            tmem_st32(o_addr + c * 32, rr);
+                        }
+                        tmem_wait_st();
+                        l *= f;
+                        m_used = m_new;
+                        ls_blk = do_exp(m_used, mt_raw);
+                    }
+                }
+                l += ls_blk;
+                tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+                tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(p_full(x));
+                ++g;
+            }
+            if (!ok)
+                break;
+
+            // Epilogue: wait for this tile's last O += P V, then O / l -> bf16 and lse.
+            if (!mbar_wait(o_done(x), (g - 1) & 1u, abort))
+                break;
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            if (row_valid)
+                p.lse[tok * H + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -FLT_MAX;
+            if ((i + 1) * BQ <= lq) {
+                // Whole tile inside the sequence: stage each 64-column block in the
+                // 128-byte swizzled layout and store it with one TMA instruction.
+                for (int db = 0; db < DB && ok; ++db) {
+                    uint32_t rr[64];
+                    tmem_ld32(o_addr + db * 64, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
+                    tmem_ld32(o_addr + db * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
+                    tmem_wait_ld();
+                    // the previous block's store must have left the stage
+                    if (!mbar_wait(stage_free(x), (stage_uses & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t row = stage + r * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        st_shared_v4(row + ((c ^ (r & 7)) << 4),
+                                     pack_bf16x2(__uint_as_float(rr[8 * c + 0]) * inv_l,
+                                                 __uint_as_float(rr[8 * c + 1]) * inv_l),
+                                     pack_bf16x2(__uint_as_float(rr[8 * c + 2]) * inv_l,
+                                                 __uint_as_float(rr[8 * c + 3]) * inv_l),
+                                     pack_bf16x2(__uint_as_float(rr[8 * c + 4]) * inv_l,
+                                                 __uint_as_float(rr[8 * c + 5]) * inv_l),
+                                     pack_bf16x2(__uint_as_float(rr[8 * c + 6]) * inv_l,
+                                                 __uint_as_float(rr[8 * c + 7]) * inv_l));
+                    fence_proxy_async_smem();
+                    mbar_arrive(stage_ready(x));
+                    if (leader) {
+                        if (!mbar_wait(stage_ready(x), stage_uses & 1u, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tma_store_3d(&p.tm_o, stage, db * 64, h, q0 + i * BQ);
+                        bulk_commit_group();
+                        bulk_wait_group_read0();          // the stage may be rewritten after this
+                        mbar_arrive(stage_free(x));
+                    }
+                    ++stage_uses;
+                }
+                if (!ok)
+                    break;
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(out + (tok * H + h) * D);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(o_addr + c * 32, rr);
+                    tmem_wait_ld();
+                    if (row_valid) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(rr[8 * e + 0]) * inv_l,
+                                              __uint_as_float(rr[8 * e + 1]) * inv_l);
+                            v.y = pack_bf16x2(__uint_as_float(rr[8 * e + 2]) * inv_l,
+                                              __uint_as_float(rr[8 * e + 3]) * inv_l);
+                            v.z = pack_bf16x2(__uint_as_float(rr[8 * e + 4]) * inv_l,
+                                              __uint_as_float(rr[8 * e + 5]) * inv_l);
+                            v.w = pack_bf16x2(__uint_as_float(rr[8 * e + 6]) * inv_l,
+                                              __uint_as_float(rr[8 * e + 7]) * inv_l);
+                            dst[c * 4 + e] = v;
+                        }
+                    }
+                }
+            }
+        }
+        // Every bulk store this warpgroup issued must complete before the CTA exits.
+        if (leader)
+            bulk_wait_group0();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort && threadIdx.x == 0)
+        atomicCAS(p.status, 0, VFA_ERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+cudaError_t launch_pair_d(const PrefillArgs &a, int grid, cudaStream_t stream)
+{
+    static int attr_done[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 64 && !attr_done[dev]) {
+        e = cudaFuncSetAttribute(prefill_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(PairCfg<D>::SMEM));
+        if (e != cudaSuccess)
+            return e;
+        attr_done[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = PairCfg<D>::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D>, a);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_pair(int head_dim, const PrefillArgs &a, int grid, cudaStream_t stream)
+{
+    switch (head_dim) {
+    case 64: return launch_pair_d<64>(a, grid, stream);
+    case 128: return launch_pair_d<128>(a, grid, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace vfa

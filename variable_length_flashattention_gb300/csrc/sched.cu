@@ -12,9 +12,18 @@
 //   * groups ordered by largest item cost, then total cost (descending),
 //     then (b, h); inside a group by cost descending, then i.  The prefill
 //     CTAs take items in this order from an atomic counter, so the longest
-//     work starts first and the tail is short.
+//     work starts first and the tail is short;
+//   * in pair mode two consecutive tiles of a group make one item, so one
+//     CTA runs both q tiles against each key/value tile it loads.
 // It also validates cu_seqlens and max_seqlen_q and reports through the
 // status word instead of trapping.
+//
+// With block_q = r * block_k (r a whole number) and block_k a power of two,
+// a causal tile costs min(C, (i + 1) * r) where C = ceil(min(Lk, Lq) /
+// block_k): costs rise by r per tile until they reach C and stay there.  So
+// a sequence's largest and total cost and each tile's rank in its group have
+// closed forms, and the kernel needs one pass over the sequences and one over
+// the tiles, in 32-bit arithmetic, with no per-tile searches.
 #include "internal.h"
 
 namespace vfa {
@@ -23,42 +32,15 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kSmemSeqs = 2048;    // per-sequence records kept in shared memory when they fit
-constexpr int kSeqRecords = 6;     // tile start, tile count, largest cost, total/first, rank, order
-constexpr size_t kSchedSmem = kSeqRecords * kSmemSeqs * sizeof(int);
-
-__host__ __device__ inline int ceil_div_i(long long a, long long b)
-{
-    return static_cast<int>((a + b - 1) / b);
-}
+// Per-sequence records in ints: total cost (64-bit, two ints), tile start,
+// tile count, cost cap C, first capped tile i0, largest cost, rank in group
+// order, rank -> sequence, first item / H.
+constexpr int kSeqInts = 10;
+constexpr size_t kSchedSmem = kSeqInts * kSmemSeqs * sizeof(int);
 
 __host__ __device__ inline int max_tiles(int batch, int total_q, int block_q)
 {
     return total_q / block_q + batch;
-}
-
-// Key tiles that q tile i of a (lq, lk) sequence visits; non-decreasing in i.
-__device__ __forceinline__ int tile_cost(int lq, int lk, int i, int bq, int bk, int causal)
-{
-    if (!causal)
-        return ceil_div_i(lk, bk);
-    const long long last_row_plus_one = min(static_cast<long long>(lq), static_cast<long long>(i + 1) * bq);
-    return ceil_div_i(min(static_cast<long long>(lk), last_row_plus_one), bk);
-}
-
-// First tile index in [0, nt) whose cost is > c (ge = false) or >= c (ge = true).
-__device__ __forceinline__ int first_tile_above(int lq, int lk, int nt, int c, bool ge, int bq,
-                                                int bk, int causal)
-{
-    int lo = 0, hi = nt;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        const int cm = tile_cost(lq, lk, mid, bq, bk, causal);
-        if (ge ? (cm >= c) : (cm > c))
-            hi = mid;
-        else
-            lo = mid + 1;
-    }
-    return lo;
 }
 
 // Exclusive prefix sum of one value per thread over the 1024-thread block.
@@ -98,67 +80,78 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const SchedArgs a)
     // grid's completion before it reads anything written here.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    extern __shared__ int sm[];
+    extern __shared__ __align__(16) int sm[];
     __shared__ long long warp_sums[32];
-    __shared__ int s_bad;
-    const int tid = threadIdx.x;
-    const int B = a.batch, H = a.num_heads, bq = a.block_q, bk = a.block_k;
+    __shared__ int s_bad, s_nseq;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = a.batch, H = a.num_heads;
+    const unsigned bq = static_cast<unsigned>(a.block_q), bk = static_cast<unsigned>(a.block_k);
+    const unsigned r = bq / bk;                          // block_q = r * block_k
+    const int lbk = __ffs(static_cast<int>(bk)) - 1;    // block_k = 2^lbk
+    const bool causal = a.causal != 0;
 
-    if (tid == 0)
-        s_bad = 0;
-    __syncthreads();
-    if (tid == 0) {
-        if (a.cu_q[0] != 0 || a.cu_k[0] != 0 || a.cu_q[B] != a.total_q || a.cu_k[B] != a.total_k)
-            s_bad = 1;
-    }
-    for (int b = tid; b < B; b += kThreads) {
-        const long long lq = static_cast<long long>(a.cu_q[b + 1]) - a.cu_q[b];
-        const long long lk = static_cast<long long>(a.cu_k[b + 1]) - a.cu_k[b];
-        if (lq < 0 || lk < 0 || lq > a.max_seqlen_q)
-            s_bad = 1;
-    }
-    __syncthreads();
-    if (s_bad) {
-        if (tid == 0) {
-            *a.n_items = 0;
-            *a.status = VFA_ERR_BAD_SEQLENS;
-        }
-        return;
-    }
-
-    const int tiles_cap = max_tiles(B, a.total_q, bq);
-    const long long need = static_cast<long long>(kSeqRecords) * (B + 1);
-    if (static_cast<long long>(tiles_cap) * H > a.item_capacity || need > a.scratch_ints) {
+    const int tiles_cap = max_tiles(B, a.total_q, a.block_q);
+    const bool in_smem = B + 1 <= kSmemSeqs;
+    if (static_cast<long long>(tiles_cap) * H > a.item_capacity ||
+        (!in_smem && static_cast<long long>(kSeqInts) * (B + 1) > a.scratch_ints)) {
         if (tid == 0) {
             *a.n_items = 0;
             *a.status = VFA_ERR_WORKSPACE;
         }
         return;
     }
-    // Per-sequence records: tile start, tile count, largest cost, total cost
-    // (later: first item / H), rank in group order, and the rank -> sequence order.
-    const bool seqs_in_smem = B + 1 <= kSmemSeqs;
-    int *g = a.scratch;
-    int *tile_start = seqs_in_smem ? sm : g;
-    int *seq_nt = seqs_in_smem ? sm + kSmemSeqs : g + (B + 1);
-    int *seq_maxc = seqs_in_smem ? sm + 2 * kSmemSeqs : g + 2 * (B + 1);
-    int *seq_total = seqs_in_smem ? sm + 3 * kSmemSeqs : g + 3 * (B + 1);
-    int *seq_rank = seqs_in_smem ? sm + 4 * kSmemSeqs : g + 4 * (B + 1);
-    int *seq_first = seq_total;      // reused once the ranks are known (as item offsets / H)
+    const int n = in_smem ? kSmemSeqs : B + 1;
+    int *rec = in_smem ? sm : a.scratch;
+    long long *seq_total = reinterpret_cast<long long *>(rec);
+    int *tile_start = rec + 2 * n;
+    int *seq_nt = rec + 3 * n;
+    int *seq_cap = rec + 4 * n;
+    int *seq_i0 = rec + 5 * n;
+    int *seq_maxc = rec + 6 * n;
+    int *seq_rank = rec + 7 * n;
+    int *ord = rec + 8 * n;
+    int *seq_first = rec + 9 * n;
 
-    // Tile counts, largest cost (the last tile's: costs never decrease in i),
-    // and the tile-start prefix sum.
+    if (tid == 0) {
+        s_bad = 0;
+        s_nseq = 0;
+    }
+    __syncthreads();
+    if (tid == 0 && (a.cu_q[0] != 0 || a.cu_k[0] != 0 || a.cu_q[B] != a.total_q ||
+                     a.cu_k[B] != a.total_k))
+        s_bad = 1;
+    // One pass over the sequences: validation, tile count, cost cap, largest
+    // and total cost, and the tile-start prefix sum.
     long long carry = 0;
     for (int base = 0; base < B; base += kThreads) {
         const int b = base + tid;
         int nt = 0;
         if (b < B) {
-            const int lq = a.cu_q[b + 1] - a.cu_q[b];
-            const int lk = a.cu_k[b + 1] - a.cu_k[b];
-            nt = ceil_div_i(lq, bq);
-            seq_nt[b] = nt;
-            seq_maxc[b] = nt > 0 ? tile_cost(lq, lk, nt - 1, bq, bk, a.causal) : -1;
-            seq_total[b] = 0;
+            const long long lq = static_cast<long long>(a.cu_q[b + 1]) - a.cu_q[b];
+            const long long lk = static_cast<long long>(a.cu_k[b + 1]) - a.cu_k[b];
+            if (lq < 0 || lk < 0 || lq > a.max_seqlen_q) {
+                s_bad = 1;
+            } else {
+                const unsigned uq = static_cast<unsigned>(lq), uk = static_cast<unsigned>(lk);
+                nt = static_cast<int>((uq + bq - 1) / bq);
+                const unsigned m = causal ? min(uq, uk) : uk;
+                const int cap = static_cast<int>((m + bk - 1) >> lbk);
+                int i0 = 0;
+                long long maxc = cap;
+                long long total = static_cast<long long>(nt) * cap;
+                if (causal) {
+                    // first tile whose cost reaches the cap: (i0 + 1) * r >= cap
+                    i0 = min(nt, max(0, static_cast<int>((cap + r - 1) / r) - 1));
+                    maxc = min(static_cast<long long>(cap), static_cast<long long>(nt) * r);
+                    const long long u = min(static_cast<long long>(nt), static_cast<long long>(cap / r));
+                    total = static_cast<long long>(r) * u * (u + 1) / 2 + (nt - u) * cap;
+                }
+                seq_nt[b] = nt;
+                seq_cap[b] = cap;
+                seq_i0[b] = i0;
+                seq_maxc[b] = nt > 0 ? static_cast<int>(maxc) : -1;
+                seq_total[b] = total;
+            }
         }
         long long total;
         const long long ex = block_exclusive_scan(nt, warp_sums, &total);
@@ -170,8 +163,62 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const SchedArgs a)
     if (tid == 0)
         tile_start[B] = ntiles;
     __syncthreads();
+    if (s_bad) {
+        if (tid == 0) {
+            *a.n_items = 0;
+            *a.status = VFA_ERR_BAD_SEQLENS;
+        }
+        return;
+    }
 
-    // Total cost per sequence.
+    // Rank of each non-empty sequence in (largest cost desc, total desc, b
+    // asc), one warp per sequence.
+    for (int b = warp; b < B; b += kThreads / 32) {
+        if (seq_nt[b] == 0) {
+            if (lane == 0)
+                seq_rank[b] = -1;
+            continue;
+        }
+        const int mb = seq_maxc[b];
+        const long long tb = seq_total[b];
+        int cnt = 0;
+        for (int o = lane; o < B; o += 32) {
+            const int mo = seq_maxc[o];            // -1 for empty sequences: never ahead
+            const long long to = seq_total[o];
+            cnt += (mo > mb) || (mo == mb && (to > tb || (to == tb && o < b)));
+        }
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
+        if (lane == 0) {
+            seq_rank[b] = cnt;
+            ord[cnt] = b;
+            atomicAdd(&s_nseq, 1);
+        }
+    }
+    __syncthreads();
+    const int nseq = s_nseq;
+
+    // Items per head of each sequence: its tiles, or its tile pairs; the
+    // groups of the sequence at rank k start after those of ranks < k.
+    auto units = [&](int nt) { return a.pair ? (nt + 1) / 2 : nt; };
+    carry = 0;
+    for (int base = 0; base < nseq; base += kThreads) {
+        const int k = base + tid;
+        const int b = k < nseq ? ord[k] : 0;
+        const int u = k < nseq ? units(seq_nt[b]) : 0;
+        long long total;
+        const long long ex = block_exclusive_scan(u, warp_sums, &total);
+        if (k < nseq)
+            seq_first[b] = static_cast<int>(carry + ex);     // in units of H items
+        carry += total;
+    }
+    const long long nitems = carry * H;
+    __syncthreads();
+
+    // Items, one thread per tile writing all its heads.  Sequence b's groups
+    // start at H * seq_first[b], head h's group at + h * units(nt); the
+    // tile's rank in its group is i - i0 for capped tiles (equal cost, i
+    // ascending) and nt - 1 - i below the cap (cost falls as i falls), and
+    // it lands in item rank (single) or rank / 2, slot rank % 2 (pairs).
     for (int t = tid; t < ntiles; t += kThreads) {
         int lo = 0, hi = B - 1;                     // largest b with tile_start[b] <= t
         while (lo < hi) {
@@ -181,84 +228,25 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const SchedArgs a)
             else
                 hi = mid - 1;
         }
-        const int lq = a.cu_q[lo + 1] - a.cu_q[lo];
-        const int lk = a.cu_k[lo + 1] - a.cu_k[lo];
-        atomicAdd(&seq_total[lo], tile_cost(lq, lk, t - tile_start[lo], bq, bk, a.causal));
-    }
-    __syncthreads();
-
-    // Rank of each non-empty sequence in (largest cost desc, total desc, b asc).
-    for (int b = tid; b < B; b += kThreads) {
-        if (seq_nt[b] == 0) {
-            seq_rank[b] = -1;
-            continue;
-        }
-        const int mb = seq_maxc[b], tb = seq_total[b];
-        int r = 0;
-        for (int o = 0; o < B; ++o) {
-            if (seq_nt[o] == 0)
-                continue;
-            const int mo = seq_maxc[o], to = seq_total[o];
-            r += (mo > mb) || (mo == mb && (to > tb || (to == tb && o < b)));
-        }
-        seq_rank[b] = r;
-    }
-    __syncthreads();
-
-    // Items before each sequence in rank order: a scan over ranks.
-    int *ord = seqs_in_smem ? sm + 5 * kSmemSeqs : g + 5 * (B + 1);
-    for (int b = tid; b < B; b += kThreads)
-        if (seq_rank[b] >= 0)
-            ord[seq_rank[b]] = b;
-    __syncthreads();
-    int nseq = 0;
-    {
-        // number of non-empty sequences
-        long long total;
-        int cnt = 0;
-        for (int b = tid; b < B; b += kThreads)
-            cnt += seq_nt[b] > 0;
-        block_exclusive_scan(cnt, warp_sums, &total);
-        nseq = static_cast<int>(total);
-    }
-    carry = 0;
-    for (int base = 0; base < nseq; base += kThreads) {
-        const int r = base + tid;
-        const int b = r < nseq ? ord[r] : 0;
-        const int n = r < nseq ? seq_nt[b] : 0;
-        long long total;
-        const long long ex = block_exclusive_scan(n, warp_sums, &total);
-        if (r < nseq)
-            seq_first[b] = static_cast<int>(carry + ex);     // in units of H items
-        carry += total;
-    }
-    __syncthreads();
-
-    // Items: sequence b's groups start at H * seq_first[b]; head h's group at
-    // + h * nt; the tile's place in its group is its rank by (cost desc, i asc).
-    const long long nitems = static_cast<long long>(ntiles) * H;
-    for (long long e = tid; e < nitems; e += kThreads) {
-        const int t = static_cast<int>(e / H);
-        const int h = static_cast<int>(e % H);
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (tile_start[mid] <= t)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
         const int b = lo;
         const int i = t - tile_start[b];
-        const int nt = seq_nt[b];
-        const int lq = a.cu_q[b + 1] - a.cu_q[b];
-        const int lk = a.cu_k[b + 1] - a.cu_k[b];
-        const int c = tile_cost(lq, lk, i, bq, bk, a.causal);
-        const int above = nt - first_tile_above(lq, lk, nt, c, false, bq, bk, a.causal);
-        const int before_equal = i - first_tile_above(lq, lk, nt, c, true, bq, bk, a.causal);
-        const long long pos = static_cast<long long>(seq_first[b]) * H +
-                              static_cast<long long>(h) * nt + above + before_equal;
-        a.items[pos] = make_int4(b, i, h, c);
+        const int nt = seq_nt[b], cap = seq_cap[b], i0 = seq_i0[b];
+        const int c = causal ? min(cap, (i + 1) * static_cast<int>(r)) : cap;
+        const int rank = i >= i0 ? i - i0 : nt - 1 - i;
+        const int slot = a.pair ? (rank & 1) : 0;
+        const int unit = a.pair ? rank >> 1 : rank;
+        const int per_head = units(nt);
+        const bool alone = !a.pair || rank == nt - 1;
+        long long pos = static_cast<long long>(seq_first[b]) * H + unit;
+        for (int h = 0; h < H; ++h, pos += per_head) {
+            if (slot == 0) {
+                a.items[2 * pos] = make_int4(b, i, h, c);
+                if (alone)
+                    a.items[2 * pos + 1] = make_int4(-1, 0, 0, 0);
+            } else {
+                a.items[2 * pos + 1] = make_int4(i, c, 0, 0);
+            }
+        }
     }
     if (tid == 0) {
         *a.n_items = static_cast<int>(nitems);
@@ -276,7 +264,7 @@ int schedule_scratch_ints(int batch, int total_q, int total_k, int block_q, int 
     (void)total_k;
     (void)block_q;
     (void)block_k;
-    return kSeqRecords * (batch + 1);
+    return kSeqInts * (batch + 1);
 }
 
 cudaError_t launch_schedule(const SchedArgs &a, cudaStream_t stream)
@@ -303,7 +291,7 @@ WorkspaceLayout workspace_layout(int batch, int total_q, int total_k, int num_he
     WorkspaceLayout w;
     w.items_offset = 256;
     w.item_capacity = max_tiles(batch, total_q, block_q) * num_heads;
-    w.scratch_offset = w.items_offset + static_cast<size_t>(w.item_capacity) * sizeof(int4);
+    w.scratch_offset = w.items_offset + static_cast<size_t>(w.item_capacity) * 2 * sizeof(int4);
     w.scratch_offset = (w.scratch_offset + 255) & ~static_cast<size_t>(255);
     w.scratch_ints = schedule_scratch_ints(batch, total_q, total_k, block_q, block_k);
     w.total_bytes = w.scratch_offset + static_cast<size_t>(w.scratch_ints) * sizeof(int);

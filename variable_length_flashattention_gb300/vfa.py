@@ -40,10 +40,10 @@ SIGNATURES = [
     ("vfa_last_error", ctypes.c_char_p, []),
     ("vfa_version", ctypes.c_char_p, []),
     ("vfa_varlen_fwd_workspace_bytes", _S, [_I, _I, _I, _I, _I]),
-    ("vfa_varlen_fwd_tile_shape", _I, [_I, _P, _P]),
+    ("vfa_varlen_fwd_tile_shape", _I, [_I, _P, _P, _P]),
     ("vfa_varlen_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _S, _P]),
     ("vfa_varlen_fwd_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
-    ("vfa_varlen_schedule", _I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _S, _P]),
+    ("vfa_varlen_schedule", _I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _S, _P]),
     ("vfa_paged_decode_init", _I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     ("vfa_paged_decode_step", _I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     ("vfa_paged_decode_finalize", _I, [_P, _P, _I, _I, _I, _P, _P]),
@@ -110,10 +110,12 @@ def version() -> str:
 
 # ----------------------------------------------------------------- varlen forward
 
-def tile_shape(head_dim: int) -> Tuple[int, int]:
-    bq, bk = ctypes.c_int(), ctypes.c_int()
-    _check(lib().vfa_varlen_fwd_tile_shape(head_dim, ctypes.byref(bq), ctypes.byref(bk)))
-    return bq.value, bk.value
+def tile_shape(head_dim: int) -> Tuple[int, int, bool]:
+    """(q tile rows, key tile rows, two q tiles per work item) for head_dim."""
+    bq, bk, pr = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().vfa_varlen_fwd_tile_shape(head_dim, ctypes.byref(bq), ctypes.byref(bk),
+                                           ctypes.byref(pr)))
+    return bq.value, bk.value, bool(pr.value)
 
 
 def workspace_bytes(batch: int, total_q: int, total_k: int, num_heads: int, head_dim: int) -> int:
@@ -190,12 +192,12 @@ def varlen_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
 
 def schedule(cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, total_q: int, total_k: int,
              max_seqlen_q: int, num_heads: int, block_q: int, block_k: int, causal: bool,
-             stream=None):
-    """Runs the device tile scheduler alone; returns (items int32 [n, 4] on device, status)."""
+             pair: bool = False, stream=None):
+    """Runs the device tile scheduler alone; returns (items int32 [n, 8] on device, status)."""
     batch = cu_seqlens_q.numel() - 1
     cap = num_heads * (total_q // block_q + batch)
     dev = cu_seqlens_q.device
-    items = torch.full((max(cap, 1), 4), -1, dtype=torch.int32, device=dev)
+    items = torch.full((max(cap, 1), 8), -7, dtype=torch.int32, device=dev)
     n_items = torch.zeros(1, dtype=torch.int32, device=dev)
     status = torch.full((1,), -1, dtype=torch.int32, device=dev)
     # scratch of vfa_varlen_fwd_workspace_bytes() bytes covers any tile shape
@@ -203,8 +205,8 @@ def schedule(cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, total_q: in
     scratch = torch.empty((nbytes + 3) // 4, dtype=torch.int32, device=dev)
     st = lib().vfa_varlen_schedule(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), total_q, total_k,
                                    int(max_seqlen_q), batch, num_heads, block_q, block_k,
-                                   int(bool(causal)), _ptr(items), cap, _ptr(n_items),
-                                   _ptr(status), _ptr(scratch), scratch.numel() * 4,
+                                   int(bool(causal)), int(bool(pair)), _ptr(items), cap,
+                                   _ptr(n_items), _ptr(status), _ptr(scratch), scratch.numel() * 4,
                                    _stream(stream))
     _check(st)
     n = int(n_items.item())
