@@ -9,7 +9,8 @@
 //
 //   * a work item holds two q tiles (a, b) of the same (sequence, head); each
 //     K/V tile is loaded once by TMA and used by both;
-//   * warp 0 loads Q and K, warp 10 loads V, each with its own ring;
+//   * warp 0 loads Q and K, warp 2 loads V, each with its own ring; that
+//     warpgroup hands registers to the softmax warpgroups (setmaxnreg);
 //   * warp 1 issues, per key tile j:  S_a = Q_a K_j^T,  O_b += P_b V_{j-1},
 //     S_b = Q_b K_j^T,  O_a += P_a V_j  -- while one softmax warpgroup works
 //     on its scores the tensor core runs the other tile's products.  P_x
@@ -17,12 +18,17 @@
 //     O_x += P_x V that reads it: tcgen05.mma instructions of one thread run
 //     in issue order, so the product has read P_x before S_x is rewritten
 //     (and waiting for its completion instead would idle the tensor core);
-//   * warps 2-5 own tile a's 128 rows, warps 6-9 tile b's, one row per
-//     thread (TMEM lane = row).  After a tile's first key block, scores are
-//     exponentiated against the current reference max in the same pass that
-//     finds the block's max; only if the max grew by more than 2^8 is the
-//     block redone at the new max (and O, l rescaled); P stays in registers
-//     until that is decided, so S is still intact for a redo;
+//   * warps 4-7 own tile a's 128 rows, warps 8-11 tile b's, one row per
+//     thread (TMEM lane = row).  A key tile's scores are taken in two halves
+//     of 64 columns held in registers; p is computed against the reference
+//     max in the same pass that finds the half's max, and only if the max
+//     grew by more than 2^8 does the reference move (O, l rescaled) and the
+//     half get redone (its scores reloaded from TMEM, still intact).  Each half of P is published on
+//     its own and O_x += P_x V runs per half, so the tensor core starts on
+//     the first 64 keys while the second half is still being exponentiated;
+//   * in a masked tile (causal diagonal, ragged key tail) a 32-column chunk
+//     that is valid for all 32 rows of a warp skips the mask, and one that
+//     is masked for all of them skips its TMEM load and its exponentials;
 //   * full output tiles leave through a swizzled shared-memory stage and a
 //     TMA tensor store; a sequence's last, partial tile is stored row by row;
 //   * TMEM: O_a, O_b (D columns each), S/P_a, S/P_b (128 columns each).
@@ -50,7 +56,7 @@ struct PairCfg {
     static constexpr uint32_t STAGE_BYTES = BQ * 128;     // one 64-column block of an O tile
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL = 2 * D;              // S_x at S_COL + x * BK; O_x at x * D
-    static constexpr int NUM_BARS = 4 + 4 * NS + 6 + 4 + 1 + 4;
+    static constexpr int NUM_BARS = 4 + 4 * NS + 19;
     static constexpr size_t SMEM = 1024 + 2 * Q_BYTES + 2 * NS * KV_BYTES + 2 * STAGE_BYTES +
                                    NUM_BARS * 8 + 64;
     static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BQ, BK, false, false);
@@ -59,10 +65,97 @@ struct PairCfg {
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-constexpr int kThreads = 352;       // 11 warps: Q/K loads, MMA, 2 x 4 softmax, V loads
-constexpr int kVWarp = 10;
+// Three warpgroups: warps 0-3 load Q/K (0), issue MMAs (1), load V (2) and
+// idle (3); warps 4-7 run tile a's softmax, warps 8-11 tile b's.  The first
+// group gives registers up to the two softmax groups (setmaxnreg): 384
+// threads launch with 168 registers each, 128 * 120 + 256 * 192 = 384 * 168.
+constexpr int kThreads = 384;
+constexpr int kVWarp = 2;
+constexpr int kFirstMathWarp = 4;
+constexpr int kLoadRegs = 120;
+constexpr int kMathRegs = 192;
 constexpr int kItemConsumers = 10;  // MMA + V loader + one arrival per softmax warp
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale when the max grows by > 2^8
+
+// Masks one 32-column chunk of scores (columns cb..cb+31 of the key tile):
+// scores at or past `lim` valid columns become -inf, so they drop out of the
+// max and 2^(-inf) = 0 (the scale is > 0, so no -inf * 0).  A chunk below
+// the warp's smallest lim needs no mask.
+__device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int cb, int lim, int lim_lo)
+{
+    if (cb + 32 <= lim_lo)
+        return;
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+        sr[e] = cb + e < lim ? sr[e] : __float_as_uint(-INFINITY);
+}
+
+// Folds the (masked) scores of the 32-column chunk at TMEM address taddr into
+// the running maxima mx.  An all-masked chunk is skipped.
+template <bool MASK>
+__device__ __forceinline__ void chunk_max(uint32_t taddr, int cb, int lim, int lim_lo, bool empty,
+                                          float (&mx)[4])
+{
+    if (empty)
+        return;
+    uint32_t sr[32];
+    tmem_ld32(taddr, sr);
+    tmem_wait_ld_r(sr);
+    if (MASK)
+        mask_chunk(sr, cb, lim, lim_lo);
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        mx[e & 3] = fmax3(mx[e & 3], __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
+}
+
+// p = 2^(s * scale_log2 - m) for the 32-column chunk at TMEM address taddr,
+// packed to bf16 pairs in pk[pb .. pb + 15], with the row sums accumulated in
+// ls (fp32) and, if WITH_MAX, the scores folded into mx.  An all-masked chunk
+// gives zeros without loads or exponentials.
+template <bool MASK, bool WITH_MAX>
+__device__ __forceinline__ void chunk_exp(uint32_t taddr, int cb, int lim, int lim_lo, bool empty,
+                                          float2 scale2, float2 negm2, float2 (&ls)[4],
+                                          float (&mx)[4], uint32_t (&pk)[32], int pb)
+{
+    if (empty) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            pk[pb + e] = 0u;
+        return;
+    }
+    uint32_t sr[32];
+    tmem_ld32(taddr, sr);
+    tmem_wait_ld_r(sr);
+    if (MASK)
+        mask_chunk(sr, cb, lim, lim_lo);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const float s0 = __uint_as_float(sr[2 * e]), s1 = __uint_as_float(sr[2 * e + 1]);
+        if (WITH_MAX)
+            mx[e & 3] = fmax3(mx[e & 3], s0, s1);
+        const float2 t = __ffma2_rn(make_float2(s0, s1), scale2, negm2);
+        const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+        ls[e & 3] = __fadd2_rn(ls[e & 3], pp);
+        pk[pb + e] = pack_bf16x2(pp.x, pp.y);
+    }
+}
+
+// O rows *= f for this warp's 32 lanes, 16 columns at a time (rare path).
+template <int D>
+__device__ __forceinline__ void rescale_rows(uint32_t o_addr, float f)
+{
+#pragma unroll 1
+    for (int c = 0; c < D / 16; ++c) {
+        uint32_t rr[16];
+        tmem_ld16(o_addr + c * 16, rr);
+        tmem_wait_ld_r16(rr);
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            rr[e] = __float_as_uint(__uint_as_float(rr[e]) * f);
+        tmem_st16(o_addr + c * 16, rr);
+    }
+    tmem_wait_st();
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -92,14 +185,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto k_empty = [&](int i) { return bars + 8u * (4 + NS + i); };
     auto v_full = [&](int i) { return bars + 8u * (4 + 2 * NS + i); };
     auto v_empty = [&](int i) { return bars + 8u * (4 + 3 * NS + i); };
-    auto s_full = [&](int x) { return bars + 8u * (4 + 4 * NS + x); };
-    auto o_done = [&](int x) { return bars + 8u * (4 + 4 * NS + 2 + x); };   // an O_x += P_x V finished
-    auto p_full = [&](int x) { return bars + 8u * (4 + 4 * NS + 4 + x); };
-    auto item_full = [&](int x) { return bars + 8u * (4 + 4 * NS + 6 + x); };
-    auto item_empty = [&](int x) { return bars + 8u * (4 + 4 * NS + 8 + x); };
-    const uint32_t drain_bar = bars + 8u * (4 + 4 * NS + 10);
-    auto stage_ready = [&](int x) { return bars + 8u * (4 + 4 * NS + 11 + x); };
-    auto stage_free = [&](int x) { return bars + 8u * (4 + 4 * NS + 13 + x); };
+    constexpr uint32_t E = 4 + 4 * NS;
+    auto s_full = [&](int x) { return bars + 8u * (E + x); };
+    // O_x += P_x V runs in two halves of 64 keys; o_h1 / o_h2 complete once
+    // per key tile each, when the half's products are in O_x.
+    auto o_h1 = [&](int x) { return bars + 8u * (E + 2 + x); };
+    auto o_h2 = [&](int x) { return bars + 8u * (E + 4 + x); };
+    auto p_half = [&](int x, int hh) { return bars + 8u * (E + 6 + 2 * x + hh); };   // P_x half ready
+    auto item_full = [&](int x) { return bars + 8u * (E + 10 + x); };
+    auto item_empty = [&](int x) { return bars + 8u * (E + 12 + x); };
+    const uint32_t drain_bar = bars + 8u * (E + 14);
+    auto stage_ready = [&](int x) { return bars + 8u * (E + 15 + x); };
+    auto stage_free = [&](int x) { return bars + 8u * (E + 17 + x); };
     volatile int *abort = &s_abort;
 
     if (threadIdx.x == 0) {
@@ -108,8 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(q_full(x), 1);
             mbar_init(q_empty(x), 1);
             mbar_init(s_full(x), 1);
-            mbar_init(o_done(x), 1);
-            mbar_init(p_full(x), 128);
+            mbar_init(o_h1(x), 1);
+            mbar_init(o_h2(x), 1);
+            mbar_init(p_half(x, 0), 128);
+            mbar_init(p_half(x, 1), 128);
             mbar_init(item_full(x), 1);
             mbar_init(item_empty(x), kItemConsumers);
             mbar_init(stage_ready(x), 128);
@@ -158,6 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_drain(bar, (k - 1) & 1u);
     };
 
+    if (warp < kFirstMathWarp) {
+    // Each role's code sits inside its setmaxnreg branch, so the register
+    // allocator gives it that branch's budget.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLoadRegs));
     if (warp == 0) {
         // ------------------------------------------------------------ items, Q and K
         if (lane == 0) {
@@ -259,7 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // All 32 lanes run this loop on warp-uniform values; one elected lane
+        // issues each MMA and commit.
+        {
             const uint64_t q_desc0 = sdesc_sw128(sQ, 16, 1024);
             const uint64_t k_desc0 = sdesc_sw128(sK, 16, 1024);
             const uint64_t v_desc0 = sdesc_sw128(sV, BK * 128, 1024);
@@ -271,16 +376,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t qd = q_desc0 + x * (C::Q_BYTES >> 4);
                 const uint64_t kd = k_desc0 + st * (C::KV_BYTES >> 4);
                 const uint32_t s_tm = tmem + C::S_COL + x * BK;
-                mma_ss_c<0>(s_tm, qd, kd, C::IDESC_QK);
+                mma_ss_w<0>(s_tm, qd, kd, C::IDESC_QK);
 #pragma unroll
                 for (int kk = 1; kk < D / 16; ++kk)
-                    mma_ss_c<1>(s_tm, qd + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4),
+                    mma_ss_w<1>(s_tm, qd + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4),
                                 kd + (((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4), C::IDESC_QK);
-                mma_commit(s_full(x));
+                mma_commit_w(s_full(x));
             };
-            // O_x += P_x V for q slot x (its tile number gt[x]), V in ring slot st.
+            // O_x += P_x V for q slot x (its tile number gt[x]), V in ring slot st,
+            // one half of the keys as soon as the softmax has published that
+            // half of P_x.
             auto issue_pv = [&](int x, int st, uint32_t v_fill, bool acc) -> bool {
-                if (!mbar_wait(p_full(x), gt[x] & 1u, abort) ||
+                if (!mbar_wait(p_half(x, 0), gt[x] & 1u, abort) ||
                     !mbar_wait(v_full(st), (v_fill / NS) & 1u, abort))
                     return false;
                 tc_fence_after();
@@ -288,20 +395,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t a_tm = tmem + C::S_COL + x * BK;
                 const uint32_t o_tm = tmem + x * D;
                 if (acc)
-                    mma_ts_c<1>(o_tm, a_tm, vd, C::IDESC_PV);
+                    mma_ts_w<1>(o_tm, a_tm, vd, C::IDESC_PV);
                 else
-                    mma_ts_c<0>(o_tm, a_tm, vd, C::IDESC_PV);
+                    mma_ts_w<0>(o_tm, a_tm, vd, C::IDESC_PV);
 #pragma unroll
-                for (int kk = 1; kk < BK / 16; ++kk)
-                    mma_ts_c<1>(o_tm, a_tm + kk * 8, vd + kk * (16 * 128 / 16), C::IDESC_PV);
-                mma_commit(o_done(x));
+                for (int kk = 1; kk < BK / 32; ++kk)
+                    mma_ts_w<1>(o_tm, a_tm + kk * 8, vd + kk * (16 * 128 / 16), C::IDESC_PV);
+                mma_commit_w(o_h1(x));
+                if (!mbar_wait(p_half(x, 1), gt[x] & 1u, abort))
+                    return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = BK / 32; kk < BK / 16; ++kk)
+                    mma_ts_w<1>(o_tm, a_tm + kk * 8, vd + kk * (16 * 128 / 16), C::IDESC_PV);
+                mma_commit_w(o_h2(x));
                 ++gt[x];
                 return true;
             };
             for (;; ++n) {
                 int4 it, itb, seq;
                 const bool more = next_item(n, it, itb, seq);
-                mbar_arrive(item_empty(n & 1));
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(item_empty(n & 1));
                 if (!more)
                     break;
                 const int nk_a = it.w;
@@ -323,27 +439,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     issue_qk(0, st);                              // S_a(j)
                     if (j == nk_a - 1)
-                        mma_commit(q_empty(0));
+                        mma_commit_w(q_empty(0));
                     if (j >= 1 && j - 1 < nk_b) {
                         // O_b += P_b(j-1) V(j-1); V(j-1) is then free
                         if (!issue_pv(1, st_prev, kv - 1, j - 1 > 0)) {
                             ok = false;
                             break;
                         }
-                        mma_commit(v_empty(st_prev));
+                        mma_commit_w(v_empty(st_prev));
                     }
                     if (j < nk_b) {
                         issue_qk(1, st);                          // S_b(j)
                         if (j == nk_b - 1)
-                            mma_commit(q_empty(1));
+                            mma_commit_w(q_empty(1));
                     }
-                    mma_commit(k_empty(st));
+                    mma_commit_w(k_empty(st));
                     if (!issue_pv(0, st, kv, j > 0)) {            // O_a += P_a(j) V(j)
                         ok = false;
                         break;
                     }
                     if (j >= nk_b)
-                        mma_commit(v_empty(st));                  // tile b does not use V(j)
+                        mma_commit_w(v_empty(st));                  // tile b does not use V(j)
                     ++kv;
                 }
                 if (!ok)
@@ -354,27 +470,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mma_commit(v_empty(st_last));
+                    mma_commit_w(v_empty(st_last));
                 }
                 ++qloads[0];
                 if (nk_b > 0)
                     ++qloads[1];
             }
             if (!ok || *abort) {
-                mma_commit(drain_bar);
+                mma_commit_w(drain_bar);
                 mbar_wait_drain(drain_bar, 0);
             }
         }
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kMathRegs));
         // ------------------------------------------------------------ softmax / epilogue
-        const int x = (warp - 2) >> 2;                // q slot: 0 = tile a (warps 2-5), 1 = tile b
+        const int x = (warp - kFirstMathWarp) >> 2;   // q slot: 0 = tile a (warps 4-7), 1 = tile b
         const int quarter = warp & 3;                 // TMEM lanes [32*quarter, +32)
         const int r = quarter * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t s_addr = tmem + lane_addr + C::S_COL + x * BK;
         const uint32_t o_addr = tmem + lane_addr + x * D;
         const uint32_t stage = sO + x * C::STAGE_BYTES;
-        const bool leader = (warp & 3) == 2 && lane == 0;   // first warp of the warpgroup
+        const bool leader = (warp & 3) == 0 && lane == 0;   // first warp of the warpgroup
         const float scale_log2 = p.scale_log2;
         const float2 scale2 = make_float2(scale_log2, scale_log2);
         const int H = p.num_heads;
@@ -414,10 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
 
-            float m_used = -INFINITY;
+            float m_used = -INFINITY;                 // reference max, log2 units
             float l = 0.f;
             bool ok = true;
-            for (int j = 0; j < nk; ++j) {
+            for (int j = 0; j < nk && ok; ++j) {
                 if (!mbar_wait(s_full(x), g & 1u, abort)) {
                     ok = false;
                     break;
@@ -426,128 +544,89 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int k_base = j * BK;
                 const bool need_mask = (k_base + BK > lk) || (p.causal && k_base + BK - 1 > i * BQ);
                 const int lim = need_mask ? (p.causal ? min(lk, q_local + 1) : lk) - k_base : BK;
+                // Warp-wide bounds of the valid-column count: a 32-column chunk
+                // below lim_lo needs no mask, one at or above lim_hi is all masked.
+                const int lim_lo = need_mask ? __reduce_min_sync(0xffffffffu, lim) : BK;
+                const int lim_hi = need_mask ? __reduce_max_sync(0xffffffffu, lim) : BK;
 
-                // Row max of the raw scores of this block (scale > 0), 32 columns at a time.
-                auto block_max = [&](auto masked) -> float {
+                // One half of the key tile: 64 scores as two 32-column chunks.
+                auto half = [&](auto masked, int hh) -> bool {
                     constexpr bool MASK = decltype(masked)::value;
-                    float mx[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        mx[e] = -INFINITY;
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t sr[32];
-                        tmem_ld32(s_addr + cc * 32, sr);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int c = 0; c < 32; c += 16)
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                float s0 = __uint_as_float(sr[c + e]);
-                                float s1 = __uint_as_float(sr[c + 8 + e]);
-                                if (MASK) {
-                                    s0 = cc * 32 + c + e < lim ? s0 : -INFINITY;
-                                    s1 = cc * 32 + c + 8 + e < lim ? s1 : -INFINITY;
-                                }
-                                mx[e] = fmax3(mx[e], s0, s1);
-                            }
-                    }
-                    return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                 fmaxf(mx[6], mx[7]));
-                };
-                // p = 2^(s * scale_log2 - m) packed to bf16 pairs in pk (not yet stored:
-                // S must stay intact in TMEM in case the block is redone); returns the
-                // block's sum of p and (through mt_raw) its raw row max.
-                uint32_t pk[64];
-                auto exp_block = [&](auto masked, float m_ref, float &mt_raw) -> float {
-                    constexpr bool MASK = decltype(masked)::value;
-                    const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-                    const float2 negm2 = make_float2(neg_m, neg_m);
+                    const int c0 = hh * 64;
+                    const bool empty0 = MASK && c0 >= lim_hi;
+                    const bool empty1 = MASK && c0 + 32 >= lim_hi;
+                    const uint32_t sa = s_addr + c0;
+                    // p is computed against the reference max in the pass that
+                    // finds the half's max; if the max grew by more than 2^8 the
+                    // half is redone at the new max from TMEM, where its scores
+                    // are still intact.  A warp with a row that has no reference
+                    // yet finds the max first.
+                    const bool fresh = __any_sync(0xffffffffu, m_used == -INFINITY);
+                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                     float2 ls[4];
-                    float mx[4];
+                    uint32_t pk[32];
+                    if (fresh) {
+                        chunk_max<MASK>(sa, c0, lim, lim_lo, empty0, mx);
+                        chunk_max<MASK>(sa + 32, c0 + 32, lim, lim_lo, empty1, mx);
+                    } else {
+                        const float2 negm2 = make_float2(-m_used, -m_used);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        ls[e] = make_float2(0.f, 0.f);
-                        mx[e] = -INFINITY;
+                        for (int e = 0; e < 4; ++e)
+                            ls[e] = make_float2(0.f, 0.f);
+                        chunk_exp<MASK, true>(sa, c0, lim, lim_lo, empty0, scale2, negm2, ls, mx, pk, 0);
+                        chunk_exp<MASK, true>(sa + 32, c0 + 32, lim, lim_lo, empty1, scale2, negm2, ls,
+                                              mx, pk, 16);
                     }
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t sr[32];
-                        tmem_ld32(s_addr + cc * 32, sr);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            float s0 = __uint_as_float(sr[2 * e]);
-                            float s1 = __uint_as_float(sr[2 * e + 1]);
-                            if (MASK) {
-                                // a masked score becomes -inf: it drops out of the max and
-                                // 2^(-inf) = 0 (the scale is > 0, so no -inf * 0)
-                                s0 = cc * 32 + 2 * e < lim ? s0 : -INFINITY;
-                                s1 = cc * 32 + 2 * e + 1 < lim ? s1 : -INFINITY;
-                            }
-                            mx[e & 3] = fmax3(mx[e & 3], s0, s1);
-                            const float2 t = __ffma2_rn(make_float2(s0, s1), scale2, negm2);
-                            const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-                            ls[e & 3] = __fadd2_rn(ls[e & 3], pp);
-                            pk[cc * 16 + e] = pack_bf16x2(pp.x, pp.y);
-                        }
-                    }
-                    mt_raw = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
-                    const float2 l2 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
-                    return l2.x + l2.y;
-                };
-                auto do_exp = [&](float m_ref, float &mt) {
-                    return need_mask ? exp_block(Masked{}, m_ref, mt) : exp_block(Plain{}, m_ref, mt);
-                };
-                auto to_log2 = [&](float raw_max) {
-                    return raw_max == -INFINITY ? -INFINITY : raw_max * scale_log2;
-                };
-                float ls_blk, mt_raw;
-                if (j == 0) {
-                    m_used = to_log2(need_mask ? block_max(Masked{}) : block_max(Plain{}));
-                    ls_blk = do_exp(m_used, mt_raw);
-                } else {
-                    // Speculate that the reference max still holds.
-                    ls_blk = do_exp(m_used, mt_raw);
-                    const float m_new = fmaxf(m_used, to_log2(mt_raw));
+                    const float mraw = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
+                    const float m_half = mraw == -INFINITY ? -INFINITY : mraw * scale_log2;
+                    const float m_new = fmaxf(m_used, m_half);
                     const bool grow = m_new > m_used + kRescaleThreshold;   // true for m_used = -inf
-                    if (__any_sync(0xffffffffu, grow)) {
-                        // O_x must hold the previous block's product before it is rescaled.
-                        if (!mbar_wait(o_done(x), (g - 1) & 1u, abort)) {
-                            ok = false;
-                            break;
+                    const bool redo = __any_sync(0xffffffffu, grow);
+                    if (redo) {
+                        if (j > 0 || hh > 0) {
+                            // O_x must hold every product issued so far before it
+                            // is rescaled: the previous tile's second half, or this
+                            // tile's first.
+                            const bool waited = hh == 0 ? mbar_wait(o_h2(x), (g - 1) & 1u, abort)
+                                                        : mbar_wait(o_h1(x), g & 1u, abort);
+                            if (!waited)
+                                return false;
+                            tc_fence_after();
+                            const float f = grow ? ex2_approx(m_used - m_new) : 1.f;
+                            rescale_rows<D>(o_addr, f);
+                            l *= f;
                         }
-                        tc_fence_after();
-                        const float f = (m_new == -INFINITY) ? 1.f : ex2_approx(m_used - m_new);
-#pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t rr[32];
-                            tmem_ld32(o_addr + c * 32, rr);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                rr[e] = __float_as_uint(__uint_as_float(rr[e]) * f);
-                            tmem_st32(o_addr + c * 32, rr);
-                        }
-                        tmem_wait_st();
-                        l *= f;
-                        m_used = m_new;
-                        ls_blk = do_exp(m_used, mt_raw);
+                        if (grow)
+                            m_used = m_new;
                     }
-                }
-                l += ls_blk;
-                tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-                tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(p_full(x));
+                    if (fresh || redo) {
+                        const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+                        const float2 negm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            ls[e] = make_float2(0.f, 0.f);
+                        chunk_exp<MASK, false>(sa, c0, lim, lim_lo, empty0, scale2, negm2, ls, mx, pk, 0);
+                        chunk_exp<MASK, false>(sa + 32, c0 + 32, lim, lim_lo, empty1, scale2, negm2, ls,
+                                               mx, pk, 16);
+                    }
+                    const float2 l2 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
+                    l += l2.x + l2.y;
+                    // P (bf16 pairs) over this half's S columns, already read.
+                    tmem_st32(s_addr + hh * 32, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(p_half(x, hh));
+                    return true;
+                };
+                for (int hh = 0; hh < 2 && ok; ++hh)
+                    ok = need_mask ? half(Masked{}, hh) : half(Plain{}, hh);
                 ++g;
             }
             if (!ok)
                 break;
 
             // Epilogue: wait for this tile's last O += P V, then O / l -> bf16 and lse.
-            if (!mbar_wait(o_done(x), (g - 1) & 1u, abort))
+            if (!mbar_wait(o_h2(x), (g - 1) & 1u, abort))
                 break;
             tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -560,7 +639,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t rr[64];
                     tmem_ld32(o_addr + db * 64, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
                     tmem_ld32(o_addr + db * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
-                    tmem_wait_ld();
+                    tmem_wait_ld_r(*reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
+                    tmem_bind_r(*reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
                     // the previous block's store must have left the stage
                     if (!mbar_wait(stage_free(x), (stage_uses & 1u) ^ 1u, abort)) {
                         ok = false;
@@ -600,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t rr[32];
                     tmem_ld32(o_addr + c * 32, rr);
-                    tmem_wait_ld();
+                    tmem_wait_ld_r(rr);
                     if (row_valid) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
