@@ -70,7 +70,7 @@ def _traffic(kernel_key):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -86,7 +86,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
         except Exception:
@@ -162,25 +162,28 @@ def _row_flops(case, rows):
 
 
 def cpu_oracle_rate(case, seconds: float, seed: int = 0):
-    """Time the oracle (as it stands) on random rows of `case` for about `seconds`."""
+    """Time the oracle (as it stands) on random rows of `case` for about `seconds`:
+    batches of rows, each sized from the previous batch's rate, until the time is spent."""
     import numpy as np
     import oracle
     rng = np.random.default_rng(seed)
-    rows = _oracle_rows_sample(case, 64, rng)
-    t0 = time.perf_counter()
-    _, _, threads = oracle.varlen_fwd_rows(case.q, case.k, case.v, case.cu_seqlens_q,
-                                           case.cu_seqlens_k, case.num_heads, case.head_dim,
-                                           case.softmax_scale, case.causal, rows)
-    dt = max(time.perf_counter() - t0, 1e-4)
-    n = int(min(case.total_q * case.num_heads, max(64, 64 * (seconds / dt))))
-    rows = _oracle_rows_sample(case, n, rng)
-    t0 = time.perf_counter()
-    _, _, threads = oracle.varlen_fwd_rows(case.q, case.k, case.v, case.cu_seqlens_q,
-                                           case.cu_seqlens_k, case.num_heads, case.head_dim,
-                                           case.softmax_scale, case.causal, rows)
-    dt = time.perf_counter() - t0
-    flops = _row_flops(case, rows)
-    return flops / dt / 1e12, threads, n, dt
+    n, flops, spent, rows_done, threads = 256, 0, 0.0, 0, 0
+    cap = case.total_q * case.num_heads
+    while spent < seconds:
+        rows = _oracle_rows_sample(case, min(n, cap), rng)
+        t0 = time.perf_counter()
+        _, _, threads = oracle.varlen_fwd_rows(case.q, case.k, case.v, case.cu_seqlens_q,
+                                               case.cu_seqlens_k, case.num_heads,
+                                               case.head_dim, case.softmax_scale, case.causal,
+                                               rows)
+        dt = max(time.perf_counter() - t0, 1e-4)
+        flops += _row_flops(case, rows)
+        spent += dt
+        rows_done += len(rows)
+        left = seconds - spent
+        # next batch: about half the remaining time (at least 1 s of work), at this rate
+        n = int(max(256, len(rows) / dt * max(1.0, 0.5 * left)))
+    return flops / spent / 1e12, threads, rows_done, spent
 
 
 def run_reference(args):
@@ -302,6 +305,14 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     launches_per_step = 2 + (2 + len(tiles))
+    if args.profile:
+        part = prefill if args.profile == "prefill" else graph.replay
+        for i in range(args.warmup + args.steps):
+            flush.fill_(float(i))
+            part()
+        torch.cuda.synchronize()
+        print(f"profile run: {args.profile} x {args.warmup + args.steps}", flush=True)
+        return
     n_ev = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
 
@@ -451,14 +462,16 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="packed",
                     choices=["packed", "longtail", "cross-d64", "cross-d256", "tiny",
                              "tiny-causal"])
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+                    help="run only W + K passes of one part (for ncu captures); no JSON line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

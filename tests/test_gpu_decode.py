@@ -72,7 +72,8 @@ def test_decode_workload(vfa, oracle_mod):
 
 
 @pytest.mark.parametrize("Hq,Hkv,D", [(8, 8, 64), (8, 4, 128), (32, 8, 128), (16, 2, 256),
-                                      (4, 1, 64), (8, 1, 256)])
+                                      (4, 1, 64), (8, 1, 256), (8, 1, 128), (8, 1, 64),
+                                      (2, 2, 256), (3, 3, 128), (4, 2, 64), (4, 2, 256)])
 def test_decode_shapes(vfa, oracle_mod, Hq, Hkv, D):
     rng = np.random.default_rng(Hq * 100 + D)
     n_blocks = [5, 0, 1, 13, 7]

@@ -111,6 +111,15 @@ vfa_status encode_packed_map(CUtensorMap *map, const void *base, int rows, int h
     return VFA_OK;
 }
 
+// [num_blocks * block_size tokens, kv_heads, head_dim] bf16 pool as the same
+// kind of 3-D TMA map as the packed tensors: one box is 64 columns of one
+// block's block_size token rows for one kv head.
+vfa_status encode_pool_map(CUtensorMap *map, const void *base, int num_blocks, int block_size,
+                           int kv_heads, int head_dim)
+{
+    return encode_packed_map(map, base, num_blocks * block_size, kv_heads, head_dim, block_size);
+}
+
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
@@ -336,6 +345,8 @@ static vfa_status check_decode_args(const void *q, const void *k_pool, const voi
         return fail(VFA_ERR_UNSUPPORTED, "head_dim %d not supported (64, 128, 256)", head_dim);
     if (block_size != 16)
         return fail(VFA_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+    if (num_blocks > (1 << 26))
+        return fail(VFA_ERR_UNSUPPORTED, "num_blocks %d above 2^26 not supported", num_blocks);
     if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || (q && !aligned(q, 16)) ||
         !aligned(tile_blocks, 4) || !aligned(counts, 4))
         return fail(VFA_ERR_INVALID_ARG, "pools and q must be 16-byte aligned");
@@ -378,7 +389,13 @@ vfa_status vfa_paged_decode_step(const void *q, const void *k_pool, const void *
     a.l = l;
     a.o = o;
     a.status = device_status;
-    cudaError_t e = vfa::launch_decode_step(a, reinterpret_cast<cudaStream_t>(stream));
+    vfa::DecodeMaps maps;
+    if ((st = encode_pool_map(&maps.tm_k, k_pool, num_blocks, block_size, num_kv_heads,
+                              head_dim)) ||
+        (st = encode_pool_map(&maps.tm_v, v_pool, num_blocks, block_size, num_kv_heads,
+                              head_dim)))
+        return st;
+    cudaError_t e = vfa::launch_decode_step(a, maps, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "decode step launch");
     return VFA_OK;

@@ -9,15 +9,16 @@
 //
 //   * one CTA per (kv head, sequence): the group of q heads that share a kv
 //     head is handled together, so each K/V block row is read from HBM once;
-//   * each warp takes every 4th listed block; a block is 16 tokens x D,
-//     read with 16-byte vector loads (16 lanes per token row, two tokens per
-//     warp-wide load); fp32 FMA dot products, no tensor cores (the
-//     contraction is 16 tokens by a handful of heads, far too thin);
-//   * per block, the 16-lane partial dot products are reduced by a transposing
-//     butterfly (each level halves the values a lane holds), the block max
-//     and exponentials follow, and the block's p values are broadcast back to
-//     the lanes that own V's columns;
-//   * the four warps' partial states are merged in shared memory with the
+//   * the listed blocks stream by TMA through a ring of shared-memory stages
+//     (48 KB per CTA), each of the CTA's four warps computing on every fourth
+//     block, so HBM reads for later blocks overlap the arithmetic on earlier
+//     ones, and four CTAs fit on an SM: all (kv head, sequence) CTAs of a
+//     64-sequence, 8-kv-head batch are resident at once;
+//   * per block, S = K Q^T and O^T += V^T P run on the warp-level tensor
+//     instruction (mma.sync, bf16 in, fp32 accumulate; q heads padded to 8):
+//     the kernel stays bound by HBM, and these 16-token products would cost
+//     an order of magnitude more instructions as scalar FMAs;
+//   * the warps' partial states are merged in shared memory with the
 //     incoming state, all relative to one max, and written back (m in
 //     natural-log units).
 // Block ids and counts are validated before any state is touched; bad ones
@@ -37,9 +38,6 @@ constexpr int kBlockSize = 16;          // tokens per KV block (the supported si
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 
-// bf16x2 word -> two floats (exact).
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Row of kv head `kh`, token `t` of physical block `blk` in a
 // [num_blocks, block_size, num_kv_heads, D] pool: the one address rule of
@@ -72,6 +70,27 @@ __device__ __forceinline__ void load_chunk(const __nv_bfloat16 *row, int l16, ui
     }
 }
 
+// Waits (bounded, like mbar_wait) until the shared counter *c exceeds n.
+__device__ __forceinline__ bool wait_count_above(const int *c, int n, volatile int *abort)
+{
+    const volatile int *vc = c;
+    if (*vc > n)
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (*vc > n)
+            return true;
+        if ((it & 63u) == 0) {
+            if (*abort)
+                return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // Validates tile_blocks[s, 0:count] and the count; every thread of the CTA
 // gets the same verdict.
 __device__ __forceinline__ bool tile_row_valid(const int32_t *tile_blocks, int count, int cap,
@@ -87,27 +106,105 @@ __device__ __forceinline__ bool tile_row_valid(const int32_t *tile_blocks, int c
     return !__syncthreads_or(bad);
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32) decode_step_kernel(const DecodeStepArgs a)
-{
-    constexpr int DPL = D / 16;             // elements per lane per token row
-    constexpr int W = DPL / 2;              // bf16x2 words per lane per row
-    constexpr int TPL = kBlockSize / 2;     // tokens per lane per block (two per warp load)
-    constexpr int NV = TPL * G;             // partial dot products per lane before reduction
-    constexpr int KPL = G >= 2 ? G / 2 : 1; // complete dot products per lane after reduction
+// ------------------------------------------------------------ step kernel
+//
+// One CTA of kStepWarps warps per (kv head, sequence).  The tile's blocks
+// stream through one ring of NS shared-memory stages: block k goes to stage
+// k % NS by TMA (K and V of one block for this kv head are D/64 boxes of 16
+// tokens x 64 columns each, 128-byte swizzled, from the pool viewed as
+// [blocks * 16 tokens, kv heads, D]); warp k % 4 consumes it and then
+// refills the stage with block k + NS, so up to NS blocks are in flight
+// while the warps compute.
+//
+// A warp's work on one block is two thin products on the warp-level tensor
+// instruction (mma.sync m16n8k16, bf16 in, fp32 accumulate), which keeps the
+// instruction count per byte low enough for HBM to be the limit:
+//   S[16 tokens x 8]   = K[16 x D] . Q^T[D x 8]       (q heads padded to 8)
+//   O^T[D x 8]        += V^T[D x 16] . P[16 tokens x 8]
+// K comes in with ldmatrix, V^T with ldmatrix.trans; P leaves S's fragment
+// transposed by movmatrix.  In both accumulators a lane holds heads
+// 2*(lane % 4) and 2*(lane % 4) + 1, so the running max, the rescale of O
+// and p need no exchange beyond a max over the 8 lanes sharing those heads.
+constexpr int kStepWarps = 4;
+constexpr int kRingBytes = 48 * 1024;
 
-    __shared__ float s_m[kWarps][G];
-    __shared__ float s_l[kWarps][G];
-    __shared__ float s_o[kWarps][G][D];
+template <int D>
+struct StepCfg {
+    static constexpr int STAGE = 2 * kBlockSize * D * 2;         // K and V of one block
+    static constexpr int NS = kRingBytes / STAGE;                 // 12, 6, 3 stages
+    static constexpr int RING = NS * STAGE;
+    static constexpr int KB = D / 64;                             // 64-column boxes per row
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movm_t(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// c[0..3] += A(16x16, a[0..3]) * B(16x8, b[0..1]), bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Shared address of the 16-byte chunk `chunk` (8 columns) of token row `row`
+// in one 16-row operand of D/64 swizzled 64-column boxes (2 KB each).
+__device__ __forceinline__ uint32_t sw_addr(uint32_t base, int row, int chunk)
+{
+    return base + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
+    const DecodeStepArgs a, const __grid_constant__ DecodeMaps t)
+{
+    using C = StepCfg<D>;
+    constexpr int NS = C::NS;
+    constexpr int MT = D / 16;                // 16-column tiles of D
+
+    extern __shared__ __align__(1024) uint8_t dsm_raw[];
+    // 128-byte swizzled TMA destinations start on a 1024-byte boundary.
+    uint8_t *dsm = dsm_raw + ((1024u - (smem_u32(dsm_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(dsm + C::RING);            // [NS]
+    __shared__ float s_m[kStepWarps][8], s_l[kStepWarps][8];
+    __shared__ float s_min[G], s_lin[G];
+    __shared__ int s_abort;
+    __shared__ int s_fills[NS], s_used[NS];   // per stage: fills issued, fills consumed
 
     const int kh = blockIdx.x;
     const int s = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int half = lane >> 4, l16 = lane & 15;
-    const int Hq = a.num_q_heads, Hkv = a.num_kv_heads;
+    const int Hq = a.num_q_heads;
+
+    // Consecutive steps are launched with programmatic serialisation: the
+    // next step may start streaming its blocks now; it waits for this grid
+    // (griddepcontrol.wait) before it touches the state or the status word.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int count = a.tile_block_counts[s];
     if (!tile_row_valid(a.tile_blocks, count, a.tile_capacity, a.num_blocks, s)) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         if (threadIdx.x == 0 && a.status)
             atomicCAS(a.status, 0, VFA_ERR_BAD_BLOCK);
         return;
@@ -115,207 +212,205 @@ __global__ void __launch_bounds__(kWarps * 32) decode_step_kernel(const DecodeSt
     if (count == 0)
         return;                                 // an empty tile leaves the state as it was
 
-    // q of the G heads of this group, pre-scaled by log2(e)/sqrt(D): this lane's columns.
-    const float qscale = kLog2e * rsqrtf(static_cast<float>(D));
-    float qv[G][DPL];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const __nv_bfloat16 *qrow =
-            static_cast<const __nv_bfloat16 *>(a.q) + (static_cast<long long>(s) * Hq + kh * G + g) * D;
-        uint32_t w[W];
-        const uint32_t *src = reinterpret_cast<const uint32_t *>(qrow + l16 * DPL);
-#pragma unroll
-        for (int e = 0; e < W; ++e)
-            w[e] = src[e];
-#pragma unroll
-        for (int e = 0; e < W; ++e) {
-            qv[g][2 * e] = bf_lo(w[e]) * qscale;
-            qv[g][2 * e + 1] = bf_hi(w[e]) * qscale;
+    const uint32_t ring = smem_u32(dsm);
+    auto stage_k = [&](int st) { return ring + st * C::STAGE; };
+    auto full = [&](int st) { return smem_u32(&bars[st]); };
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(smem_u32(&bars[i]), 1);
+            s_fills[i] = 0;
+            s_used[i] = 0;
         }
-    }
-
-    float m_run[G], l_part[G], o[G][DPL];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m_run[g] = -INFINITY;
-        l_part[g] = 0.f;
-#pragma unroll
-        for (int d = 0; d < DPL; ++d)
-            o[g][d] = 0.f;
-    }
-
-    const int32_t *row_ids = a.tile_blocks + static_cast<long long>(s) * a.tile_capacity;
-    for (int bi = warp; bi < count; bi += kWarps) {
-        const int blk = row_ids[bi];
-        uint32_t kw[TPL][W], vw[TPL][W];
-#pragma unroll
-        for (int i = 0; i < TPL; ++i)
-            load_chunk<D>(kv_row<D>(a.k_pool, blk, 2 * i + half, kh, Hkv), l16, kw[i]);
-#pragma unroll
-        for (int i = 0; i < TPL; ++i)
-            load_chunk<D>(kv_row<D>(a.v_pool, blk, 2 * i + half, kh, Hkv), l16, vw[i]);
-
-        // Partial logits: value index v = i * G + g (token 2i + half, head g).
-        float acc[NV];
-#pragma unroll
-        for (int i = 0; i < TPL; ++i) {
-            float kf[DPL];
-#pragma unroll
-            for (int e = 0; e < W; ++e) {
-                kf[2 * e] = bf_lo(kw[i][e]);
-                kf[2 * e + 1] = bf_hi(kw[i][e]);
-            }
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float t = 0.f;
-#pragma unroll
-                for (int d = 0; d < DPL; ++d)
-                    t = fmaf(qv[g][d], kf[d], t);
-                acc[i * G + g] = t;
-            }
-        }
-        // Transposing butterfly over the 16 lanes of this half: each level keeps
-        // the half of the values selected by the lane bit and adds the partner's.
-        int n = NV;
-#pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) {
-            const bool upper = (l16 & off) != 0;
-            if (n > 1) {
-                const int hn = n / 2;
-#pragma unroll
-                for (int j = 0; j < NV / 2; ++j) {
-                    if (j < hn) {
-                        const float send = upper ? acc[j] : acc[j + hn];
-                        const float keep = upper ? acc[j + hn] : acc[j];
-                        acc[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                    }
-                }
-                n = hn;
-            } else {
-                acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], off);
-            }
-        }
-        // Now this lane holds KPL complete logits: token 2*(l16>>1) + half, heads
-        // hbase .. hbase+KPL-1 with hbase = (l16 & 1) * KPL (G >= 2), or head 0 (G = 1).
-        const int hbase = G >= 2 ? (l16 & 1) * KPL : 0;
-        float bm[KPL];
-#pragma unroll
-        for (int k = 0; k < KPL; ++k) {
-            float x = acc[k];
-#pragma unroll
-            for (int off = 2; off <= 16; off <<= 1)
-                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
-            bm[k] = x;
-        }
-        // Every lane learns the block max of all G heads.
-        float mx[G];
-#pragma unroll
-        for (int k = 0; k < KPL; ++k) {
-            if (G >= 2) {
-                const float other = __shfl_xor_sync(0xffffffffu, bm[k], 1);
-                mx[k] = (l16 & 1) ? other : bm[k];
-                mx[KPL + k < G ? KPL + k : k] = (l16 & 1) ? bm[k] : other;
-            } else {
-                mx[0] = bm[0];
-            }
-        }
-        float mnew[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            mnew[g] = fmaxf(m_run[g], mx[g]);
-            if (mnew[g] > m_run[g]) {                         // uniform across the warp
-                const float f = ex2_approx(m_run[g] - mnew[g]);   // 0 when m_run = -inf
-                l_part[g] *= f;
-#pragma unroll
-                for (int d = 0; d < DPL; ++d)
-                    o[g][d] *= f;
-                m_run[g] = mnew[g];
-            }
-        }
-        float pk[KPL];
-#pragma unroll
-        for (int k = 0; k < KPL; ++k) {
-            const int hg = hbase + k;
-            pk[k] = ex2_approx(acc[k] - m_run[hg]);
-            // in G = 1 the lane pair (l16, l16^1) holds the same value: count it once
-            if (G >= 2 || (l16 & 1) == 0)
-                l_part[hg] += pk[k];
-        }
-        // PV: lane owns columns [l16*DPL, +DPL) of its tokens 2i + half.
-#pragma unroll
-        for (int i = 0; i < TPL; ++i) {
-            float pv[G];
-#pragma unroll
-            for (int grp = 0; grp < (G >= 2 ? 2 : 1); ++grp) {
-                const int src = half * 16 + 2 * i + grp;
-#pragma unroll
-                for (int k = 0; k < KPL; ++k)
-                    pv[grp * KPL + k] = __shfl_sync(0xffffffffu, pk[k], src);
-            }
-#pragma unroll
-            for (int e = 0; e < W; ++e) {
-                const float v0 = bf_lo(vw[i][e]), v1 = bf_hi(vw[i][e]);
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    o[g][2 * e] = fmaf(pv[g], v0, o[g][2 * e]);
-                    o[g][2 * e + 1] = fmaf(pv[g], v1, o[g][2 * e + 1]);
-                }
-            }
-        }
-    }
-
-    // Warp totals: l over all lanes, o over the two token halves.
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        float x = l_part[g];
-#pragma unroll
-        for (int off = 1; off <= 16; off <<= 1)
-            x += __shfl_xor_sync(0xffffffffu, x, off);
-        l_part[g] = x;
-#pragma unroll
-        for (int d = 0; d < DPL; ++d)
-            o[g][d] += __shfl_xor_sync(0xffffffffu, o[g][d], 16);
-    }
-    if (lane == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            s_m[warp][g] = m_run[g];
-            s_l[warp][g] = l_part[g];
-        }
-    }
-    if (half == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int d = 0; d < DPL; ++d)
-                s_o[warp][g][l16 * DPL + d] = o[g][d];
+        fence_barrier_init();
     }
     __syncthreads();
+    volatile int *abort = &s_abort;
 
-    // Merge the warps with the incoming state (stored m is in natural-log units).
-    __shared__ float s_min[G], s_lin[G];
+    const int32_t *row_ids = a.tile_blocks + static_cast<long long>(s) * a.tile_capacity;
+    // Block k of the tile into stage k % NS (one thread issues a fill).
+    auto issue = [&](int k) {
+        const int blk = row_ids[k];
+        const int st = k % NS;
+        mbar_arrive_expect_tx(full(st), C::STAGE);
+#pragma unroll
+        for (int b = 0; b < C::KB; ++b) {
+            tma_load_3d(stage_k(st) + b * 2048, &t.tm_k, full(st), b * 64, kh, blk * kBlockSize);
+            tma_load_3d(stage_k(st) + C::STAGE / 2 + b * 2048, &t.tm_v, full(st), b * 64, kh,
+                        blk * kBlockSize);
+        }
+        // Published after the arrive: a consumer that sees the new count waits
+        // on a barrier already armed for this fill.
+        __threadfence_block();
+        atomicAdd(&s_fills[st], 1);
+    };
+    if (threadIdx.x == 0)
+        for (int k = 0; k < NS && k < count; ++k)
+            issue(k);
+
+    // Q^T fragments (B operand of S = K Q^T): head n = lane / 4, columns
+    // 16 * kt + 2 * (lane % 4) + {0, 1} and + 8; heads past G are zero.
+    const int n_q = lane >> 2, t4 = lane & 3;
+    uint32_t qb[MT][2];
+    {
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+            static_cast<const __nv_bfloat16 *>(a.q) +
+            (static_cast<long long>(s) * Hq + kh * G + (n_q < G ? n_q : 0)) * D);
+#pragma unroll
+        for (int kt = 0; kt < MT; ++kt) {
+            qb[kt][0] = n_q < G ? qrow[(16 * kt + 2 * t4) / 2] : 0u;
+            qb[kt][1] = n_q < G ? qrow[(16 * kt + 8 + 2 * t4) / 2] : 0u;
+        }
+    }
+    const float sc = kLog2e * rsqrtf(static_cast<float>(D));   // logits in log2 units
+
+    // This lane's two heads: 2 * t4 and 2 * t4 + 1.
+    float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
+    float o[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            o[mt][e] = 0.f;
+    // ldmatrix row addresses: lane L serves row L % 8 of 8x8 matrix L / 8.
+    const int mi = lane >> 3, mr = lane & 7;
+    const int k_row = ((mi & 1) << 3) + mr, k_chunk = mi >> 1;     // K: A of S = K Q^T
+    const int v_row = ((mi >> 1) << 3) + mr, v_chunk = mi & 1;     // V^T: A of O^T += V^T P
+
+    for (int k = warp; k < count; k += kStepWarps) {
+        const int st = k % NS;
+        const int fill = k / NS;
+        // The parity wait below is only unambiguous once this stage's previous
+        // fill has completed, and another warp may get here first: wait until
+        // this fill has been issued (its issuer consumed the previous one).
+        if (!wait_count_above(&s_fills[st], fill, abort) ||
+            !mbar_wait(full(st), fill & 1u, abort))
+            break;
+        const uint32_t sk = stage_k(st), sv = sk + C::STAGE / 2;
+
+        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kt = 0; kt < MT; ++kt) {
+            uint32_t af[4];
+            ldsm_x4(sw_addr(sk, k_row, 2 * kt + k_chunk), af);
+            mma_bf16(sacc, af, qb[kt][0], qb[kt][1]);
+        }
+        // sacc: tokens lane/4 (0, 1) and lane/4 + 8 (2, 3); heads 2*t4 (0, 2), 2*t4+1 (1, 3).
+        float bm[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float x = fmaxf(sacc[h], sacc[h + 2]) * sc;
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1)
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+            bm[h] = x;
+        }
+        float f[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float mnew = fmaxf(m_run[h], bm[h]);
+            f[h] = ex2_approx(m_run[h] - mnew);            // 0 when m_run = -inf, 1 if unchanged
+            m_run[h] = mnew;
+            l_part[h] *= f[h];
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            o[mt][0] *= f[0];
+            o[mt][1] *= f[1];
+            o[mt][2] *= f[0];
+            o[mt][3] *= f[1];
+        }
+        const float p0 = ex2_approx(sacc[0] * sc - m_run[0]);
+        const float p1 = ex2_approx(sacc[1] * sc - m_run[1]);
+        const float p2 = ex2_approx(sacc[2] * sc - m_run[0]);
+        const float p3 = ex2_approx(sacc[3] * sc - m_run[1]);
+        l_part[0] += p0 + p2;
+        l_part[1] += p1 + p3;
+        // P as two 8x8 tiles (tokens 0-7, 8-15) x 8 heads, transposed into the
+        // B operand (k = token, n = head) of O^T += V^T P.
+        const uint32_t pb0 = movm_t(pack_bf16x2(p0, p1));
+        const uint32_t pb1 = movm_t(pack_bf16x2(p2, p3));
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            uint32_t af[4];
+            ldsm_x4_t(sw_addr(sv, v_row, 2 * mt + v_chunk), af);
+            mma_bf16(o[mt], af, pb0, pb1);
+        }
+        // Every lane is done with this stage: refill it with block k + NS.
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            ++s_used[st];
+            if (k + NS < count)
+                issue(k + NS);
+        }
+    }
+    // Warp totals of l: the 8 lanes sharing this lane's heads (lane % 4).
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float x = l_part[h];
+#pragma unroll
+        for (int off = 4; off <= 16; off <<= 1)
+            x += __shfl_xor_sync(0xffffffffu, x, off);
+        l_part[h] = x;
+    }
+    __syncthreads();                                    // every warp is out of the ring
+    // The previous step (or the init) must be complete before its state is read.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (*abort) {
+        // A stage's last fill may still be in flight if nobody consumed it:
+        // wait for it (bounded) before the CTA exits; the state is left as it was.
+        if (threadIdx.x == 0) {
+            for (int st = 0; st < NS; ++st)
+                if (s_fills[st] > s_used[st])
+                    mbar_wait_drain(full(st), (s_fills[st] - 1) & 1u);
+            if (a.status)
+                atomicCAS(a.status, 0, VFA_ERR_TIMEOUT);
+        }
+        return;
+    }
+    float *s_o = reinterpret_cast<float *>(dsm);        // [warps][G][D], over the ring
+    if (lane < 4) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            s_m[warp][2 * lane + h] = m_run[h];
+            s_l[warp][2 * lane + h] = l_part[h];
+        }
+    }
+    // o[mt]: columns 16*mt + lane/4 (0, 1) and + 8 (2, 3); heads 2*t4 (0, 2), 2*t4+1 (1, 3).
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int h = 2 * t4 + (e & 1);
+            const int col = 16 * mt + (lane >> 2) + ((e >> 1) << 3);
+            if (h < G)
+                s_o[(warp * G + h) * D + col] = o[mt][e];
+        }
     if (threadIdx.x < G) {
         const long long sh = static_cast<long long>(s) * Hq + kh * G + threadIdx.x;
         s_min[threadIdx.x] = a.m[sh] * kLog2e;
         s_lin[threadIdx.x] = a.l[sh];
     }
     __syncthreads();
+
+    // Merge the warps with the incoming state (stored m is in natural-log units).
     for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
         const int g = e / D, d = e % D;
         const long long sh = static_cast<long long>(s) * Hq + kh * G + g;
         const float m_in = s_min[g];
         float mt = m_in;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w)
+        for (int w = 0; w < kStepWarps; ++w)
             mt = fmaxf(mt, s_m[w][g]);
         const float f_in = ex2_approx(m_in - mt);      // 0 for a fresh state (m_in = -inf)
         float acc_o = a.o[sh * D + d] * f_in;
         float acc_l = s_lin[g] * f_in;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float f = ex2_approx(s_m[w][g] - mt);
-            acc_o = fmaf(s_o[w][g][d], f, acc_o);
-            acc_l = fmaf(s_l[w][g], f, acc_l);
+        for (int w = 0; w < kStepWarps; ++w) {
+            const float fw = ex2_approx(s_m[w][g] - mt);   // 0 for a warp with no blocks
+            acc_o = fmaf(s_o[(w * G + g) * D + d], fw, acc_o);
+            acc_l = fmaf(s_l[w][g], fw, acc_l);
         }
         a.o[sh * D + d] = acc_o;
         if (d == 0) {
@@ -325,9 +420,18 @@ __global__ void __launch_bounds__(kWarps * 32) decode_step_kernel(const DecodeSt
     }
 }
 
+template <int D, int G>
+size_t step_smem_bytes()
+{
+    return 1024 + StepCfg<D>::RING + StepCfg<D>::NS * sizeof(uint64_t);
+}
+
 __global__ void decode_init_kernel(float *m, float *l, float *o, long long n_state, int head_dim,
                                    int32_t *status)
 {
+    // A following step may launch now; it waits for this grid before it
+    // reads the state.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
          i < n_state * head_dim; i += stride) {
@@ -404,21 +508,46 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gather_kernel(const Decode
 }
 
 template <int D, int G>
-cudaError_t step_dg(const DecodeStepArgs &a, cudaStream_t stream)
+cudaError_t step_dg(const DecodeStepArgs &a, const DecodeMaps &maps, cudaStream_t stream)
 {
-    dim3 grid(a.num_kv_heads, a.num_seqs);
-    decode_step_kernel<D, G><<<grid, kWarps * 32, 0, stream>>>(a);
+    static int attr_done[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const size_t smem = step_smem_bytes<D, G>();
+    if (dev < 64 && !attr_done[dev]) {
+        e = cudaFuncSetAttribute(decode_step_kernel<D, G>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess)
+            return e;
+        attr_done[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_kv_heads, a.num_seqs);
+    cfg.blockDim = dim3(kStepWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_step_kernel<D, G>, a, maps);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t step_d(const DecodeStepArgs &a, cudaStream_t stream)
+cudaError_t step_d(const DecodeStepArgs &a, const DecodeMaps &maps, cudaStream_t stream)
 {
     switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return step_dg<D, 1>(a, stream);
-    case 2: return step_dg<D, 2>(a, stream);
-    case 4: return step_dg<D, 4>(a, stream);
-    case 8: return step_dg<D, 8>(a, stream);
+    case 1: return step_dg<D, 1>(a, maps, stream);
+    case 2: return step_dg<D, 2>(a, maps, stream);
+    case 4: return step_dg<D, 4>(a, maps, stream);
+    case 8: return step_dg<D, 8>(a, maps, stream);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -444,12 +573,13 @@ cudaError_t launch_decode_init(float *m, float *l, float *o, int num_seqs, int n
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode_step(const DecodeStepArgs &a, cudaStream_t stream)
+cudaError_t launch_decode_step(const DecodeStepArgs &a, const DecodeMaps &maps,
+                               cudaStream_t stream)
 {
     switch (a.head_dim) {
-    case 64: return step_d<64>(a, stream);
-    case 128: return step_d<128>(a, stream);
-    case 256: return step_d<256>(a, stream);
+    case 64: return step_d<64>(a, maps, stream);
+    case 128: return step_d<128>(a, maps, stream);
+    case 256: return step_d<256>(a, maps, stream);
     default: return cudaErrorInvalidValue;
     }
 }

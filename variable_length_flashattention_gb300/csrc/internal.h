@@ -105,7 +105,15 @@ struct DecodeStepArgs {
 
 cudaError_t launch_decode_init(float *m, float *l, float *o, int num_seqs, int num_q_heads,
                                int head_dim, int32_t *status, cudaStream_t stream);
-cudaError_t launch_decode_step(const DecodeStepArgs &a, cudaStream_t stream);
+// K and V pools as 3-D TMA maps over [num_blocks * block_size tokens,
+// num_kv_heads, head_dim] (innermost first: dim, kv head, token); box =
+// head_dim x 1 x block_size, no swizzle.
+struct DecodeMaps {
+    CUtensorMap tm_k, tm_v;
+};
+
+cudaError_t launch_decode_step(const DecodeStepArgs &a, const DecodeMaps &maps,
+                               cudaStream_t stream);
 cudaError_t launch_decode_finalize(const float *l, const float *o, int num_seqs,
                                    int num_q_heads, int head_dim, void *out,
                                    cudaStream_t stream);
