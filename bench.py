@@ -438,6 +438,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": ach_dec, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": ach_dec / peaks["hbm_gbs"],
                          "traffic": _traffic("decode_step_d128_g4"),
+                         "traffic_unit": "DRAM bytes per step launch (ncu, tile 4)",
                          "kernel": "whole decode pass (init + steps + finalize)",
                          "peak_source": peaks["source"]},
         },
