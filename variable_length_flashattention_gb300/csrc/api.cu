@@ -282,8 +282,7 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     memset(&pa, 0, sizeof pa);
     if ((st = encode_packed_map(&pa.tm_q, q, total_q, num_heads, head_dim, bq)) ||
         (st = encode_packed_map(&pa.tm_k, k, total_k, num_heads, head_dim, bk)) ||
-        (st = encode_packed_map(&pa.tm_v, v, total_k, num_heads, head_dim, bk)) ||
-        (st = encode_packed_map(&pa.tm_o, out, total_q, num_heads, head_dim, bq)))
+        (st = encode_packed_map(&pa.tm_v, v, total_k, num_heads, head_dim, bk)))
         return st;
     pa.cu_q = cu_seqlens_q;
     pa.cu_k = cu_seqlens_k;

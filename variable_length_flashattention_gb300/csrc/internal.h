@@ -67,7 +67,7 @@ int schedule_scratch_ints(int batch, int total_q, int total_k, int block_q, int 
 // ------------------------------------------------------------ prefill
 
 struct PrefillArgs {
-    CUtensorMap tm_q, tm_k, tm_v, tm_o;   // tm_o: the output, for tile stores
+    CUtensorMap tm_q, tm_k, tm_v;
     const int32_t *cu_q;
     const int32_t *cu_k;
     const int4 *items;    // two int4 per item

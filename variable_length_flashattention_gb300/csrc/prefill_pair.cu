@@ -29,8 +29,9 @@
 //   * in a masked tile (causal diagonal, ragged key tail) a 32-column chunk
 //     that is valid for all 32 rows of a warp skips the mask, and one that
 //     is masked for all of them skips its TMEM load and its exponentials;
-//   * full output tiles leave through a swizzled shared-memory stage and a
-//     TMA tensor store; a sequence's last, partial tile is stored row by row;
+//   * O / l leaves through a 2 KB shared-memory stage per warp (no cross-warp
+//     handshake, no TMA completion to wait for): every store instruction
+//     writes eight whole 64-byte row segments;
 //   * TMEM: O_a, O_b (D columns each), S/P_a, S/P_b (128 columns each).
 // Everything else (item ring fed by an atomic counter, bounded waits with
 // drain-and-report on expiry) is as in prefill.cu.
@@ -53,11 +54,11 @@ struct PairCfg {
     static constexpr int DB = D / 64;                     // 128-byte column blocks per row
     static constexpr uint32_t Q_BYTES = BQ * D * 2;
     static constexpr uint32_t KV_BYTES = BK * D * 2;
-    static constexpr uint32_t STAGE_BYTES = BQ * 128;     // one 64-column block of an O tile
+    static constexpr uint32_t WARP_STAGE = 32 * 64;       // one warp's 32 rows x 32 output columns
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL = 2 * D;              // S_x at S_COL + x * BK; O_x at x * D
-    static constexpr int NUM_BARS = 4 + 4 * NS + 19;
-    static constexpr size_t SMEM = 1024 + 2 * Q_BYTES + 2 * NS * KV_BYTES + 2 * STAGE_BYTES +
+    static constexpr int NUM_BARS = 4 + 4 * NS + 15;
+    static constexpr size_t SMEM = 1024 + 2 * Q_BYTES + 2 * NS * KV_BYTES + 8 * WARP_STAGE +
                                    NUM_BARS * 8 + 64;
     static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BQ, BK, false, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BQ, D, false, true);
@@ -177,8 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = base;                           // Q_a, Q_b
     const uint32_t sK = sQ + 2 * C::Q_BYTES;
     const uint32_t sV = sK + NS * C::KV_BYTES;
-    const uint32_t sO = sV + NS * C::KV_BYTES;          // output staging, one block per q slot
-    const uint32_t bars = sO + 2 * C::STAGE_BYTES;
+    const uint32_t sO = sV + NS * C::KV_BYTES;          // output staging, 2 KB per softmax warp
+    const uint32_t bars = sO + 8 * C::WARP_STAGE;
     auto q_full = [&](int x) { return bars + 8u * x; };
     auto q_empty = [&](int x) { return bars + 8u * (2 + x); };
     auto k_full = [&](int i) { return bars + 8u * (4 + i); };
@@ -195,8 +196,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto item_full = [&](int x) { return bars + 8u * (E + 10 + x); };
     auto item_empty = [&](int x) { return bars + 8u * (E + 12 + x); };
     const uint32_t drain_bar = bars + 8u * (E + 14);
-    auto stage_ready = [&](int x) { return bars + 8u * (E + 15 + x); };
-    auto stage_free = [&](int x) { return bars + 8u * (E + 17 + x); };
     volatile int *abort = &s_abort;
 
     if (threadIdx.x == 0) {
@@ -211,8 +210,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(p_half(x, 1), 128);
             mbar_init(item_full(x), 1);
             mbar_init(item_empty(x), kItemConsumers);
-            mbar_init(stage_ready(x), 128);
-            mbar_init(stage_free(x), 1);
         }
         for (int i = 0; i < NS; ++i) {
             mbar_init(k_full(i), 1);
@@ -231,7 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&p.tm_q);
         tma_prefetch_map(&p.tm_k);
         tma_prefetch_map(&p.tm_v);
-        tma_prefetch_map(&p.tm_o);
     }
     tc_fence_before();
     __syncthreads();
@@ -491,13 +487,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t s_addr = tmem + lane_addr + C::S_COL + x * BK;
         const uint32_t o_addr = tmem + lane_addr + x * D;
-        const uint32_t stage = sO + x * C::STAGE_BYTES;
-        const bool leader = (warp & 3) == 0 && lane == 0;   // first warp of the warpgroup
+        const uint32_t wstage = sO + (warp - kFirstMathWarp) * C::WARP_STAGE;
         const float scale_log2 = p.scale_log2;
         const float2 scale2 = make_float2(scale_log2, scale_log2);
         const int H = p.num_heads;
         uint32_t g = 0;                               // this slot's tiles so far
-        uint32_t stage_uses = 0;                      // output blocks staged so far
         __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
         using Masked = std::integral_constant<bool, true>;
         using Plain = std::integral_constant<bool, false>;
@@ -632,76 +626,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             if (row_valid)
                 p.lse[tok * H + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -FLT_MAX;
-            if ((i + 1) * BQ <= lq) {
-                // Whole tile inside the sequence: stage each 64-column block in the
-                // 128-byte swizzled layout and store it with one TMA instruction.
-                for (int db = 0; db < DB && ok; ++db) {
-                    uint32_t rr[64];
-                    tmem_ld32(o_addr + db * 64, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
-                    tmem_ld32(o_addr + db * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
-                    tmem_wait_ld_r(*reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
-                    tmem_bind_r(*reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
-                    // the previous block's store must have left the stage
-                    if (!mbar_wait(stage_free(x), (stage_uses & 1u) ^ 1u, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t row = stage + r * 128;
+            // O / l -> bf16, 32 columns at a time through this warp's stage: each
+            // thread writes its row segment (swizzled, conflict-free), then every
+            // store instruction writes eight whole 64-byte row segments.
+            const int tile_rows = min(BQ, lq - i * BQ);
+            __nv_bfloat16 *out_tile = out + ((static_cast<long long>(q0) + i * BQ) * H + h) * D;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        st_shared_v4(row + ((c ^ (r & 7)) << 4),
-                                     pack_bf16x2(__uint_as_float(rr[8 * c + 0]) * inv_l,
-                                                 __uint_as_float(rr[8 * c + 1]) * inv_l),
-                                     pack_bf16x2(__uint_as_float(rr[8 * c + 2]) * inv_l,
-                                                 __uint_as_float(rr[8 * c + 3]) * inv_l),
-                                     pack_bf16x2(__uint_as_float(rr[8 * c + 4]) * inv_l,
-                                                 __uint_as_float(rr[8 * c + 5]) * inv_l),
-                                     pack_bf16x2(__uint_as_float(rr[8 * c + 6]) * inv_l,
-                                                 __uint_as_float(rr[8 * c + 7]) * inv_l));
-                    fence_proxy_async_smem();
-                    mbar_arrive(stage_ready(x));
-                    if (leader) {
-                        if (!mbar_wait(stage_ready(x), stage_uses & 1u, abort)) {
-                            ok = false;
-                            break;
-                        }
-                        tma_store_3d(&p.tm_o, stage, db * 64, h, q0 + i * BQ);
-                        bulk_commit_group();
-                        bulk_wait_group_read0();          // the stage may be rewritten after this
-                        mbar_arrive(stage_free(x));
-                    }
-                    ++stage_uses;
+            for (int cb = 0; cb < D / 32; ++cb) {
+                uint32_t rr[32];
+                tmem_ld32(o_addr + cb * 32, rr);
+                tmem_wait_ld_r(rr);
+                const uint32_t row = wstage + lane * 64;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    st_shared_v4(row + ((c ^ ((lane >> 1) & 3)) << 4),
+                                 pack_bf16x2(__uint_as_float(rr[8 * c + 0]) * inv_l,
+                                             __uint_as_float(rr[8 * c + 1]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(rr[8 * c + 2]) * inv_l,
+                                             __uint_as_float(rr[8 * c + 3]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(rr[8 * c + 4]) * inv_l,
+                                             __uint_as_float(rr[8 * c + 5]) * inv_l),
+                                 pack_bf16x2(__uint_as_float(rr[8 * c + 6]) * inv_l,
+                                             __uint_as_float(rr[8 * c + 7]) * inv_l));
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int rw = 8 * k + (lane >> 2), ch = lane & 3;
+                    const int rt = quarter * 32 + rw;          // row within the tile
+                    const uint4 v = ld_shared_v4(wstage + rw * 64 + ((ch ^ ((rw >> 1) & 3)) << 4));
+                    if (rt < tile_rows)
+                        *reinterpret_cast<uint4 *>(out_tile + static_cast<long long>(rt) * H * D +
+                                                   cb * 32 + ch * 8) = v;
                 }
-                if (!ok)
-                    break;
-            } else {
-                uint4 *dst = reinterpret_cast<uint4 *>(out + (tok * H + h) * D);
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(o_addr + c * 32, rr);
-                    tmem_wait_ld_r(rr);
-                    if (row_valid) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            uint4 v;
-                            v.x = pack_bf16x2(__uint_as_float(rr[8 * e + 0]) * inv_l,
-                                              __uint_as_float(rr[8 * e + 1]) * inv_l);
-                            v.y = pack_bf16x2(__uint_as_float(rr[8 * e + 2]) * inv_l,
-                                              __uint_as_float(rr[8 * e + 3]) * inv_l);
-                            v.z = pack_bf16x2(__uint_as_float(rr[8 * e + 4]) * inv_l,
-                                              __uint_as_float(rr[8 * e + 5]) * inv_l);
-                            v.w = pack_bf16x2(__uint_as_float(rr[8 * e + 6]) * inv_l,
-                                              __uint_as_float(rr[8 * e + 7]) * inv_l);
-                            dst[c * 4 + e] = v;
-                        }
-                    }
-                }
+                __syncwarp();
             }
         }
-        // Every bulk store this warpgroup issued must complete before the CTA exits.
-        if (leader)
-            bulk_wait_group0();
     }
 
     tc_fence_before();
