@@ -110,6 +110,28 @@ def test_large_logits_rescale_path(vfa, oracle_mod):
     _check_full(vfa, oracle_mod, case)
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rising_scores_rescale_every_half(vfa, oracle_mod, D, causal):
+    # q . k grows by more than 2^8 (in log2 units) every 64 keys along each
+    # sequence: every half-tile after the first moves the reference max, so the
+    # kernel takes its rescale-and-redo path in both halves of every key tile
+    # (including the rescale that must wait for the first half's O += P V).
+    lengths = [700, 300, 64, 129]
+    case = W.make_varlen("rising", lengths, lengths, 2, D, causal, 0.3, value_seed=D + 7)
+    q = case.q.float()
+    k = case.k.float()
+    q[:, :, 0] = 4.0
+    cq = case.cu_seqlens_q
+    for b in range(len(lengths)):
+        pos = torch.arange(lengths[b], dtype=torch.float32)
+        k[int(cq[b]):int(cq[b + 1]), :, 0] = (0.5 * pos)[:, None]
+    case.q = q.to(torch.bfloat16)
+    case.k = k.to(torch.bfloat16)
+    case.v = W.bf16_normal(tuple(case.v.shape), 1.0, torch.Generator().manual_seed(D))
+    _check_full(vfa, oracle_mod, case)
+
+
 def test_single_long_sequence_sampled(vfa, oracle_mod):
     case = W.make_varlen("long", [16384], [16384], 1, 128, True, 1.0, value_seed=4)
     out, lse, status = run_varlen(vfa, case)
