@@ -67,8 +67,8 @@ def _load():
         lib.oracle_varlen_fwd_rows.restype = i32
         lib.oracle_decode_init.argtypes = [P, P, P, i32, i32, i32]
         lib.oracle_decode_init.restype = None
-        lib.oracle_decode_step.argtypes = [P, P, P, i64, P, P, i32, i32, i32, i32, i32, i32,
-                                           P, P, P, i32]
+        lib.oracle_decode_step.argtypes = [P, P, P, i64, P, P, P, i32, i32, i32, i32, i32, i32,
+                                           f64, P, P, P, i32]
         lib.oracle_decode_step.restype = i32
         lib.oracle_decode_finalize.argtypes = [P, P, i32, i32, i32, P]
         lib.oracle_decode_finalize.restype = None
@@ -161,12 +161,17 @@ class DecodeState:
 
 
 def decode_step(state: DecodeState, q, k_pool, v_pool, tile_blocks, tile_block_counts,
-                num_kv_heads: int, block_size: int, nthreads: int = 0) -> int:
-    """One step_tile over every sequence; updates `state` in place.  Returns threads used."""
+                num_kv_heads: int, block_size: int, nthreads: int = 0,
+                tile_token_counts=None, scale: float = 0.0) -> int:
+    """One step_tile over every sequence; updates `state` in place.  Returns threads used.
+
+    tile_token_counts (optional, [S]): absorb only the first n tokens of each
+    sequence's listed blocks; scale <= 0 means 1/sqrt(head_dim)."""
     lib = _load()
     qb, kb, vb = _bits(q), _bits(k_pool), _bits(v_pool)
     tb = _i32(tile_blocks)
     tc = _i32(tile_block_counts)
+    tt = None if tile_token_counts is None else _i32(tile_token_counts)
     S, Hq, D = state.num_seqs, state.num_q_heads, state.head_dim
     cap = tb.shape[1] if tb.ndim == 2 else (tb.size // S if S else 0)
     per_block = block_size * num_kv_heads * D
@@ -174,8 +179,9 @@ def decode_step(state: DecodeState, q, k_pool, v_pool, tile_blocks, tile_block_c
     if kb.size != num_blocks * per_block or vb.size != kb.size or qb.size != S * Hq * D:
         raise ValueError("decode_step: inconsistent buffer sizes")
     n = lib.oracle_decode_step(_ptr(qb), _ptr(kb), _ptr(vb), num_blocks, _ptr(tb), _ptr(tc),
-                               int(cap), S, Hq, num_kv_heads, D, block_size,
-                               _ptr(state.m), _ptr(state.l), _ptr(state.o), int(nthreads))
+                               None if tt is None else _ptr(tt), int(cap), S, Hq, num_kv_heads,
+                               D, block_size, float(scale), _ptr(state.m), _ptr(state.l),
+                               _ptr(state.o), int(nthreads))
     if n <= 0:
         raise ValueError(f"oracle_decode_step rejected its arguments ({n})")
     return int(n)

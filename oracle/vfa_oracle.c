@@ -29,8 +29,12 @@
  *   - an empty key set gives out = 0 and lse = -FLT_MAX (the kernel's
  *     inv_l = 0 and lse epilogue);
  *   - lse is the natural log of sum_j exp(scale * q.k_j);
- *   - decode: every listed block contributes all block_size tokens; the
- *     decode scale is 1/sqrt(head_dim).
+ *   - decode: every listed block contributes all block_size tokens and the
+ *     decode scale is 1/sqrt(head_dim), as in step_tile_ref; two optional
+ *     arguments extend it for callers whose contexts end inside a block or
+ *     who use another scale: a per-sequence count of the tile's tokens to
+ *     absorb (the first n of the listed blocks' tokens, in list order) and an
+ *     explicit scale.
  *
  * Parity pins (independent checks of this file) live in tests/: a numpy
  * brute-force formulation, torch float64 scaled_dot_product_attention, the
@@ -320,6 +324,8 @@ void oracle_decode_init(double *m, double *l, double *o, int num_seqs,
 typedef struct {
     const uint16_t *q, *k_pool, *v_pool;
     const int32_t *tile_blocks, *tile_block_counts;
+    const int32_t *tile_token_counts;      /* NULL: every token of every listed block */
+    double scale;
     int tile_capacity, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
     int64_t num_blocks;
     double *m, *l, *o;
@@ -329,8 +335,9 @@ typedef struct {
 
 /*
  * One (sequence, q head) of one tile step.  The tokens of this step are all
- * block_size tokens of every block id tile_blocks[seq, 0:count].  With x
- * their logits (q . k) / sqrt(D), the state that describes every token seen
+ * block_size tokens of every block id tile_blocks[seq, 0:count] (or the first
+ * tile_token_counts[seq] of them, taken in list order).  With x their logits
+ * scale * (q . k), the state that describes every token seen
  * so far is m = max x, l = sum exp(x - m), o = sum exp(x - m) v; merging the
  * old state with this step's set re-expresses both sums at the new max.
  */
@@ -340,20 +347,21 @@ static void decode_unit(decode_job *job, int seq, int qh, double *x, int64_t *to
     const int group = Hq / Hkv;
     const int kh = qh / group;
     const int count = job->tile_block_counts[seq];
-    const double inv_sqrt_d = 1.0 / sqrt((double)D);
+    const int64_t take = job->tile_token_counts ? job->tile_token_counts[seq]
+                                                : (int64_t)count * job->block_size;
     const size_t sidx = (size_t)seq * Hq + qh;
     const uint16_t *qrow = job->q + sidx * D;
 
     int64_t n = 0;
     for (int b = 0; b < count; ++b) {
         const int64_t blk = job->tile_blocks[(size_t)seq * job->tile_capacity + b];
-        for (int t = 0; t < job->block_size; ++t) {
+        for (int t = 0; t < job->block_size && n < take; ++t) {
             /* pool layout [num_blocks, block_size, num_kv_heads, head_dim] */
             const int64_t base = ((blk * job->block_size + t) * Hkv + kh) * (int64_t)D;
             double dot = 0.0;
             for (int d = 0; d < D; ++d)
                 dot += bf16_to_double(qrow[d]) * bf16_to_double(job->k_pool[base + d]);
-            x[n] = dot * inv_sqrt_d;
+            x[n] = dot * job->scale;
             tok[n] = base;
             ++n;
         }
@@ -407,14 +415,16 @@ static void *decode_worker(void *arg)
 /*
  * One tile step over every sequence.  q: [S, Hq, D]; pools: [num_blocks,
  * block_size, Hkv, D] (bf16 bits); tile_blocks: [S, tile_capacity];
- * tile_block_counts: [S].  m, l: double [S, Hq]; o: double [S, Hq, D] (in/out).
+ * tile_block_counts: [S]; tile_token_counts: [S] or NULL; scale <= 0 means
+ * 1/sqrt(D).  m, l: double [S, Hq]; o: double [S, Hq, D] (in/out).
  * Returns threads used (> 0) or < 0 on bad arguments (nothing is changed).
  */
 int oracle_decode_step(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
                        int64_t num_blocks, const int32_t *tile_blocks,
-                       const int32_t *tile_block_counts, int tile_capacity, int num_seqs,
-                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                       double *m, double *l, double *o, int nthreads)
+                       const int32_t *tile_block_counts, const int32_t *tile_token_counts,
+                       int tile_capacity, int num_seqs, int num_q_heads, int num_kv_heads,
+                       int head_dim, int block_size, double scale, double *m, double *l,
+                       double *o, int nthreads)
 {
     if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 ||
         block_size < 1 || tile_capacity < 0 || num_q_heads % num_kv_heads != 0)
@@ -428,11 +438,16 @@ int oracle_decode_step(const uint16_t *q, const uint16_t *k_pool, const uint16_t
             if (blk < 0 || blk >= num_blocks)
                 return -3;
         }
+        if (tile_token_counts &&
+            (tile_token_counts[s] < 0 || (int64_t)tile_token_counts[s] > (int64_t)c * block_size))
+            return -4;
     }
     decode_job job;
     memset(&job, 0, sizeof job);
     job.q = q; job.k_pool = k_pool; job.v_pool = v_pool;
     job.tile_blocks = tile_blocks; job.tile_block_counts = tile_block_counts;
+    job.tile_token_counts = tile_token_counts;
+    job.scale = scale > 0.0 ? scale : 1.0 / sqrt((double)head_dim);
     job.tile_capacity = tile_capacity; job.num_seqs = num_seqs;
     job.num_q_heads = num_q_heads; job.num_kv_heads = num_kv_heads;
     job.head_dim = head_dim; job.block_size = block_size; job.num_blocks = num_blocks;

@@ -8,7 +8,11 @@
     head qh / group, scale 1/sqrt(D);
   * a numpy brute force that walks the block table token by token;
   * closed forms: no blocks ever gives m = -inf, l = 0, out = 0; one block
-    whose keys are all equal gives the mean of its V rows.
+    whose keys are all equal gives the mean of its V rows;
+  * the extension for contexts that end inside a block and an explicit scale
+    (per-step token counts): a numpy brute force over the first ctx tokens of
+    each sequence in block-table order, with that scale; full token counts
+    reproduce the default bit for bit.
 """
 import math
 
@@ -138,3 +142,76 @@ def test_rejects_out_of_range_block_and_count(oracle_mod):
         oracle_mod.decode_step(st, case.q, case.k_pool, case.v_pool, tb, badc,
                                case.num_kv_heads, case.block_size)
     assert np.all(np.isneginf(st.m)) and np.all(st.l == 0)   # nothing was changed
+
+
+def _brute_exact(case, scale):
+    q = case.q.double().numpy()
+    K = case.k_pool.double().numpy()
+    V = case.v_pool.double().numpy()
+    g = case.num_q_heads // case.num_kv_heads
+    out = np.zeros((case.num_seqs, case.num_q_heads, case.head_dim))
+    lse = np.full((case.num_seqs, case.num_q_heads), -np.inf)
+    for s in range(case.num_seqs):
+        toks = [(blk, t) for blk in case.block_table[s] for t in range(case.block_size)]
+        toks = toks[:case.context_lengths[s]]
+        if not toks:
+            continue
+        for qh in range(case.num_q_heads):
+            kh = qh // g
+            ks = np.array([K[b, t, kh] for b, t in toks])
+            vs = np.array([V[b, t, kh] for b, t in toks])
+            x = scale * (ks @ q[s, qh])
+            w = np.exp(x - x.max())
+            out[s, qh] = (w[:, None] * vs).sum(0) / w.sum()
+            lse[s, qh] = x.max() + math.log(w.sum())
+    return out, lse
+
+
+def _run_exact(oracle_mod, case, scale):
+    st = oracle_mod.DecodeState(case.num_seqs, case.num_q_heads, case.head_dim)
+    for t in range(case.num_steps):
+        tb, tc = case.tile(t)
+        oracle_mod.decode_step(st, case.q, case.k_pool, case.v_pool, tb, tc, case.num_kv_heads,
+                               case.block_size, tile_token_counts=case.tile_tokens(t),
+                               scale=scale)
+    return st, oracle_mod.decode_finalize(st)
+
+
+@pytest.mark.parametrize("scale", [0.0, 0.37])
+def test_exact_context_and_scale_match_brute_force(oracle_mod, scale):
+    n_blocks = (3, 1, 7, 2, 5, 1)
+    ctx = [9, 1, 27, 8, 17, 0]          # partial last blocks, a one-token and an empty context
+    rng = np.random.default_rng(7)
+    perm = rng.permutation(sum(n_blocks)).astype(np.int32)
+    case = W.make_decode("exact", list(n_blocks), 8, 2, 16, 4, 2, perm, value_seed=7,
+                         context_lengths=ctx)
+    eff = scale if scale > 0 else 1.0 / math.sqrt(case.head_dim)
+    st, out = _run_exact(oracle_mod, case, scale)
+    ref, ref_lse = _brute_exact(case, eff)
+    np.testing.assert_allclose(out, ref, atol=1e-12, rtol=0)
+    live = np.isfinite(ref_lse)
+    assert live.sum() == 5 * 8
+    np.testing.assert_allclose(st.m[live] + np.log(st.l[live]), ref_lse[live], atol=1e-12)
+    assert np.all(st.l[~live] == 0) and np.all(np.isneginf(st.m[~live]))
+
+
+def test_full_token_counts_equal_default(oracle_mod):
+    case = _small(3)
+    a = oracle_mod.DecodeState(case.num_seqs, case.num_q_heads, case.head_dim)
+    b = a.copy()
+    for t in range(case.num_steps):
+        tb, tc = case.tile(t)
+        oracle_mod.decode_step(a, case.q, case.k_pool, case.v_pool, tb, tc, case.num_kv_heads,
+                               case.block_size)
+        oracle_mod.decode_step(b, case.q, case.k_pool, case.v_pool, tb, tc, case.num_kv_heads,
+                               case.block_size, tile_token_counts=tc * case.block_size)
+    assert np.array_equal(a.m, b.m) and np.array_equal(a.l, b.l) and np.array_equal(a.o, b.o)
+
+
+def test_token_count_beyond_listed_blocks_rejected(oracle_mod):
+    case = _small(4)
+    st = oracle_mod.DecodeState(case.num_seqs, case.num_q_heads, case.head_dim)
+    tb, tc = case.tile(0)
+    with pytest.raises(ValueError):
+        oracle_mod.decode_step(st, case.q, case.k_pool, case.v_pool, tb, tc, case.num_kv_heads,
+                               case.block_size, tile_token_counts=tc * case.block_size + 1)

@@ -213,6 +213,14 @@ class DecodeCase:
             tb[s, :len(part)] = part
         return tb, tc
 
+    def tile_tokens(self, t: int) -> np.ndarray:
+        """Tokens of step t that lie inside each sequence's context: int32 [S],
+        min(tile_block_counts * block_size, context_length - t * cap * block_size), >= 0."""
+        tb, tc = self.tile(t)
+        start = t * self.tile_capacity * self.block_size
+        ctx = np.asarray(self.context_lengths, dtype=np.int64)
+        return np.clip(ctx - start, 0, tc.astype(np.int64) * self.block_size).astype(np.int32)
+
     def kv_bytes(self) -> int:
         """Bytes of K and V the listed blocks hold (each read once)."""
         per_block = self.block_size * self.num_kv_heads * self.head_dim * 2
