@@ -208,25 +208,40 @@ vfa_status vfa_paged_decode_init(float *m, float *l, float *o, int num_seqs, int
  * exp(logit - m), o = sum exp(logit - m) v over all tokens absorbed so far
  * (m is in natural-log units).  Each KV block is read once per kv head group.
  *
+ * Two arguments extend the page's step (which always takes whole blocks and
+ * 1/sqrt(head_dim)) for contexts that end inside their last block and for
+ * other scales: with tile_token_counts the step absorbs only the first
+ * tile_token_counts[s] tokens of sequence s's listed blocks, in list order
+ * (blocks holding none of them are not read); softmax_scale > 0 replaces
+ * 1/sqrt(head_dim).
+ *
  * q                 device bf16 [num_seqs, num_q_heads, head_dim].
  * k_pool, v_pool    device bf16 [num_blocks, block_size, num_kv_heads, head_dim].
  * tile_blocks       device int32 [num_seqs, tile_capacity]: physical block ids.
  * tile_block_counts device int32 [num_seqs]: entries used per row (0 = no-op).
+ * tile_token_counts nullable device int32 [num_seqs]: tokens to absorb, in
+ *                   [0, tile_block_counts[s] * block_size] (0 = no-op); NULL
+ *                   = every token of every listed block.
+ * softmax_scale     logit scale; <= 0 means 1/sqrt(head_dim); NaN or inf is
+ *                   VFA_ERR_INVALID_ARG.
  * m, l, o           the state (in/out), as in vfa_paged_decode_init.
  * device_status     nullable device int32 [1]: a count outside
- *                   [0, tile_capacity] or a block id outside [0, num_blocks)
- *                   stores VFA_ERR_BAD_BLOCK here (first error wins) and that
- *                   sequence's state is left unchanged for this step.
+ *                   [0, tile_capacity], a token count outside its range or a
+ *                   block id outside [0, num_blocks) stores VFA_ERR_BAD_BLOCK
+ *                   here (first error wins) and that sequence's state is left
+ *                   unchanged for this step.
  *
  * Supported: head_dim in {64, 128, 256}; block_size == 16;
- * num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8}; num_blocks <= 2^26.
  */
 vfa_status vfa_paged_decode_step(const void *q, const void *k_pool, const void *v_pool,
                                  int num_blocks, const int32_t *tile_blocks,
-                                 const int32_t *tile_block_counts, int tile_capacity,
+                                 const int32_t *tile_block_counts,
+                                 const int32_t *tile_token_counts, int tile_capacity,
                                  int num_seqs, int num_q_heads, int num_kv_heads,
-                                 int head_dim, int block_size, float *m, float *l, float *o,
-                                 int32_t *device_status, vfa_stream_t stream);
+                                 int head_dim, int block_size, float softmax_scale, float *m,
+                                 float *l, float *o, int32_t *device_status,
+                                 vfa_stream_t stream);
 
 /*
  * finalize_ref of "attention_ref.rs": out = bf16(o * (l > 0 ? 1 / l : 0)),

@@ -30,26 +30,29 @@ def _gpu_state(case):
     return m, l, o
 
 
-def _run_gpu(vfa, case, status=None):
+def _run_gpu(vfa, case, status=None, exact=False, scale=0.0):
     m, l, o = _gpu_state(case)
     q, kp, vp = case.q.cuda(), case.k_pool.cuda(), case.v_pool.cuda()
     vfa.decode_init(m, l, o, status)
     for t in range(case.num_steps):
         tb, tc = case.tile(t)
+        tt = torch.from_numpy(case.tile_tokens(t)).cuda() if exact else None
         vfa.decode_step(q, kp, vp, torch.from_numpy(tb).cuda(), torch.from_numpy(tc).cuda(),
-                        m, l, o, status)
+                        m, l, o, status, tile_token_counts=tt, softmax_scale=scale)
     out = vfa.decode_finalize(l, o)
     torch.cuda.synchronize()
     return m.cpu().double().numpy(), l.cpu().double().numpy(), o.cpu().double().numpy(), \
         out.float().cpu().double().numpy()
 
 
-def _run_oracle(oracle_mod, case):
+def _run_oracle(oracle_mod, case, exact=False, scale=0.0):
     st = oracle_mod.DecodeState(case.num_seqs, case.num_q_heads, case.head_dim)
     for t in range(case.num_steps):
         tb, tc = case.tile(t)
         oracle_mod.decode_step(st, case.q, case.k_pool, case.v_pool, tb, tc, case.num_kv_heads,
-                               case.block_size)
+                               case.block_size,
+                               tile_token_counts=case.tile_tokens(t) if exact else None,
+                               scale=scale)
     return st, oracle_mod.decode_finalize(st)
 
 
@@ -167,3 +170,45 @@ def test_bad_block_table_sets_status_and_skips_sequence(vfa, bad):
     assert vfa.read_status(status) == vfa.VFA_ERR_BAD_BLOCK
     assert torch.all(torch.isneginf(m[1])) and torch.all(l[1] == 0) and torch.all(o[1] == 0)
     assert torch.all(l[0] > 0)                     # the valid sequence was still updated
+
+
+# Contexts that end inside their last block, and an explicit scale: the step
+# absorbs only the first tile_token_counts[s] tokens of the listed blocks.
+
+def test_decode_workload_exact_context(vfa, oracle_mod):
+    case = W.decode(1)
+    assert any(c % case.block_size for c in case.context_lengths)
+    m, l, o, out = _run_gpu(vfa, case, exact=True)
+    st, ref = _run_oracle(oracle_mod, case, exact=True)
+    _compare(m, l, o, out, st, ref, "decode exact context")
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 8, 64), (32, 8, 128), (8, 1, 128), (16, 2, 256),
+                                      (4, 2, 64)])
+@pytest.mark.parametrize("scale", [0.0, 0.05])
+def test_decode_exact_context_shapes(vfa, oracle_mod, Hq, Hkv, D, scale):
+    rng = np.random.default_rng(Hq + D)
+    n_blocks = [5, 0, 1, 13, 7, 3]
+    ctx = [5 * 16 - 3, 0, 1, 13 * 16, 7 * 16 - 15, 33]       # 33: last listed block unread
+    perm = rng.permutation(sum(n_blocks)).astype(np.int32)
+    case = W.make_decode("exact", n_blocks, Hq, Hkv, D, 16, 3, perm, value_seed=D + Hq,
+                         context_lengths=ctx)
+    m, l, o, out = _run_gpu(vfa, case, exact=True, scale=scale)
+    st, ref = _run_oracle(oracle_mod, case, exact=True, scale=scale)
+    _compare(m, l, o, out, st, ref, f"decode exact {Hq}/{Hkv}/{D} scale {scale}")
+
+
+def test_bad_token_count_sets_status_and_skips_sequence(vfa):
+    case = W.make_decode("badtok", [2, 2], 4, 2, 64, 16, 2, np.arange(4, dtype=np.int32), 3)
+    m, l, o = _gpu_state(case)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    vfa.decode_init(m, l, o, status)
+    tb, tc = case.tile(0)
+    tt = torch.tensor([2 * 16 + 1, 20], dtype=torch.int32, device="cuda")   # seq 0: too many
+    vfa.decode_step(case.q.cuda(), case.k_pool.cuda(), case.v_pool.cuda(),
+                    torch.from_numpy(tb).cuda(), torch.from_numpy(tc).cuda(), m, l, o, status,
+                    tile_token_counts=tt)
+    torch.cuda.synchronize()
+    assert int(status.item()) == vfa.VFA_ERR_BAD_BLOCK
+    assert torch.all(torch.isneginf(m[0])) and torch.all(l[0] == 0)      # left as it was
+    assert torch.all(torch.isfinite(m[1])) and torch.all(l[1] > 0)       # the valid one ran

@@ -78,15 +78,18 @@ def test_host_rejects_null_and_unsupported(vfa):
                           fake, 1 << 20, nul)
     assert st == vfa.VFA_ERR_INVALID_ARG and b"aligned" in L.vfa_last_error()
     # decode: unsupported group size / block size / head_dim
-    st = L.vfa_paged_decode_step(fake, fake, fake, 4, fake, fake, 2, 1, 12, 4, 128, 16, fake,
-                                 fake, fake, nul, nul)
+    st = L.vfa_paged_decode_step(fake, fake, fake, 4, fake, fake, nul, 2, 1, 12, 4, 128, 16, 0.0,
+                                 fake, fake, fake, nul, nul)
     assert st == vfa.VFA_ERR_UNSUPPORTED
-    st = L.vfa_paged_decode_step(fake, fake, fake, 4, fake, fake, 2, 1, 8, 2, 128, 32, fake,
-                                 fake, fake, nul, nul)
+    st = L.vfa_paged_decode_step(fake, fake, fake, 4, fake, fake, nul, 2, 1, 8, 2, 128, 32, 0.0,
+                                 fake, fake, fake, nul, nul)
     assert st == vfa.VFA_ERR_UNSUPPORTED
-    st = L.vfa_paged_decode_step(fake, fake, fake, 4, fake, fake, 2, 1, 9, 2, 128, 16, fake,
-                                 fake, fake, nul, nul)
+    st = L.vfa_paged_decode_step(fake, fake, fake, 4, fake, fake, nul, 2, 1, 9, 2, 128, 16, 0.0,
+                                 fake, fake, fake, nul, nul)
     assert st == vfa.VFA_ERR_INVALID_ARG
+    st = L.vfa_paged_decode_step(fake, fake, fake, 4, fake, fake, nul, 2, 1, 8, 2, 128, 16,
+                                 float("nan"), fake, fake, fake, nul, nul)
+    assert st == vfa.VFA_ERR_INVALID_ARG and b"softmax_scale" in L.vfa_last_error()
     st = L.vfa_paged_decode_finalize(fake, fake, 1, 1, 12, fake, nul)
     assert st == vfa.VFA_ERR_INVALID_ARG
 

@@ -3,6 +3,7 @@
 // frees device memory.
 #include <cfloat>
 #include <cstdarg>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -354,13 +355,18 @@ static vfa_status check_decode_args(const void *q, const void *k_pool, const voi
 
 vfa_status vfa_paged_decode_step(const void *q, const void *k_pool, const void *v_pool,
                                  int num_blocks, const int32_t *tile_blocks,
-                                 const int32_t *tile_block_counts, int tile_capacity,
+                                 const int32_t *tile_block_counts,
+                                 const int32_t *tile_token_counts, int tile_capacity,
                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                                 int block_size, float *m, float *l, float *o,
-                                 int32_t *device_status, vfa_stream_t stream)
+                                 int block_size, float softmax_scale, float *m, float *l,
+                                 float *o, int32_t *device_status, vfa_stream_t stream)
 {
     if (!q || !m || !l || !o)
         return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
+    if (!std::isfinite(softmax_scale))
+        return fail(VFA_ERR_INVALID_ARG, "softmax_scale must be finite");
+    if (tile_token_counts && !aligned(tile_token_counts, 4))
+        return fail(VFA_ERR_INVALID_ARG, "tile_token_counts must be 4-byte aligned");
     vfa_status st = check_decode_args(q, k_pool, v_pool, num_blocks, tile_blocks,
                                       tile_block_counts, tile_capacity, num_seqs, num_q_heads,
                                       num_kv_heads, head_dim, block_size);
@@ -388,6 +394,10 @@ vfa_status vfa_paged_decode_step(const void *q, const void *k_pool, const void *
     a.l = l;
     a.o = o;
     a.status = device_status;
+    a.tile_token_counts = tile_token_counts;
+    a.scale_log2 = static_cast<float>(
+        (softmax_scale > 0.f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt(double(head_dim))) *
+        1.4426950408889634);
     vfa::DecodeMaps maps;
     if ((st = encode_pool_map(&maps.tm_k, k_pool, num_blocks, block_size, num_kv_heads,
                               head_dim)) ||

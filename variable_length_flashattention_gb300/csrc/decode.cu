@@ -203,14 +203,20 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int count = a.tile_block_counts[s];
-    if (!tile_row_valid(a.tile_blocks, count, a.tile_capacity, a.num_blocks, s)) {
+    // Tokens to absorb: the first n_tok of the listed blocks' tokens.
+    const int n_tok = a.tile_token_counts ? a.tile_token_counts[s]
+                      : (count >= 0 && count <= a.tile_capacity ? count * kBlockSize : 0);
+    const bool tok_bad = n_tok < 0 || static_cast<long long>(n_tok) >
+                                          static_cast<long long>(count) * kBlockSize;
+    if (!tile_row_valid(a.tile_blocks, count, a.tile_capacity, a.num_blocks, s) || tok_bad) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         if (threadIdx.x == 0 && a.status)
             atomicCAS(a.status, 0, VFA_ERR_BAD_BLOCK);
         return;
     }
-    if (count == 0)
+    if (count == 0 || n_tok == 0)
         return;                                 // an empty tile leaves the state as it was
+    const int nb = (n_tok + kBlockSize - 1) / kBlockSize;   // blocks holding those tokens
 
     const uint32_t ring = smem_u32(dsm);
     auto stage_k = [&](int st) { return ring + st * C::STAGE; };
@@ -245,7 +251,7 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
         atomicAdd(&s_fills[st], 1);
     };
     if (threadIdx.x == 0)
-        for (int k = 0; k < NS && k < count; ++k)
+        for (int k = 0; k < NS && k < nb; ++k)
             issue(k);
 
     // Q^T fragments (B operand of S = K Q^T): head n = lane / 4, columns
@@ -262,7 +268,7 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
             qb[kt][1] = n_q < G ? qrow[(16 * kt + 8 + 2 * t4) / 2] : 0u;
         }
     }
-    const float sc = kLog2e * rsqrtf(static_cast<float>(D));   // logits in log2 units
+    const float sc = a.scale_log2;                            // logits in log2 units
 
     // This lane's two heads: 2 * t4 and 2 * t4 + 1.
     float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
@@ -277,7 +283,7 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
     const int k_row = ((mi & 1) << 3) + mr, k_chunk = mi >> 1;     // K: A of S = K Q^T
     const int v_row = ((mi >> 1) << 3) + mr, v_chunk = mi & 1;     // V^T: A of O^T += V^T P
 
-    for (int k = warp; k < count; k += kStepWarps) {
+    for (int k = warp; k < nb; k += kStepWarps) {
         const int st = k % NS;
         const int fill = k / NS;
         // The parity wait below is only unambiguous once this stage's previous
@@ -296,6 +302,20 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
             mma_bf16(sacc, af, qb[kt][0], qb[kt][1]);
         }
         // sacc: tokens lane/4 (0, 1) and lane/4 + 8 (2, 3); heads 2*t4 (0, 2), 2*t4+1 (1, 3).
+        // Tokens past n_tok (only in the last block) get weight zero; every
+        // block read holds at least one token that counts.
+        const int valid = n_tok - k * kBlockSize;
+        if (valid < kBlockSize) {
+            const int t0 = lane >> 2;
+            if (t0 >= valid) {
+                sacc[0] = -INFINITY;
+                sacc[1] = -INFINITY;
+            }
+            if (t0 + 8 >= valid) {
+                sacc[2] = -INFINITY;
+                sacc[3] = -INFINITY;
+            }
+        }
         float bm[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -341,7 +361,7 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
         __syncwarp();
         if (lane == 0) {
             ++s_used[st];
-            if (k + NS < count)
+            if (k + NS < nb)
                 issue(k + NS);
         }
     }

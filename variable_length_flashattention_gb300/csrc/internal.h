@@ -98,6 +98,8 @@ cudaError_t launch_prefill_pair(int head_dim, const PrefillArgs &a, int grid,
 struct DecodeStepArgs {
     const void *q, *k_pool, *v_pool;
     const int32_t *tile_blocks, *tile_block_counts;
+    const int32_t *tile_token_counts;   // nullable: every token of every listed block
+    float scale_log2;                   // logit scale * log2(e), > 0
     int num_blocks, tile_capacity, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
     float *m, *l, *o;
     int32_t *status;      // nullable

@@ -45,7 +45,8 @@ SIGNATURES = [
     ("vfa_varlen_fwd_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
     ("vfa_varlen_schedule", _I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _S, _P]),
     ("vfa_paged_decode_init", _I, [_P, _P, _P, _I, _I, _I, _P, _P]),
-    ("vfa_paged_decode_step", _I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    ("vfa_paged_decode_step", _I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
+                                   _P, _P, _P, _P]),
     ("vfa_paged_decode_finalize", _I, [_P, _P, _I, _I, _I, _P, _P]),
     ("vfa_debug_paged_gather", _I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     ("vfa_read_status", _I, [_P, _P, _P]),
@@ -234,8 +235,13 @@ def decode_init(m: torch.Tensor, l: torch.Tensor, o: torch.Tensor,
 def decode_step(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                 tile_blocks: torch.Tensor, tile_block_counts: torch.Tensor,
                 m: torch.Tensor, l: torch.Tensor, o: torch.Tensor,
-                status: Optional[torch.Tensor] = None, stream=None):
+                status: Optional[torch.Tensor] = None, stream=None,
+                tile_token_counts: Optional[torch.Tensor] = None, softmax_scale: float = 0.0):
+    """vfa_paged_decode_step; tile_token_counts (int32 [S], optional) and
+    softmax_scale (<= 0: 1/sqrt(D)) as in include/vfa.h."""
     _need(q, torch.bfloat16, "q")
+    if tile_token_counts is not None:
+        _need(tile_token_counts, torch.int32, "tile_token_counts")
     _need(k_pool, torch.bfloat16, "k_pool")
     _need(v_pool, torch.bfloat16, "v_pool")
     _need(tile_blocks, torch.int32, "tile_blocks")
@@ -245,9 +251,10 @@ def decode_step(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
     if D2 != D or v_pool.shape != k_pool.shape or tile_blocks.shape[0] != S:
         raise ValueError("inconsistent decode shapes")
     _check(lib().vfa_paged_decode_step(_ptr(q), _ptr(k_pool), _ptr(v_pool), nb, _ptr(tile_blocks),
-                                       _ptr(tile_block_counts), tile_blocks.shape[1], S, Hq, Hkv,
-                                       D, bs, _ptr(m), _ptr(l), _ptr(o), _ptr(status),
-                                       _stream(stream)))
+                                       _ptr(tile_block_counts), _ptr(tile_token_counts),
+                                       tile_blocks.shape[1], S, Hq, Hkv, D, bs,
+                                       float(softmax_scale), _ptr(m), _ptr(l), _ptr(o),
+                                       _ptr(status), _stream(stream)))
 
 
 def decode_finalize(l: torch.Tensor, o: torch.Tensor, out: Optional[torch.Tensor] = None,
