@@ -60,10 +60,10 @@ def _load():
         P = ctypes.c_void_p
         i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
         lib.oracle_default_threads.restype = i32
-        lib.oracle_varlen_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, f64, i32, P, P, i32]
+        lib.oracle_varlen_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, i32, P, P, i32]
         lib.oracle_varlen_fwd.restype = i32
-        lib.oracle_varlen_fwd_rows.argtypes = [P, P, P, P, P, i32, i32, i32, f64, i32, P, i64,
-                                               P, P, i32]
+        lib.oracle_varlen_fwd_rows.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, i32, P,
+                                               i64, P, P, i32]
         lib.oracle_varlen_fwd_rows.restype = i32
         lib.oracle_decode_init.argtypes = [P, P, P, i32, i32, i32]
         lib.oracle_decode_init.restype = None
@@ -101,29 +101,35 @@ def default_threads() -> int:
 
 
 def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_dim: int,
-               softmax_scale: float, causal: bool, nthreads: int = 0):
-    """Full forward.  Returns (out float64 [Tq,H,D], lse float64 [Tq,H], threads used)."""
+               softmax_scale: float, causal: bool, nthreads: int = 0,
+               num_kv_heads: int = 0):
+    """Full forward.  Returns (out float64 [Tq,H,D], lse float64 [Tq,H], threads used).
+
+    k, v hold num_kv_heads heads (default: num_heads); query head h reads kv
+    head h // (num_heads // num_kv_heads)."""
     lib = _load()
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     cq, ck = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
     batch = len(cq) - 1
     tq = int(cq[-1])
+    hkv = num_kv_heads or num_heads
     if qb.size != tq * num_heads * head_dim:
         raise ValueError("q size does not match cu_seqlens_q[-1] * H * D")
-    if kb.size != int(ck[-1]) * num_heads * head_dim or vb.size != kb.size:
-        raise ValueError("k/v size does not match cu_seqlens_k[-1] * H * D")
+    if kb.size != int(ck[-1]) * hkv * head_dim or vb.size != kb.size:
+        raise ValueError("k/v size does not match cu_seqlens_k[-1] * Hkv * D")
     out = np.zeros((tq, num_heads, head_dim), dtype=np.float64)
     lse = np.zeros((tq, num_heads), dtype=np.float64)
     n = lib.oracle_varlen_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cq), _ptr(ck), batch,
-                              num_heads, head_dim, float(softmax_scale), int(bool(causal)),
-                              _ptr(out), _ptr(lse), int(nthreads))
+                              num_heads, hkv, head_dim, float(softmax_scale),
+                              int(bool(causal)), _ptr(out), _ptr(lse), int(nthreads))
     if n <= 0:
         raise ValueError(f"oracle_varlen_fwd rejected its arguments ({n})")
     return out, lse, int(n)
 
 
 def varlen_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_dim: int,
-                    softmax_scale: float, causal: bool, rows, nthreads: int = 0):
+                    softmax_scale: float, causal: bool, rows, nthreads: int = 0,
+                    num_kv_heads: int = 0):
     """Selected rows.  rows: int array [n, 2] of (packed token, head).
 
     Returns (out float64 [n, D], lse float64 [n], threads used)."""
@@ -134,7 +140,8 @@ def varlen_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_di
     out = np.zeros((r.shape[0], head_dim), dtype=np.float64)
     lse = np.zeros((r.shape[0],), dtype=np.float64)
     n = lib.oracle_varlen_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cq), _ptr(ck),
-                                   len(cq) - 1, num_heads, head_dim, float(softmax_scale),
+                                   len(cq) - 1, num_heads, num_kv_heads or num_heads, head_dim,
+                                   float(softmax_scale),
                                    int(bool(causal)), _ptr(r), r.shape[0], _ptr(out), _ptr(lse),
                                    int(nthreads))
     if n <= 0:

@@ -77,16 +77,17 @@ int oracle_default_threads(void)
 typedef struct {
     const uint16_t *q, *k, *v;
     const int32_t *cu_q, *cu_k;
-    int batch, num_heads, head_dim;
+    int batch, num_heads, num_kv_heads, head_dim;
     double scale;
     int causal;
 } varlen_problem;
 
 /*
- * One query row: local row i of sequence b, head h.
+ * One query row: local row i of sequence b, head h; its keys and values are
+ * those of kv head kh = h / (H / Hkv) (kh = h when Hkv = H).
  *
  *   K_set = { j : 0 <= j < Lk_b  and  (not causal or j <= i) }
- *   s_j   = scale * sum_d q[tq, h, d] * k[cu_k[b] + j, h, d]
+ *   s_j   = scale * sum_d q[tq, h, d] * k[cu_k[b] + j, kh, d]
  *   empty K_set: out = 0, lse = -FLT_MAX
  *   else: M = max_j s_j, Z = sum_j exp(s_j - M),
  *         out[d] = sum_j exp(s_j - M) * v[cu_k[b] + j, h, d] / Z,
@@ -98,7 +99,8 @@ static void varlen_row(const varlen_problem *p, int b, int i, int h,
                        double *out_row, double *lse_out,
                        double *s, double *w, int *kidx)
 {
-    const int D = p->head_dim, H = p->num_heads;
+    const int D = p->head_dim, H = p->num_heads, Hkv = p->num_kv_heads;
+    const int kh = h / (H / Hkv);
     const int64_t tq = (int64_t)p->cu_q[b] + i;
     const int64_t k0 = p->cu_k[b];
     const int Lk = p->cu_k[b + 1] - p->cu_k[b];
@@ -120,7 +122,7 @@ static void varlen_row(const varlen_problem *p, int b, int i, int h,
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
             dot += bf16_to_double(p->q[packed_index(tq, h, d, H, D)]) *
-                   bf16_to_double(p->k[packed_index(tk, h, d, H, D)]);
+                   bf16_to_double(p->k[packed_index(tk, kh, d, Hkv, D)]);
         s[a] = p->scale * dot;
     }
     double M = s[0];
@@ -135,7 +137,7 @@ static void varlen_row(const varlen_problem *p, int b, int i, int h,
     for (int d = 0; d < D; ++d) {
         double acc = 0.0;
         for (int a = 0; a < n; ++a)
-            acc += w[a] * bf16_to_double(p->v[packed_index(k0 + kidx[a], h, d, H, D)]);
+            acc += w[a] * bf16_to_double(p->v[packed_index(k0 + kidx[a], kh, d, Hkv, D)]);
         out_row[d] = acc / Z;
     }
     *lse_out = M + log(Z);
@@ -250,20 +252,23 @@ static int max_len(const int32_t *cu, int batch)
 }
 
 /*
- * Full varlen forward.  q: [cu_q[B], H, D], k/v: [cu_k[B], H, D] (bf16 bits).
+ * Full varlen forward.  q: [cu_q[B], H, D], k/v: [cu_k[B], Hkv, D] (bf16 bits),
+ * H a multiple of Hkv (query head h reads kv head h / (H / Hkv)).
  * out: double [cu_q[B], H, D]; lse: double [cu_q[B], H].
  * Returns the number of threads used (> 0), or < 0 on bad arguments.
  */
 int oracle_varlen_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                       const int32_t *cu_q, const int32_t *cu_k, int batch,
-                      int num_heads, int head_dim, double scale, int causal,
+                      int num_heads, int num_kv_heads, int head_dim, double scale, int causal,
                       double *out, double *lse, int nthreads)
 {
-    if (batch < 1 || num_heads < 1 || head_dim < 1)
+    if (batch < 1 || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads != 0 ||
+        head_dim < 1)
         return -1;
     if (check_cu(cu_q, batch) || check_cu(cu_k, batch))
         return -2;
-    varlen_problem p = {q, k, v, cu_q, cu_k, batch, num_heads, head_dim, scale, causal != 0};
+    varlen_problem p = {q, k, v, cu_q, cu_k, batch, num_heads, num_kv_heads, head_dim, scale,
+                        causal != 0};
     varlen_job job;
     memset(&job, 0, sizeof job);
     job.p = &p;
@@ -281,11 +286,12 @@ int oracle_varlen_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
  */
 int oracle_varlen_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                            const int32_t *cu_q, const int32_t *cu_k, int batch,
-                           int num_heads, int head_dim, double scale, int causal,
-                           const int64_t *rows, int64_t n_rows,
+                           int num_heads, int num_kv_heads, int head_dim, double scale,
+                           int causal, const int64_t *rows, int64_t n_rows,
                            double *out_rows, double *lse_rows, int nthreads)
 {
-    if (batch < 1 || num_heads < 1 || head_dim < 1 || n_rows < 0)
+    if (batch < 1 || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads != 0 ||
+        head_dim < 1 || n_rows < 0)
         return -1;
     if (check_cu(cu_q, batch) || check_cu(cu_k, batch))
         return -2;
@@ -293,7 +299,8 @@ int oracle_varlen_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t 
         if (rows[2 * r] < 0 || rows[2 * r] >= cu_q[batch] ||
             rows[2 * r + 1] < 0 || rows[2 * r + 1] >= num_heads)
             return -3;
-    varlen_problem p = {q, k, v, cu_q, cu_k, batch, num_heads, head_dim, scale, causal != 0};
+    varlen_problem p = {q, k, v, cu_q, cu_k, batch, num_heads, num_kv_heads, head_dim, scale,
+                        causal != 0};
     varlen_job job;
     memset(&job, 0, sizeof job);
     job.p = &p;

@@ -3,6 +3,8 @@
 Each check ties the fp64 oracle to something other than itself:
   * a brute-force numpy formulation (whole masked score matrix, softmax
     without the max shift, lse = log of the plain sum);
+  * grouped-query attention (K/V with fewer heads than Q): torch float64
+    scaled_dot_product_attention on K/V heads expanded by repeat_interleave;
   * torch float64 scaled_dot_product_attention per sequence (its causal mask
     is tril(ones(L, S)), i.e. top-left) and torch.logsumexp;
   * the worked examples the implementation plan's CPU tests print
@@ -253,3 +255,38 @@ def test_rejects_bad_cu_seqlens(oracle_mod):
     with pytest.raises(ValueError):
         oracle_mod.varlen_fwd(x, x, x, np.array([1, 4], np.int32), np.array([0, 4], np.int32),
                               1, 8, 0.5, False)
+
+
+@pytest.mark.parametrize("Hkv", [1, 2])
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_kv_heads_match_torch_sdpa_float64(oracle_mod, causal, Hkv):
+    lq, lk = [3, 40, 17, 1], [3, 25, 60, 1]
+    H, D = 8, 32
+    case = _case(lq, lk, H, D, causal, seed=11)
+    k = case.k[:, :Hkv].contiguous()           # K/V with Hkv heads
+    v = case.v[:, :Hkv].contiguous()
+    out, lse, _ = oracle_mod.varlen_fwd(case.q, k, v, case.cu_seqlens_q, case.cu_seqlens_k, H, D,
+                                        case.softmax_scale, causal, num_kv_heads=Hkv)
+    g = H // Hkv
+    q, kd, vd = case.q.double(), k.double(), v.double()
+    for b in range(case.batch):
+        q0, q1 = int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1])
+        k0, k1 = int(case.cu_seqlens_k[b]), int(case.cu_seqlens_k[b + 1])
+        qs = q[q0:q1].transpose(0, 1)
+        ks = kd[k0:k1].repeat_interleave(g, dim=1).transpose(0, 1)   # head h <- kv head h // g
+        vs = vd[k0:k1].repeat_interleave(g, dim=1).transpose(0, 1)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qs, ks, vs, is_causal=causal, scale=case.softmax_scale)
+        np.testing.assert_allclose(out[q0:q1], ref.transpose(0, 1).numpy(), rtol=1e-10, atol=1e-12)
+        s_ = case.softmax_scale * (qs @ ks.transpose(1, 2))
+        if causal:
+            s_ = s_.masked_fill(~torch.ones(q1 - q0, k1 - k0, dtype=torch.bool).tril(),
+                                float("-inf"))
+        np.testing.assert_allclose(lse[q0:q1], torch.logsumexp(s_, dim=-1).transpose(0, 1).numpy(),
+                                   rtol=1e-12, atol=1e-12)
+    rng = np.random.default_rng(1)
+    rows = np.stack([rng.integers(0, case.total_q, 40), rng.integers(0, H, 40)], axis=1)
+    ro, rl, _ = oracle_mod.varlen_fwd_rows(case.q, k, v, case.cu_seqlens_q, case.cu_seqlens_k, H,
+                                           D, case.softmax_scale, causal, rows, num_kv_heads=Hkv)
+    np.testing.assert_array_equal(ro, out[rows[:, 0], rows[:, 1]])
+    np.testing.assert_array_equal(rl, lse[rows[:, 0], rows[:, 1]])
