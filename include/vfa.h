@@ -84,7 +84,9 @@ vfa_status vfa_varlen_fwd_tile_shape(int head_dim, int *block_q, int *block_k, i
  * work list on the device and covers every query row.
  *
  * q            device bf16 [total_q, num_heads, head_dim], packed row-major.
- * k, v         device bf16 [total_k, num_heads, head_dim].
+ * k, v         device bf16 [total_k, num_kv_heads, head_dim]; query head h
+ *              reads kv head h / (num_heads / num_kv_heads) (grouped-query
+ *              attention; num_kv_heads == num_heads is the plan's layout).
  * cu_seqlens_q device int32 [batch + 1]: 0, running sums of the q lengths;
  *              cu_seqlens_q[batch] == total_q.  Sequence b owns q rows
  *              [cu_seqlens_q[b], cu_seqlens_q[b+1]).
@@ -105,7 +107,8 @@ vfa_status vfa_varlen_fwd_tile_shape(int head_dim, int *block_q, int *block_k, i
  *              bytes, 256-byte aligned; reused across calls; calls that share
  *              one workspace must be stream-ordered.
  *
- * Supported: head_dim in {64, 128, 256}; num_heads >= 1; batch >= 1; q, k,
+ * Supported: head_dim in {64, 128, 256}; num_heads >= 1, a multiple of
+ * num_kv_heads >= 1; batch >= 1; q, k,
  * v, out 16-byte aligned.  Sequences of length 0 are allowed (no rows, or no
  * keys).  Device-detected: cu_seqlens not starting at 0, decreasing, not
  * ending at total_q / total_k, or a q length above max_seqlen_q
@@ -114,9 +117,9 @@ vfa_status vfa_varlen_fwd_tile_shape(int head_dim, int *block_q, int *block_k, i
 vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
                           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                           int total_q, int total_k, int max_seqlen_q, int batch,
-                          int num_heads, int head_dim, float softmax_scale, int causal,
-                          void *out, float *lse, void *workspace, size_t workspace_bytes,
-                          vfa_stream_t stream);
+                          int num_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                          int causal, void *out, float *lse, void *workspace,
+                          size_t workspace_bytes, vfa_stream_t stream);
 
 /*
  * vfa_varlen_fwd without a caller workspace.  The pages have no counterpart:
@@ -148,9 +151,9 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
 vfa_status vfa_varlen_fwd_noalloc(const void *q, const void *k, const void *v,
                                   const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                                   int total_q, int total_k, int max_seqlen_q, int batch,
-                                  int num_heads, int head_dim, float softmax_scale, int causal,
-                                  void *out, float *lse, int32_t *device_status,
-                                  vfa_stream_t stream);
+                                  int num_heads, int num_kv_heads, int head_dim,
+                                  float softmax_scale, int causal, void *out, float *lse,
+                                  int32_t *device_status, vfa_stream_t stream);
 
 /*
  * The device tile scheduler alone (the first kernel vfa_varlen_fwd runs),

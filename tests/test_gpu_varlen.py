@@ -132,6 +132,23 @@ def test_rising_scores_rescale_every_half(vfa, oracle_mod, D, causal):
     _check_full(vfa, oracle_mod, case)
 
 
+@pytest.mark.parametrize("H,Hkv,D", [(8, 2, 128), (8, 1, 64), (4, 2, 256), (16, 4, 128)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_kv_heads(vfa, oracle_mod, H, Hkv, D, causal):
+    # K/V with fewer heads than Q: query head h reads kv head h // (H // Hkv)
+    lq, lk = [300, 7, 129, 0, 64, 1], [300, 40, 129, 5, 200, 1]
+    case = W.make_varlen("gqa", lq, lk, H, D, causal, 1.0, value_seed=10 * H + Hkv + D)
+    case.k = case.k[:, :Hkv].contiguous()
+    case.v = case.v[:, :Hkv].contiguous()
+    out, lse, status = run_varlen(vfa, case)
+    assert status == 0
+    ref_out, ref_lse, _ = oracle_mod.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens_q,
+                                                case.cu_seqlens_k, H, D, case.softmax_scale,
+                                                causal, num_kv_heads=Hkv)
+    assert_out_close(out, ref_out, f"gqa {H}/{Hkv}/{D}")
+    assert_lse_close(lse, ref_lse, f"gqa {H}/{Hkv}/{D}")
+
+
 def test_single_long_sequence_sampled(vfa, oracle_mod):
     case = W.make_varlen("long", [16384], [16384], 1, 128, True, 1.0, value_seed=4)
     out, lse, status = run_varlen(vfa, case)

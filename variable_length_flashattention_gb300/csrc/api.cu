@@ -213,15 +213,19 @@ vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_se
 
 vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
                           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int total_q,
-                          int total_k, int max_seqlen_q, int batch, int num_heads, int head_dim,
-                          float softmax_scale, int causal, void *out, float *lse, void *workspace,
-                          size_t workspace_bytes, vfa_stream_t stream)
+                          int total_k, int max_seqlen_q, int batch, int num_heads,
+                          int num_kv_heads, int head_dim, float softmax_scale, int causal,
+                          void *out, float *lse, void *workspace, size_t workspace_bytes,
+                          vfa_stream_t stream)
 {
     if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out || !lse || !workspace)
         return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
     if (batch < 1 || num_heads < 1 || total_q < 0 || total_k < 0 || max_seqlen_q < 0)
         return fail(VFA_ERR_INVALID_ARG, "bad size argument (batch %d, heads %d, totals %d/%d)",
                     batch, num_heads, total_q, total_k);
+    if (num_kv_heads < 1 || num_heads % num_kv_heads != 0)
+        return fail(VFA_ERR_INVALID_ARG, "num_heads %d is not a multiple of num_kv_heads %d",
+                    num_heads, num_kv_heads);
     if (!supported_head_dim(head_dim))
         return fail(VFA_ERR_UNSUPPORTED, "head_dim %d not supported (64, 128, 256)", head_dim);
     if (!(softmax_scale >= 0.f) || softmax_scale > FLT_MAX)
@@ -282,8 +286,8 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     vfa::PrefillArgs pa;
     memset(&pa, 0, sizeof pa);
     if ((st = encode_packed_map(&pa.tm_q, q, total_q, num_heads, head_dim, bq)) ||
-        (st = encode_packed_map(&pa.tm_k, k, total_k, num_heads, head_dim, bk)) ||
-        (st = encode_packed_map(&pa.tm_v, v, total_k, num_heads, head_dim, bk)))
+        (st = encode_packed_map(&pa.tm_k, k, total_k, num_kv_heads, head_dim, bk)) ||
+        (st = encode_packed_map(&pa.tm_v, v, total_k, num_kv_heads, head_dim, bk)))
         return st;
     pa.cu_q = cu_seqlens_q;
     pa.cu_k = cu_seqlens_k;
@@ -294,6 +298,7 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     pa.out = out;
     pa.lse = lse;
     pa.num_heads = num_heads;
+    pa.kv_group = num_heads / num_kv_heads;
     // The kernel takes row maxima on raw scores, which needs a positive scale;
     // a zero scale (uniform weights) becomes the smallest normal float, which
     // gives the same weights for every finite score.

@@ -77,6 +77,7 @@ struct PrefillArgs {
     void *out;
     float *lse;
     int num_heads;
+    int kv_group;         // query heads per kv head: K/V of head h live at h / kv_group
     float scale_log2;     // softmax_scale * log2(e), > 0
     int causal;
 };

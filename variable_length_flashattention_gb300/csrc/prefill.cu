@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     mbar_arrive_expect_tx(k_full(st), C::KV_BYTES);
                     for (int db = 0; db < DB; ++db)
                         tma_load_3d(sK + st * C::KV_BYTES + db * (BK * 128), &p.tm_k, k_full(st),
-                                    db * 64, h, k_row0 + j * BK);
+                                    db * 64, h / p.kv_group, k_row0 + j * BK);
                     ++kfills;
                     if (!mbar_wait(v_empty(st), ((vfills / NS) & 1u) ^ 1u, abort)) {
                         ok = false;
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     mbar_arrive_expect_tx(v_full(st), C::KV_BYTES);
                     for (int db = 0; db < DB; ++db)
                         tma_load_3d(sV + st * C::KV_BYTES + db * (BK * 128), &p.tm_v, v_full(st),
-                                    db * 64, h, k_row0 + j * BK);
+                                    db * 64, h / p.kv_group, k_row0 + j * BK);
                     ++vfills;
                 }
                 if (!ok)

@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(k_full(st), C::KV_BYTES);
                     for (int db = 0; db < DB; ++db)
                         tma_load_3d(sK + st * C::KV_BYTES + db * (BK * 128), &p.tm_k, k_full(st),
-                                    db * 64, h, seq.w + j * BK);
+                                    db * 64, h / p.kv_group, seq.w + j * BK);
                     ++kfills;
                 }
                 if (!ok)
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(v_full(st), C::KV_BYTES);
                     for (int db = 0; db < DB; ++db)
                         tma_load_3d(sV + st * C::KV_BYTES + db * (BK * 128), &p.tm_v, v_full(st),
-                                    db * 64, h, seq.w + j * BK);
+                                    db * 64, h / p.kv_group, seq.w + j * BK);
                     ++vfills;
                 }
                 if (!ok)

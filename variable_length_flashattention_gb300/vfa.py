@@ -41,8 +41,10 @@ SIGNATURES = [
     ("vfa_version", ctypes.c_char_p, []),
     ("vfa_varlen_fwd_workspace_bytes", _S, [_I, _I, _I, _I, _I]),
     ("vfa_varlen_fwd_tile_shape", _I, [_I, _P, _P, _P]),
-    ("vfa_varlen_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _S, _P]),
-    ("vfa_varlen_fwd_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
+    ("vfa_varlen_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _S,
+                            _P]),
+    ("vfa_varlen_fwd_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P,
+                                    _P, _P]),
     ("vfa_varlen_schedule", _I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _S, _P]),
     ("vfa_paged_decode_init", _I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     ("vfa_paged_decode_step", _I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
@@ -137,14 +139,19 @@ def varlen_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: 
                causal: bool, out: Optional[torch.Tensor] = None,
                lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                stream=None):
-    """out bf16 [Tq, H, D], lse f32 [Tq, H] = varlen attention forward (vfa_varlen_fwd)."""
+    """out bf16 [Tq, H, D], lse f32 [Tq, H] = varlen attention forward (vfa_varlen_fwd).
+
+    k, v may hold fewer heads than q (a divisor of H): query head h reads kv
+    head h // (H // Hkv)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, torch.bfloat16, n)
     _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
     _need(cu_seqlens_k, torch.int32, "cu_seqlens_k")
-    if q.dim() != 3 or k.shape != v.shape or k.dim() != 3 or q.shape[1:] != k.shape[1:]:
-        raise ValueError("q, k, v must be [tokens, heads, head_dim] with matching heads/head_dim")
+    if (q.dim() != 3 or k.shape != v.shape or k.dim() != 3 or q.shape[2] != k.shape[2] or
+            q.shape[1] % k.shape[1] != 0):
+        raise ValueError("q, k, v must be [tokens, heads, head_dim]; k/v heads must divide q heads")
     total_q, H, D = q.shape
+    Hkv = k.shape[1]
     total_k = k.shape[0]
     batch = cu_seqlens_q.numel() - 1
     if cu_seqlens_k.numel() != batch + 1:
@@ -158,7 +165,7 @@ def varlen_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: 
     if workspace is None:
         workspace = alloc_workspace(batch, total_q, total_k, H, D, device=q.device)
     st = lib().vfa_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
-                              total_q, total_k, int(max_seqlen_q), batch, H, D,
+                              total_q, total_k, int(max_seqlen_q), batch, H, Hkv, D,
                               float(softmax_scale), int(bool(causal)), _ptr(out), _ptr(lse),
                               _ptr(workspace), workspace.numel() * workspace.element_size(),
                               _stream(stream))
@@ -184,7 +191,8 @@ def varlen_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     total_q, H, D = q.shape
     st = lib().vfa_varlen_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q),
                                       _ptr(cu_seqlens_k), total_q, k.shape[0], int(max_seqlen_q),
-                                      cu_seqlens_q.numel() - 1, H, D, float(softmax_scale),
+                                      cu_seqlens_q.numel() - 1, H, k.shape[1], D,
+                                      float(softmax_scale),
                                       int(bool(causal)), _ptr(out), _ptr(lse), _ptr(device_status),
                                       _stream(stream))
     _check(st)
