@@ -105,8 +105,10 @@ def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_dim: in
                num_kv_heads: int = 0):
     """Full forward.  Returns (out float64 [Tq,H,D], lse float64 [Tq,H], threads used).
 
-    k, v hold num_kv_heads heads (default: num_heads); query head h reads kv
-    head h // (num_heads // num_kv_heads)."""
+    causal: 0 (or False) no mask, 1 (or True) top-left, 2 bottom-right (local
+    key j visible to local query i iff j <= i + Lk - Lq).  k, v hold
+    num_kv_heads heads (default: num_heads); query head h reads kv head
+    h // (num_heads // num_kv_heads)."""
     lib = _load()
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     cq, ck = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
@@ -121,7 +123,7 @@ def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_dim: in
     lse = np.zeros((tq, num_heads), dtype=np.float64)
     n = lib.oracle_varlen_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cq), _ptr(ck), batch,
                               num_heads, hkv, head_dim, float(softmax_scale),
-                              int(bool(causal)), _ptr(out), _ptr(lse), int(nthreads))
+                              int(causal), _ptr(out), _ptr(lse), int(nthreads))
     if n <= 0:
         raise ValueError(f"oracle_varlen_fwd rejected its arguments ({n})")
     return out, lse, int(n)
@@ -142,7 +144,7 @@ def varlen_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_di
     n = lib.oracle_varlen_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cq), _ptr(ck),
                                    len(cq) - 1, num_heads, num_kv_heads or num_heads, head_dim,
                                    float(softmax_scale),
-                                   int(bool(causal)), _ptr(r), r.shape[0], _ptr(out), _ptr(lse),
+                                   int(causal), _ptr(r), r.shape[0], _ptr(out), _ptr(lse),
                                    int(nthreads))
     if n <= 0:
         raise ValueError(f"oracle_varlen_fwd_rows rejected its arguments ({n})")

@@ -9,9 +9,10 @@ schedule here is the plain rule the scheduler kernel must reproduce:
     sequence with Lq_b > 0, where tile i holds local query rows
     [i*BQ, min(Lq_b, (i+1)*BQ));
   * its cost is the number of BK-wide key tiles that hold at least one key
-    the tile's rows may see: ceil(Lk_b / BK) without a mask, and with the
-    top-left causal mask ceil(min(Lk_b, min(Lq_b, (i+1)*BQ)) / BK), because
-    the tile's last row min(Lq_b, (i+1)*BQ) - 1 sees keys 0 .. that row;
+    the tile's rows may see: ceil(Lk_b / BK) without a mask, and with a
+    causal mask ceil(clamp(min(Lq_b, (i+1)*BQ) + off, 0, Lk_b) / BK), because
+    the tile's last row min(Lq_b, (i+1)*BQ) - 1 sees keys 0 .. that row + off
+    (off = 0 for the top-left mask, Lk_b - Lq_b for the bottom-right one);
   * the items of one (b, h) form a group and stay next to each other, so
     the q tiles that share a sequence's keys and values run at the same time;
   * groups are ordered by their largest item cost, then their total cost,
@@ -35,16 +36,19 @@ def _ceil_div(a: int, b: int) -> int:
     return -(-a // b)
 
 
-def tile_cost(lq: int, lk: int, i: int, bq: int, bk: int, causal: bool) -> int:
-    """Number of key tiles that q tile i of a (lq, lk) sequence must visit."""
+def tile_cost(lq: int, lk: int, i: int, bq: int, bk: int, causal) -> int:
+    """Number of key tiles that q tile i of a (lq, lk) sequence must visit.
+
+    causal: 0 / False no mask, 1 / True top-left, 2 bottom-right."""
     if not causal:
         return _ceil_div(lk, bk)
+    off = lk - lq if int(causal) == 2 else 0
     last_row_plus_one = min(lq, (i + 1) * bq)
-    return _ceil_div(min(lk, last_row_plus_one), bk)
+    return _ceil_div(max(0, min(lk, last_row_plus_one + off)), bk)
 
 
 def schedule(cu_seqlens_q, cu_seqlens_k, num_heads: int, bq: int, bk: int,
-             causal: bool, pair: bool = False) -> np.ndarray:
+             causal, pair: bool = False) -> np.ndarray:
     """The ordered work list, int32 [n_items, 8] of (b, i_a, h, cost_a, i_b, cost_b, 0, 0)."""
     cq = [int(x) for x in cu_seqlens_q]
     ck = [int(x) for x in cu_seqlens_k]

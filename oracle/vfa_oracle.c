@@ -23,7 +23,9 @@
  * Readings taken where the pages are silent or disagree (each is also listed
  * in the design notes):
  *   - causal alignment is top-left: local key j is visible to local query i
- *     iff j <= i (the kernel compares local positions k_pos > q_pos);
+ *     iff j <= i (the kernel compares local positions k_pos > q_pos); the
+ *     bottom-right alignment (the last query sees every key: j <= i + Lk - Lq)
+ *     is offered as a second causal mode;
  *   - masked keys carry weight exactly zero (the kernel's -FLT_MAX sentinel
  *     and the CPU reference's -inf sentinel both give that);
  *   - an empty key set gives out = 0 and lse = -FLT_MAX (the kernel's
@@ -86,7 +88,9 @@ typedef struct {
  * One query row: local row i of sequence b, head h; its keys and values are
  * those of kv head kh = h / (H / Hkv) (kh = h when Hkv = H).
  *
- *   K_set = { j : 0 <= j < Lk_b  and  (not causal or j <= i) }
+ *   K_set = { j : 0 <= j < Lk_b  and  (causal == 0 or j <= i + off) }
+ *   off   = 0 for causal == 1 (top-left), Lk_b - Lq_b for causal == 2
+ *           (bottom-right)
  *   s_j   = scale * sum_d q[tq, h, d] * k[cu_k[b] + j, kh, d]
  *   empty K_set: out = 0, lse = -FLT_MAX
  *   else: M = max_j s_j, Z = sum_j exp(s_j - M),
@@ -104,10 +108,12 @@ static void varlen_row(const varlen_problem *p, int b, int i, int h,
     const int64_t tq = (int64_t)p->cu_q[b] + i;
     const int64_t k0 = p->cu_k[b];
     const int Lk = p->cu_k[b + 1] - p->cu_k[b];
+    const int Lq = p->cu_q[b + 1] - p->cu_q[b];
+    const int off = p->causal == 2 ? Lk - Lq : 0;
 
     int n = 0;
     for (int j = 0; j < Lk; ++j) {
-        if (p->causal && j > i)
+        if (p->causal && j > i + off)
             continue;                       /* masked: weight exactly zero */
         kidx[n++] = j;
     }
@@ -263,12 +269,12 @@ int oracle_varlen_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                       double *out, double *lse, int nthreads)
 {
     if (batch < 1 || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads != 0 ||
-        head_dim < 1)
+        head_dim < 1 || causal < 0 || causal > 2)
         return -1;
     if (check_cu(cu_q, batch) || check_cu(cu_k, batch))
         return -2;
     varlen_problem p = {q, k, v, cu_q, cu_k, batch, num_heads, num_kv_heads, head_dim, scale,
-                        causal != 0};
+                        causal};
     varlen_job job;
     memset(&job, 0, sizeof job);
     job.p = &p;
@@ -291,7 +297,7 @@ int oracle_varlen_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t 
                            double *out_rows, double *lse_rows, int nthreads)
 {
     if (batch < 1 || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads != 0 ||
-        head_dim < 1 || n_rows < 0)
+        head_dim < 1 || n_rows < 0 || causal < 0 || causal > 2)
         return -1;
     if (check_cu(cu_q, batch) || check_cu(cu_k, batch))
         return -2;
@@ -300,7 +306,7 @@ int oracle_varlen_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t 
             rows[2 * r + 1] < 0 || rows[2 * r + 1] >= num_heads)
             return -3;
     varlen_problem p = {q, k, v, cu_q, cu_k, batch, num_heads, num_kv_heads, head_dim, scale,
-                        causal != 0};
+                        causal};
     varlen_job job;
     memset(&job, 0, sizeof job);
     job.p = &p;

@@ -16,15 +16,16 @@ from variable_length_flashattention_gb300 import workloads as W
 
 def _brute_cost(lq, lk, i, bq, bk, causal):
     rows = range(i * bq, min(lq, (i + 1) * bq))
+    off = lk - lq if causal == 2 else 0          # 2: bottom-right alignment
     n = 0
     for j in range(-(-lk // bk)):
         keys = range(j * bk, min(lk, (j + 1) * bk))
-        if any((not causal) or c <= r for r in rows for c in keys):
+        if any((not causal) or c <= r + off for r in rows for c in keys):
             n += 1
     return n
 
 
-@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("causal", [False, True, 2])
 @pytest.mark.parametrize("bq,bk", [(128, 128), (128, 64), (64, 128)])
 def test_cost_matches_enumeration(oracle_mod, causal, bq, bk):
     rng = np.random.default_rng(0)
@@ -52,7 +53,7 @@ def _tiles(items):
 
 
 @pytest.mark.parametrize("pair", [False, True])
-@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("causal", [False, True, 2])
 def test_coverage_and_order(oracle_mod, causal, pair):
     lq, lk = W.cross_lengths(3)
     H = 5

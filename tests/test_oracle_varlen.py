@@ -290,3 +290,36 @@ def test_grouped_kv_heads_match_torch_sdpa_float64(oracle_mod, causal, Hkv):
                                            D, case.softmax_scale, causal, rows, num_kv_heads=Hkv)
     np.testing.assert_array_equal(ro, out[rows[:, 0], rows[:, 1]])
     np.testing.assert_array_equal(rl, lse[rows[:, 0], rows[:, 1]])
+
+
+def test_bottom_right_causal_matches_torch_sdpa_float64(oracle_mod):
+    # causal == 2: local key j visible to local query i iff j <= i + Lk - Lq
+    lq, lk = [3, 40, 60, 1, 25], [3, 25, 17, 9, 0]
+    H, D = 4, 32
+    case = _case(lq, lk, H, D, True, seed=13)
+    out, lse, _ = oracle_mod.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens_q,
+                                        case.cu_seqlens_k, H, D, case.softmax_scale, 2)
+    q, k, v = case.q.double(), case.k.double(), case.v.double()
+    for b in range(case.batch):
+        q0, q1 = int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1])
+        k0, k1 = int(case.cu_seqlens_k[b]), int(case.cu_seqlens_k[b + 1])
+        Lq, Lk = q1 - q0, k1 - k0
+        allowed = torch.ones(Lq, Lk, dtype=torch.bool).tril(diagonal=Lk - Lq)
+        for r in range(Lq):
+            if Lk == 0 or not allowed[r].any():
+                assert np.all(out[q0 + r] == 0) and np.all(lse[q0 + r] == -oracle_mod.FLT_MAX)
+        live = allowed.any(dim=1)
+        if not live.any():
+            continue
+        qs = q[q0:q1].transpose(0, 1)[:, live]
+        ks = k[k0:k1].transpose(0, 1)
+        vs = v[k0:k1].transpose(0, 1)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qs, ks, vs, attn_mask=allowed[live], scale=case.softmax_scale)
+        np.testing.assert_allclose(out[q0:q1][live.numpy()], ref.transpose(0, 1).numpy(),
+                                   rtol=1e-10, atol=1e-12)
+        s_ = (case.softmax_scale * (qs @ ks.transpose(1, 2))).masked_fill(~allowed[live],
+                                                                          float("-inf"))
+        np.testing.assert_allclose(lse[q0:q1][live.numpy()],
+                                   torch.logsumexp(s_, dim=-1).transpose(0, 1).numpy(),
+                                   rtol=1e-12, atol=1e-12)
