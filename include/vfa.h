@@ -95,8 +95,12 @@ vfa_status vfa_varlen_fwd_tile_shape(int head_dim, int *block_q, int *block_k, i
  *              the tensors to the TMA engine).
  * max_seqlen_q an upper bound on every q length (checked on the device).
  * softmax_scale the factor applied to q.k before the softmax.
- * causal       non-zero: top-left causal mask in local positions -- local key
- *              j is visible to local query i iff j <= i.
+ * causal       0: no mask; 1: top-left causal mask in local positions --
+ *              local key j is visible to local query i iff j <= i (the
+ *              plan's kernel); 2: bottom-right -- j <= i + Lk_b - Lq_b, so the
+ *              last query sees every key (a query block at the end of a longer
+ *              key sequence) and rows with i + Lk_b - Lq_b < 0 see none.
+ *              Other values: VFA_ERR_INVALID_ARG.
  * out          device bf16 [total_q, num_heads, head_dim]: out = sum_j p_j v_j /
  *              sum_j p_j, rounded to nearest even; 0 for a query with no
  *              visible key.
@@ -161,8 +165,8 @@ vfa_status vfa_varlen_fwd_noalloc(const void *q, const void *k, const void *v,
  *
  * A tile is q tile i (local rows [i*block_q, min(Lq_b, (i+1)*block_q))) of
  * sequence b and head h; its cost is the number of key tiles it visits
- * (ceil(Lk_b / block_k); causal: ceil(min(Lk_b, min(Lq_b, (i+1)*block_q)) /
- * block_k)).  The tiles of one (b, h) stay together; groups are ordered by
+ * (ceil(Lk_b / block_k); causal: ceil(clamp(min(Lq_b, (i+1)*block_q) + off, 0,
+ * Lk_b) / block_k), off = 0 for causal == 1 and Lk_b - Lq_b for causal == 2).  The tiles of one (b, h) stay together; groups are ordered by
  * their largest cost, then total cost (descending), then (b, h); inside a
  * group by cost descending, then i.  With pair_tiles != 0 two consecutive
  * tiles of a group form one item (what vfa_varlen_fwd uses for head_dim <=

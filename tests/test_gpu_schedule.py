@@ -39,7 +39,7 @@ def test_workload_schedules(vfa, oracle_mod, name):
 
 
 @pytest.mark.parametrize("seed", range(6))
-@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("causal", [False, True, 2])
 def test_random_mixes(vfa, oracle_mod, seed, causal):
     rng = np.random.default_rng(seed)
     B = int(rng.integers(1, 3000 if seed == 5 else 60))

@@ -149,6 +149,23 @@ def test_grouped_kv_heads(vfa, oracle_mod, H, Hkv, D, causal):
     assert_lse_close(lse, ref_lse, f"gqa {H}/{Hkv}/{D}")
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_bottom_right_causal(vfa, oracle_mod, D):
+    # causal == 2: local key j visible to local query i iff j <= i + Lk - Lq
+    # (chunked-prefill shape: a query block at the end of a longer key sequence,
+    # and the reverse, where the first rows see no key at all)
+    lq = [64, 300, 129, 500, 1, 0, 200]
+    lk = [1000, 300, 40, 128, 77, 5, 0]
+    case = W.make_varlen("bottom-right", lq, lk, 2, D, True, 1.0, value_seed=D + 3)
+    case.causal = 2
+    out, lse, status = run_varlen(vfa, case)
+    assert status == 0
+    ref_out, ref_lse, _ = oracle_mod.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens_q,
+                                                case.cu_seqlens_k, 2, D, case.softmax_scale, 2)
+    assert_out_close(out, ref_out, f"bottom-right D={D}")
+    assert_lse_close(lse, ref_lse, f"bottom-right D={D}")
+
+
 def test_single_long_sequence_sampled(vfa, oracle_mod):
     case = W.make_varlen("long", [16384], [16384], 1, 128, True, 1.0, value_seed=4)
     out, lse, status = run_varlen(vfa, case)

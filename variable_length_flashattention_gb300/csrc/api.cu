@@ -172,6 +172,8 @@ vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_se
     if (batch < 1 || num_heads < 1 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
         block_q < 1 || block_k < 1 || items_capacity < 0)
         return fail(VFA_ERR_INVALID_ARG, "bad size argument");
+    if (causal < 0 || causal > 2)
+        return fail(VFA_ERR_INVALID_ARG, "causal must be 0, 1 (top-left) or 2 (bottom-right)");
     if (!aligned(items, 16) || !aligned(scratch, 8))
         return fail(VFA_ERR_INVALID_ARG, "items must be 16-byte and scratch 8-byte aligned");
     if ((block_k & (block_k - 1)) != 0 || block_q % block_k != 0)
@@ -196,7 +198,7 @@ vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_se
     a.num_heads = num_heads;
     a.block_q = block_q;
     a.block_k = block_k;
-    a.causal = causal != 0;
+    a.causal = causal;
     a.pair = pair_tiles != 0;
     a.items = reinterpret_cast<int4 *>(items);
     a.item_capacity = items_capacity;
@@ -226,6 +228,8 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     if (num_kv_heads < 1 || num_heads % num_kv_heads != 0)
         return fail(VFA_ERR_INVALID_ARG, "num_heads %d is not a multiple of num_kv_heads %d",
                     num_heads, num_kv_heads);
+    if (causal < 0 || causal > 2)
+        return fail(VFA_ERR_INVALID_ARG, "causal must be 0, 1 (top-left) or 2 (bottom-right)");
     if (!supported_head_dim(head_dim))
         return fail(VFA_ERR_UNSUPPORTED, "head_dim %d not supported (64, 128, 256)", head_dim);
     if (!(softmax_scale >= 0.f) || softmax_scale > FLT_MAX)
@@ -267,7 +271,7 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     sa.num_heads = num_heads;
     sa.block_q = bq;
     sa.block_k = bk;
-    sa.causal = causal != 0;
+    sa.causal = causal;
     sa.pair = vfa::pairs_for(head_dim) ? 1 : 0;
     sa.items = items;
     sa.item_capacity = wl.item_capacity;
@@ -303,7 +307,7 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     // a zero scale (uniform weights) becomes the smallest normal float, which
     // gives the same weights for every finite score.
     pa.scale_log2 = softmax_scale > 0.f ? softmax_scale * 1.4426950408889634f : FLT_MIN;
-    pa.causal = causal != 0;
+    pa.causal = causal;
     const int grid = wl.item_capacity < dev.sm_count ? wl.item_capacity : dev.sm_count;
     e = vfa::launch_prefill(head_dim, pa, grid, s);
     if (e != cudaSuccess)

@@ -48,7 +48,8 @@ WorkspaceLayout workspace_layout(int batch, int total_q, int total_k, int num_he
 struct SchedArgs {
     const int32_t *cu_q;
     const int32_t *cu_k;
-    int batch, total_q, total_k, max_seqlen_q, num_heads, block_q, block_k, causal;
+    int batch, total_q, total_k, max_seqlen_q, num_heads, block_q, block_k;
+    int causal;           // 0 none, 1 top-left, 2 bottom-right
     int pair;             // non-zero: two consecutive tiles of a group per item
     int4 *items;          // two int4 per item
     int item_capacity;
@@ -79,7 +80,7 @@ struct PrefillArgs {
     int num_heads;
     int kv_group;         // query heads per kv head: K/V of head h live at h / kv_group
     float scale_log2;     // softmax_scale * log2(e), > 0
-    int causal;
+    int causal;           // 0 none, 1 top-left, 2 bottom-right
 };
 
 // Whether the forward for `head_dim` runs two q tiles per work item.

@@ -386,9 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 // Row max of the raw scores (the scale is positive): eight
                 // independent three-input max chains.
                 const int k_base = j * BK;
-                const bool need_mask = (k_base + BK > lk) || (p.causal && k_base + BK - 1 > i * BQ);
+                // causal: row q sees keys <= q + off (off = 0 top-left, Lk - Lq bottom-right)
+                const int off = p.causal == 2 ? lk - lq : 0;
+                const bool need_mask =
+                    (k_base + BK > lk) || (p.causal && k_base + BK - 1 > i * BQ + off);
                 if (need_mask) {
-                    const int lim = (p.causal ? min(lk, q_local + 1) : lk) - k_base;   // keys < lim visible
+                    // keys < lim visible
+                    const int lim = (p.causal ? min(lk, max(0, q_local + off + 1)) : lk) - k_base;
 #pragma unroll
                     for (int c = 0; c < BK; ++c)
                         s[c] = c < lim ? s[c] : -INFINITY;

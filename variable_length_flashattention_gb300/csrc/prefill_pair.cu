@@ -536,8 +536,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const int k_base = j * BK;
-                const bool need_mask = (k_base + BK > lk) || (p.causal && k_base + BK - 1 > i * BQ);
-                const int lim = need_mask ? (p.causal ? min(lk, q_local + 1) : lk) - k_base : BK;
+                // causal: row q sees keys <= q + off (off = 0 top-left, Lk - Lq bottom-right)
+                const int off = p.causal == 2 ? lk - lq : 0;
+                const bool need_mask =
+                    (k_base + BK > lk) || (p.causal && k_base + BK - 1 > i * BQ + off);
+                const int lim =
+                    need_mask ? (p.causal ? min(lk, max(0, q_local + off + 1)) : lk) - k_base : BK;
                 // Warp-wide bounds of the valid-column count: a 32-column chunk
                 // below lim_lo needs no mask, one at or above lim_hi is all masked.
                 const int lim_lo = need_mask ? __reduce_min_sync(0xffffffffu, lim) : BK;

@@ -19,11 +19,13 @@
 // status word instead of trapping.
 //
 // With block_q = r * block_k (r a whole number) and block_k a power of two,
-// a causal tile costs min(C, (i + 1) * r) where C = ceil(min(Lk, Lq) /
-// block_k): costs rise by r per tile until they reach C and stay there.  So
-// a sequence's largest and total cost and each tile's rank in its group have
-// closed forms, and the kernel needs one pass over the sequences and one over
-// the tiles, in 32-bit arithmetic, with no per-tile searches.
+// a causal tile costs clamp((i + 1) * r + e, 0, C), where off = 0 (top-left)
+// or Lk - Lq (bottom-right), e = ceil(off / block_k) and C = ceil(clamp(Lq +
+// off, 0, Lk) / block_k): zero for the first tiles when off < 0, then rising
+// by r per tile until it reaches C.  So a sequence's largest and total cost
+// and each tile's rank in its group have closed forms, and the kernel needs
+// one pass over the sequences and one over the tiles, with no per-tile
+// searches.
 #include "internal.h"
 
 namespace vfa {
@@ -33,9 +35,10 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kSmemSeqs = 2048;    // per-sequence records kept in shared memory when they fit
 // Per-sequence records in ints: total cost (64-bit, two ints), tile start,
-// tile count, cost cap C, first capped tile i0, largest cost, rank in group
-// order, rank -> sequence, first item / H.
-constexpr int kSeqInts = 10;
+// tile count, cost cap C, offset term e, first tile with a non-zero cost,
+// first capped tile, largest cost, rank in group order, rank -> sequence,
+// first item / H.
+constexpr int kSeqInts = 12;
 constexpr size_t kSchedSmem = kSeqInts * kSmemSeqs * sizeof(int);
 
 __host__ __device__ inline int max_tiles(int batch, int total_q, int block_q)
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const SchedArgs a)
     const unsigned bq = static_cast<unsigned>(a.block_q), bk = static_cast<unsigned>(a.block_k);
     const unsigned r = bq / bk;                          // block_q = r * block_k
     const int lbk = __ffs(static_cast<int>(bk)) - 1;    // block_k = 2^lbk
-    const bool causal = a.causal != 0;
+    const int causal = a.causal;                         // 0 none, 1 top-left, 2 bottom-right
 
     const int tiles_cap = max_tiles(B, a.total_q, a.block_q);
     const bool in_smem = B + 1 <= kSmemSeqs;
@@ -106,11 +109,13 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const SchedArgs a)
     int *tile_start = rec + 2 * n;
     int *seq_nt = rec + 3 * n;
     int *seq_cap = rec + 4 * n;
-    int *seq_i0 = rec + 5 * n;
-    int *seq_maxc = rec + 6 * n;
-    int *seq_rank = rec + 7 * n;
-    int *ord = rec + 8 * n;
-    int *seq_first = rec + 9 * n;
+    int *seq_e = rec + 5 * n;
+    int *seq_ilo = rec + 6 * n;
+    int *seq_ihi = rec + 7 * n;
+    int *seq_maxc = rec + 8 * n;
+    int *seq_rank = rec + 9 * n;
+    int *ord = rec + 10 * n;
+    int *seq_first = rec + 11 * n;
 
     if (tid == 0) {
         s_bad = 0;
@@ -134,21 +139,41 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const SchedArgs a)
             } else {
                 const unsigned uq = static_cast<unsigned>(lq), uk = static_cast<unsigned>(lk);
                 nt = static_cast<int>((uq + bq - 1) / bq);
-                const unsigned m = causal ? min(uq, uk) : uk;
-                const int cap = static_cast<int>((m + bk - 1) >> lbk);
-                int i0 = 0;
-                long long maxc = cap;
-                long long total = static_cast<long long>(nt) * cap;
-                if (causal) {
-                    // first tile whose cost reaches the cap: (i0 + 1) * r >= cap
-                    i0 = min(nt, max(0, static_cast<int>((cap + r - 1) / r) - 1));
-                    maxc = min(static_cast<long long>(cap), static_cast<long long>(nt) * r);
-                    const long long u = min(static_cast<long long>(nt), static_cast<long long>(cap / r));
-                    total = static_cast<long long>(r) * u * (u + 1) / 2 + (nt - u) * cap;
+                int cap, e = 0, i_lo = 0, i_hi = 0;
+                long long maxc, total;
+                if (!causal) {
+                    cap = static_cast<int>((uk + bk - 1) >> lbk);
+                    maxc = cap;
+                    total = static_cast<long long>(nt) * cap;
+                } else {
+                    // tile i's last row sees keys 0 .. row + off
+                    const long long off = causal == 2 ? lk - lq : 0;
+                    const long long m = min(lk, max(0ll, lq + off));
+                    cap = static_cast<int>((m + bk - 1) >> lbk);
+                    e = off >= 0 ? static_cast<int>((off + bk - 1) >> lbk)
+                                 : -static_cast<int>((-off) >> lbk);     // ceil(off / bk)
+                    const int ir = static_cast<int>(r);
+                    if (cap == 0) {
+                        i_lo = i_hi = nt;                  // every tile costs 0
+                    } else {
+                        // zero-cost tiles: (i + 1) r + e <= 0; capped: (i + 1) r + e >= cap
+                        i_lo = e < 0 ? min(nt, (-e) / ir) : 0;
+                        i_hi = min(nt, max(0, (cap - e + ir - 1) / ir - 1));
+                    }
+                    maxc = min(static_cast<long long>(cap),
+                               max(0ll, static_cast<long long>(nt) * ir + e));
+                    // sum over the rising tiles i_lo .. i_hi - 1 of (i + 1) r + e, plus the capped
+                    const long long a0 = i_lo + 1, a1 = i_hi;
+                    const long long rising = a1 >= a0 ? (a0 + a1) * (a1 - a0 + 1) / 2 : 0;
+                    total = cap > 0 ? ir * rising + static_cast<long long>(e) * (i_hi - i_lo) +
+                                          static_cast<long long>(nt - i_hi) * cap
+                                    : 0;
                 }
                 seq_nt[b] = nt;
                 seq_cap[b] = cap;
-                seq_i0[b] = i0;
+                seq_e[b] = e;
+                seq_ilo[b] = i_lo;
+                seq_ihi[b] = i_hi;
                 seq_maxc[b] = nt > 0 ? static_cast<int>(maxc) : -1;
                 seq_total[b] = total;
             }
@@ -216,9 +241,10 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const SchedArgs a)
 
     // Items, one thread per tile writing all its heads.  Sequence b's groups
     // start at H * seq_first[b], head h's group at + h * units(nt); the
-    // tile's rank in its group is i - i0 for capped tiles (equal cost, i
-    // ascending) and nt - 1 - i below the cap (cost falls as i falls), and
-    // it lands in item rank (single) or rank / 2, slot rank % 2 (pairs).
+    // tile's rank in its group (cost descending, then i) is i - i_hi for
+    // capped tiles (equal cost, i ascending), then the rising tiles with i
+    // falling, then the zero-cost tiles with i ascending; it lands in item
+    // rank (single) or rank / 2, slot rank % 2 (pairs).
     for (int t = tid; t < ntiles; t += kThreads) {
         int lo = 0, hi = B - 1;                     // largest b with tile_start[b] <= t
         while (lo < hi) {
@@ -230,9 +256,11 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const SchedArgs a)
         }
         const int b = lo;
         const int i = t - tile_start[b];
-        const int nt = seq_nt[b], cap = seq_cap[b], i0 = seq_i0[b];
-        const int c = causal ? min(cap, (i + 1) * static_cast<int>(r)) : cap;
-        const int rank = i >= i0 ? i - i0 : nt - 1 - i;
+        const int nt = seq_nt[b], cap = seq_cap[b], i_lo = seq_ilo[b], i_hi = seq_ihi[b];
+        const int c = causal ? min(cap, max(0, (i + 1) * static_cast<int>(r) + seq_e[b])) : cap;
+        const int rank = i >= i_hi ? i - i_hi
+                         : i >= i_lo ? (nt - i_hi) + (i_hi - 1 - i)
+                                     : (nt - i_lo) + i;
         const int slot = a.pair ? (rank & 1) : 0;
         const int unit = a.pair ? rank >> 1 : rank;
         const int per_head = units(nt);

@@ -136,7 +136,7 @@ def alloc_workspace(batch: int, total_q: int, total_k: int, num_heads: int, head
 
 def varlen_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
                cu_seqlens_k: torch.Tensor, max_seqlen_q: int, softmax_scale: float,
-               causal: bool, out: Optional[torch.Tensor] = None,
+               causal, out: Optional[torch.Tensor] = None,
                lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                stream=None):
     """out bf16 [Tq, H, D], lse f32 [Tq, H] = varlen attention forward (vfa_varlen_fwd).
@@ -166,7 +166,7 @@ def varlen_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: 
         workspace = alloc_workspace(batch, total_q, total_k, H, D, device=q.device)
     st = lib().vfa_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
                               total_q, total_k, int(max_seqlen_q), batch, H, Hkv, D,
-                              float(softmax_scale), int(bool(causal)), _ptr(out), _ptr(lse),
+                              float(softmax_scale), int(causal), _ptr(out), _ptr(lse),
                               _ptr(workspace), workspace.numel() * workspace.element_size(),
                               _stream(stream))
     _check(st)
@@ -193,7 +193,7 @@ def varlen_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                       _ptr(cu_seqlens_k), total_q, k.shape[0], int(max_seqlen_q),
                                       cu_seqlens_q.numel() - 1, H, k.shape[1], D,
                                       float(softmax_scale),
-                                      int(bool(causal)), _ptr(out), _ptr(lse), _ptr(device_status),
+                                      int(causal), _ptr(out), _ptr(lse), _ptr(device_status),
                                       _stream(stream))
     _check(st)
     return out, lse
@@ -214,7 +214,7 @@ def schedule(cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, total_q: in
     scratch = torch.empty((nbytes + 3) // 4, dtype=torch.int32, device=dev)
     st = lib().vfa_varlen_schedule(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), total_q, total_k,
                                    int(max_seqlen_q), batch, num_heads, block_q, block_k,
-                                   int(bool(causal)), int(bool(pair)), _ptr(items), cap,
+                                   int(causal), int(bool(pair)), _ptr(items), cap,
                                    _ptr(n_items), _ptr(status), _ptr(scratch), scratch.numel() * 4,
                                    _stream(stream))
     _check(st)
