@@ -331,14 +331,19 @@ def run_ours(args):
     torch.cuda.synchronize()
     sampler.mark("start")
     t0 = time.perf_counter()
+    nvtx = torch.cuda.nvtx
     for i in range(args.steps):
         flush.fill_(float(i))
         ev[i][0].record(stream)
+        nvtx.range_push("varlen_fwd")
         prefill()
+        nvtx.range_pop()
         ev[i][1].record(stream)
         flush.fill_(float(-i))
         ev[i][2].record(stream)
+        nvtx.range_push("decode_pass")
         graph.replay()
+        nvtx.range_pop()
         ev[i][3].record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -371,6 +376,7 @@ def run_ours(args):
     e2e_steps = max(5, min(args.steps, 200))
 
     def e2e_step():
+        torch.cuda.nvtx.range_push("e2e_step")
         d_q.copy_(h_q, non_blocking=True)
         d_k.copy_(h_k, non_blocking=True)
         d_v.copy_(h_v, non_blocking=True)
@@ -380,6 +386,7 @@ def run_ours(args):
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
         torch.cuda.current_stream().synchronize()
+        torch.cuda.nvtx.range_pop()
 
     for _ in range(3):
         e2e_step()

@@ -273,6 +273,15 @@ vfa_status vfa_debug_paged_gather(const void *k_pool, const void *v_pool, int nu
                                   int head_dim, int block_size, void *k_out, void *v_out,
                                   int32_t *device_status, vfa_stream_t stream);
 
+/*
+ * Test hook for the bounded waits of every kernel in this library (no
+ * counterpart on the pages): one CTA waits on a barrier that nothing
+ * arrives on, gives up after the same limit as the pipeline waits (1 s),
+ * stores VFA_ERR_TIMEOUT in device_status (first error wins) and exits; the
+ * context stays usable.  device_status: device int32 [1], not NULL.
+ */
+vfa_status vfa_debug_bounded_wait(int32_t *device_status, vfa_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status                                                                    */
 /* ------------------------------------------------------------------------ */

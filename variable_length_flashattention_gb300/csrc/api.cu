@@ -440,6 +440,21 @@ vfa_status vfa_paged_decode_finalize(const float *l, const float *o, int num_seq
     return VFA_OK;
 }
 
+vfa_status vfa_debug_bounded_wait(int32_t *device_status, vfa_stream_t stream)
+{
+    if (!device_status || !aligned(device_status, 4))
+        return fail(VFA_ERR_INVALID_ARG, "device_status must be a non-null, aligned pointer");
+    DeviceInfo dev;
+    vfa_status st = current_device(&dev);
+    if (st)
+        return st;
+    cudaError_t e = vfa::launch_debug_bounded_wait(device_status,
+                                                   reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "bounded-wait hook launch");
+    return VFA_OK;
+}
+
 vfa_status vfa_debug_paged_gather(const void *k_pool, const void *v_pool, int num_blocks,
                                   const int32_t *tile_blocks, const int32_t *tile_block_counts,
                                   int tile_capacity, int num_seqs, int num_kv_heads, int head_dim,

@@ -124,4 +124,8 @@ cudaError_t launch_decode_finalize(const float *l, const float *o, int num_seqs,
 cudaError_t launch_decode_gather(const DecodeStepArgs &a, void *k_out, void *v_out,
                                  cudaStream_t stream);
 
+// ------------------------------------------------------------ test hooks
+
+cudaError_t launch_debug_bounded_wait(int32_t *status, cudaStream_t stream);
+
 }  // namespace vfa

@@ -51,6 +51,7 @@ SIGNATURES = [
                                    _P, _P, _P, _P]),
     ("vfa_paged_decode_finalize", _I, [_P, _P, _I, _I, _I, _P, _P]),
     ("vfa_debug_paged_gather", _I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    ("vfa_debug_bounded_wait", _I, [_P, _P]),
     ("vfa_read_status", _I, [_P, _P, _P]),
 ]
 
@@ -273,6 +274,12 @@ def decode_finalize(l: torch.Tensor, o: torch.Tensor, out: Optional[torch.Tensor
     _check(lib().vfa_paged_decode_finalize(_ptr(l), _ptr(o), S, Hq, D, _ptr(out),
                                            _stream(stream)))
     return out
+
+
+def debug_bounded_wait(status: torch.Tensor, stream=None):
+    """vfa_debug_bounded_wait: a wait nothing satisfies must end in VFA_ERR_TIMEOUT."""
+    _need(status, torch.int32, "status")
+    _check(lib().vfa_debug_bounded_wait(_ptr(status), _stream(stream)))
 
 
 def debug_paged_gather(k_pool: torch.Tensor, v_pool: torch.Tensor, tile_blocks: torch.Tensor,
