@@ -60,10 +60,11 @@ def _load():
         P = ctypes.c_void_p
         i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
         lib.oracle_default_threads.restype = i32
-        lib.oracle_varlen_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, i32, P, P, i32]
+        lib.oracle_varlen_fwd.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, i32, i32, P, P,
+                                          i32]
         lib.oracle_varlen_fwd.restype = i32
-        lib.oracle_varlen_fwd_rows.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, i32, P,
-                                               i64, P, P, i32]
+        lib.oracle_varlen_fwd_rows.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, i32, i32,
+                                               P, i64, P, P, i32]
         lib.oracle_varlen_fwd_rows.restype = i32
         lib.oracle_decode_init.argtypes = [P, P, P, i32, i32, i32]
         lib.oracle_decode_init.restype = None
@@ -102,11 +103,12 @@ def default_threads() -> int:
 
 def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_dim: int,
                softmax_scale: float, causal: bool, nthreads: int = 0,
-               num_kv_heads: int = 0):
+               num_kv_heads: int = 0, window_left: int = -1):
     """Full forward.  Returns (out float64 [Tq,H,D], lse float64 [Tq,H], threads used).
 
     causal: 0 (or False) no mask, 1 (or True) top-left, 2 bottom-right (local
-    key j visible to local query i iff j <= i + Lk - Lq).  k, v hold
+    key j visible to local query i iff j <= i + Lk - Lq); window_left >= 0
+    (with a causal mode) also hides keys j < i + off - window_left.  k, v hold
     num_kv_heads heads (default: num_heads); query head h reads kv head
     h // (num_heads // num_kv_heads)."""
     lib = _load()
@@ -123,7 +125,7 @@ def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_dim: in
     lse = np.zeros((tq, num_heads), dtype=np.float64)
     n = lib.oracle_varlen_fwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cq), _ptr(ck), batch,
                               num_heads, hkv, head_dim, float(softmax_scale),
-                              int(causal), _ptr(out), _ptr(lse), int(nthreads))
+                              int(causal), int(window_left), _ptr(out), _ptr(lse), int(nthreads))
     if n <= 0:
         raise ValueError(f"oracle_varlen_fwd rejected its arguments ({n})")
     return out, lse, int(n)
@@ -131,7 +133,7 @@ def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_dim: in
 
 def varlen_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_dim: int,
                     softmax_scale: float, causal: bool, rows, nthreads: int = 0,
-                    num_kv_heads: int = 0):
+                    num_kv_heads: int = 0, window_left: int = -1):
     """Selected rows.  rows: int array [n, 2] of (packed token, head).
 
     Returns (out float64 [n, D], lse float64 [n], threads used)."""
@@ -144,7 +146,8 @@ def varlen_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_di
     n = lib.oracle_varlen_fwd_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cq), _ptr(ck),
                                    len(cq) - 1, num_heads, num_kv_heads or num_heads, head_dim,
                                    float(softmax_scale),
-                                   int(causal), _ptr(r), r.shape[0], _ptr(out), _ptr(lse),
+                                   int(causal), int(window_left), _ptr(r), r.shape[0], _ptr(out),
+                                   _ptr(lse),
                                    int(nthreads))
     if n <= 0:
         raise ValueError(f"oracle_varlen_fwd_rows rejected its arguments ({n})")

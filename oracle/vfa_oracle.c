@@ -25,7 +25,8 @@
  *   - causal alignment is top-left: local key j is visible to local query i
  *     iff j <= i (the kernel compares local positions k_pos > q_pos); the
  *     bottom-right alignment (the last query sees every key: j <= i + Lk - Lq)
- *     is offered as a second causal mode;
+ *     is offered as a second causal mode, and either mode may be narrowed to
+ *     a sliding window of the window_left keys before the diagonal;
  *   - masked keys carry weight exactly zero (the kernel's -FLT_MAX sentinel
  *     and the CPU reference's -inf sentinel both give that);
  *   - an empty key set gives out = 0 and lse = -FLT_MAX (the kernel's
@@ -82,15 +83,17 @@ typedef struct {
     int batch, num_heads, num_kv_heads, head_dim;
     double scale;
     int causal;
+    int window_left;                        /* < 0: none; else keys j >= i + off - window_left */
 } varlen_problem;
 
 /*
  * One query row: local row i of sequence b, head h; its keys and values are
  * those of kv head kh = h / (H / Hkv) (kh = h when Hkv = H).
  *
- *   K_set = { j : 0 <= j < Lk_b  and  (causal == 0 or j <= i + off) }
+ *   K_set = { j : 0 <= j < Lk_b  and  (causal == 0 or j <= i + off)
+ *               and  (window_left < 0 or j >= i + off - window_left) }
  *   off   = 0 for causal == 1 (top-left), Lk_b - Lq_b for causal == 2
- *           (bottom-right)
+ *           (bottom-right); a window needs a causal mode
  *   s_j   = scale * sum_d q[tq, h, d] * k[cu_k[b] + j, kh, d]
  *   empty K_set: out = 0, lse = -FLT_MAX
  *   else: M = max_j s_j, Z = sum_j exp(s_j - M),
@@ -115,6 +118,8 @@ static void varlen_row(const varlen_problem *p, int b, int i, int h,
     for (int j = 0; j < Lk; ++j) {
         if (p->causal && j > i + off)
             continue;                       /* masked: weight exactly zero */
+        if (p->window_left >= 0 && j < i + off - p->window_left)
+            continue;                       /* left of the sliding window */
         kidx[n++] = j;
     }
     if (n == 0) {
@@ -266,15 +271,15 @@ static int max_len(const int32_t *cu, int batch)
 int oracle_varlen_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                       const int32_t *cu_q, const int32_t *cu_k, int batch,
                       int num_heads, int num_kv_heads, int head_dim, double scale, int causal,
-                      double *out, double *lse, int nthreads)
+                      int window_left, double *out, double *lse, int nthreads)
 {
     if (batch < 1 || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads != 0 ||
-        head_dim < 1 || causal < 0 || causal > 2)
+        head_dim < 1 || causal < 0 || causal > 2 || (window_left >= 0 && causal == 0))
         return -1;
     if (check_cu(cu_q, batch) || check_cu(cu_k, batch))
         return -2;
     varlen_problem p = {q, k, v, cu_q, cu_k, batch, num_heads, num_kv_heads, head_dim, scale,
-                        causal};
+                        causal, window_left};
     varlen_job job;
     memset(&job, 0, sizeof job);
     job.p = &p;
@@ -293,11 +298,12 @@ int oracle_varlen_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 int oracle_varlen_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                            const int32_t *cu_q, const int32_t *cu_k, int batch,
                            int num_heads, int num_kv_heads, int head_dim, double scale,
-                           int causal, const int64_t *rows, int64_t n_rows,
+                           int causal, int window_left, const int64_t *rows, int64_t n_rows,
                            double *out_rows, double *lse_rows, int nthreads)
 {
     if (batch < 1 || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads != 0 ||
-        head_dim < 1 || n_rows < 0 || causal < 0 || causal > 2)
+        head_dim < 1 || n_rows < 0 || causal < 0 || causal > 2 ||
+        (window_left >= 0 && causal == 0))
         return -1;
     if (check_cu(cu_q, batch) || check_cu(cu_k, batch))
         return -2;
@@ -306,7 +312,7 @@ int oracle_varlen_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t 
             rows[2 * r + 1] < 0 || rows[2 * r + 1] >= num_heads)
             return -3;
     varlen_problem p = {q, k, v, cu_q, cu_k, batch, num_heads, num_kv_heads, head_dim, scale,
-                        causal};
+                        causal, window_left};
     varlen_job job;
     memset(&job, 0, sizeof job);
     job.p = &p;

@@ -323,3 +323,91 @@ def test_bottom_right_causal_matches_torch_sdpa_float64(oracle_mod):
         np.testing.assert_allclose(lse[q0:q1][live.numpy()],
                                    torch.logsumexp(s_, dim=-1).transpose(0, 1).numpy(),
                                    rtol=1e-12, atol=1e-12)
+
+
+def _band(Lq, Lk, causal, window_left):
+    """Visible-key mask of one sequence: j <= i + off, and j >= i + off - window_left."""
+    off = Lk - Lq if causal == 2 else 0
+    i = torch.arange(Lq)[:, None]
+    j = torch.arange(Lk)[None, :]
+    allowed = j <= i + off
+    if window_left >= 0:
+        allowed &= j >= i + off - window_left
+    return allowed
+
+
+@pytest.mark.parametrize("causal", [1, 2])
+@pytest.mark.parametrize("window_left", [0, 3, 37, 130])
+def test_sliding_window_matches_torch_sdpa_float64(oracle_mod, causal, window_left):
+    # keys j with i + off - window_left <= j <= i + off, the rest weight zero
+    lq, lk = [3, 140, 60, 1, 25, 200], [3, 170, 17, 9, 0, 90]
+    H, D = 2, 32
+    case = _case(lq, lk, H, D, True, seed=17 + window_left)
+    out, lse, _ = oracle_mod.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens_q,
+                                        case.cu_seqlens_k, H, D, case.softmax_scale, causal,
+                                        window_left=window_left)
+    q, k, v = case.q.double(), case.k.double(), case.v.double()
+    for b in range(case.batch):
+        q0, q1 = int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1])
+        k0, k1 = int(case.cu_seqlens_k[b]), int(case.cu_seqlens_k[b + 1])
+        allowed = _band(q1 - q0, k1 - k0, causal, window_left)
+        live = allowed.any(dim=1) if k1 > k0 else torch.zeros(q1 - q0, dtype=torch.bool)
+        dead = ~live.numpy()
+        assert np.all(out[q0:q1][dead] == 0) and np.all(lse[q0:q1][dead] == -oracle_mod.FLT_MAX)
+        if not live.any():
+            continue
+        qs = q[q0:q1].transpose(0, 1)[:, live]
+        ks = k[k0:k1].transpose(0, 1)
+        vs = v[k0:k1].transpose(0, 1)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qs, ks, vs, attn_mask=allowed[live], scale=case.softmax_scale)
+        np.testing.assert_allclose(out[q0:q1][live.numpy()], ref.transpose(0, 1).numpy(),
+                                   rtol=1e-10, atol=1e-12)
+        s_ = (case.softmax_scale * (qs @ ks.transpose(1, 2))).masked_fill(~allowed[live],
+                                                                          float("-inf"))
+        np.testing.assert_allclose(lse[q0:q1][live.numpy()],
+                                   torch.logsumexp(s_, dim=-1).transpose(0, 1).numpy(),
+                                   rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [1, 2])
+def test_zero_window_gives_the_diagonal_v(oracle_mod, causal):
+    # window_left = 0: the only visible key is j = i + off, weight exactly 1,
+    # so out is that key's v row and lse its scaled score
+    lq, lk = [5, 40, 1], [9, 40, 4]
+    H, D = 2, 16
+    case = _case(lq, lk, H, D, True, seed=23)
+    out, lse, _ = oracle_mod.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens_q,
+                                        case.cu_seqlens_k, H, D, case.softmax_scale, causal,
+                                        window_left=0)
+    q, k, v = _f64(case.q), _f64(case.k), _f64(case.v)
+    for b in range(case.batch):
+        q0, k0 = int(case.cu_seqlens_q[b]), int(case.cu_seqlens_k[b])
+        off = lk[b] - lq[b] if causal == 2 else 0
+        for i in range(lq[b]):
+            j = i + off
+            if not 0 <= j < lk[b]:
+                assert np.all(out[q0 + i] == 0)
+                continue
+            np.testing.assert_array_equal(out[q0 + i], v[k0 + j])
+            s = case.softmax_scale * np.einsum("hd,hd->h", q[q0 + i], k[k0 + j])
+            np.testing.assert_allclose(lse[q0 + i], s, rtol=1e-14, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [1, 2])
+def test_window_wider_than_keys_changes_nothing(oracle_mod, causal):
+    lq, lk = [70, 3, 128], [70, 50, 100]
+    case = _case(lq, lk, 2, 32, True, seed=29)
+    args = (case.q, case.k, case.v, case.cu_seqlens_q, case.cu_seqlens_k, 2, 32,
+            case.softmax_scale, causal)
+    o0, l0, _ = oracle_mod.varlen_fwd(*args)
+    o1, l1, _ = oracle_mod.varlen_fwd(*args, window_left=max(lq) + max(lk))
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+
+
+def test_window_needs_a_causal_mode(oracle_mod):
+    case = _case([4], [4], 1, 16, False, seed=1)
+    with pytest.raises(ValueError):
+        oracle_mod.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens_q, case.cu_seqlens_k, 1, 16,
+                              case.softmax_scale, 0, window_left=2)
