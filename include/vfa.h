@@ -101,6 +101,14 @@ vfa_status vfa_varlen_fwd_tile_shape(int head_dim, int *block_q, int *block_k, i
  *              last query sees every key (a query block at the end of a longer
  *              key sequence) and rows with i + Lk_b - Lq_b < 0 see none.
  *              Other values: VFA_ERR_INVALID_ARG.
+ * window_left  < 0: no window.  >= 0 (needs causal 1 or 2, else
+ *              VFA_ERR_INVALID_ARG): a sliding window -- local key j is
+ *              visible to local query i only if j >= i + off - window_left
+ *              as well (off = 0 top-left, Lk_b - Lq_b bottom-right), so each
+ *              query sees at most window_left + 1 keys ending at its
+ *              diagonal.  The pages name sliding-window masks among the
+ *              varlen variants without defining one; this is the reading
+ *              taken.
  * out          device bf16 [total_q, num_heads, head_dim]: out = sum_j p_j v_j /
  *              sum_j p_j, rounded to nearest even; 0 for a query with no
  *              visible key.
@@ -122,7 +130,7 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
                           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                           int total_q, int total_k, int max_seqlen_q, int batch,
                           int num_heads, int num_kv_heads, int head_dim, float softmax_scale,
-                          int causal, void *out, float *lse, void *workspace,
+                          int causal, int window_left, void *out, float *lse, void *workspace,
                           size_t workspace_bytes, vfa_stream_t stream);
 
 /*
@@ -156,23 +164,29 @@ vfa_status vfa_varlen_fwd_noalloc(const void *q, const void *k, const void *v,
                                   const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                                   int total_q, int total_k, int max_seqlen_q, int batch,
                                   int num_heads, int num_kv_heads, int head_dim,
-                                  float softmax_scale, int causal, void *out, float *lse,
-                                  int32_t *device_status, vfa_stream_t stream);
+                                  float softmax_scale, int causal, int window_left, void *out,
+                                  float *lse, int32_t *device_status, vfa_stream_t stream);
 
 /*
  * The device tile scheduler alone (the first kernel vfa_varlen_fwd runs),
  * writing into caller buffers so the work list can be inspected.
  *
  * A tile is q tile i (local rows [i*block_q, min(Lq_b, (i+1)*block_q))) of
- * sequence b and head h; its cost is the number of key tiles it visits
- * (ceil(Lk_b / block_k); causal: ceil(clamp(min(Lq_b, (i+1)*block_q) + off, 0,
- * Lk_b) / block_k), off = 0 for causal == 1 and Lk_b - Lq_b for causal == 2).  The tiles of one (b, h) stay together; groups are ordered by
- * their largest cost, then total cost (descending), then (b, h); inside a
- * group by cost descending, then i.  With pair_tiles != 0 two consecutive
- * tiles of a group form one item (what vfa_varlen_fwd uses for head_dim <=
- * 128); otherwise each tile is one item.  Each item is eight int32:
- * (b, i_a, h, cost_a, i_b, cost_b, 0, 0), with i_b = -1 and cost_b = 0 when
- * the second slot is empty.  Sequences with Lq_b == 0 give no items.
+ * sequence b and head h; it visits the key tiles [first, end) that hold a
+ * key its rows may see, and its cost is end - first.  Without a window
+ * first = 0 and end = ceil(Lk_b / block_k), or with a causal mask
+ * ceil(clamp(min(Lq_b, (i+1)*block_q) + off, 0, Lk_b) / block_k), off = 0 for
+ * causal == 1 and Lk_b - Lq_b for causal == 2; a window (window_left >= 0,
+ * as in vfa_varlen_fwd) gives first = floor(max(0, i*block_q + off -
+ * window_left) / block_k); a tile that sees no key has first = end = 0.
+ * The tiles of one (b, h) stay together; groups are ordered by their
+ * largest cost, then total cost (descending), then (b, h); inside a group
+ * by cost descending, then i (with a window: by i descending).  With
+ * pair_tiles != 0 two consecutive tiles of a group form one item (what
+ * vfa_varlen_fwd uses for head_dim <= 128); otherwise each tile is one
+ * item.  Each item is eight int32: (b, i_a, h, end_a, i_b, end_b, first_a,
+ * first_b), with i_b = -1 and end_b = first_b = 0 when the second slot is
+ * empty.  Sequences with Lq_b == 0 give no items.
  *
  * block_k must be a power of two and block_q a multiple of block_k
  * (VFA_ERR_UNSUPPORTED otherwise); vfa_varlen_fwd_tile_shape() only returns
@@ -187,7 +201,8 @@ vfa_status vfa_varlen_fwd_noalloc(const void *q, const void *k, const void *v,
 vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                                int total_q, int total_k, int max_seqlen_q, int batch,
                                int num_heads, int block_q, int block_k, int causal,
-                               int pair_tiles, int32_t *items, int items_capacity,
+                               int window_left, int pair_tiles, int32_t *items,
+                               int items_capacity,
                                int32_t *n_items, int32_t *status, void *scratch,
                                size_t scratch_bytes, vfa_stream_t stream);
 

@@ -20,7 +20,7 @@ def to_dev(case, device="cuda"):
                 cu_k=torch.from_numpy(case.cu_seqlens_k).to(device))
 
 
-def run_varlen(vfa, case, device="cuda", workspace=None):
+def run_varlen(vfa, case, device="cuda", workspace=None, window_left=-1):
     """GPU forward with NaN-canary outputs; returns (out f64 numpy, lse f64 numpy, status)."""
     d = to_dev(case, device)
     out = torch.full_like(d["q"].view(torch.int16), BF16_NAN).view(torch.bfloat16)
@@ -30,7 +30,8 @@ def run_varlen(vfa, case, device="cuda", workspace=None):
         workspace = vfa.alloc_workspace(case.batch, case.total_q, case.total_k, case.num_heads,
                                         case.head_dim, device=device)
     vfa.varlen_fwd(d["q"], d["k"], d["v"], d["cu_q"], d["cu_k"], max(case.max_seqlen_q, 0),
-                   case.softmax_scale, case.causal, out=out, lse=lse, workspace=workspace)
+                   case.softmax_scale, case.causal, out=out, lse=lse, workspace=workspace,
+                   window_left=window_left)
     status = vfa.read_status(workspace)
     torch.cuda.synchronize()
     return (out.float().cpu().double().numpy(), lse.cpu().double().numpy(), status)

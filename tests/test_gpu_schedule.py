@@ -18,12 +18,13 @@ def vfa():
     return binding
 
 
-def _check(vfa, oracle_mod, lq, lk, H, bq, bk, causal, pair=False):
+def _check(vfa, oracle_mod, lq, lk, H, bq, bk, causal, pair=False, window_left=-1):
     cq, ck = W.cu_seqlens(lq), W.cu_seqlens(lk)
     items, status = vfa.schedule(torch.from_numpy(cq).cuda(), torch.from_numpy(ck).cuda(),
-                                 int(cq[-1]), int(ck[-1]), max(lq), H, bq, bk, causal, pair)
+                                 int(cq[-1]), int(ck[-1]), max(lq), H, bq, bk, causal, pair,
+                                 window_left=window_left)
     assert status == 0
-    ref = oracle_mod.schedule(cq, ck, H, bq, bk, causal, pair)
+    ref = oracle_mod.schedule(cq, ck, H, bq, bk, causal, pair, window_left=window_left)
     got = items.cpu().numpy()
     assert got.shape == ref.shape
     np.testing.assert_array_equal(got, ref)
@@ -51,12 +52,28 @@ def test_random_mixes(vfa, oracle_mod, seed, causal):
             _check(vfa, oracle_mod, lq, lk, int(rng.integers(1, 5)), bq, bk, causal, pair)
 
 
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("causal", [1, 2])
+def test_window_random_mixes(vfa, oracle_mod, seed, causal):
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 3000 if seed == 3 else 60))
+    lq = [int(x) for x in rng.integers(0, 3000, B)]
+    lk = [int(x) for x in rng.integers(0, 3000, B)]
+    lq[0] = max(lq[0], 1)
+    for window_left in (0, 1, 100, 128, 1000, int(rng.integers(0, 5000)), 1 << 30):
+        for bq, bk in ((128, 128), (128, 64)):
+            for pair in (False, True):
+                _check(vfa, oracle_mod, lq, lk, int(rng.integers(1, 4)), bq, bk, causal, pair,
+                       window_left)
+
+
 def test_many_tiles_use_global_scratch(vfa, oracle_mod):
     # more than 4096 q tiles and 4096 cost buckets: the scheduler's global-memory path
     lq = [128] * 4200 + [700000]
     lk = [1] * 4200 + [700000]
     _check(vfa, oracle_mod, lq, lk, 1, 128, 128, True)
     _check(vfa, oracle_mod, lq, lk, 1, 128, 128, True, pair=True)
+    _check(vfa, oracle_mod, lq, lk, 1, 128, 128, True, pair=True, window_left=5000)
 
 
 def test_bad_seqlens_status(vfa):

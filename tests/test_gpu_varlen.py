@@ -166,6 +166,54 @@ def test_bottom_right_causal(vfa, oracle_mod, D):
     assert_lse_close(lse, ref_lse, f"bottom-right D={D}")
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("causal", [1, 2])
+@pytest.mark.parametrize("window_left", [0, 37, 128, 300])
+def test_sliding_window(vfa, oracle_mod, D, causal, window_left):
+    # keys j with i + off - window_left <= j <= i + off; ragged lengths, Lq > Lk
+    # (rows past the keys' end see nothing) and Lq < Lk both ways
+    lq = [64, 700, 129, 500, 1, 0, 260, 1000]
+    lk = [1000, 700, 40, 128, 77, 5, 0, 600]
+    case = W.make_varlen("window", lq, lk, 2, D, True, 1.0, value_seed=D + window_left)
+    case.causal = causal
+    out, lse, status = run_varlen(vfa, case, window_left=window_left)
+    assert status == 0
+    ref_out, ref_lse, _ = oracle_mod.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens_q,
+                                                case.cu_seqlens_k, 2, D, case.softmax_scale,
+                                                causal, window_left=window_left)
+    what = f"window {window_left} causal {causal} D={D}"
+    assert_out_close(out, ref_out, what)
+    assert_lse_close(lse, ref_lse, what)
+
+
+def test_sliding_window_grouped_kv_heads(vfa, oracle_mod):
+    lq, lk = [300, 1, 900, 77], [300, 50, 900, 500]
+    case = W.make_varlen("window-gqa", lq, lk, 8, 128, True, 1.0, value_seed=5)
+    case.k = case.k[:, :2].contiguous()
+    case.v = case.v[:, :2].contiguous()
+    out, lse, status = run_varlen(vfa, case, window_left=200)
+    assert status == 0
+    ref_out, ref_lse, _ = oracle_mod.varlen_fwd(case.q, case.k, case.v, case.cu_seqlens_q,
+                                                case.cu_seqlens_k, 8, 128, case.softmax_scale,
+                                                True, num_kv_heads=2, window_left=200)
+    assert_out_close(out, ref_out, "window gqa")
+    assert_lse_close(lse, ref_lse, "window gqa")
+
+
+@pytest.mark.parametrize("window_left", [1000, 4095])
+def test_sliding_window_long_sequence_sampled(vfa, oracle_mod, window_left):
+    case = W.make_varlen("long-window", [16384], [16384], 1, 128, True, 1.0, value_seed=6)
+    out, lse, status = run_varlen(vfa, case, window_left=window_left)
+    assert status == 0
+    rows = np.stack([np.r_[0:64, 8000:8064, 16320:16384], np.zeros(192, int)], 1).astype(np.int64)
+    ref_out, ref_lse, _ = oracle_mod.varlen_fwd_rows(case.q, case.k, case.v, case.cu_seqlens_q,
+                                                     case.cu_seqlens_k, 1, 128,
+                                                     case.softmax_scale, True, rows,
+                                                     window_left=window_left)
+    assert_out_close(out[rows[:, 0], rows[:, 1]], ref_out, "long window")
+    assert_lse_close(lse[rows[:, 0], rows[:, 1]], ref_lse, "long window")
+
+
 def test_single_long_sequence_sampled(vfa, oracle_mod):
     case = W.make_varlen("long", [16384], [16384], 1, 128, True, 1.0, value_seed=4)
     out, lse, status = run_varlen(vfa, case)

@@ -63,24 +63,28 @@ def test_workspace_bound_covers_worst_case(vfa):
 def test_host_rejects_null_and_unsupported(vfa):
     L = vfa.lib()
     nul = None
-    st = L.vfa_varlen_fwd(nul, nul, nul, nul, nul, 1, 1, 1, 1, 1, 1, 128, 1.0, 0, nul, nul, nul, 0,
+    st = L.vfa_varlen_fwd(nul, nul, nul, nul, nul, 1, 1, 1, 1, 1, 1, 128, 1.0, 0, -1, nul, nul, nul, 0,
                           nul)
     assert st == vfa.VFA_ERR_INVALID_ARG
     assert b"null" in L.vfa_last_error()
     fake = ctypes.c_void_p(0x100000)   # never dereferenced: rejected before any device work
-    st = L.vfa_varlen_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 1, 1, 1, 96, 1.0, 0, fake, fake,
+    st = L.vfa_varlen_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 1, 1, 1, 96, 1.0, 0, -1, fake, fake,
                           fake, 1 << 20, nul)
     assert st == vfa.VFA_ERR_UNSUPPORTED
-    st = L.vfa_varlen_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 1, 1, 1, 128, 1.0, 0, fake, fake,
+    st = L.vfa_varlen_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 1, 1, 1, 128, 1.0, 0, -1, fake, fake,
                           fake, 16, nul)
     assert st == vfa.VFA_ERR_INVALID_ARG and b"workspace too small" in L.vfa_last_error()
-    st = L.vfa_varlen_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 1, 6, 4, 128, 1.0, 0, fake, fake,
+    st = L.vfa_varlen_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 1, 6, 4, 128, 1.0, 0, -1, fake, fake,
                           fake, 1 << 20, nul)
     assert st == vfa.VFA_ERR_INVALID_ARG and b"num_kv_heads" in L.vfa_last_error()
     odd = ctypes.c_void_p(0x100002)
-    st = L.vfa_varlen_fwd(odd, fake, fake, fake, fake, 1, 1, 1, 1, 1, 1, 128, 1.0, 0, fake, fake,
+    st = L.vfa_varlen_fwd(odd, fake, fake, fake, fake, 1, 1, 1, 1, 1, 1, 128, 1.0, 0, -1, fake, fake,
                           fake, 1 << 20, nul)
     assert st == vfa.VFA_ERR_INVALID_ARG and b"aligned" in L.vfa_last_error()
+    # a sliding window without a causal mode
+    st = L.vfa_varlen_fwd(fake, fake, fake, fake, fake, 1, 1, 1, 1, 1, 1, 128, 1.0, 0, 16, fake, fake,
+                          fake, 1 << 20, nul)
+    assert st == vfa.VFA_ERR_INVALID_ARG and b"window" in L.vfa_last_error()
     # decode: unsupported group size / block size / head_dim
     st = L.vfa_paged_decode_step(fake, fake, fake, 4, fake, fake, nul, 2, 1, 12, 4, 128, 16, 0.0,
                                  fake, fake, fake, nul, nul)

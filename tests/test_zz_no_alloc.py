@@ -59,6 +59,6 @@ def test_noalloc_rejects_problems_beyond_the_static_scratch(vfa):
     L = vfa.lib()
     fake = None
     st = L.vfa_varlen_fwd_noalloc(fake, fake, fake, fake, fake, 100000, 100000, 1, 100000, 8,
-                                  8, 128, 0.1, 0, fake, fake, fake, None)
+                                  8, 128, 0.1, 0, -1, fake, fake, fake, None)
     assert st == vfa.VFA_ERR_UNSUPPORTED
     assert b"static scratch" in L.vfa_last_error()

@@ -163,7 +163,8 @@ vfa_status vfa_varlen_fwd_tile_shape(int head_dim, int *block_q, int *block_k, i
 vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                                int total_q, int total_k, int max_seqlen_q, int batch,
                                int num_heads, int block_q, int block_k, int causal,
-                               int pair_tiles, int32_t *items, int items_capacity,
+                               int window_left, int pair_tiles, int32_t *items,
+                               int items_capacity,
                                int32_t *n_items, int32_t *status, void *scratch,
                                size_t scratch_bytes, vfa_stream_t stream)
 {
@@ -174,6 +175,8 @@ vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_se
         return fail(VFA_ERR_INVALID_ARG, "bad size argument");
     if (causal < 0 || causal > 2)
         return fail(VFA_ERR_INVALID_ARG, "causal must be 0, 1 (top-left) or 2 (bottom-right)");
+    if (window_left >= 0 && causal == 0)
+        return fail(VFA_ERR_INVALID_ARG, "a sliding window needs a causal mode");
     if (!aligned(items, 16) || !aligned(scratch, 8))
         return fail(VFA_ERR_INVALID_ARG, "items must be 16-byte and scratch 8-byte aligned");
     if ((block_k & (block_k - 1)) != 0 || block_q % block_k != 0)
@@ -199,6 +202,7 @@ vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_se
     a.block_q = block_q;
     a.block_k = block_k;
     a.causal = causal;
+    a.window_left = window_left < 0 ? -1 : window_left;
     a.pair = pair_tiles != 0;
     a.items = reinterpret_cast<int4 *>(items);
     a.item_capacity = items_capacity;
@@ -217,8 +221,8 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
                           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int total_q,
                           int total_k, int max_seqlen_q, int batch, int num_heads,
                           int num_kv_heads, int head_dim, float softmax_scale, int causal,
-                          void *out, float *lse, void *workspace, size_t workspace_bytes,
-                          vfa_stream_t stream)
+                          int window_left, void *out, float *lse, void *workspace,
+                          size_t workspace_bytes, vfa_stream_t stream)
 {
     if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out || !lse || !workspace)
         return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
@@ -230,6 +234,8 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
                     num_heads, num_kv_heads);
     if (causal < 0 || causal > 2)
         return fail(VFA_ERR_INVALID_ARG, "causal must be 0, 1 (top-left) or 2 (bottom-right)");
+    if (window_left >= 0 && causal == 0)
+        return fail(VFA_ERR_INVALID_ARG, "a sliding window needs a causal mode");
     if (!supported_head_dim(head_dim))
         return fail(VFA_ERR_UNSUPPORTED, "head_dim %d not supported (64, 128, 256)", head_dim);
     if (!(softmax_scale >= 0.f) || softmax_scale > FLT_MAX)
@@ -272,6 +278,7 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     sa.block_q = bq;
     sa.block_k = bk;
     sa.causal = causal;
+    sa.window_left = window_left < 0 ? -1 : window_left;
     sa.pair = vfa::pairs_for(head_dim) ? 1 : 0;
     sa.items = items;
     sa.item_capacity = wl.item_capacity;
@@ -308,6 +315,7 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     // gives the same weights for every finite score.
     pa.scale_log2 = softmax_scale > 0.f ? softmax_scale * 1.4426950408889634f : FLT_MIN;
     pa.causal = causal;
+    pa.window_left = sa.window_left;
     const int grid = wl.item_capacity < dev.sm_count ? wl.item_capacity : dev.sm_count;
     e = vfa::launch_prefill(head_dim, pa, grid, s);
     if (e != cudaSuccess)

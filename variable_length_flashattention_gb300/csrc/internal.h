@@ -29,8 +29,9 @@ __host__ __device__ constexpr int block_k_for(int head_dim)
 //   [0]   int32 status word
 //   [4]   int32 number of work items
 //   [8]   int32 next item to take (the prefill's atomic counter)
-//   [256] items[item_capacity], 32 bytes each: int4 (b, i_a, h, cost_a),
-//         int4 (i_b, cost_b, 0, 0) with i_b = -1 when the second slot is empty
+//   [256] items[item_capacity], 32 bytes each: int4 (b, i_a, h, end_a),
+//         int4 (i_b, end_b, first_a, first_b); slot x visits key tiles
+//         [first_x, end_x); i_b = -1 when the second slot is empty
 //   then  int32 scheduler scratch
 struct WorkspaceLayout {
     size_t items_offset;
@@ -50,6 +51,7 @@ struct SchedArgs {
     const int32_t *cu_k;
     int batch, total_q, total_k, max_seqlen_q, num_heads, block_q, block_k;
     int causal;           // 0 none, 1 top-left, 2 bottom-right
+    int window_left;      // < 0 none; else keys j >= row + off - window_left only (causal != 0)
     int pair;             // non-zero: two consecutive tiles of a group per item
     int4 *items;          // two int4 per item
     int item_capacity;
@@ -81,6 +83,7 @@ struct PrefillArgs {
     int kv_group;         // query heads per kv head: K/V of head h live at h / kv_group
     float scale_log2;     // softmax_scale * log2(e), > 0
     int causal;           // 0 none, 1 top-left, 2 bottom-right
+    int window_left;      // < 0 none; else keys j >= row + off - window_left only
 };
 
 // Whether the forward for `head_dim` runs two q tiles per work item.

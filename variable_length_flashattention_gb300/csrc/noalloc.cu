@@ -50,8 +50,8 @@ extern "C" vfa_status vfa_varlen_fwd_noalloc(const void *q, const void *k, const
                                              const int32_t *cu_seqlens_k, int total_q,
                                              int total_k, int max_seqlen_q, int batch,
                                              int num_heads, int num_kv_heads, int head_dim,
-                                             float softmax_scale, int causal, void *out,
-                                             float *lse, int32_t *device_status,
+                                             float softmax_scale, int causal, int window_left,
+                                             void *out, float *lse, int32_t *device_status,
                                              vfa_stream_t stream)
 {
     char msg[256];
@@ -78,7 +78,8 @@ extern "C" vfa_status vfa_varlen_fwd_noalloc(const void *q, const void *k, const
     // is read as input.
     vfa_status st = vfa_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, total_q, total_k,
                                    max_seqlen_q, batch, num_heads, num_kv_heads, head_dim,
-                                   softmax_scale, causal, out, lse, ws, kStaticScratchBytes,
+                                   softmax_scale, causal, window_left, out, lse, ws,
+                                   kStaticScratchBytes,
                                    stream);
     if (st != VFA_OK || device_status == nullptr)
         return st;

@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
-    __shared__ int4 s_item[2][2];     // (b, i, h, cost), (q row 0 of b, Lq, Lk, k row 0 of b)
+    // (b, i, h, end key tile), (q row 0 of b, Lq, Lk, k row 0 of b), (first key tile, -, -, -)
+    __shared__ int4 s_item[2][3];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -145,12 +146,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Take the next item from the ring (consumer side); false at the end.
-    auto next_item = [&](uint32_t n, int4 &it, int4 &seq) -> bool {
+    // The item visits key tiles [first, it.w).
+    auto next_item = [&](uint32_t n, int4 &it, int4 &seq, int &first) -> bool {
         const int slot = n & 1;
         if (!mbar_wait(item_full(slot), (n >> 1) & 1u, abort))
             return false;
         it = s_item[slot][0];
         seq = s_item[slot][1];
+        first = s_item[slot][2].x;
         return it.x >= 0;
     };
 
@@ -169,17 +172,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 const int idx = atomicAdd(p.next_item, 1);
                 const int4 it = idx < n_items ? p.items[2 * idx] : make_int4(-1, 0, 0, 0);
                 int4 seq = make_int4(0, 0, 0, 0);
+                int first = 0;
                 if (it.x >= 0) {
                     const int q0 = p.cu_q[it.x], k0 = p.cu_k[it.x];
                     seq = make_int4(q0, p.cu_q[it.x + 1] - q0, p.cu_k[it.x + 1] - k0, k0);
+                    first = p.items[2 * idx + 1].z;
                 }
                 s_item[slot][0] = it;
                 s_item[slot][1] = seq;
+                s_item[slot][2] = make_int4(first, 0, 0, 0);
                 mbar_arrive(item_full(slot));
                 if (it.x < 0)
                     break;
-                const int i = it.y, h = it.z, nk = it.w;
-                if (nk == 0)
+                const int i = it.y, h = it.z, j_end = it.w;
+                if (j_end <= first)
                     continue;
                 const int q_row0 = seq.x + i * BQ;
                 const int k_row0 = seq.w;
@@ -193,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     tma_load_3d(sQ + qb * C::Q_BYTES + db * (BQ * 128), &p.tm_q, q_full(qb),
                                 db * 64, h, q_row0);
                 ++qit;
-                for (int j = 0; j < nk; ++j) {
+                for (int j = first; j < j_end; ++j) {
                     const int st = kfills % NS;
                     if (!mbar_wait(k_empty(st), ((kfills / NS) & 1u) ^ 1u, abort)) {
                         ok = false;
@@ -269,12 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             };
             for (;; ++n) {
                 int4 it, seq;
-                const bool more = next_item(n, it, seq);
+                int first;
+                const bool more = next_item(n, it, seq, first);
                 mbar_arrive(item_empty(n & 1));
                 if (!more)
                     break;
-                const int nk = it.w;
-                if (nk == 0)
+                const int j_end = it.w;
+                if (j_end <= first)
                     continue;
                 const int qb = qit % NQ;
                 if (!mbar_wait(q_full(qb), (qit / NQ) & 1u, abort)) {
@@ -282,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     break;
                 }
                 const uint64_t qd = q_desc0 + qb * (C::Q_BYTES >> 4);
-                for (int j = 0; j < nk; ++j) {
+                for (int j = first; j < j_end; ++j) {
                     const int st = kv % NS;
                     const int x = g % NSB;
                     if (!mbar_wait(k_full(st), (kv / NS) & 1u, abort) ||
@@ -301,9 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                                     C::IDESC_QK);
                     mma_commit(s_full(x));
                     mma_commit(k_empty(st));
-                    if (j == nk - 1)
+                    if (j == j_end - 1)
                         mma_commit(q_empty(qb));
-                    if (j > 0 && !issue_pv(g - 1, kv - 1, j - 1 > 0)) {
+                    if (j > first && !issue_pv(g - 1, kv - 1, j - 1 > first)) {
                         ok = false;
                         break;
                     }
@@ -312,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 }
                 if (!ok)
                     break;
-                if (!issue_pv(g - 1, kv - 1, nk - 1 > 0)) {
+                if (!issue_pv(g - 1, kv - 1, j_end - 1 > first)) {
                     ok = false;
                     break;
                 }
@@ -337,19 +344,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const float2 scale2 = make_float2(scale_log2, scale_log2);
         for (uint32_t n = 0;; ++n) {
             int4 it, seq;
-            const bool more = next_item(n, it, seq);
+            int first;
+            const bool more = next_item(n, it, seq, first);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(item_empty(n & 1));
             if (!more)
                 break;
-            const int i = it.y, h = it.z, nk = it.w;
+            const int i = it.y, h = it.z, j_end = it.w;
             const int q0 = seq.x, lq = seq.y, lk = seq.z;
             const int q_local = i * BQ + r;
             const bool row_valid = q_local < lq;
             const long long tok = static_cast<long long>(q0) + q_local;
 
-            if (nk == 0) {
+            if (j_end <= first) {
                 if (row_valid) {
                     uint4 z = make_uint4(0, 0, 0, 0);
                     uint4 *dst = reinterpret_cast<uint4 *>(out + (tok * H + h) * D);
@@ -364,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             float m_used = -INFINITY;     // reference max, log2 units of the scaled score
             float l = 0.f;
             bool ok = true;
-            for (int j = 0; j < nk; ++j) {
+            for (int j = first; j < j_end; ++j) {
                 const int x = g % NSB;
                 if (!mbar_wait(s_full(x), (g / NSB) & 1u, abort)) {
                     ok = false;
@@ -386,16 +394,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 // Row max of the raw scores (the scale is positive): eight
                 // independent three-input max chains.
                 const int k_base = j * BK;
-                // causal: row q sees keys <= q + off (off = 0 top-left, Lk - Lq bottom-right)
+                // causal: row q sees keys <= q + off (off = 0 top-left, Lk - Lq
+                // bottom-right); a window also hides keys < q + off - window_left
                 const int off = p.causal == 2 ? lk - lq : 0;
-                const bool need_mask =
-                    (k_base + BK > lk) || (p.causal && k_base + BK - 1 > i * BQ + off);
+                const int wl = p.window_left;
+                const bool need_lo =
+                    wl >= 0 && k_base < static_cast<long long>(i) * BQ + BQ - 1 + off - wl;
+                const bool need_mask = need_lo || (k_base + BK > lk) ||
+                                       (p.causal && k_base + BK - 1 > i * BQ + off);
                 if (need_mask) {
-                    // keys < lim visible
+                    // keys in [lo, lim) visible
                     const int lim = (p.causal ? min(lk, max(0, q_local + off + 1)) : lk) - k_base;
+                    const int lo = need_lo ? static_cast<int>(min(
+                                                 static_cast<long long>(BK),
+                                                 max(0ll, static_cast<long long>(q_local) + off -
+                                                              wl - k_base)))
+                                           : 0;
 #pragma unroll
                     for (int c = 0; c < BK; ++c)
-                        s[c] = c < lim ? s[c] : -INFINITY;
+                        s[c] = (c < lim && c >= lo) ? s[c] : -INFINITY;
                 }
                 float mx[8];
 #pragma unroll
@@ -411,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 const float m_tile = mt_raw == -INFINITY ? -INFINITY : mt_raw * scale_log2;
                 const float m_new = fmaxf(m_used, m_tile);
                 const bool grow = m_new > m_used + 8.0f;    // also true for m_used = -inf
-                if (j == 0) {
+                if (j == first) {
                     m_used = m_new;
                 } else if (__any_sync(0xffffffffu, grow)) {
                     // O must hold the previous tile's product before it is rescaled.

@@ -79,31 +79,35 @@ constexpr int kItemConsumers = 10;  // MMA + V loader + one arrival per softmax 
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale when the max grows by > 2^8
 
 // Masks one 32-column chunk of scores (columns cb..cb+31 of the key tile):
-// scores at or past `lim` valid columns become -inf, so they drop out of the
-// max and 2^(-inf) = 0 (the scale is > 0, so no -inf * 0).  A chunk below
-// the warp's smallest lim needs no mask.
-__device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int cb, int lim, int lim_lo)
+// a row's visible columns are [lo, lim), and scores outside become -inf, so
+// they drop out of the max and 2^(-inf) = 0 (the scale is > 0, so no
+// -inf * 0).  lim_lo / lo_hi are the warp's smallest lim and largest lo: a
+// chunk inside [lo_hi, lim_lo) needs no mask.  LO: a sliding window's edge
+// can cut into the tile (otherwise lo = 0).
+template <bool LO>
+__device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int cb, int lim, int lim_lo, int lo,
+                                           int lo_hi)
 {
-    if (cb + 32 <= lim_lo)
+    if (cb + 32 <= lim_lo && (!LO || cb >= lo_hi))
         return;
 #pragma unroll
     for (int e = 0; e < 32; ++e)
-        sr[e] = cb + e < lim ? sr[e] : __float_as_uint(-INFINITY);
+        sr[e] = (cb + e < lim && (!LO || cb + e >= lo)) ? sr[e] : __float_as_uint(-INFINITY);
 }
 
 // Folds the (masked) scores of the 32-column chunk at TMEM address taddr into
 // the running maxima mx.  An all-masked chunk is skipped.
-template <bool MASK>
-__device__ __forceinline__ void chunk_max(uint32_t taddr, int cb, int lim, int lim_lo, bool empty,
-                                          float (&mx)[4])
+template <int MK>
+__device__ __forceinline__ void chunk_max(uint32_t taddr, int cb, int lim, int lim_lo, int lo,
+                                          int lo_hi, bool empty, float (&mx)[4])
 {
     if (empty)
         return;
     uint32_t sr[32];
     tmem_ld32(taddr, sr);
     tmem_wait_ld_r(sr);
-    if (MASK)
-        mask_chunk(sr, cb, lim, lim_lo);
+    if (MK > 0)
+        mask_chunk<MK == 2>(sr, cb, lim, lim_lo, lo, lo_hi);
 #pragma unroll
     for (int e = 0; e < 16; ++e)
         mx[e & 3] = fmax3(mx[e & 3], __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
@@ -112,9 +116,11 @@ __device__ __forceinline__ void chunk_max(uint32_t taddr, int cb, int lim, int l
 // p = 2^(s * scale_log2 - m) for the 32-column chunk at TMEM address taddr,
 // packed to bf16 pairs in pk[pb .. pb + 15], with the row sums accumulated in
 // ls (fp32) and, if WITH_MAX, the scores folded into mx.  An all-masked chunk
-// gives zeros without loads or exponentials.
-template <bool MASK, bool WITH_MAX>
-__device__ __forceinline__ void chunk_exp(uint32_t taddr, int cb, int lim, int lim_lo, bool empty,
+// gives zeros without loads or exponentials.  MK: 0 no mask, 1 upper bound
+// only, 2 both bounds.
+template <int MK, bool WITH_MAX>
+__device__ __forceinline__ void chunk_exp(uint32_t taddr, int cb, int lim, int lim_lo, int lo,
+                                          int lo_hi, bool empty,
                                           float2 scale2, float2 negm2, float2 (&ls)[4],
                                           float (&mx)[4], uint32_t (&pk)[32], int pb)
 {
@@ -127,8 +133,8 @@ __device__ __forceinline__ void chunk_exp(uint32_t taddr, int cb, int lim, int l
     uint32_t sr[32];
     tmem_ld32(taddr, sr);
     tmem_wait_ld_r(sr);
-    if (MASK)
-        mask_chunk(sr, cb, lim, lim_lo);
+    if (MK > 0)
+        mask_chunk<MK == 2>(sr, cb, lim, lim_lo, lo, lo_hi);
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
         const float s0 = __uint_as_float(sr[2 * e]), s1 = __uint_as_float(sr[2 * e + 1]);
@@ -158,7 +164,38 @@ __device__ __forceinline__ void rescale_rows(uint32_t o_addr, float f)
     tmem_wait_st();
 }
 
-template <int D>
+// The key tiles of one work item: slot x (0 = tile a, 1 = tile b) visits
+// [first[x], end[x]) (empty when end <= first), and the item loads the union
+// [j0, j1) of the non-empty ranges, which the scheduler keeps contiguous.
+struct ItemSpan {
+    int first[2], end[2];
+    int j0, j1;
+    __device__ __forceinline__ bool live(int x) const { return end[x] > first[x]; }
+    __device__ __forceinline__ bool has(int x, int j) const { return j >= first[x] && j < end[x]; }
+};
+
+__device__ __forceinline__ ItemSpan item_span(const int4 &it, const int4 &itb)
+{
+    ItemSpan sp;
+    const bool has_b = itb.x >= 0;
+    sp.first[0] = itb.z;
+    sp.end[0] = it.w;
+    sp.first[1] = has_b ? itb.w : 0;
+    sp.end[1] = has_b ? itb.y : 0;
+    sp.j0 = 0;
+    sp.j1 = 0;
+    bool any = false;
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+        if (sp.live(x)) {
+            sp.j0 = any ? min(sp.j0, sp.first[x]) : sp.first[x];
+            sp.j1 = any ? max(sp.j1, sp.end[x]) : sp.end[x];
+            any = true;
+        }
+    return sp;
+}
+
+template <int D, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ PrefillArgs p)
 {
@@ -284,13 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(item_full(slot));
                 if (it.x < 0)
                     break;
-                const int h = it.z, nk_a = it.w;
-                const int nk_b = itb.x >= 0 ? itb.y : 0;
-                if (nk_a == 0)
+                const int h = it.z;
+                const ItemSpan sp = item_span(it, itb);
+                if (sp.j1 <= sp.j0)
                     continue;
                 for (int x = 0; x < 2 && ok; ++x) {
-                    if (x == 1 && nk_b == 0)
-                        break;
+                    if (!sp.live(x))
+                        continue;
                     const int i = x == 0 ? it.y : itb.x;
                     if (!mbar_wait(q_empty(x), (qloads[x] & 1u) ^ 1u, abort)) {
                         ok = false;
@@ -302,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     db * 64, h, seq.x + i * BQ);
                     ++qloads[x];
                 }
-                for (int j = 0; j < nk_a && ok; ++j) {
+                for (int j = sp.j0; j < sp.j1 && ok; ++j) {
                     const int st = kfills % NS;
                     if (!mbar_wait(k_empty(st), ((kfills / NS) & 1u) ^ 1u, abort)) {
                         ok = false;
@@ -336,8 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(item_empty(n & 1));
                 if (!more)
                     break;
-                const int h = it.z, nk_a = it.w;
-                for (int j = 0; j < nk_a; ++j) {
+                const int h = it.z;
+                const ItemSpan sp = item_span(it, itb);
+                for (int j = sp.j0; j < sp.j1; ++j) {
                     const int st = vfills % NS;
                     if (!mbar_wait(v_empty(st), ((vfills / NS) & 1u) ^ 1u, abort)) {
                         ok = false;
@@ -416,60 +454,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(item_empty(n & 1));
                 if (!more)
                     break;
-                const int nk_a = it.w;
-                const int nk_b = itb.x >= 0 ? itb.y : 0;
-                if (nk_a == 0)
+                const ItemSpan sp = item_span(it, itb);
+                if (sp.j1 <= sp.j0)
                     continue;
-                if (!mbar_wait(q_full(0), qloads[0] & 1u, abort) ||
-                    (nk_b > 0 && !mbar_wait(q_full(1), qloads[1] & 1u, abort))) {
+                if ((sp.live(0) && !mbar_wait(q_full(0), qloads[0] & 1u, abort)) ||
+                    (sp.live(1) && !mbar_wait(q_full(1), qloads[1] & 1u, abort))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                for (int j = 0; j < nk_a && ok; ++j) {
+                // Slot x runs key tiles [first[x], end[x]) of the item's [j0, j1);
+                // without a window both start at 0 and b's range ends first.
+                for (int j = sp.j0; j < sp.j1 && ok; ++j) {
                     const int st = kv % NS;
                     const int st_prev = (kv + NS - 1) % NS;
+                    const bool a_in = sp.has(0, j), b_in = sp.has(1, j);
                     if (!mbar_wait(k_full(st), (kv / NS) & 1u, abort)) {
                         ok = false;
                         break;
                     }
-                    issue_qk(0, st);                              // S_a(j)
-                    if (j == nk_a - 1)
-                        mma_commit_w(q_empty(0));
-                    if (j >= 1 && j - 1 < nk_b) {
+                    if (a_in) {
+                        issue_qk(0, st);                          // S_a(j)
+                        if (j == sp.end[0] - 1)
+                            mma_commit_w(q_empty(0));
+                    }
+                    if (sp.has(1, j - 1)) {
                         // O_b += P_b(j-1) V(j-1); V(j-1) is then free
-                        if (!issue_pv(1, st_prev, kv - 1, j - 1 > 0)) {
+                        if (!issue_pv(1, st_prev, kv - 1, j - 1 > sp.first[1])) {
                             ok = false;
                             break;
                         }
                         mma_commit_w(v_empty(st_prev));
                     }
-                    if (j < nk_b) {
+                    if (b_in) {
                         issue_qk(1, st);                          // S_b(j)
-                        if (j == nk_b - 1)
+                        if (j == sp.end[1] - 1)
                             mma_commit_w(q_empty(1));
                     }
                     mma_commit_w(k_empty(st));
-                    if (!issue_pv(0, st, kv, j > 0)) {            // O_a += P_a(j) V(j)
+                    if (a_in && !issue_pv(0, st, kv, j > sp.first[0])) {   // O_a += P_a(j) V(j)
                         ok = false;
                         break;
                     }
-                    if (j >= nk_b)
-                        mma_commit_w(v_empty(st));                  // tile b does not use V(j)
+                    if (!b_in) {
+                        // tile b does not use V(j): free it now (after its fill
+                        // has landed, if no product read it)
+                        if (!a_in && !mbar_wait(v_full(st), (kv / NS) & 1u, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        mma_commit_w(v_empty(st));
+                    }
                     ++kv;
                 }
                 if (!ok)
                     break;
-                if (nk_b == nk_a) {
+                if (sp.has(1, sp.j1 - 1)) {
                     const int st_last = (kv + NS - 1) % NS;
-                    if (!issue_pv(1, st_last, kv - 1, nk_a - 1 > 0)) {
+                    if (!issue_pv(1, st_last, kv - 1, sp.j1 - 1 > sp.first[1])) {
                         ok = false;
                         break;
                     }
                     mma_commit_w(v_empty(st_last));
                 }
-                ++qloads[0];
-                if (nk_b > 0)
+                if (sp.live(0))
+                    ++qloads[0];
+                if (sp.live(1))
                     ++qloads[1];
             }
             if (!ok || *abort) {
@@ -493,8 +543,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int H = p.num_heads;
         uint32_t g = 0;                               // this slot's tiles so far
         __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
-        using Masked = std::integral_constant<bool, true>;
-        using Plain = std::integral_constant<bool, false>;
+        // Masked tiles mask the keys past a row's last visible one and, in the
+        // sliding-window instantiation, those below the window's edge too (one
+        // masked variant per instantiation keeps the register allocation of
+        // the plain kernel).
+        using Plain = std::integral_constant<int, 0>;
+        using Masked = std::integral_constant<int, WIN ? 2 : 1>;
 
         for (uint32_t n = 0;; ++n) {
             int4 it, itb, seq;
@@ -508,13 +562,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (i < 0)
                 continue;                             // no second tile in this item
             const int h = it.z;
-            const int nk = x == 0 ? it.w : itb.y;
+            // this slot's key tiles [j_first, j_end)
+            const int j_first = x == 0 ? itb.z : itb.w;
+            const int j_end = x == 0 ? it.w : itb.y;
             const int q0 = seq.x, lq = seq.y, lk = seq.z;
             const int q_local = i * BQ + r;
             const bool row_valid = q_local < lq;
             const long long tok = static_cast<long long>(q0) + q_local;
 
-            if (nk == 0) {
+            if (j_end <= j_first) {
                 if (row_valid) {
                     uint4 z = make_uint4(0, 0, 0, 0);
                     uint4 *dst = reinterpret_cast<uint4 *>(out + (tok * H + h) * D);
@@ -529,30 +585,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_used = -INFINITY;                 // reference max, log2 units
             float l = 0.f;
             bool ok = true;
-            for (int j = 0; j < nk && ok; ++j) {
+            for (int j = j_first; j < j_end && ok; ++j) {
                 if (!mbar_wait(s_full(x), g & 1u, abort)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const int k_base = j * BK;
-                // causal: row q sees keys <= q + off (off = 0 top-left, Lk - Lq bottom-right)
+                // causal: row q sees keys <= q + off (off = 0 top-left, Lk - Lq
+                // bottom-right); a window also hides keys < q + off - window_left
                 const int off = p.causal == 2 ? lk - lq : 0;
-                const bool need_mask =
+                const bool need_hi =
                     (k_base + BK > lk) || (p.causal && k_base + BK - 1 > i * BQ + off);
+                // the tile's last row has the highest window edge
+                const bool need_lo = WIN && k_base < static_cast<long long>(i) * BQ + BQ - 1 +
+                                                         off - p.window_left;
+                // this row's visible columns end at lim; warp-wide bounds of lim
+                const bool need_mask = need_hi || need_lo;
                 const int lim =
                     need_mask ? (p.causal ? min(lk, max(0, q_local + off + 1)) : lk) - k_base : BK;
-                // Warp-wide bounds of the valid-column count: a 32-column chunk
-                // below lim_lo needs no mask, one at or above lim_hi is all masked.
                 const int lim_lo = need_mask ? __reduce_min_sync(0xffffffffu, lim) : BK;
                 const int lim_hi = need_mask ? __reduce_max_sync(0xffffffffu, lim) : BK;
 
                 // One half of the key tile: 64 scores as two 32-column chunks.
                 auto half = [&](auto masked, int hh) -> bool {
-                    constexpr bool MASK = decltype(masked)::value;
+                    constexpr int MK = decltype(masked)::value;
                     const int c0 = hh * 64;
-                    const bool empty0 = MASK && c0 >= lim_hi;
-                    const bool empty1 = MASK && c0 + 32 >= lim_hi;
+                    // banded tiles: this row's visible columns start at lo
+                    int lo = 0, lo_lo = 0, lo_hi = 0;
+                    if (MK == 2) {
+                        const int off = p.causal == 2 ? lk - lq : 0;
+                        lo = static_cast<int>(
+                            min(static_cast<long long>(BK),
+                                max(0ll, static_cast<long long>(q_local) + off - p.window_left -
+                                             k_base)));
+                        lo_lo = __reduce_min_sync(0xffffffffu, lo);
+                        lo_hi = __reduce_max_sync(0xffffffffu, lo);
+                    }
+                    // a chunk every row of the warp masks entirely
+                    const bool empty0 = MK > 0 && (c0 >= lim_hi || (MK == 2 && c0 + 32 <= lo_lo));
+                    const bool empty1 =
+                        MK > 0 && (c0 + 32 >= lim_hi || (MK == 2 && c0 + 64 <= lo_lo));
                     const uint32_t sa = s_addr + c0;
                     // p is computed against the reference max in the pass that
                     // finds the half's max; if the max grew by more than 2^8 the
@@ -564,16 +637,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float2 ls[4];
                     uint32_t pk[32];
                     if (fresh) {
-                        chunk_max<MASK>(sa, c0, lim, lim_lo, empty0, mx);
-                        chunk_max<MASK>(sa + 32, c0 + 32, lim, lim_lo, empty1, mx);
+                        chunk_max<MK>(sa, c0, lim, lim_lo, lo, lo_hi, empty0, mx);
+                        chunk_max<MK>(sa + 32, c0 + 32, lim, lim_lo, lo, lo_hi, empty1, mx);
                     } else {
                         const float2 negm2 = make_float2(-m_used, -m_used);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             ls[e] = make_float2(0.f, 0.f);
-                        chunk_exp<MASK, true>(sa, c0, lim, lim_lo, empty0, scale2, negm2, ls, mx, pk, 0);
-                        chunk_exp<MASK, true>(sa + 32, c0 + 32, lim, lim_lo, empty1, scale2, negm2, ls,
-                                              mx, pk, 16);
+                        chunk_exp<MK, true>(sa, c0, lim, lim_lo, lo, lo_hi, empty0, scale2, negm2,
+                                            ls, mx, pk, 0);
+                        chunk_exp<MK, true>(sa + 32, c0 + 32, lim, lim_lo, lo, lo_hi, empty1, scale2,
+                                            negm2, ls, mx, pk, 16);
                     }
                     const float mraw = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
                     const float m_half = mraw == -INFINITY ? -INFINITY : mraw * scale_log2;
@@ -581,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool grow = m_new > m_used + kRescaleThreshold;   // true for m_used = -inf
                     const bool redo = __any_sync(0xffffffffu, grow);
                     if (redo) {
-                        if (j > 0 || hh > 0) {
+                        if (j > j_first || hh > 0) {
                             // O_x must hold every product issued so far before it
                             // is rescaled: the previous tile's second half, or this
                             // tile's first.
@@ -603,9 +677,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             ls[e] = make_float2(0.f, 0.f);
-                        chunk_exp<MASK, false>(sa, c0, lim, lim_lo, empty0, scale2, negm2, ls, mx, pk, 0);
-                        chunk_exp<MASK, false>(sa + 32, c0 + 32, lim, lim_lo, empty1, scale2, negm2, ls,
-                                               mx, pk, 16);
+                        chunk_exp<MK, false>(sa, c0, lim, lim_lo, lo, lo_hi, empty0, scale2, negm2,
+                                             ls, mx, pk, 0);
+                        chunk_exp<MK, false>(sa + 32, c0 + 32, lim, lim_lo, lo, lo_hi, empty1,
+                                             scale2, negm2, ls, mx, pk, 16);
                     }
                     const float2 l2 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
                     l += l2.x + l2.y;
@@ -677,8 +752,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
-cudaError_t launch_pair_d(const PrefillArgs &a, int grid, cudaStream_t stream)
+template <int D, bool WIN>
+cudaError_t launch_pair_dw(const PrefillArgs &a, int grid, cudaStream_t stream)
 {
     static int attr_done[64] = {0};
     int dev = 0;
@@ -686,7 +761,8 @@ cudaError_t launch_pair_d(const PrefillArgs &a, int grid, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     if (dev < 64 && !attr_done[dev]) {
-        e = cudaFuncSetAttribute(prefill_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(prefill_pair_kernel<D, WIN>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(PairCfg<D>::SMEM));
         if (e != cudaSuccess)
             return e;
@@ -702,10 +778,18 @@ cudaError_t launch_pair_d(const PrefillArgs &a, int grid, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D>, a);
+    e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D, WIN>, a);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
+}
+
+// The sliding-window mask has its own instantiation.
+template <int D>
+cudaError_t launch_pair_d(const PrefillArgs &a, int grid, cudaStream_t stream)
+{
+    return a.window_left >= 0 ? launch_pair_dw<D, true>(a, grid, stream)
+                              : launch_pair_dw<D, false>(a, grid, stream);
 }
 
 }  // namespace

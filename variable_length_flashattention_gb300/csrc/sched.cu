@@ -26,6 +26,15 @@
 // and each tile's rank in its group have closed forms, and the kernel needs
 // one pass over the sequences and one over the tiles, with no per-tile
 // searches.
+//
+// A sliding window of W keys (with either causal mode) also hides keys below
+// row + off - W.  Tile i then visits key tiles [F(i), c(i)) with F(i) =
+// max(0, i * r + g), g = floor((off - W) / block_k), except that the tiles
+// from i_z = ceil((Lk - off + W) / block_q) on see no key at all.  Its cost
+// c(i) - F(i) rises, stays flat, then falls: the sum is a difference of two
+// clamped arithmetic series, the largest cost sits next to the first index
+// where the flat part begins, and a group keeps its tiles in i-descending
+// order (longest first wherever the keys reach past the last query).
 #include "internal.h"
 
 namespace vfa {
@@ -37,13 +46,32 @@ constexpr int kSmemSeqs = 2048;    // per-sequence records kept in shared memory
 // Per-sequence records in ints: total cost (64-bit, two ints), tile start,
 // tile count, cost cap C, offset term e, first tile with a non-zero cost,
 // first capped tile, largest cost, rank in group order, rank -> sequence,
-// first item / H.
-constexpr int kSeqInts = 12;
+// first item / H, window edge term g, tiles before the window's empty tail.
+constexpr int kSeqInts = 14;
 constexpr size_t kSchedSmem = kSeqInts * kSmemSeqs * sizeof(int);
 
 __host__ __device__ inline int max_tiles(int batch, int total_q, int block_q)
 {
     return total_q / block_q + batch;
+}
+
+// sum over i in [0, n) of clamp(i * r + a, 0, C), for r >= 1.
+__device__ long long sum_lin_clamp(long long n, long long r, long long a, long long C)
+{
+    if (n <= 0 || C <= 0)
+        return 0;
+    long long i0 = a > 0 ? 0 : (-a) / r + 1;                 // first positive term
+    long long i1 = C - a <= 0 ? 0 : (C - a + r - 1) / r;     // first capped term
+    i0 = min(i0, n);
+    i1 = min(max(i1, i0), n);
+    // (i0 + i1 - 1) (i1 - i0) is even: one factor always is
+    const long long rising = r * ((i0 + i1 - 1) * (i1 - i0) / 2) + a * (i1 - i0);
+    return rising + (n - i1) * C;
+}
+
+__device__ __forceinline__ int floor_div_pow2(long long x, int lb)
+{
+    return static_cast<int>(x >= 0 ? x >> lb : -((-x + (1ll << lb) - 1) >> lb));
 }
 
 // Exclusive prefix sum of one value per thread over the 1024-thread block.
@@ -92,6 +120,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const SchedArgs a)
     const unsigned r = bq / bk;                          // block_q = r * block_k
     const int lbk = __ffs(static_cast<int>(bk)) - 1;    // block_k = 2^lbk
     const int causal = a.causal;                         // 0 none, 1 top-left, 2 bottom-right
+    const bool window = causal && a.window_left >= 0;
 
     const int tiles_cap = max_tiles(B, a.total_q, a.block_q);
     const bool in_smem = B + 1 <= kSmemSeqs;
@@ -116,6 +145,8 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const SchedArgs a)
     int *seq_rank = rec + 9 * n;
     int *ord = rec + 10 * n;
     int *seq_first = rec + 11 * n;
+    int *seq_g = rec + 12 * n;
+    int *seq_n1 = rec + 13 * n;
 
     if (tid == 0) {
         s_bad = 0;
@@ -168,6 +199,29 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const SchedArgs a)
                     total = cap > 0 ? ir * rising + static_cast<long long>(e) * (i_hi - i_lo) +
                                           static_cast<long long>(nt - i_hi) * cap
                                     : 0;
+                    if (window) {
+                        // tile i costs c(i) - max(0, i r + g) below n1, nothing after
+                        const int g = floor_div_pow2(off - a.window_left, lbk);
+                        const long long iz = (max(0ll, lk - off + a.window_left) + bq - 1) / bq;
+                        const int n1 = static_cast<int>(min(static_cast<long long>(nt), iz));
+                        const long long ar = ir + e;                 // c(i) = clamp(i r + ar, 0, C)
+                        total = sum_lin_clamp(n1, ir, ar, cap) -
+                                sum_lin_clamp(n1, ir, g, 1ll << 60);
+                        maxc = 0;
+                        if (n1 > 0) {
+                            // the cost is flat from u = i r = min(-g, C - ar) on; the
+                            // largest is at the first index past that point or just before
+                            const long long ulo = min(static_cast<long long>(-g), cap - ar);
+                            const long long i1 = ulo >= 0 ? (ulo + ir - 1) / ir : -((-ulo) / ir);
+                            for (int k = 0; k < 2; ++k) {
+                                const long long ic = min(max(i1 - k, 0ll), static_cast<long long>(n1 - 1));
+                                const long long ci = min(static_cast<long long>(cap), max(0ll, ic * ir + ar));
+                                maxc = max(maxc, ci > 0 ? ci - max(0ll, ic * ir + g) : 0ll);
+                            }
+                        }
+                        seq_g[b] = g;
+                        seq_n1[b] = n1;
+                    }
                 }
                 seq_nt[b] = nt;
                 seq_cap[b] = cap;
@@ -257,22 +311,40 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const SchedArgs a)
         const int b = lo;
         const int i = t - tile_start[b];
         const int nt = seq_nt[b], cap = seq_cap[b], i_lo = seq_ilo[b], i_hi = seq_ihi[b];
-        const int c = causal ? min(cap, max(0, (i + 1) * static_cast<int>(r) + seq_e[b])) : cap;
-        const int rank = i >= i_hi ? i - i_hi
-                         : i >= i_lo ? (nt - i_hi) + (i_hi - 1 - i)
-                                     : (nt - i_lo) + i;
+        int c = causal ? min(cap, max(0, (i + 1) * static_cast<int>(r) + seq_e[b])) : cap;
+        int f = 0;                                  // first key tile
+        int rank;
+        if (window) {
+            // key tiles [max(0, i r + g), c(i)) below n1; none from n1 on
+            if (i < seq_n1[b] && c > 0)
+                f = max(0, i * static_cast<int>(r) + seq_g[b]);
+            else
+                c = 0;
+            rank = nt - 1 - i;
+        } else {
+            rank = i >= i_hi ? i - i_hi
+                   : i >= i_lo ? (nt - i_hi) + (i_hi - 1 - i)
+                               : (nt - i_lo) + i;
+        }
         const int slot = a.pair ? (rank & 1) : 0;
         const int unit = a.pair ? rank >> 1 : rank;
         const int per_head = units(nt);
         const bool alone = !a.pair || rank == nt - 1;
         long long pos = static_cast<long long>(seq_first[b]) * H + unit;
         for (int h = 0; h < H; ++h, pos += per_head) {
+            // slot a writes its first key tile into the second int4's z, slot b
+            // into w; each slot writes only its own words
+            int *w = reinterpret_cast<int *>(a.items + 2 * pos);
             if (slot == 0) {
                 a.items[2 * pos] = make_int4(b, i, h, c);
                 if (alone)
-                    a.items[2 * pos + 1] = make_int4(-1, 0, 0, 0);
+                    a.items[2 * pos + 1] = make_int4(-1, 0, f, 0);
+                else
+                    w[6] = f;
             } else {
-                a.items[2 * pos + 1] = make_int4(i, c, 0, 0);
+                w[4] = i;
+                w[5] = c;
+                w[7] = f;
             }
         }
     }

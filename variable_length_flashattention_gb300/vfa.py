@@ -41,11 +41,12 @@ SIGNATURES = [
     ("vfa_version", ctypes.c_char_p, []),
     ("vfa_varlen_fwd_workspace_bytes", _S, [_I, _I, _I, _I, _I]),
     ("vfa_varlen_fwd_tile_shape", _I, [_I, _P, _P, _P]),
-    ("vfa_varlen_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _S,
-                            _P]),
-    ("vfa_varlen_fwd_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P,
-                                    _P, _P]),
-    ("vfa_varlen_schedule", _I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _S, _P]),
+    ("vfa_varlen_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P,
+                            _S, _P]),
+    ("vfa_varlen_fwd_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P,
+                                    _P, _P, _P]),
+    ("vfa_varlen_schedule", _I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P,
+                                 _S, _P]),
     ("vfa_paged_decode_init", _I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     ("vfa_paged_decode_step", _I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                                    _P, _P, _P, _P]),
@@ -139,11 +140,12 @@ def varlen_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: 
                cu_seqlens_k: torch.Tensor, max_seqlen_q: int, softmax_scale: float,
                causal, out: Optional[torch.Tensor] = None,
                lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-               stream=None):
+               stream=None, window_left: int = -1):
     """out bf16 [Tq, H, D], lse f32 [Tq, H] = varlen attention forward (vfa_varlen_fwd).
 
     k, v may hold fewer heads than q (a divisor of H): query head h reads kv
-    head h // (H // Hkv)."""
+    head h // (H // Hkv).  causal: 0 / False, 1 / True (top-left), 2
+    (bottom-right); window_left >= 0 adds a sliding window (needs causal)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, torch.bfloat16, n)
     _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
@@ -167,8 +169,9 @@ def varlen_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: 
         workspace = alloc_workspace(batch, total_q, total_k, H, D, device=q.device)
     st = lib().vfa_varlen_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
                               total_q, total_k, int(max_seqlen_q), batch, H, Hkv, D,
-                              float(softmax_scale), int(causal), _ptr(out), _ptr(lse),
-                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              float(softmax_scale), int(causal), int(window_left), _ptr(out),
+                              _ptr(lse), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(),
                               _stream(stream))
     _check(st)
     return out, lse
@@ -177,7 +180,8 @@ def varlen_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: 
 def varlen_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                        cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, max_seqlen_q: int,
                        softmax_scale: float, causal: bool, out: torch.Tensor, lse: torch.Tensor,
-                       device_status: Optional[torch.Tensor] = None, stream=None):
+                       device_status: Optional[torch.Tensor] = None, stream=None,
+                       window_left: int = -1):
     """vfa_varlen_fwd_noalloc: the forward with the library's static scratch.
 
     For callers that cannot allocate device memory: the caller passes only
@@ -194,7 +198,8 @@ def varlen_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                       _ptr(cu_seqlens_k), total_q, k.shape[0], int(max_seqlen_q),
                                       cu_seqlens_q.numel() - 1, H, k.shape[1], D,
                                       float(softmax_scale),
-                                      int(causal), _ptr(out), _ptr(lse), _ptr(device_status),
+                                      int(causal), int(window_left), _ptr(out), _ptr(lse),
+                                      _ptr(device_status),
                                       _stream(stream))
     _check(st)
     return out, lse
@@ -202,7 +207,7 @@ def varlen_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
 
 def schedule(cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, total_q: int, total_k: int,
              max_seqlen_q: int, num_heads: int, block_q: int, block_k: int, causal: bool,
-             pair: bool = False, stream=None):
+             pair: bool = False, stream=None, window_left: int = -1):
     """Runs the device tile scheduler alone; returns (items int32 [n, 8] on device, status)."""
     batch = cu_seqlens_q.numel() - 1
     cap = num_heads * (total_q // block_q + batch)
@@ -215,7 +220,8 @@ def schedule(cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, total_q: in
     scratch = torch.empty((nbytes + 3) // 4, dtype=torch.int32, device=dev)
     st = lib().vfa_varlen_schedule(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), total_q, total_k,
                                    int(max_seqlen_q), batch, num_heads, block_q, block_k,
-                                   int(causal), int(bool(pair)), _ptr(items), cap,
+                                   int(causal), int(window_left), int(bool(pair)), _ptr(items),
+                                   cap,
                                    _ptr(n_items), _ptr(status), _ptr(scratch), scratch.numel() * 4,
                                    _stream(stream))
     _check(st)
