@@ -66,6 +66,9 @@ def _load():
         lib.oracle_varlen_fwd_rows.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, i32, i32,
                                                P, i64, P, P, i32]
         lib.oracle_varlen_fwd_rows.restype = i32
+        lib.oracle_varlen_bwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f64, i32, i32, P,
+                                          P, P, i32]
+        lib.oracle_varlen_bwd.restype = i32
         lib.oracle_decode_init.argtypes = [P, P, P, i32, i32, i32]
         lib.oracle_decode_init.restype = None
         lib.oracle_decode_step.argtypes = [P, P, P, i64, P, P, P, i32, i32, i32, i32, i32, i32,
@@ -154,6 +157,34 @@ def varlen_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_di
     return out, lse, int(n)
 
 
+def varlen_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_dim: int,
+               softmax_scale: float, causal, nthreads: int = 0, num_kv_heads: int = 0,
+               window_left: int = -1):
+    """Gradients of the forward for upstream gradient dout.
+
+    Returns (dq float64 [Tq,H,D], dk float64 [Tk,Hkv,D], dv float64 [Tk,Hkv,D],
+    threads used); masks and head grouping as in varlen_fwd."""
+    lib = _load()
+    qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
+    cq, ck = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    batch = len(cq) - 1
+    tq, tk = int(cq[-1]), int(ck[-1])
+    hkv = num_kv_heads or num_heads
+    if qb.size != tq * num_heads * head_dim or gb.size != qb.size:
+        raise ValueError("q / dout size does not match cu_seqlens_q[-1] * H * D")
+    if kb.size != tk * hkv * head_dim or vb.size != kb.size:
+        raise ValueError("k/v size does not match cu_seqlens_k[-1] * Hkv * D")
+    dq = np.zeros((tq, num_heads, head_dim), dtype=np.float64)
+    dk = np.zeros((tk, hkv, head_dim), dtype=np.float64)
+    dv = np.zeros((tk, hkv, head_dim), dtype=np.float64)
+    n = lib.oracle_varlen_bwd(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), _ptr(cq), _ptr(ck), batch,
+                              num_heads, hkv, head_dim, float(softmax_scale), int(causal),
+                              int(window_left), _ptr(dq), _ptr(dk), _ptr(dv), int(nthreads))
+    if n <= 0:
+        raise ValueError(f"oracle_varlen_bwd rejected its arguments ({n})")
+    return dq, dk, dv, int(n)
+
+
 class DecodeState:
     """fp64 (m, l, o) -- AttnState of attention_ref.rs, kept in double."""
 
@@ -209,5 +240,5 @@ def decode_finalize(state: DecodeState) -> np.ndarray:
 
 from .schedule import schedule, tile_cost  # noqa: E402  (integer rule, pure Python)
 
-__all__ = ["build", "default_threads", "varlen_fwd", "varlen_fwd_rows", "DecodeState",
+__all__ = ["build", "default_threads", "varlen_fwd", "varlen_fwd_rows", "varlen_bwd", "DecodeState",
            "decode_step", "decode_finalize", "schedule", "tile_cost", "FLT_MAX"]

@@ -12,6 +12,8 @@
  *     cu_seqlens prefix sums, scaled scores, causal and boundary masks,
  *     epilogue out = acc / l and lse = log(l) + m) and Task 2 Step 1
  *     (varlen_attention_cpu: per-sequence masked softmax times V).
+ *   - the backward is the derivative of that forward (the plan names a
+ *     backward without giving one), written out per query row;
  *   - "attention_ref.rs" (spark_storage): AttnState::new, step_tile_ref,
  *     finalize_ref -- the paged GQA decode state (m, l, o), its update over
  *     the tokens of the blocks listed for one tile, and the final o / l.
@@ -322,6 +324,190 @@ int oracle_varlen_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t 
     job.out = out_rows;
     job.lse = lse_rows;
     return run_varlen_job(&job, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Varlen attention backward                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Gradients of the forward above for an upstream gradient dout = dL/dout
+ * (the pages only name a backward; this is the derivative of the forward's
+ * definition, written out).  For one query row (b, i, h) with visible key
+ * set K_set, weights P_j = exp(s_j - M) / Z (j in K_set) and
+ *
+ *   dP_j    = sum_d dout[tq, h, d] * v[k0 + j, kh, d]
+ *   Delta   = sum_{j in K_set} P_j * dP_j
+ *   dS_j    = P_j * (dP_j - Delta)                 (softmax Jacobian)
+ *   dq[tq, h, :]     = scale * sum_j dS_j * k[k0 + j, kh, :]
+ *   dk[k0 + j, kh, :] += scale * dS_j * q[tq, h, :]
+ *   dv[k0 + j, kh, :] += P_j * dout[tq, h, :]
+ *
+ * dk and dv of kv head kh sum over the query heads h with h / (H / Hkv) = kh
+ * and over every row that sees the key.  A row with an empty K_set adds
+ * nothing and gets dq = 0.
+ */
+typedef struct {
+    const varlen_problem *p;
+    const uint16_t *dout;
+    double *dq, *dk, *dv;
+    int64_t n_units;       /* (b, kh) pairs */
+    int64_t next;
+    int max_lk;
+    int status;
+} bwd_job;
+
+static void bwd_unit(bwd_job *job, int b, int kh, double *s, double *w, int *kidx)
+{
+    const varlen_problem *p = job->p;
+    const int D = p->head_dim, H = p->num_heads, Hkv = p->num_kv_heads;
+    const int group = H / Hkv;
+    const int64_t q0 = p->cu_q[b], k0 = p->cu_k[b];
+    const int Lq = p->cu_q[b + 1] - p->cu_q[b];
+    const int Lk = p->cu_k[b + 1] - p->cu_k[b];
+    const int off = p->causal == 2 ? Lk - Lq : 0;
+    double *dp = (double *)malloc((size_t)(Lk > 0 ? Lk : 1) * sizeof(double));
+    if (!dp) {
+        __atomic_store_n(&job->status, -1, __ATOMIC_SEQ_CST);
+        return;
+    }
+    for (int h = kh * group; h < (kh + 1) * group; ++h) {
+        for (int i = 0; i < Lq; ++i) {
+            const int64_t tq = q0 + i;
+            int n = 0;
+            for (int j = 0; j < Lk; ++j) {
+                if (p->causal && j > i + off)
+                    continue;
+                if (p->window_left >= 0 && j < i + off - p->window_left)
+                    continue;
+                kidx[n++] = j;
+            }
+            double *dq_row = job->dq + packed_index(tq, h, 0, H, D);
+            for (int d = 0; d < D; ++d)
+                dq_row[d] = 0.0;
+            if (n == 0)
+                continue;
+            /* softmax weights of the row */
+            for (int a = 0; a < n; ++a) {
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d)
+                    dot += bf16_to_double(p->q[packed_index(tq, h, d, H, D)]) *
+                           bf16_to_double(p->k[packed_index(k0 + kidx[a], kh, d, Hkv, D)]);
+                s[a] = p->scale * dot;
+            }
+            double M = s[0];
+            for (int a = 1; a < n; ++a)
+                if (s[a] > M)
+                    M = s[a];
+            double Z = 0.0;
+            for (int a = 0; a < n; ++a) {
+                w[a] = exp(s[a] - M);
+                Z += w[a];
+            }
+            for (int a = 0; a < n; ++a)
+                w[a] /= Z;                              /* P_j */
+            /* dP_j and Delta */
+            double delta = 0.0;
+            for (int a = 0; a < n; ++a) {
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d)
+                    dot += bf16_to_double(job->dout[packed_index(tq, h, d, H, D)]) *
+                           bf16_to_double(p->v[packed_index(k0 + kidx[a], kh, d, Hkv, D)]);
+                dp[a] = dot;
+                delta += w[a] * dot;
+            }
+            for (int a = 0; a < n; ++a) {
+                const double ds = w[a] * (dp[a] - delta);
+                const int64_t tk = k0 + kidx[a];
+                double *dk_row = job->dk + packed_index(tk, kh, 0, Hkv, D);
+                double *dv_row = job->dv + packed_index(tk, kh, 0, Hkv, D);
+                for (int d = 0; d < D; ++d) {
+                    dq_row[d] += p->scale * ds *
+                                 bf16_to_double(p->k[packed_index(tk, kh, d, Hkv, D)]);
+                    dk_row[d] += p->scale * ds *
+                                 bf16_to_double(p->q[packed_index(tq, h, d, H, D)]);
+                    dv_row[d] += w[a] * bf16_to_double(job->dout[packed_index(tq, h, d, H, D)]);
+                }
+            }
+        }
+    }
+    free(dp);
+}
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job *job = (bwd_job *)arg;
+    const int Hkv = job->p->num_kv_heads;
+    size_t nscratch = (size_t)(job->max_lk > 0 ? job->max_lk : 1);
+    double *s = (double *)malloc(nscratch * sizeof(double));
+    double *w = (double *)malloc(nscratch * sizeof(double));
+    int *kidx = (int *)malloc(nscratch * sizeof(int));
+    if (!s || !w || !kidx) {
+        __atomic_store_n(&job->status, -1, __ATOMIC_SEQ_CST);
+        free(s); free(w); free(kidx);
+        return NULL;
+    }
+    for (;;) {
+        int64_t u = __atomic_fetch_add(&job->next, 1, __ATOMIC_RELAXED);
+        if (u >= job->n_units)
+            break;
+        bwd_unit(job, (int)(u / Hkv), (int)(u % Hkv), s, w, kidx);
+    }
+    free(s); free(w); free(kidx);
+    return NULL;
+}
+
+/*
+ * Full varlen backward.  q, dout: [cu_q[B], H, D]; k, v: [cu_k[B], Hkv, D]
+ * (bf16 bits).  dq: double [cu_q[B], H, D]; dk, dv: double [cu_k[B], Hkv, D]
+ * (overwritten).  Same masks and argument rules as oracle_varlen_fwd.
+ * Returns the number of threads used (> 0), or < 0 on bad arguments.
+ */
+int oracle_varlen_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const uint16_t *dout, const int32_t *cu_q, const int32_t *cu_k,
+                      int batch, int num_heads, int num_kv_heads, int head_dim, double scale,
+                      int causal, int window_left, double *dq, double *dk, double *dv,
+                      int nthreads)
+{
+    if (batch < 1 || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads != 0 ||
+        head_dim < 1 || causal < 0 || causal > 2 || (window_left >= 0 && causal == 0))
+        return -1;
+    if (check_cu(cu_q, batch) || check_cu(cu_k, batch))
+        return -2;
+    varlen_problem p = {q, k, v, cu_q, cu_k, batch, num_heads, num_kv_heads, head_dim, scale,
+                        causal, window_left};
+    memset(dk, 0, (size_t)cu_k[batch] * (size_t)num_kv_heads * (size_t)head_dim * sizeof(double));
+    memset(dv, 0, (size_t)cu_k[batch] * (size_t)num_kv_heads * (size_t)head_dim * sizeof(double));
+    bwd_job job;
+    memset(&job, 0, sizeof job);
+    job.p = &p;
+    job.dout = dout;
+    job.dq = dq;
+    job.dk = dk;
+    job.dv = dv;
+    job.n_units = (int64_t)batch * num_kv_heads;
+    job.max_lk = max_len(cu_k, batch);
+    if (nthreads <= 0)
+        nthreads = oracle_default_threads();
+    if ((int64_t)nthreads > job.n_units)
+        nthreads = (int)job.n_units;
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!tid)
+        return -1;
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (pthread_create(&tid[t], NULL, bwd_worker, &job) != 0)
+            break;
+        ++started;
+    }
+    if (started == 0)
+        bwd_worker(&job);
+    for (int t = 0; t < started; ++t)
+        pthread_join(tid[t], NULL);
+    free(tid);
+    if (job.status != 0)
+        return -1;
+    return started > 0 ? started : 1;
 }
 
 /* ------------------------------------------------------------------------ */
