@@ -206,6 +206,49 @@ vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_se
                                int32_t *n_items, int32_t *status, void *scratch,
                                size_t scratch_bytes, vfa_stream_t stream);
 
+/*
+ * Gradients of vfa_varlen_fwd: dq, dk, dv for an upstream gradient dout.
+ *
+ * The pages name a varlen backward without defining it; this computes the
+ * exact derivative of the forward's definition (same masks, head grouping
+ * and window): with P = exp(scale * q.k - lse) over a row's visible keys,
+ * dP = dout . v, Delta = sum_d dout * out and dS = P * (dP - Delta):
+ *   dv[j] = sum_i P_ij dout_i,  dk[j] = scale * sum_i dS_ij q_i,
+ *   dq[i] = scale * sum_j dS_ij k_j,
+ * with dk, dv of a kv head summed over its query heads.  P and dS are
+ * rounded to bf16 for the products (fp32 accumulation), as the forward's P.
+ *
+ * q, out, dout  device bf16 [total_q, num_heads, head_dim] (out and lse are
+ *               the forward's results for these q, k, v).
+ * k, v          device bf16 [total_k, num_kv_heads, head_dim].
+ * lse           device f32 [total_q, num_heads], natural log (-FLT_MAX for
+ *               rows without visible keys, which get dq = 0).
+ * cu_seqlens_q/k, total_q/k, batch, num_heads, num_kv_heads, softmax_scale,
+ * causal, window_left: as in vfa_varlen_fwd (softmax_scale must be > 0).
+ * dq            device bf16 [total_q, num_heads, head_dim] (output).
+ * dk, dv        device bf16 [total_k, num_kv_heads, head_dim] (output; keys
+ *               no query sees get 0).
+ * workspace     device scratch of vfa_varlen_bwd_workspace_bytes() bytes,
+ *               256-byte aligned (status word, per-sequence key-tile starts,
+ *               Delta, an fp32 dq sum); calls sharing it must be
+ *               stream-ordered.  Its first int32 is the device status word
+ *               (read with vfa_read_status): VFA_ERR_BAD_SEQLENS for invalid
+ *               cu_seqlens (nothing written), VFA_ERR_TIMEOUT if a bounded
+ *               wait expired.
+ *
+ * Supported: head_dim 64 or 128 (others: VFA_ERR_UNSUPPORTED); 16-byte
+ * aligned tensors.  dq is accumulated with fp32 atomics, so its last bits
+ * can vary between runs; dk and dv are deterministic.
+ */
+size_t vfa_varlen_bwd_workspace_bytes(int batch, int total_q, int num_heads, int head_dim);
+
+vfa_status vfa_varlen_bwd(const void *q, const void *k, const void *v, const void *out,
+                          const void *dout, const float *lse, const int32_t *cu_seqlens_q,
+                          const int32_t *cu_seqlens_k, int total_q, int total_k, int batch,
+                          int num_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                          int causal, int window_left, void *dq, void *dk, void *dv,
+                          void *workspace, size_t workspace_bytes, vfa_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Paged GQA decode                                                          */
 /* ------------------------------------------------------------------------ */

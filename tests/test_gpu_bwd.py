@@ -1,0 +1,138 @@
+"""GPU parity of vfa_varlen_bwd against the fp64 backward oracle (through the C ABI).
+
+The forward's out and lse come from the GPU forward, as in training.  P and
+dS are rounded to bf16 for the tensor-core products and the gradients to bf16
+at the end, so each gradient tensor t is held to
+    |got - ref| <= BWD_ATOL * max|ref_t| + BWD_RTOL * |ref|   elementwise
+and a relative L2 error <= BWD_L2.  Outputs start as NaN canaries.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import to_dev
+from variable_length_flashattention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+BWD_ATOL = 1e-2      # of the tensor's largest |ref|
+BWD_RTOL = 2e-2
+BWD_L2 = 1e-2
+GRAD_FLOOR = 1e-2
+
+
+@pytest.fixture(scope="module")
+def vfa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from variable_length_flashattention_gb300 import build, vfa as binding
+    build.build()
+    return binding
+
+
+def _nan_like(t):
+    return torch.full_like(t.view(torch.int16), 0x7FC0).view(torch.bfloat16)
+
+
+def _run(vfa, case, dout, causal, window_left=-1):
+    d = to_dev(case)
+    out, lse = vfa.varlen_fwd(d["q"], d["k"], d["v"], d["cu_q"], d["cu_k"], case.max_seqlen_q,
+                              case.softmax_scale, causal, window_left=window_left)
+    g = dout.cuda()
+    dq, dk, dv = _nan_like(d["q"]), _nan_like(d["k"]), _nan_like(d["v"])
+    _, _, _, ws = vfa.varlen_bwd(d["q"], d["k"], d["v"], out, g, lse, d["cu_q"], d["cu_k"],
+                                 case.softmax_scale, causal, window_left, dq=dq, dk=dk, dv=dv)
+    status = vfa.read_status(ws)
+    torch.cuda.synchronize()
+    f = lambda t: t.float().cpu().double().numpy()
+    return f(dq), f(dk), f(dv), status
+
+
+def _check(got, ref, what):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite (unwritten?) gradients"
+    # inputs and dout are O(1), so gradient magnitudes below GRAD_FLOOR are
+    # rounding noise (e.g. a window of 0 keys: dS = P (dP - Delta) is exactly
+    # 0, and the kernel's dP and Delta differ only in summation order)
+    scale = max(np.abs(ref).max(), GRAD_FLOOR)
+    err = np.abs(got - ref)
+    bad = err > BWD_ATOL * scale + BWD_RTOL * np.abs(ref)
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst "
+                           f"{err.max():.4g} (scale {scale:.4g})")
+    l2 = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), GRAD_FLOOR * np.sqrt(ref.size))
+    assert l2 <= BWD_L2, f"{what}: relative L2 error {l2:.3g}"
+
+
+def _compare(vfa, oracle_mod, case, causal, window_left=-1, Hkv=None, seed=0):
+    dout = W.upstream_grad(case, seed)
+    dq, dk, dv, status = _run(vfa, case, dout, causal, window_left)
+    assert status == 0
+    H, D = case.num_heads, case.head_dim
+    rq, rk, rv, _ = oracle_mod.varlen_bwd(case.q, case.k, case.v, dout, case.cu_seqlens_q,
+                                          case.cu_seqlens_k, H, D, case.softmax_scale, causal,
+                                          num_kv_heads=Hkv or H, window_left=window_left)
+    what = f"causal {causal} window {window_left} D={D} H={H}/{Hkv or H}"
+    _check(dq, rq, "dq " + what)
+    _check(dk, rk, "dk " + what)
+    _check(dv, rv, "dv " + what)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_small_mixes(vfa, oracle_mod, D, causal):
+    lq = [1, 7, 64, 129, 300, 0, 257]
+    lk = [1, 7, 64, 129, 300, 5, 90] if causal == 2 else [1, 7, 64, 129, 300, 5, 257]
+    case = W.make_varlen("bwd", lq, lk, 2, D, bool(causal), 1.0, value_seed=D + causal)
+    _compare(vfa, oracle_mod, case, causal, seed=causal)
+
+
+@pytest.mark.parametrize("window_left", [0, 100, 300])
+@pytest.mark.parametrize("causal", [1, 2])
+def test_sliding_window(vfa, oracle_mod, window_left, causal):
+    lq, lk = [500, 64, 700, 1], [500, 300, 400, 50]
+    case = W.make_varlen("bwd-window", lq, lk, 2, 128, True, 1.0, value_seed=7 + window_left)
+    _compare(vfa, oracle_mod, case, causal, window_left=window_left, seed=window_left)
+
+
+@pytest.mark.parametrize("H,Hkv,D", [(8, 2, 128), (4, 1, 64)])
+def test_grouped_kv_heads(vfa, oracle_mod, H, Hkv, D):
+    lq, lk = [300, 7, 129, 64], [300, 40, 129, 200]
+    case = W.make_varlen("bwd-gqa", lq, lk, H, D, True, 1.0, value_seed=H + Hkv)
+    case.k = case.k[:, :Hkv].contiguous()
+    case.v = case.v[:, :Hkv].contiguous()
+    _compare(vfa, oracle_mod, case, 1, Hkv=Hkv, seed=3)
+
+
+def test_packed_batch_sequences(vfa, oracle_mod):
+    # the packed workload (16 sequences up to 2048 tokens, H=16, D=128, causal)
+    # runs whole on the GPU; sequences are independent, so the oracle checks
+    # three of them (the longest, a short one, one in between) on their own
+    case = W.packed(0)
+    dout = W.upstream_grad(case, 0)
+    dq, dk, dv, status = _run(vfa, case, dout, 1)
+    assert status == 0
+    L = case.lengths_q
+    picks = [int(np.argmax(L)), int(np.argmin(L)), len(L) // 2]
+    for b in picks:
+        q0, q1 = int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1])
+        sub = W.make_varlen("one", [L[b]], [L[b]], 16, 128, True, 1.0, value_seed=0)
+        sub.q, sub.k, sub.v = case.q[q0:q1], case.k[q0:q1], case.v[q0:q1]
+        rq, rk, rv, _ = oracle_mod.varlen_bwd(sub.q, sub.k, sub.v, dout[q0:q1],
+                                              sub.cu_seqlens_q, sub.cu_seqlens_k, 16, 128,
+                                              case.softmax_scale, 1)
+        _check(dq[q0:q1], rq, f"dq seq {b}")
+        _check(dk[q0:q1], rk, f"dk seq {b}")
+        _check(dv[q0:q1], rv, f"dv seq {b}")
+
+
+def test_bad_cu_seqlens_sets_status(vfa):
+    case = W.make_varlen("bad", [10, 20], [10, 20], 1, 64, True, 1.0, value_seed=1)
+    d = to_dev(case)
+    out, lse = vfa.varlen_fwd(d["q"], d["k"], d["v"], d["cu_q"], d["cu_k"], 20,
+                              case.softmax_scale, True)
+    bad = d["cu_q"].clone()
+    bad[1] = 35                                  # [0, 35, 30]: decreasing
+    dq = _nan_like(d["q"])
+    _, _, _, ws = vfa.varlen_bwd(d["q"], d["k"], d["v"], out, out, lse, bad, d["cu_k"],
+                                 case.softmax_scale, 1, dq=dq)
+    assert vfa.read_status(ws) == vfa.VFA_ERR_BAD_SEQLENS
+    assert torch.isnan(dq.float()).all()

@@ -323,6 +323,92 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     return VFA_OK;
 }
 
+size_t vfa_varlen_bwd_workspace_bytes(int batch, int total_q, int num_heads, int head_dim)
+{
+    if (batch < 1 || total_q < 0 || num_heads < 1 || (head_dim != 64 && head_dim != 128))
+        return 0;
+    return vfa::bwd_workspace_bytes(batch, total_q, num_heads, head_dim);
+}
+
+vfa_status vfa_varlen_bwd(const void *q, const void *k, const void *v, const void *out,
+                          const void *dout, const float *lse, const int32_t *cu_seqlens_q,
+                          const int32_t *cu_seqlens_k, int total_q, int total_k, int batch,
+                          int num_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                          int causal, int window_left, void *dq, void *dk, void *dv,
+                          void *workspace, size_t workspace_bytes, vfa_stream_t stream)
+{
+    if (!q || !k || !v || !out || !dout || !lse || !cu_seqlens_q || !cu_seqlens_k || !dq ||
+        !dk || !dv || !workspace)
+        return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
+    if (batch < 1 || num_heads < 1 || total_q < 0 || total_k < 0)
+        return fail(VFA_ERR_INVALID_ARG, "bad size argument (batch %d, heads %d, totals %d/%d)",
+                    batch, num_heads, total_q, total_k);
+    if (num_kv_heads < 1 || num_heads % num_kv_heads != 0)
+        return fail(VFA_ERR_INVALID_ARG, "num_heads %d is not a multiple of num_kv_heads %d",
+                    num_heads, num_kv_heads);
+    if (causal < 0 || causal > 2)
+        return fail(VFA_ERR_INVALID_ARG, "causal must be 0, 1 (top-left) or 2 (bottom-right)");
+    if (window_left >= 0 && causal == 0)
+        return fail(VFA_ERR_INVALID_ARG, "a sliding window needs a causal mode");
+    if (head_dim != 64 && head_dim != 128)
+        return fail(VFA_ERR_UNSUPPORTED, "backward head_dim %d not supported (64, 128)",
+                    head_dim);
+    if (!(softmax_scale > 0.f) || softmax_scale > FLT_MAX)
+        return fail(VFA_ERR_INVALID_ARG, "softmax_scale must be finite and > 0 (got %g)",
+                    static_cast<double>(softmax_scale));
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+        !aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+        !aligned(lse, 4) || !aligned(workspace, 256))
+        return fail(VFA_ERR_INVALID_ARG,
+                    "tensors must be 16-byte aligned, lse 4-byte, workspace 256-byte");
+    if (static_cast<long long>(total_q) * num_heads * head_dim > (1LL << 31) ||
+        static_cast<long long>(total_k) * num_heads > (1LL << 31))
+        return fail(VFA_ERR_UNSUPPORTED, "tensor too large");
+    const size_t need = vfa::bwd_workspace_bytes(batch, total_q, num_heads, head_dim);
+    if (workspace_bytes < need)
+        return fail(VFA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
+                    need);
+    DeviceInfo dev;
+    vfa_status st = current_device(&dev);
+    if (st)
+        return st;
+    vfa::BwdArgs a;
+    memset(&a, 0, sizeof a);
+    if ((st = encode_packed_map(&a.tm_q, q, total_q, num_heads, head_dim, 128)) ||
+        (st = encode_packed_map(&a.tm_do, dout, total_q, num_heads, head_dim, 128)) ||
+        (st = encode_packed_map(&a.tm_k, k, total_k, num_kv_heads, head_dim, 128)) ||
+        (st = encode_packed_map(&a.tm_v, v, total_k, num_kv_heads, head_dim, 128)))
+        return st;
+    vfa::bwd_workspace_split(workspace, batch, total_q, num_heads, &a);
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.out = out;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.batch = batch;
+    a.total_q = total_q;
+    a.total_k = total_k;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.scale = softmax_scale;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.causal = causal;
+    a.window_left = window_left < 0 ? -1 : window_left;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(a.dq_acc, 0,
+                                    static_cast<size_t>(total_q) * num_heads * head_dim * 4, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "dQ accumulator clear");
+    const int key_tile_bound = total_k / 128 + batch;
+    e = vfa::launch_bwd(head_dim, a, key_tile_bound, dev.sm_count, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "backward launch");
+    return VFA_OK;
+}
+
 vfa_status vfa_paged_decode_init(float *m, float *l, float *o, int num_seqs, int num_q_heads,
                                  int head_dim, int32_t *device_status, vfa_stream_t stream)
 {

@@ -1,0 +1,545 @@
+// bwd.cu -- variable-length attention backward on sm_103a (head_dim 64, 128).
+//
+// Gradients of the forward (scaled scores, causal / bottom-right / sliding-
+// window masks on local positions, softmax over the visible keys) for an
+// upstream gradient dO, given the forward's out and natural-log lse.  With
+// P = exp(scale * q.k - lse), dP = dO V^T, Delta = rowsum(dO * out) and
+// dS = P * (dP - Delta):
+//   dV = P^T dO,   dK = scale * dS^T Q,   dQ = scale * dS K.
+//
+// Four kernels:
+//   * bwd_prep: one CTA validates cu_seqlens and writes each sequence's first
+//     global key tile (a prefix sum of ceil(Lk_b / 128));
+//   * bwd_delta: Delta[t, h] = sum_d dO * out, one warp per (token, head);
+//   * bwd_kernel: one CTA per (128-key tile, kv head).  K and V stay in
+//     shared memory; for every query head of the group and every 128-row q
+//     tile that sees one of the tile's keys, TMA brings Q and dO, and
+//     tcgen05.mma computes S^T = K Q^T and dP^T = V dO^T into TMEM; one
+//     thread per key row forms P^T and dS^T in bf16 (128-byte-swizzled shared
+//     memory), and three more MMAs accumulate dV += P^T dO and dK += dS^T Q in
+//     TMEM across the whole loop and compute this q tile's dQ = dS K, which
+//     the threads (now one per query row) add into an fp32 buffer with
+//     vector atomics.  At the end dK (scaled) and dV leave as bf16;
+//   * bwd_dq: dQ = bf16(scale * the fp32 sum).
+// TMEM: S^T 128 columns, dP^T 128 (dQ reuses them once dP is read), dV and
+// dK D each -- 512 for D = 128.  Every wait is bounded; on expiry the CTA
+// records VFA_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
+#include <cfloat>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace vfa {
+
+namespace {
+
+constexpr int kT = 128;            // key rows and query rows per tile
+constexpr int kThreads = 128;      // one thread per tile row
+constexpr int kPrepThreads = 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int DB = D / 64;                       // 64-column blocks per row
+    static constexpr uint32_t TILE_BYTES = kT * D * 2;      // a 128-row tile of K, V, Q or dO
+    static constexpr uint32_t PS_BYTES = kT * kT * 2;       // P^T or dS^T, 128 x 128 bf16
+    static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + D;
+    static constexpr uint32_t COL_DQ = COL_DPT;             // dQ takes dP^T's columns
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int NUM_BARS = 7;
+    static constexpr size_t SMEM = 1024 + 4 * TILE_BYTES + 2 * PS_BYTES + 2 * kT * 4 +
+                                   NUM_BARS * 8 + 64;
+    static constexpr uint32_t IDESC_T = idesc_bf16_f32(kT, kT, false, false);   // S^T, dP^T
+    static constexpr uint32_t IDESC_KV = idesc_bf16_f32(kT, D, false, true);    // dV, dK
+    static constexpr uint32_t IDESC_Q = idesc_bf16_f32(kT, D, true, true);      // dQ
+    static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+// ------------------------------------------------------------ prep
+
+__global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const BwdArgs a)
+{
+    __shared__ int warp_sums[32];
+    __shared__ int s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = a.batch;
+    if (tid == 0)
+        s_bad = (a.cu_q[0] != 0 || a.cu_k[0] != 0 || a.cu_q[B] != a.total_q ||
+                 a.cu_k[B] != a.total_k);
+    __syncthreads();
+    int carry = 0;
+    for (int base = 0; base < B; base += kPrepThreads) {
+        const int b = base + tid;
+        int nt = 0;
+        if (b < B) {
+            const int lq = a.cu_q[b + 1] - a.cu_q[b], lk = a.cu_k[b + 1] - a.cu_k[b];
+            if (lq < 0 || lk < 0)
+                s_bad = 1;
+            else
+                nt = (lk + kT - 1) / kT;
+        }
+        int x = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o)
+                x += y;
+        }
+        if (lane == 31)
+            warp_sums[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o)
+                    w += y;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        const int excl = x - nt + (warp > 0 ? warp_sums[warp - 1] : 0);
+        if (b < B)
+            a.ktile_start[b] = carry + excl;
+        carry += warp_sums[31];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        a.ktile_start[B] = carry;
+        *a.status = s_bad ? VFA_ERR_BAD_SEQLENS : VFA_OK;
+    }
+}
+
+// ------------------------------------------------------------ Delta
+
+template <int D>
+__global__ void bwd_delta_kernel(const BwdArgs a)
+{
+    if (*a.status != VFA_OK)
+        return;
+    const int lane = threadIdx.x & 31;
+    const long long rows = static_cast<long long>(a.total_q) * a.num_heads;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const __nv_bfloat16 *o = static_cast<const __nv_bfloat16 *>(a.out);
+    const __nv_bfloat16 *g = static_cast<const __nv_bfloat16 *>(a.dout);
+    for (long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+         r < rows; r += warps) {
+        float s = 0.f;
+#pragma unroll
+        for (int d = lane * 2; d < D; d += 64) {
+            const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(o + r * D + d);
+            const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162 *>(g + r * D + d);
+            s += __bfloat162float(x.x) * __bfloat162float(y.x) +
+                 __bfloat162float(x.y) * __bfloat162float(y.y);
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1)
+            s += __shfl_xor_sync(0xffffffffu, s, o2);
+        if (lane == 0)
+            a.delta[r] = s;
+    }
+}
+
+// ------------------------------------------------------------ main
+
+// Byte offset of the 16-byte chunk holding columns 8*c8 .. 8*c8+7 of row r in
+// a 128-row operand of 128 bf16 columns stored as two 64-column blocks with
+// the 128-byte swizzle (the layout TMA's SWIZZLE_128B gives).
+__device__ __forceinline__ uint32_t sw_chunk(int r, int c8)
+{
+    return static_cast<uint32_t>((c8 >> 3) * (kT * 128) + r * 128 + (((c8 & 7) ^ (r & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdArgs a)
+{
+    using C = BwdCfg<D>;
+    constexpr int DB = C::DB;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem_base;
+    __shared__ int s_abort;
+
+    if (*a.status != VFA_OK)
+        return;
+    const int B = a.batch, H = a.num_heads, Hkv = a.num_kv_heads;
+    const int gt = blockIdx.x, kh = blockIdx.y;
+    if (gt >= a.ktile_start[B])
+        return;
+    int lo = 0, hi = B - 1;                       // largest b with ktile_start[b] <= gt
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.ktile_start[mid] <= gt)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int b = lo, kt = gt - a.ktile_start[b];
+    const int q0 = a.cu_q[b], lq = a.cu_q[b + 1] - q0;
+    const int k0 = a.cu_k[b], lk = a.cu_k[b + 1] - k0;
+    const long long off = a.causal == 2 ? lk - lq : 0;
+    const int j_lo = kt * kT, j_hi = min(lk, j_lo + kT);
+    // query rows that see a key of this tile: i >= j - off (causal) and
+    // i <= j - off + window_left (window)
+    long long i_min = a.causal ? max(0ll, j_lo - off) : 0;
+    long long i_max = lq - 1;
+    if (a.window_left >= 0)
+        i_max = min(i_max, static_cast<long long>(j_hi) - 1 - off + a.window_left);
+    const int it0 = i_min <= i_max ? static_cast<int>(i_min / kT) : 0;
+    const int it1 = i_min <= i_max ? static_cast<int>(i_max / kT) + 1 : 0;
+    const int group = H / Hkv;
+    const int n_steps = (it1 - it0) * group;
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int r = tid;                            // this thread's tile row
+    const int j = j_lo + r;                       // its key (local position)
+    __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(a.dk);
+    __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(a.dv);
+
+    if (n_steps == 0) {
+        // no query sees these keys: zero gradients
+        if (j < lk) {
+            const size_t row = (static_cast<size_t>(k0 + j) * Hkv + kh) * D;
+#pragma unroll
+            for (int d = 0; d < D; d += 8) {
+                *reinterpret_cast<uint4 *>(dk + row + d) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(dv + row + d) = make_uint4(0, 0, 0, 0);
+            }
+        }
+        return;
+    }
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t sK = base, sV = sK + C::TILE_BYTES, sQ = sV + C::TILE_BYTES;
+    const uint32_t sDO = sQ + C::TILE_BYTES, sP = sDO + C::TILE_BYTES, sDS = sP + C::PS_BYTES;
+    const uint32_t sLse = sDS + C::PS_BYTES, sDelta = sLse + kT * 4;
+    const uint32_t bars = sDelta + kT * 4;
+    const uint32_t bar_kv = bars, bar_q = bars + 8, bar_mma = bars + 16, bar_ld = bars + 24;
+    const uint32_t bar_p = bars + 32, bar_dq = bars + 40, bar_drain = bars + 48;
+    float *lse_s = reinterpret_cast<float *>(smem_raw + (sLse - raw));
+    float *delta_s = reinterpret_cast<float *>(smem_raw + (sDelta - raw));
+    volatile int *abort = &s_abort;
+
+    if (tid == 0) {
+        s_abort = 0;
+        mbar_init(bar_kv, 1);
+        mbar_init(bar_q, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init(bar_ld, kThreads);
+        mbar_init(bar_p, kThreads);
+        mbar_init(bar_dq, kThreads);
+        mbar_init(bar_drain, 1);
+        fence_barrier_init();
+        tma_prefetch_map(&a.tm_q);
+        tma_prefetch_map(&a.tm_k);
+        tma_prefetch_map(&a.tm_v);
+        tma_prefetch_map(&a.tm_do);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&s_tmem_base), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem_base;
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
+        for (int db = 0; db < DB; ++db) {
+            tma_load_3d(sK + db * (kT * 128), &a.tm_k, bar_kv, db * 64, kh, k0 + j_lo);
+            tma_load_3d(sV + db * (kT * 128), &a.tm_v, bar_kv, db * 64, kh, k0 + j_lo);
+        }
+    }
+    const float scale_log2 = a.scale_log2;
+    const float *lse_g = a.lse;
+    const float *delta_g = a.delta;
+    const int wl = a.window_left;
+    bool ok = true;
+    int step = 0;
+    uint32_t q_issued = 0;
+    for (int hq = kh * group; hq < (kh + 1) * group && ok; ++hq) {
+        for (int it = it0; it < it1 && ok; ++it, ++step) {
+            const uint32_t ph = static_cast<uint32_t>(step) & 1u;
+            // Q and dO of this q tile; the previous step's MMAs, which read
+            // them, have completed (every thread waited for them)
+            if (tid == 0) {
+                mbar_arrive_expect_tx(bar_q, 2 * C::TILE_BYTES);
+                for (int db = 0; db < DB; ++db) {
+                    tma_load_3d(sQ + db * (kT * 128), &a.tm_q, bar_q, db * 64, hq, q0 + it * kT);
+                    tma_load_3d(sDO + db * (kT * 128), &a.tm_do, bar_q, db * 64, hq,
+                                q0 + it * kT);
+                }
+                ++q_issued;
+            }
+            {
+                const int i = it * kT + r;
+                const bool v = i < lq;
+                const size_t row = static_cast<size_t>(q0 + i) * H + hq;
+                lse_s[r] = v ? lse_g[row] * kLog2e : 0.f;
+                delta_s[r] = v ? delta_g[row] : 0.f;
+            }
+            mbar_arrive(bar_ld);
+            if (tid == 0) {
+                // S^T = K Q^T and dP^T = V dO^T, once the previous step's dQ
+                // (in dP^T's columns) has been read
+                if ((step == 0 && !mbar_wait(bar_kv, 0, abort)) ||
+                    (step > 0 && !mbar_wait(bar_dq, ph ^ 1u, abort)) ||
+                    !mbar_wait(bar_q, ph, abort)) {
+                    ok = false;
+                } else {
+                    tc_fence_after();
+                    const uint64_t k_d = sdesc_sw128(sK, 16, 1024), q_d = sdesc_sw128(sQ, 16, 1024);
+                    const uint64_t v_d = sdesc_sw128(sV, 16, 1024), o_d = sdesc_sw128(sDO, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t o16 = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
+                        mma_ss(tmem + C::COL_ST, k_d + o16, q_d + o16, C::IDESC_T, kk > 0);
+                        mma_ss(tmem + C::COL_DPT, v_d + o16, o_d + o16, C::IDESC_T, kk > 0);
+                    }
+                    mma_commit(bar_mma);
+                }
+            }
+            // warp-uniform from here: the TMEM loads below are warp-collective
+            ok = __all_sync(0xffffffffu,
+                            ok && mbar_wait(bar_ld, ph, abort) && mbar_wait(bar_mma, 0, abort));
+            if (!ok)
+                break;
+            tc_fence_after();
+            // P^T and dS^T for key row j: column c is query it * 128 + c
+#pragma unroll 1
+            for (int cb = 0; cb < kT; cb += 32) {
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_addr + C::COL_ST + cb, sr);
+                tmem_ld32(tmem + lane_addr + C::COL_DPT + cb, dr);
+                tmem_wait_ld();
+                uint32_t pk[16], dk2[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float p2[2], d2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int c = cb + e + u;
+                        const long long i = static_cast<long long>(it) * kT + c;
+                        bool valid = j < lk && i < lq;
+                        if (a.causal)
+                            valid = valid && j <= i + off;
+                        if (wl >= 0)
+                            valid = valid && j >= i + off - wl;
+                        const float p =
+                            valid ? ex2_approx(__uint_as_float(sr[e + u]) * scale_log2 - lse_s[c])
+                                  : 0.f;
+                        p2[u] = p;
+                        d2[u] = p * (__uint_as_float(dr[e + u]) - delta_s[c]);
+                    }
+                    pk[e >> 1] = pack_bf16x2(p2[0], p2[1]);
+                    dk2[e >> 1] = pack_bf16x2(d2[0], d2[1]);
+                }
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    const uint32_t o = sw_chunk(r, (cb >> 3) + q8);
+                    st_shared_v4(sP + o, pk[4 * q8], pk[4 * q8 + 1], pk[4 * q8 + 2], pk[4 * q8 + 3]);
+                    st_shared_v4(sDS + o, dk2[4 * q8], dk2[4 * q8 + 1], dk2[4 * q8 + 2],
+                                 dk2[4 * q8 + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_p);
+            if (tid == 0) {
+                // dV += P^T dO, dK += dS^T Q, dQ = dS K
+                if (!mbar_wait(bar_p, ph, abort)) {
+                    ok = false;
+                } else {
+                    tc_fence_after();
+                    const uint64_t p_d = sdesc_sw128(sP, 16, 1024);
+                    const uint64_t ds_d = sdesc_sw128(sDS, 16, 1024);
+                    const uint64_t do_mn = sdesc_sw128(sDO, kT * 128, 1024);
+                    const uint64_t q_mn = sdesc_sw128(sQ, kT * 128, 1024);
+                    const uint64_t ds_mn = sdesc_sw128(sDS, kT * 128, 1024);
+                    const uint64_t k_mn = sdesc_sw128(sK, kT * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kT / 16; ++kk) {
+                        const uint32_t ko = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
+                        const uint32_t mo = (kk * 16 * 128) >> 4;
+                        const uint32_t acc_kv = (step > 0 || kk > 0) ? 1u : 0u;
+                        mma_ss(tmem + C::COL_DV, p_d + ko, do_mn + mo, C::IDESC_KV, acc_kv);
+                        mma_ss(tmem + C::COL_DK, ds_d + ko, q_mn + mo, C::IDESC_KV, acc_kv);
+                        mma_ss(tmem + C::COL_DQ, ds_mn + mo, k_mn + mo, C::IDESC_Q, kk > 0);
+                    }
+                    mma_commit(bar_mma);
+                }
+            }
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(bar_mma, 1, abort));
+            if (!ok)
+                break;
+            tc_fence_after();
+            // this q tile's dQ rows (TMEM lane = query row) into the fp32 sum
+            {
+                float4 acc[D / 4];
+#pragma unroll
+                for (int cb = 0; cb < D; cb += 32) {
+                    uint32_t qr[32];
+                    tmem_ld32(tmem + lane_addr + C::COL_DQ + cb, qr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        acc[(cb + e) >> 2] =
+                            make_float4(__uint_as_float(qr[e]), __uint_as_float(qr[e + 1]),
+                                        __uint_as_float(qr[e + 2]), __uint_as_float(qr[e + 3]));
+                }
+                tc_fence_before();
+                mbar_arrive(bar_dq);
+                const int i = it * kT + r;
+                if (i < lq) {
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        a.dq_acc + (static_cast<size_t>(q0 + i) * H + hq) * D);
+#pragma unroll
+                    for (int c = 0; c < D / 4; ++c)
+                        atomicAdd(dst + c, acc[c]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort == 0) {
+        // dK (scaled) and dV rows of this key tile
+        const float sc = a.scale;
+        const size_t row = (static_cast<size_t>(k0 + j) * Hkv + kh) * D;
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+            const uint32_t col = which == 0 ? C::COL_DV : C::COL_DK;
+            const float f = which == 0 ? 1.f : sc;
+            __nv_bfloat16 *dst = which == 0 ? dv : dk;
+#pragma unroll
+            for (int cb = 0; cb < D; cb += 32) {
+                uint32_t rr[32];
+                tmem_ld32(tmem + lane_addr + col + cb, rr);
+                tmem_wait_ld();
+                if (j < lk) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(rr[e]) * f, __uint_as_float(rr[e + 1]) * f);
+                        v.y = pack_bf16x2(__uint_as_float(rr[e + 2]) * f,
+                                          __uint_as_float(rr[e + 3]) * f);
+                        v.z = pack_bf16x2(__uint_as_float(rr[e + 4]) * f,
+                                          __uint_as_float(rr[e + 5]) * f);
+                        v.w = pack_bf16x2(__uint_as_float(rr[e + 6]) * f,
+                                          __uint_as_float(rr[e + 7]) * f);
+                        *reinterpret_cast<uint4 *>(dst + row + cb + e) = v;
+                    }
+                }
+            }
+        }
+    } else if (tid == 0) {
+        // drain: every MMA this thread issued, and the copies in flight
+        mma_commit(bar_drain);
+        mbar_wait_drain(bar_drain, 0);
+        mbar_wait_drain(bar_kv, 0);
+        if (q_issued > 0)
+            mbar_wait_drain(bar_q, (q_issued - 1) & 1u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort && tid == 0)
+        atomicCAS(a.status, VFA_OK, VFA_ERR_TIMEOUT);
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------ dQ
+
+template <int D>
+__global__ void bwd_dq_kernel(const BwdArgs a)
+{
+    if (*a.status != VFA_OK)
+        return;
+    const long long n4 = static_cast<long long>(a.total_q) * a.num_heads * D / 4;
+    const float sc = a.scale;
+    const float4 *src = reinterpret_cast<const float4 *>(a.dq_acc);
+    uint2 *dst = reinterpret_cast<uint2 *>(a.dq);
+    for (long long x = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; x < n4;
+         x += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const float4 v = src[x];
+        dst[x] = make_uint2(pack_bf16x2(v.x * sc, v.y * sc), pack_bf16x2(v.z * sc, v.w * sc));
+    }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdArgs &a, int key_tile_bound, int sm_count, cudaStream_t s)
+{
+    static int attr_done[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 64 && !attr_done[dev]) {
+        e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(BwdCfg<D>::SMEM));
+        if (e != cudaSuccess)
+            return e;
+        attr_done[dev] = 1;
+    }
+    bwd_prep_kernel<<<1, kPrepThreads, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    const int grid_rows = sm_count * 8;
+    bwd_delta_kernel<D><<<grid_rows, 256, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    if (key_tile_bound > 0) {
+        bwd_kernel<D><<<dim3(key_tile_bound, a.num_kv_heads), kThreads, BwdCfg<D>::SMEM, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return e;
+    }
+    bwd_dq_kernel<D><<<grid_rows, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int batch, int total_q, int num_heads, int head_dim)
+{
+    size_t n = 256;                                                   // status word
+    n += (static_cast<size_t>(batch) + 1) * sizeof(int32_t);          // key tile starts
+    n = (n + 255) & ~static_cast<size_t>(255);
+    n += static_cast<size_t>(total_q) * num_heads * sizeof(float);    // Delta
+    n = (n + 255) & ~static_cast<size_t>(255);
+    n += static_cast<size_t>(total_q) * num_heads * head_dim * sizeof(float);   // dQ sum
+    return (n + 255) & ~static_cast<size_t>(255);
+}
+
+void bwd_workspace_split(void *ws, int batch, int total_q, int num_heads, BwdArgs *a)
+{
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    a->status = reinterpret_cast<int32_t *>(p);
+    size_t n = 256;
+    a->ktile_start = reinterpret_cast<int32_t *>(p + n);
+    n += (static_cast<size_t>(batch) + 1) * sizeof(int32_t);
+    n = (n + 255) & ~static_cast<size_t>(255);
+    a->delta = reinterpret_cast<float *>(p + n);
+    n += static_cast<size_t>(total_q) * num_heads * sizeof(float);
+    n = (n + 255) & ~static_cast<size_t>(255);
+    a->dq_acc = reinterpret_cast<float *>(p + n);
+}
+
+cudaError_t launch_bwd(int head_dim, const BwdArgs &a, int key_tile_bound, int sm_count,
+                       cudaStream_t stream)
+{
+    switch (head_dim) {
+    case 64: return launch_bwd_d<64>(a, key_tile_bound, sm_count, stream);
+    case 128: return launch_bwd_d<128>(a, key_tile_bound, sm_count, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace vfa

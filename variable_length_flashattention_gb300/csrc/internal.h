@@ -127,6 +127,31 @@ cudaError_t launch_decode_finalize(const float *l, const float *o, int num_seqs,
 cudaError_t launch_decode_gather(const DecodeStepArgs &a, void *k_out, void *v_out,
                                  cudaStream_t stream);
 
+// ------------------------------------------------------------ backward
+
+struct BwdArgs {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;   // boxes of 64 x 1 x 128 rows, 128-byte swizzle
+    const int32_t *cu_q;
+    const int32_t *cu_k;
+    const void *out, *dout;                 // bf16 [total_q, H, D]
+    const float *lse;                       // f32 [total_q, H], natural log
+    void *dq, *dk, *dv;                     // bf16 outputs
+    int32_t *status;                        // workspace: status word
+    int32_t *ktile_start;                   // workspace: [batch + 1] first key tile per sequence
+    float *delta;                           // workspace: [total_q, H]
+    float *dq_acc;                          // workspace: [total_q, H, D] fp32 dQ / scale
+    int batch, total_q, total_k, num_heads, num_kv_heads;
+    float scale, scale_log2;
+    int causal, window_left;
+};
+
+// Workspace bytes of the backward and its split into the BwdArgs pointers.
+size_t bwd_workspace_bytes(int batch, int total_q, int num_heads, int head_dim);
+void bwd_workspace_split(void *ws, int batch, int total_q, int num_heads, BwdArgs *a);
+// prep, Delta, main (grid: key_tile_bound x num_kv_heads) and dQ kernels.
+cudaError_t launch_bwd(int head_dim, const BwdArgs &a, int key_tile_bound, int sm_count,
+                       cudaStream_t stream);
+
 // ------------------------------------------------------------ test hooks
 
 cudaError_t launch_debug_bounded_wait(int32_t *status, cudaStream_t stream);

@@ -47,6 +47,9 @@ SIGNATURES = [
                                     _P, _P, _P]),
     ("vfa_varlen_schedule", _I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P,
                                  _S, _P]),
+    ("vfa_varlen_bwd_workspace_bytes", _S, [_I, _I, _I, _I]),
+    ("vfa_varlen_bwd", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                            _P, _P, _P, _P, _S, _P]),
     ("vfa_paged_decode_init", _I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     ("vfa_paged_decode_step", _I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                                    _P, _P, _P, _P]),
@@ -175,6 +178,48 @@ def varlen_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: 
                               _stream(stream))
     _check(st)
     return out, lse
+
+
+def alloc_bwd_workspace(batch: int, total_q: int, num_heads: int, head_dim: int,
+                        device="cuda") -> torch.Tensor:
+    n = lib().vfa_varlen_bwd_workspace_bytes(batch, total_q, num_heads, head_dim)
+    if n == 0:
+        raise VfaError(VFA_ERR_UNSUPPORTED, "backward workspace size query rejected its arguments")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def varlen_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+               dout: torch.Tensor, lse: torch.Tensor, cu_seqlens_q: torch.Tensor,
+               cu_seqlens_k: torch.Tensor, softmax_scale: float, causal,
+               window_left: int = -1, dq: Optional[torch.Tensor] = None,
+               dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+               workspace: Optional[torch.Tensor] = None, stream=None):
+    """(dq, dk, dv) bf16 = gradients of varlen_fwd for upstream gradient dout (vfa_varlen_bwd)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _need(cu_seqlens_k, torch.int32, "cu_seqlens_k")
+    if (q.dim() != 3 or k.shape != v.shape or out.shape != q.shape or dout.shape != q.shape or
+            q.shape[2] != k.shape[2] or q.shape[1] % k.shape[1] != 0):
+        raise ValueError("q, out, dout [Tq, H, D] and k, v [Tk, Hkv, D] with Hkv dividing H")
+    total_q, H, D = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    batch = cu_seqlens_q.numel() - 1
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, torch.bfloat16, n)
+    if workspace is None:
+        workspace = alloc_bwd_workspace(batch, total_q, H, D, device=q.device)
+    st = lib().vfa_varlen_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                              _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), total_q, total_k, batch, H,
+                              Hkv, D, float(softmax_scale), int(causal), int(window_left),
+                              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st)
+    return dq, dk, dv, workspace
 
 
 def varlen_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -147,6 +147,12 @@ def tiny(causal: bool, seed: int = 0) -> VarlenCase:
                        value_seed=seed)
 
 
+def upstream_grad(case: VarlenCase, seed: int) -> torch.Tensor:
+    """Seeded upstream gradient dL/dout for the backward: N(0, 1) in bf16, shaped like q."""
+    g = torch.Generator().manual_seed(1_000_003 + seed)
+    return torch.randn(case.q.shape, generator=g).to(torch.bfloat16)
+
+
 def packed(seed: int = 0) -> VarlenCase:
     L = packed_lengths(seed)
     return make_varlen("packed", L, L, 16, 128, True, 1.0, value_seed=seed)
