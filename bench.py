@@ -304,9 +304,27 @@ def run_ours(args):
         decode_pass()
     torch.cuda.synchronize()
 
+    # backward inputs: the forward's out / lse for these q, k, v and a seeded dout
+    has_bwd = case.head_dim in (64, 128) and not args.no_backward
+    if has_bwd:
+        g_out = W.upstream_grad(case, args.seed + rank).to(dev)
+        b_dq, b_dk, b_dv = torch.empty_like(d_q), torch.empty_like(d_k), torch.empty_like(d_v)
+        b_ws = vfa.alloc_bwd_workspace(case.batch, case.total_q, case.num_heads, case.head_dim,
+                                       device=dev)
+
+        def backward():
+            vfa.varlen_bwd(d_q, d_k, d_v, out, g_out, lse, d_cuq, d_cuk, case.softmax_scale,
+                           case.causal, dq=b_dq, dk=b_dk, dv=b_dv, workspace=b_ws)
+
+        backward()
+        torch.cuda.synchronize()
+        if vfa.read_status(b_ws) != 0:
+            raise RuntimeError("backward device status not OK in warm-up")
+
     launches_per_step = 2 + (2 + len(tiles))
     if args.profile:
-        part = prefill if args.profile == "prefill" else graph.replay
+        part = {"prefill": prefill, "decode": graph.replay,
+                "backward": backward if has_bwd else None}[args.profile]
         for i in range(args.warmup + args.steps):
             flush.fill_(float(i))
             part()
@@ -357,6 +375,29 @@ def run_ours(args):
         raise RuntimeError("device status not OK after timing")
     pre_mean = sum(pre_ms) / len(pre_ms)
     dec_mean = sum(dec_ms) / len(dec_ms)
+
+    # ---------------- backward: its own timed loop (not part of the step)
+    bwd_mean = None
+    if has_bwd:
+        b_steps = max(5, min(args.steps, 300))
+        for _ in range(max(3, args.warmup)):
+            flush.fill_(3.0)
+            backward()
+        bev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(b_steps)]
+        torch.cuda.synchronize()
+        for i in range(b_steps):
+            flush.fill_(float(i))
+            bev[i][0].record(stream)
+            backward()
+            bev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if vfa.read_status(b_ws) != 0:
+            raise RuntimeError("backward device status not OK after timing")
+        bwd_mean = sum(e[0].elapsed_time(e[1]) for e in bev) / b_steps
+        if world > 1:
+            t = torch.tensor([bwd_mean], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            bwd_mean = float(t.item())
     step_ms = pre_mean + dec_mean
     if world > 1:
         t = torch.tensor([pre_mean, dec_mean, step_ms], device=dev)
@@ -509,6 +550,21 @@ def run_ours(args):
         "clocks": clocks,
         "wall_s": wall,
     }
+    if bwd_mean is not None:
+        bflops = A.varlen_bwd_flops(case)
+        ach_b = bflops / (bwd_mean * 1e-3) / 1e12
+        line["backward"] = {
+            "value": world * ach_b, "unit": "TFLOP/s", "ms": bwd_mean,
+            "gflop": bflops / 1e9, "steps": b_steps, "gpu_launches": 4 * b_steps,
+            "how": "vfa_varlen_bwd on the same batch (its forward's out / lse, seeded dout); "
+                   "own timed loop with an L2 flush before each call",
+            "roofline": {"bound": "tensor", "achieved": ach_b, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": ach_b / peaks["bf16_tflops"],
+                         "traffic": _traffic("bwd_d128"),
+                         "kernel": "vfa_varlen_bwd (prep + Delta + main + dQ kernels, "
+                                   "timed together)",
+                         "peak_source": peaks["source"] + " bf16 burst"},
+        }
     if not args.no_cpu_baseline:
         rate, threads, nrows, secs = cpu_oracle_rate(case, args.cpu_seconds, args.seed)
         line["cpu_baseline"] = {
@@ -531,7 +587,9 @@ def main():
                              "tiny-causal"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the backward's timed loop")
+    ap.add_argument("--profile", choices=["prefill", "decode", "backward"], default=None,
                     help="run only W + K passes of one part (for ncu captures); no JSON line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=4,

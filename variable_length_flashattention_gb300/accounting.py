@@ -27,6 +27,13 @@ def varlen_flops(case) -> int:
                                                               case.causal)
 
 
+def varlen_bwd_flops(case) -> int:
+    """Backward: five products per attended pair (S = q.k, dP = dout.v, dV += P dout,
+    dK += dS q, dQ += dS k), 2 * D each, so 10 * H * D per pair (2.5 x the forward)."""
+    return 10 * case.num_heads * case.head_dim * attended_pairs(case.lengths_q, case.lengths_k,
+                                                               case.causal)
+
+
 def varlen_context_bytes(case) -> int:
     """Bytes read (q, k, v bf16) and written (out bf16, lse f32) once each."""
     H, D = case.num_heads, case.head_dim

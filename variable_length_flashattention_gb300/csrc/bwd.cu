@@ -13,13 +13,15 @@
 //   * bwd_delta: Delta[t, h] = sum_d dO * out, one warp per (token, head);
 //   * bwd_kernel: one CTA per (128-key tile, kv head).  K and V stay in
 //     shared memory; for every query head of the group and every 128-row q
-//     tile that sees one of the tile's keys, TMA brings Q and dO, and
-//     tcgen05.mma computes S^T = K Q^T and dP^T = V dO^T into TMEM; one
-//     thread per key row forms P^T and dS^T in bf16 (128-byte-swizzled shared
-//     memory), and three more MMAs accumulate dV += P^T dO and dK += dS^T Q in
-//     TMEM across the whole loop and compute this q tile's dQ = dS K, which
-//     the threads (now one per query row) add into an fp32 buffer with
-//     vector atomics.  At the end dK (scaled) and dV leave as bf16;
+//     tile that sees one of the tile's keys, TMA brings Q and dO (two
+//     buffers, so the next tile's copies overlap this one's work), and
+//     tcgen05.mma computes S^T = K Q^T and dP^T = V dO^T into TMEM; two
+//     threads per key row form P^T (bf16, back into TMEM over the S^T
+//     columns) and dS^T (bf16, 128-byte-swizzled shared memory), and three
+//     more MMAs accumulate dV += P^T dO and dK += dS^T Q in TMEM across the
+//     whole loop and compute this q tile's dQ = dS K, which the threads (now
+//     two per query row) add into an fp32 buffer with vector atomics.  At the
+//     end dK (scaled) and dV leave as bf16;
 //   * bwd_dq: dQ = bf16(scale * the fp32 sum).
 // TMEM: S^T 128 columns, dP^T 128 (dQ reuses them once dP is read), dV and
 // dK D each -- 512 for D = 128.  Every wait is bounded; on expiry the CTA
@@ -35,7 +37,9 @@ namespace vfa {
 namespace {
 
 constexpr int kT = 128;            // key rows and query rows per tile
-constexpr int kThreads = 128;      // one thread per tile row
+constexpr int kComputeWarps = 8;   // two threads per tile row, one per column half
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kThreads = kComputeThreads + 32;   // + the TMA / MMA issuing warp
 constexpr int kPrepThreads = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -43,12 +47,15 @@ template <int D>
 struct BwdCfg {
     static constexpr int DB = D / 64;                       // 64-column blocks per row
     static constexpr uint32_t TILE_BYTES = kT * D * 2;      // a 128-row tile of K, V, Q or dO
-    static constexpr uint32_t PS_BYTES = kT * kT * 2;       // P^T or dS^T, 128 x 128 bf16
+    static constexpr uint32_t PS_BYTES = kT * kT * 2;       // dS^T, 128 x 128 bf16
     static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + D;
     static constexpr uint32_t COL_DQ = COL_DPT;             // dQ takes dP^T's columns
+    // P^T (bf16 pairs) goes over the S^T columns: queries 0-63 to columns
+    // 0-31, queries 64-127 to columns 64-95
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int NUM_BARS = 7;
-    static constexpr size_t SMEM = 1024 + 4 * TILE_BYTES + 2 * PS_BYTES + 2 * kT * 4 +
+    static constexpr int NUM_BARS = 9;
+    // K, V, two Q and two dO buffers, dS^T, lse, Delta, barriers
+    static constexpr size_t SMEM = 1024 + 6 * TILE_BYTES + PS_BYTES + 2 * kT * 4 +
                                    NUM_BARS * 8 + 64;
     static constexpr uint32_t IDESC_T = idesc_bf16_f32(kT, kT, false, false);   // S^T, dP^T
     static constexpr uint32_t IDESC_KV = idesc_bf16_f32(kT, D, false, true);    // dV, dK
@@ -153,11 +160,88 @@ __device__ __forceinline__ uint32_t sw_chunk(int r, int c8)
     return static_cast<uint32_t>((c8 >> 3) * (kT * 128) + r * 128 + (((c8 & 7) ^ (r & 7)) << 4));
 }
 
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
+{
+    const uint4 v = ld_shared_v4(addr);
+    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                       __uint_as_float(v.w));
+}
+
+// Where the key row of this thread sees query column c of the tile (only
+// for tiles that are not fully visible).
+struct BwdMask {
+    int j, lk, lq, causal, wl;
+    long long i_lo, off;
+    __device__ __forceinline__ bool visible(int c) const
+    {
+        const long long i = i_lo + c;
+        bool v = j < lk && i < lq;
+        if (causal)
+            v = v && j <= i + off;
+        if (wl >= 0)
+            v = v && j >= i + off - wl;
+        return v;
+    }
+};
+
+// P^T and dS^T of one 16-column chunk of this thread's key row: p = 2^(s *
+// scale_log2 - lse2) (masked entries 0), ds = p * (dp - Delta); lse2 and
+// Delta of the chunk's columns come from shared memory (nl = -lse2).  The
+// bf16 pairs land in pk[0..7] and dk2[0..7].
+template <bool FULL>
+__device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[16], const uint32_t (&dr)[16],
+                                          float scale_log2, uint32_t s_nl, uint32_t s_delta,
+                                          int cb, const BwdMask &m, uint32_t *pk, uint32_t *dk2)
+{
+#pragma unroll
+    for (int e = 0; e < 16; e += 4) {
+        const float4 nl = ld_shared_f4(s_nl + (cb + e) * 4);
+        const float4 dl = ld_shared_f4(s_delta + (cb + e) * 4);
+        const float nls[4] = {nl.x, nl.y, nl.z, nl.w};
+        const float dls[4] = {dl.x, dl.y, dl.z, dl.w};
+        float p[4], d[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float x = ex2_approx(fmaf(__uint_as_float(sr[e + u]), scale_log2, nls[u]));
+            p[u] = FULL ? x : (m.visible(cb + e + u) ? x : 0.f);
+            d[u] = p[u] * (__uint_as_float(dr[e + u]) - dls[u]);
+        }
+        pk[(e >> 1)] = pack_bf16x2(p[0], p[1]);
+        pk[(e >> 1) + 1] = pack_bf16x2(p[2], p[3]);
+        dk2[(e >> 1)] = pack_bf16x2(d[0], d[1]);
+        dk2[(e >> 1) + 1] = pack_bf16x2(d[2], d[3]);
+    }
+}
+
+// Adds this thread's dQ row segment (DH floats) into the fp32 sum.
+template <int DH>
+__device__ __forceinline__ void flush_dq(float4 *dst, const float4 (&acc)[DH / 4])
+{
+#pragma unroll
+    for (int c = 0; c < DH / 4; ++c)
+        atomicAdd(dst + c, acc[c]);
+}
+
+// Warps 0-7 compute (warp w: TMEM lanes / tile rows 32 (w % 4) .. +31,
+// column half w / 4); warp 8 lane 0 issues the TMA copies and the MMAs.
+//
+// Per step s (one query head, one q tile):
+//   issuer:  [Q, dO of step s landed; dQ of step s-1 read]  S^T, dP^T -> bar_s
+//            [P^T in TMEM and dS^T in shared memory]  dV += P^T dO (A from
+//            TMEM), dK += dS^T Q, dQ = dS K -> bar_m2; then, once step s's
+//            products are done, the copies of step s + 2 into the freed buffer;
+//   compute: lse, Delta -> shared (bar_ld); [bar_s] P^T = exp(S^T scale -
+//            lse) into TMEM over the S^T columns it has read, dS^T = P^T (dP^T
+//            - Delta) into shared memory (bar_p); the previous step's dQ rows
+//            into the fp32 sum with vector atomics while the tensor core runs
+//            this step's products; [bar_m2] this step's dQ rows out of TMEM
+//            into registers (bar_dq).
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdArgs a)
 {
     using C = BwdCfg<D>;
     constexpr int DB = C::DB;
+    constexpr int DH = D / 2;                     // columns of dQ, dK, dV per thread
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
@@ -180,30 +264,32 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     const int q0 = a.cu_q[b], lq = a.cu_q[b + 1] - q0;
     const int k0 = a.cu_k[b], lk = a.cu_k[b + 1] - k0;
     const long long off = a.causal == 2 ? lk - lq : 0;
+    const int wl = a.window_left;
     const int j_lo = kt * kT, j_hi = min(lk, j_lo + kT);
     // query rows that see a key of this tile: i >= j - off (causal) and
     // i <= j - off + window_left (window)
     long long i_min = a.causal ? max(0ll, j_lo - off) : 0;
     long long i_max = lq - 1;
-    if (a.window_left >= 0)
-        i_max = min(i_max, static_cast<long long>(j_hi) - 1 - off + a.window_left);
+    if (wl >= 0)
+        i_max = min(i_max, static_cast<long long>(j_hi) - 1 - off + wl);
     const int it0 = i_min <= i_max ? static_cast<int>(i_min / kT) : 0;
-    const int it1 = i_min <= i_max ? static_cast<int>(i_max / kT) + 1 : 0;
+    const int n_it = i_min <= i_max ? static_cast<int>(i_max / kT) + 1 - it0 : 0;
     const int group = H / Hkv;
-    const int n_steps = (it1 - it0) * group;
+    const int n_steps = n_it * group;
 
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int r = tid;                            // this thread's tile row
-    const int j = j_lo + r;                       // its key (local position)
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = (warp & 3) * 32 + lane;         // tile row (TMEM lane) of compute threads
+    const int half = (warp >> 2) & 1;             // column half of compute threads
+    const int j = j_lo + r;                       // key (local position) of row r
     __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(a.dk);
     __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(a.dv);
 
     if (n_steps == 0) {
         // no query sees these keys: zero gradients
-        if (j < lk) {
-            const size_t row = (static_cast<size_t>(k0 + j) * Hkv + kh) * D;
+        if (warp < kComputeWarps && j < lk) {
+            const size_t row = (static_cast<size_t>(k0 + j) * Hkv + kh) * D + half * DH;
 #pragma unroll
-            for (int d = 0; d < D; d += 8) {
+            for (int d = 0; d < DH; d += 8) {
                 *reinterpret_cast<uint4 *>(dk + row + d) = make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4 *>(dv + row + d) = make_uint4(0, 0, 0, 0);
             }
@@ -213,30 +299,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t sK = base, sV = sK + C::TILE_BYTES, sQ = sV + C::TILE_BYTES;
-    const uint32_t sDO = sQ + C::TILE_BYTES, sP = sDO + C::TILE_BYTES, sDS = sP + C::PS_BYTES;
+    const uint32_t sK = base, sV = sK + C::TILE_BYTES;
+    const uint32_t sQ = sV + C::TILE_BYTES;           // two buffers
+    const uint32_t sDO = sQ + 2 * C::TILE_BYTES;      // two buffers
+    const uint32_t sDS = sDO + 2 * C::TILE_BYTES;
     const uint32_t sLse = sDS + C::PS_BYTES, sDelta = sLse + kT * 4;
     const uint32_t bars = sDelta + kT * 4;
-    const uint32_t bar_kv = bars, bar_q = bars + 8, bar_mma = bars + 16, bar_ld = bars + 24;
+    const uint32_t bar_kv = bars, bar_s = bars + 8, bar_m2 = bars + 16, bar_ld = bars + 24;
     const uint32_t bar_p = bars + 32, bar_dq = bars + 40, bar_drain = bars + 48;
-    float *lse_s = reinterpret_cast<float *>(smem_raw + (sLse - raw));
+    auto bar_q = [&](int x) { return bars + 56 + 8u * x; };
+    float *nl_s = reinterpret_cast<float *>(smem_raw + (sLse - raw));     // -lse * log2(e)
     float *delta_s = reinterpret_cast<float *>(smem_raw + (sDelta - raw));
     volatile int *abort = &s_abort;
 
     if (tid == 0) {
         s_abort = 0;
         mbar_init(bar_kv, 1);
-        mbar_init(bar_q, 1);
-        mbar_init(bar_mma, 1);
-        mbar_init(bar_ld, kThreads);
-        mbar_init(bar_p, kThreads);
-        mbar_init(bar_dq, kThreads);
+        mbar_init(bar_q(0), 1);
+        mbar_init(bar_q(1), 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_m2, 1);
+        mbar_init(bar_ld, kComputeThreads);
+        mbar_init(bar_p, kComputeThreads);
+        mbar_init(bar_dq, kComputeThreads);
         mbar_init(bar_drain, 1);
         fence_barrier_init();
-        tma_prefetch_map(&a.tm_q);
-        tma_prefetch_map(&a.tm_k);
-        tma_prefetch_map(&a.tm_v);
-        tma_prefetch_map(&a.tm_do);
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(&s_tmem_base), C::TMEM_COLS);
@@ -246,179 +333,215 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem_base;
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
 
-    if (tid == 0) {
-        mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
-        for (int db = 0; db < DB; ++db) {
-            tma_load_3d(sK + db * (kT * 128), &a.tm_k, bar_kv, db * 64, kh, k0 + j_lo);
-            tma_load_3d(sV + db * (kT * 128), &a.tm_v, bar_kv, db * 64, kh, k0 + j_lo);
-        }
-    }
-    const float scale_log2 = a.scale_log2;
-    const float *lse_g = a.lse;
-    const float *delta_g = a.delta;
-    const int wl = a.window_left;
-    bool ok = true;
-    int step = 0;
-    uint32_t q_issued = 0;
-    for (int hq = kh * group; hq < (kh + 1) * group && ok; ++hq) {
-        for (int it = it0; it < it1 && ok; ++it, ++step) {
-            const uint32_t ph = static_cast<uint32_t>(step) & 1u;
-            // Q and dO of this q tile; the previous step's MMAs, which read
-            // them, have completed (every thread waited for them)
-            if (tid == 0) {
-                mbar_arrive_expect_tx(bar_q, 2 * C::TILE_BYTES);
+    // step s -> (query head, q tile)
+    auto step_hq = [&](int s) { return kh * group + s / n_it; };
+    auto step_it = [&](int s) { return it0 + s % n_it; };
+
+    if (warp == kComputeWarps) {
+        // ------------------------------------------------------------ issuer
+        if (lane == 0) {
+            tma_prefetch_map(&a.tm_q);
+            tma_prefetch_map(&a.tm_k);
+            tma_prefetch_map(&a.tm_v);
+            tma_prefetch_map(&a.tm_do);
+            auto load_q = [&](int s) {
+                const int x = s & 1;
+                mbar_arrive_expect_tx(bar_q(x), 2 * C::TILE_BYTES);
+                const int row = q0 + step_it(s) * kT, hq = step_hq(s);
                 for (int db = 0; db < DB; ++db) {
-                    tma_load_3d(sQ + db * (kT * 128), &a.tm_q, bar_q, db * 64, hq, q0 + it * kT);
-                    tma_load_3d(sDO + db * (kT * 128), &a.tm_do, bar_q, db * 64, hq,
-                                q0 + it * kT);
+                    tma_load_3d(sQ + x * C::TILE_BYTES + db * (kT * 128), &a.tm_q, bar_q(x),
+                                db * 64, hq, row);
+                    tma_load_3d(sDO + x * C::TILE_BYTES + db * (kT * 128), &a.tm_do, bar_q(x),
+                                db * 64, hq, row);
                 }
-                ++q_issued;
+            };
+            mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
+            for (int db = 0; db < DB; ++db) {
+                tma_load_3d(sK + db * (kT * 128), &a.tm_k, bar_kv, db * 64, kh, k0 + j_lo);
+                tma_load_3d(sV + db * (kT * 128), &a.tm_v, bar_kv, db * 64, kh, k0 + j_lo);
             }
+            load_q(0);
+            int q_loads = 1;
+            if (n_steps > 1) {
+                load_q(1);
+                q_loads = 2;
+            }
+            const uint64_t k_d = sdesc_sw128(sK, 16, 1024), v_d = sdesc_sw128(sV, 16, 1024);
+            const uint64_t k_mn = sdesc_sw128(sK, kT * 128, 1024);
+            const uint64_t ds_d = sdesc_sw128(sDS, 16, 1024);
+            const uint64_t ds_mn = sdesc_sw128(sDS, kT * 128, 1024);
+            bool ok = mbar_wait(bar_kv, 0, abort);
+            for (int s = 0; s < n_steps && ok; ++s) {
+                const int x = s & 1;
+                const uint32_t ph = static_cast<uint32_t>(s) & 1u;
+                if (!mbar_wait(bar_q(x), static_cast<uint32_t>(s >> 1) & 1u, abort) ||
+                    (s > 0 && !mbar_wait(bar_dq, ph ^ 1u, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t q_d = sdesc_sw128(sQ + x * C::TILE_BYTES, 16, 1024);
+                const uint64_t o_d = sdesc_sw128(sDO + x * C::TILE_BYTES, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t o16 = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + C::COL_ST, k_d + o16, q_d + o16, C::IDESC_T, kk > 0);
+                    mma_ss(tmem + C::COL_DPT, v_d + o16, o_d + o16, C::IDESC_T, kk > 0);
+                }
+                mma_commit(bar_s);
+                if (!mbar_wait(bar_p, ph, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t do_mn = sdesc_sw128(sDO + x * C::TILE_BYTES, kT * 128, 1024);
+                const uint64_t q_mn = sdesc_sw128(sQ + x * C::TILE_BYTES, kT * 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kT / 16; ++kk) {
+                    // P^T of queries 16 kk .. 16 kk + 15: columns 0-31 hold
+                    // queries 0-63, columns 64-95 queries 64-127 (bf16 pairs)
+                    const uint32_t p_col = (kk < 4 ? 0u : 64u) + (kk & 3) * 8;
+                    const uint32_t ko = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
+                    const uint32_t mo = (kk * 16 * 128) >> 4;
+                    const uint32_t acc_kv = (s > 0 || kk > 0) ? 1u : 0u;
+                    mma_ts(tmem + C::COL_DV, tmem + C::COL_ST + p_col, do_mn + mo, C::IDESC_KV,
+                           acc_kv);
+                    mma_ss(tmem + C::COL_DK, ds_d + ko, q_mn + mo, C::IDESC_KV, acc_kv);
+                    mma_ss(tmem + C::COL_DQ, ds_mn + mo, k_mn + mo, C::IDESC_Q, kk > 0);
+                }
+                mma_commit(bar_m2);
+                // step s + 2's copies into this buffer once step s's products are done
+                if (s + 2 < n_steps) {
+                    if (!mbar_wait(bar_m2, ph, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    load_q(s + 2);
+                    ++q_loads;
+                }
+            }
+            if (!ok || *abort) {
+                mma_commit(bar_drain);
+                mbar_wait_drain(bar_drain, 0);
+                mbar_wait_drain(bar_kv, 0);
+                for (int x = 0; x < 2; ++x) {
+                    const int n = q_loads / 2 + (x < q_loads % 2 ? 1 : 0);   // copies into buffer x
+                    if (n > 0)
+                        mbar_wait_drain(bar_q(x), static_cast<uint32_t>(n - 1) & 1u);
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ compute
+        const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const float scale_log2 = a.scale_log2;
+        float4 acc[DH / 4];                       // dQ row segment of the previous step
+        float4 *acc_dst = nullptr;                // where it goes (null: nothing pending)
+        bool ok = true;
+        for (int s = 0; s < n_steps && ok; ++s) {
+            const uint32_t ph = static_cast<uint32_t>(s) & 1u;
+            const int hq = step_hq(s), it = step_it(s);
             {
-                const int i = it * kT + r;
-                const bool v = i < lq;
+                // -lse (log2 units) and Delta of the tile's query rows; the
+                // previous step's readers are past bar_m2, which needed them all
+                const int c = tid & (kT - 1);
+                const int i = it * kT + c;
                 const size_t row = static_cast<size_t>(q0 + i) * H + hq;
-                lse_s[r] = v ? lse_g[row] * kLog2e : 0.f;
-                delta_s[r] = v ? delta_g[row] : 0.f;
+                if (tid < kT)
+                    nl_s[c] = i < lq ? -a.lse[row] * kLog2e : 0.f;
+                else
+                    delta_s[c] = i < lq ? a.delta[row] : 0.f;
             }
             mbar_arrive(bar_ld);
-            if (tid == 0) {
-                // S^T = K Q^T and dP^T = V dO^T, once the previous step's dQ
-                // (in dP^T's columns) has been read
-                if ((step == 0 && !mbar_wait(bar_kv, 0, abort)) ||
-                    (step > 0 && !mbar_wait(bar_dq, ph ^ 1u, abort)) ||
-                    !mbar_wait(bar_q, ph, abort)) {
-                    ok = false;
-                } else {
-                    tc_fence_after();
-                    const uint64_t k_d = sdesc_sw128(sK, 16, 1024), q_d = sdesc_sw128(sQ, 16, 1024);
-                    const uint64_t v_d = sdesc_sw128(sV, 16, 1024), o_d = sdesc_sw128(sDO, 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t o16 = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
-                        mma_ss(tmem + C::COL_ST, k_d + o16, q_d + o16, C::IDESC_T, kk > 0);
-                        mma_ss(tmem + C::COL_DPT, v_d + o16, o_d + o16, C::IDESC_T, kk > 0);
-                    }
-                    mma_commit(bar_mma);
-                }
-            }
-            // warp-uniform from here: the TMEM loads below are warp-collective
-            ok = __all_sync(0xffffffffu,
-                            ok && mbar_wait(bar_ld, ph, abort) && mbar_wait(bar_mma, 0, abort));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_ld, ph, abort) && mbar_wait(bar_s, ph, abort));
             if (!ok)
                 break;
             tc_fence_after();
-            // P^T and dS^T for key row j: column c is query it * 128 + c
-#pragma unroll 1
-            for (int cb = 0; cb < kT; cb += 32) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_addr + C::COL_ST + cb, sr);
-                tmem_ld32(tmem + lane_addr + C::COL_DPT + cb, dr);
+            // a tile every (key, query) pair of which is visible needs no mask
+            BwdMask m;
+            m.j = j;
+            m.lk = lk;
+            m.lq = lq;
+            m.causal = a.causal;
+            m.wl = wl;
+            m.i_lo = static_cast<long long>(it) * kT;
+            m.off = off;
+            const bool full = j_lo + kT <= lk && m.i_lo + kT <= lq &&
+                              (!a.causal || j_lo + kT - 1 <= m.i_lo + off) &&
+                              (wl < 0 || j_lo >= m.i_lo + kT - 1 + off - wl);
+            uint32_t pk[16];
+#pragma unroll
+            for (int h4 = 0; h4 < 4; ++h4) {
+                const int cb = half * 64 + h4 * 16;       // first query column of the chunk
+                uint32_t sr[16], dr[16];
+                tmem_ld16(tmem + lane_addr + C::COL_ST + cb, sr);
+                tmem_ld16(tmem + lane_addr + C::COL_DPT + cb, dr);
                 tmem_wait_ld();
-                uint32_t pk[16], dk2[16];
+                uint32_t dk2[8];
+                if (full)
+                    bwd_chunk<true>(sr, dr, scale_log2, sLse, sDelta, cb, m, pk + (h4 & 1) * 8,
+                                    dk2);
+                else
+                    bwd_chunk<false>(sr, dr, scale_log2, sLse, sDelta, cb, m, pk + (h4 & 1) * 8,
+                                     dk2);
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float p2[2], d2[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int c = cb + e + u;
-                        const long long i = static_cast<long long>(it) * kT + c;
-                        bool valid = j < lk && i < lq;
-                        if (a.causal)
-                            valid = valid && j <= i + off;
-                        if (wl >= 0)
-                            valid = valid && j >= i + off - wl;
-                        const float p =
-                            valid ? ex2_approx(__uint_as_float(sr[e + u]) * scale_log2 - lse_s[c])
-                                  : 0.f;
-                        p2[u] = p;
-                        d2[u] = p * (__uint_as_float(dr[e + u]) - delta_s[c]);
-                    }
-                    pk[e >> 1] = pack_bf16x2(p2[0], p2[1]);
-                    dk2[e >> 1] = pack_bf16x2(d2[0], d2[1]);
-                }
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    const uint32_t o = sw_chunk(r, (cb >> 3) + q8);
-                    st_shared_v4(sP + o, pk[4 * q8], pk[4 * q8 + 1], pk[4 * q8 + 2], pk[4 * q8 + 3]);
-                    st_shared_v4(sDS + o, dk2[4 * q8], dk2[4 * q8 + 1], dk2[4 * q8 + 2],
-                                 dk2[4 * q8 + 3]);
-                }
+                for (int q8 = 0; q8 < 2; ++q8)
+                    st_shared_v4(sDS + sw_chunk(r, (cb >> 3) + q8), dk2[4 * q8], dk2[4 * q8 + 1],
+                                 dk2[4 * q8 + 2], dk2[4 * q8 + 3]);
+                // P^T (bf16 pairs) of 32 queries over S^T columns already read
+                if (h4 & 1)
+                    tmem_st16(tmem + lane_addr + C::COL_ST + half * 64 + (h4 >> 1) * 16, pk);
             }
+            tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar_p);
-            if (tid == 0) {
-                // dV += P^T dO, dK += dS^T Q, dQ = dS K
-                if (!mbar_wait(bar_p, ph, abort)) {
-                    ok = false;
-                } else {
-                    tc_fence_after();
-                    const uint64_t p_d = sdesc_sw128(sP, 16, 1024);
-                    const uint64_t ds_d = sdesc_sw128(sDS, 16, 1024);
-                    const uint64_t do_mn = sdesc_sw128(sDO, kT * 128, 1024);
-                    const uint64_t q_mn = sdesc_sw128(sQ, kT * 128, 1024);
-                    const uint64_t ds_mn = sdesc_sw128(sDS, kT * 128, 1024);
-                    const uint64_t k_mn = sdesc_sw128(sK, kT * 128, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < kT / 16; ++kk) {
-                        const uint32_t ko = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
-                        const uint32_t mo = (kk * 16 * 128) >> 4;
-                        const uint32_t acc_kv = (step > 0 || kk > 0) ? 1u : 0u;
-                        mma_ss(tmem + C::COL_DV, p_d + ko, do_mn + mo, C::IDESC_KV, acc_kv);
-                        mma_ss(tmem + C::COL_DK, ds_d + ko, q_mn + mo, C::IDESC_KV, acc_kv);
-                        mma_ss(tmem + C::COL_DQ, ds_mn + mo, k_mn + mo, C::IDESC_Q, kk > 0);
-                    }
-                    mma_commit(bar_mma);
-                }
-            }
-            ok = __all_sync(0xffffffffu, ok && mbar_wait(bar_mma, 1, abort));
+            if (acc_dst != nullptr)
+                flush_dq<DH>(acc_dst, acc);
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_m2, ph, abort));
             if (!ok)
                 break;
             tc_fence_after();
-            // this q tile's dQ rows (TMEM lane = query row) into the fp32 sum
-            {
-                float4 acc[D / 4];
+            // this half of the q tile's dQ rows (TMEM lane = query row)
 #pragma unroll
-                for (int cb = 0; cb < D; cb += 32) {
-                    uint32_t qr[32];
-                    tmem_ld32(tmem + lane_addr + C::COL_DQ + cb, qr);
-                    tmem_wait_ld();
+            for (int cb = 0; cb < DH; cb += 32) {
+                uint32_t qr[32];
+                tmem_ld32(tmem + lane_addr + C::COL_DQ + half * DH + cb, qr);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        acc[(cb + e) >> 2] =
-                            make_float4(__uint_as_float(qr[e]), __uint_as_float(qr[e + 1]),
-                                        __uint_as_float(qr[e + 2]), __uint_as_float(qr[e + 3]));
-                }
-                tc_fence_before();
-                mbar_arrive(bar_dq);
-                const int i = it * kT + r;
-                if (i < lq) {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        a.dq_acc + (static_cast<size_t>(q0 + i) * H + hq) * D);
-#pragma unroll
-                    for (int c = 0; c < D / 4; ++c)
-                        atomicAdd(dst + c, acc[c]);
-                }
+                for (int e = 0; e < 32; e += 4)
+                    acc[(cb + e) >> 2] =
+                        make_float4(__uint_as_float(qr[e]), __uint_as_float(qr[e + 1]),
+                                    __uint_as_float(qr[e + 2]), __uint_as_float(qr[e + 3]));
             }
+            tc_fence_before();
+            mbar_arrive(bar_dq);
+            const int i = it * kT + r;
+            acc_dst = i < lq ? reinterpret_cast<float4 *>(
+                                   a.dq_acc + (static_cast<size_t>(q0 + i) * H + hq) * D +
+                                   half * DH)
+                             : nullptr;
         }
+        if (ok && acc_dst != nullptr)
+            flush_dq<DH>(acc_dst, acc);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (*abort == 0) {
-        // dK (scaled) and dV rows of this key tile
+    if (*abort == 0 && warp < kComputeWarps) {
+        // dK (scaled) and dV rows of this key tile, this thread's column half
+        tc_fence_after();
+        const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const float sc = a.scale;
-        const size_t row = (static_cast<size_t>(k0 + j) * Hkv + kh) * D;
+        const size_t row = (static_cast<size_t>(k0 + j) * Hkv + kh) * D + half * DH;
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
-            const uint32_t col = which == 0 ? C::COL_DV : C::COL_DK;
+            const uint32_t col = (which == 0 ? C::COL_DV : C::COL_DK) + half * DH;
             const float f = which == 0 ? 1.f : sc;
             __nv_bfloat16 *dst = which == 0 ? dv : dk;
 #pragma unroll
-            for (int cb = 0; cb < D; cb += 32) {
+            for (int cb = 0; cb < DH; cb += 32) {
                 uint32_t rr[32];
                 tmem_ld32(tmem + lane_addr + col + cb, rr);
                 tmem_wait_ld();
@@ -438,13 +561,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
                 }
             }
         }
-    } else if (tid == 0) {
-        // drain: every MMA this thread issued, and the copies in flight
-        mma_commit(bar_drain);
-        mbar_wait_drain(bar_drain, 0);
-        mbar_wait_drain(bar_kv, 0);
-        if (q_issued > 0)
-            mbar_wait_drain(bar_q, (q_issued - 1) & 1u);
     }
     tc_fence_before();
     __syncthreads();
