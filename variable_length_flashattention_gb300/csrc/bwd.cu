@@ -53,11 +53,11 @@ struct BwdCfg {
     // P^T (bf16 pairs) goes over the S^T columns: queries 0-63 to columns
     // 0-31, queries 64-127 to columns 64-95
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int NUM_BARS = 9;
+    static constexpr int NUM_BARS = 11;
     // K, V, two Q and two dO buffers, dS^T, lse, Delta, barriers
     static constexpr size_t SMEM = 1024 + 6 * TILE_BYTES + PS_BYTES + 2 * kT * 4 +
                                    NUM_BARS * 8 + 64;
-    static constexpr uint32_t IDESC_T = idesc_bf16_f32(kT, kT, false, false);   // S^T, dP^T
+    static constexpr uint32_t IDESC_T = idesc_bf16_f32(kT, 64, false, false);   // S^T, dP^T halves
     static constexpr uint32_t IDESC_KV = idesc_bf16_f32(kT, D, false, true);    // dV, dK
     static constexpr uint32_t IDESC_Q = idesc_bf16_f32(kT, D, true, true);      // dQ
     static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
@@ -226,11 +226,13 @@ __device__ __forceinline__ void flush_dq(float4 *dst, const float4 (&acc)[DH / 4
 // column half w / 4); warp 8 lane 0 issues the TMA copies and the MMAs.
 //
 // Per step s (one query head, one q tile):
-//   issuer:  [Q, dO of step s landed; dQ of step s-1 read]  S^T, dP^T -> bar_s
-//            [P^T in TMEM and dS^T in shared memory]  dV += P^T dO (A from
-//            TMEM), dK += dS^T Q, dQ = dS K -> bar_m2; then, once step s's
-//            products are done, the copies of step s + 2 into the freed buffer;
-//   compute: lse, Delta -> shared (bar_ld); [bar_s] P^T = exp(S^T scale -
+//   issuer:  per query half h (64 columns): S^T_h, dP^T_h -> bar_s<h> (S^T_0
+//            right away, dP^T once step s-1's dQ, which it overwrites, has
+//            been read; that also frees step s-1's Q / dO buffer for step
+//            s+1's copies); [P^T_h in TMEM, dS^T_h in shared memory, bar_p<h>]
+//            dV += P^T_h dO_h (A from TMEM), dK += dS^T_h Q_h; after half 1,
+//            dQ = dS K -> bar_m2;
+//   compute: lse, Delta -> shared (bar_ld); [bar_s<h>] P^T = exp(S^T scale -
 //            lse) into TMEM over the S^T columns it has read, dS^T = P^T (dP^T
 //            - Delta) into shared memory (bar_p); the previous step's dQ rows
 //            into the fp32 sum with vector atomics while the tensor core runs
@@ -305,9 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     const uint32_t sDS = sDO + 2 * C::TILE_BYTES;
     const uint32_t sLse = sDS + C::PS_BYTES, sDelta = sLse + kT * 4;
     const uint32_t bars = sDelta + kT * 4;
-    const uint32_t bar_kv = bars, bar_s = bars + 8, bar_m2 = bars + 16, bar_ld = bars + 24;
-    const uint32_t bar_p = bars + 32, bar_dq = bars + 40, bar_drain = bars + 48;
-    auto bar_q = [&](int x) { return bars + 56 + 8u * x; };
+    const uint32_t bar_kv = bars, bar_s0 = bars + 8, bar_s1 = bars + 16, bar_m2 = bars + 24;
+    const uint32_t bar_ld = bars + 32, bar_p0 = bars + 40, bar_p1 = bars + 48;
+    const uint32_t bar_dq = bars + 56, bar_drain = bars + 64;
+    auto bar_q = [&](int x) { return bars + 72 + 8u * x; };
     float *nl_s = reinterpret_cast<float *>(smem_raw + (sLse - raw));     // -lse * log2(e)
     float *delta_s = reinterpret_cast<float *>(smem_raw + (sDelta - raw));
     volatile int *abort = &s_abort;
@@ -317,10 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         mbar_init(bar_kv, 1);
         mbar_init(bar_q(0), 1);
         mbar_init(bar_q(1), 1);
-        mbar_init(bar_s, 1);
+        mbar_init(bar_s0, 1);
+        mbar_init(bar_s1, 1);
         mbar_init(bar_m2, 1);
         mbar_init(bar_ld, kComputeThreads);
-        mbar_init(bar_p, kComputeThreads);
+        mbar_init(bar_p0, kComputeThreads / 2);
+        mbar_init(bar_p1, kComputeThreads / 2);
         mbar_init(bar_dq, kComputeThreads);
         mbar_init(bar_drain, 1);
         fence_barrier_init();
@@ -340,12 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 
     if (warp == kComputeWarps) {
         // ------------------------------------------------------------ issuer
+        // All 32 lanes run this loop on warp-uniform values; one elected lane
+        // issues each MMA and commit, lane 0 the copies.
         if (lane == 0) {
             tma_prefetch_map(&a.tm_q);
             tma_prefetch_map(&a.tm_k);
             tma_prefetch_map(&a.tm_v);
             tma_prefetch_map(&a.tm_do);
-            auto load_q = [&](int s) {
+        }
+        auto load_q = [&](int s) {
+            if (lane == 0) {
                 const int x = s & 1;
                 mbar_arrive_expect_tx(bar_q(x), 2 * C::TILE_BYTES);
                 const int row = q0 + step_it(s) * kT, hq = step_hq(s);
@@ -355,81 +364,124 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
                     tma_load_3d(sDO + x * C::TILE_BYTES + db * (kT * 128), &a.tm_do, bar_q(x),
                                 db * 64, hq, row);
                 }
-            };
+            }
+            __syncwarp();
+        };
+        if (lane == 0) {
             mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
             for (int db = 0; db < DB; ++db) {
                 tma_load_3d(sK + db * (kT * 128), &a.tm_k, bar_kv, db * 64, kh, k0 + j_lo);
                 tma_load_3d(sV + db * (kT * 128), &a.tm_v, bar_kv, db * 64, kh, k0 + j_lo);
             }
-            load_q(0);
-            int q_loads = 1;
-            if (n_steps > 1) {
-                load_q(1);
-                q_loads = 2;
+        }
+        load_q(0);
+        int q_loads = 1;
+        if (n_steps > 1) {
+            load_q(1);
+            q_loads = 2;
+        }
+        const uint64_t k_d = sdesc_sw128(sK, 16, 1024), v_d = sdesc_sw128(sV, 16, 1024);
+        const uint64_t k_mn = sdesc_sw128(sK, kT * 128, 1024);
+        const uint64_t ds_d = sdesc_sw128(sDS, 16, 1024);
+        const uint64_t ds_mn = sdesc_sw128(sDS, kT * 128, 1024);
+        // S^T_h or dP^T_h = (K or V) (Q or dO)^T for query half h (N = 64):
+        // queries 64 h .. 64 h + 63 start 64 h rows into each 64-column block
+        auto issue_t = [&](uint32_t d_col, uint64_t a_d, uint32_t b_buf, int h) {
+            const uint64_t b_d = sdesc_sw128(b_buf + h * 64 * 128, 16, 1024);
+            mma_ss_w<0>(tmem + d_col + h * 64, a_d, b_d, C::IDESC_T);
+#pragma unroll
+            for (int kk = 1; kk < D / 16; ++kk) {
+                const uint32_t o16 = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
+                mma_ss_w<1>(tmem + d_col + h * 64, a_d + o16, b_d + o16, C::IDESC_T);
             }
-            const uint64_t k_d = sdesc_sw128(sK, 16, 1024), v_d = sdesc_sw128(sV, 16, 1024);
-            const uint64_t k_mn = sdesc_sw128(sK, kT * 128, 1024);
-            const uint64_t ds_d = sdesc_sw128(sDS, 16, 1024);
-            const uint64_t ds_mn = sdesc_sw128(sDS, kT * 128, 1024);
-            bool ok = mbar_wait(bar_kv, 0, abort);
-            for (int s = 0; s < n_steps && ok; ++s) {
-                const int x = s & 1;
-                const uint32_t ph = static_cast<uint32_t>(s) & 1u;
-                if (!mbar_wait(bar_q(x), static_cast<uint32_t>(s >> 1) & 1u, abort) ||
-                    (s > 0 && !mbar_wait(bar_dq, ph ^ 1u, abort))) {
+        };
+        // dV += P^T dO and dK += dS^T Q over the queries of half h (K = 64)
+        auto issue_kv = [&](int h, uint32_t x, bool first) {
+            const uint64_t do_mn = sdesc_sw128(sDO + x * C::TILE_BYTES, kT * 128, 1024);
+            const uint64_t q_mn = sdesc_sw128(sQ + x * C::TILE_BYTES, kT * 128, 1024);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int kk = h * 4 + k4;
+                // P^T of queries 16 kk .. +15: bf16 pairs at columns 64 h + 8 k4
+                const uint32_t p_col = h * 64 + k4 * 8;
+                const uint32_t ko = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
+                const uint32_t mo = (kk * 16 * 128) >> 4;
+                if (k4 == 0 && first) {
+                    mma_ts_w<0>(tmem + C::COL_DV, tmem + C::COL_ST + p_col, do_mn + mo,
+                                C::IDESC_KV);
+                    mma_ss_w<0>(tmem + C::COL_DK, ds_d + ko, q_mn + mo, C::IDESC_KV);
+                } else {
+                    mma_ts_w<1>(tmem + C::COL_DV, tmem + C::COL_ST + p_col, do_mn + mo,
+                                C::IDESC_KV);
+                    mma_ss_w<1>(tmem + C::COL_DK, ds_d + ko, q_mn + mo, C::IDESC_KV);
+                }
+            }
+        };
+        // a wait the whole warp agrees on (the elected issue needs all lanes)
+        auto wait_all = [&](uint32_t bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+        };
+        bool ok = wait_all(bar_kv, 0);
+        for (int s = 0; s < n_steps && ok; ++s) {
+            const uint32_t x = static_cast<uint32_t>(s) & 1u;
+            const uint32_t ph = x;
+            if (!wait_all(bar_q(x), static_cast<uint32_t>(s >> 1) & 1u)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t q_buf = sQ + x * C::TILE_BYTES, o_buf = sDO + x * C::TILE_BYTES;
+            // S^T_0 needs no wait: it overwrites only P^T of the previous step,
+            // which that step's dV product (issued earlier) has read
+            issue_t(C::COL_ST, k_d, q_buf, 0);
+            if (s > 0) {
+                // dP^T goes over the previous step's dQ: wait until it is read;
+                // that step's products are then done, so its buffer takes the
+                // next step's Q and dO
+                if (!wait_all(bar_dq, ph ^ 1u)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t q_d = sdesc_sw128(sQ + x * C::TILE_BYTES, 16, 1024);
-                const uint64_t o_d = sdesc_sw128(sDO + x * C::TILE_BYTES, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t o16 = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + C::COL_ST, k_d + o16, q_d + o16, C::IDESC_T, kk > 0);
-                    mma_ss(tmem + C::COL_DPT, v_d + o16, o_d + o16, C::IDESC_T, kk > 0);
-                }
-                mma_commit(bar_s);
-                if (!mbar_wait(bar_p, ph, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t do_mn = sdesc_sw128(sDO + x * C::TILE_BYTES, kT * 128, 1024);
-                const uint64_t q_mn = sdesc_sw128(sQ + x * C::TILE_BYTES, kT * 128, 1024);
-#pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk) {
-                    // P^T of queries 16 kk .. 16 kk + 15: columns 0-31 hold
-                    // queries 0-63, columns 64-95 queries 64-127 (bf16 pairs)
-                    const uint32_t p_col = (kk < 4 ? 0u : 64u) + (kk & 3) * 8;
-                    const uint32_t ko = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
-                    const uint32_t mo = (kk * 16 * 128) >> 4;
-                    const uint32_t acc_kv = (s > 0 || kk > 0) ? 1u : 0u;
-                    mma_ts(tmem + C::COL_DV, tmem + C::COL_ST + p_col, do_mn + mo, C::IDESC_KV,
-                           acc_kv);
-                    mma_ss(tmem + C::COL_DK, ds_d + ko, q_mn + mo, C::IDESC_KV, acc_kv);
-                    mma_ss(tmem + C::COL_DQ, ds_mn + mo, k_mn + mo, C::IDESC_Q, kk > 0);
-                }
-                mma_commit(bar_m2);
-                // step s + 2's copies into this buffer once step s's products are done
-                if (s + 2 < n_steps) {
-                    if (!mbar_wait(bar_m2, ph, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    load_q(s + 2);
+                if (s + 1 < n_steps) {
+                    load_q(s + 1);
                     ++q_loads;
                 }
             }
-            if (!ok || *abort) {
-                mma_commit(bar_drain);
-                mbar_wait_drain(bar_drain, 0);
-                mbar_wait_drain(bar_kv, 0);
-                for (int x = 0; x < 2; ++x) {
-                    const int n = q_loads / 2 + (x < q_loads % 2 ? 1 : 0);   // copies into buffer x
-                    if (n > 0)
-                        mbar_wait_drain(bar_q(x), static_cast<uint32_t>(n - 1) & 1u);
-                }
+            issue_t(C::COL_DPT, v_d, o_buf, 0);
+            mma_commit_w(bar_s0);
+            issue_t(C::COL_ST, k_d, q_buf, 1);
+            issue_t(C::COL_DPT, v_d, o_buf, 1);
+            mma_commit_w(bar_s1);
+            if (!wait_all(bar_p0, ph)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            issue_kv(0, x, s == 0);
+            if (!wait_all(bar_p1, ph)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            issue_kv(1, x, false);
+            // dQ = dS K over all 128 keys
+            mma_ss_w<0>(tmem + C::COL_DQ, ds_mn, k_mn, C::IDESC_Q);
+#pragma unroll
+            for (int kk = 1; kk < kT / 16; ++kk) {
+                const uint32_t mo = (kk * 16 * 128) >> 4;
+                mma_ss_w<1>(tmem + C::COL_DQ, ds_mn + mo, k_mn + mo, C::IDESC_Q);
+            }
+            mma_commit_w(bar_m2);
+        }
+        if (!ok || *abort) {
+            mma_commit_w(bar_drain);
+            mbar_wait_drain(bar_drain, 0);
+            mbar_wait_drain(bar_kv, 0);
+            for (int xb = 0; xb < 2; ++xb) {
+                const int n = q_loads / 2 + (xb < q_loads % 2 ? 1 : 0);   // copies into buffer xb
+                if (n > 0)
+                    mbar_wait_drain(bar_q(xb), static_cast<uint32_t>(n - 1) & 1u);
             }
         }
     } else {
@@ -454,7 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
                     delta_s[c] = i < lq ? a.delta[row] : 0.f;
             }
             mbar_arrive(bar_ld);
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_ld, ph, abort) && mbar_wait(bar_s, ph, abort));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_ld, ph, abort) &&
+                                             mbar_wait(half ? bar_s1 : bar_s0, ph, abort));
             if (!ok)
                 break;
             tc_fence_after();
@@ -496,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar_p);
+            mbar_arrive(half ? bar_p1 : bar_p0);
             if (acc_dst != nullptr)
                 flush_dq<DH>(acc_dst, acc);
             ok = __all_sync(0xffffffffu, mbar_wait(bar_m2, ph, abort));
