@@ -10,7 +10,9 @@ a full paged-decode pass (init, every 32-block tile step, finalize) over the
 decode workload (64 sequences, context U{128..8192}, 32 q / 8 kv heads,
 D=128, block size 16), captured as one CUDA graph.  `value` is the forward's
 algorithmic TFLOP/s (4 * H * D * attended pairs); the decode half is
-reported under "decode" in GB/s of algorithmic bytes.  L2 is flushed (a
+reported under "decode" in GB/s of algorithmic bytes, and the varlen backward
+(vfa_varlen_bwd on the same batch) under "backward", timed in its own loop
+outside the step.  L2 is flushed (a
 256 MiB write) before each timed part; device time comes from CUDA events
 on the launching stream.  Under torchrun each rank runs its own replica
 (the path has no exchange step), so scaling is weak.
@@ -561,6 +563,7 @@ def run_ours(args):
             "roofline": {"bound": "tensor", "achieved": ach_b, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": ach_b / peaks["bf16_tflops"],
                          "traffic": _traffic("bwd_d128"),
+                         "traffic_unit": "DRAM bytes per launch of the main kernel (ncu)",
                          "kernel": "vfa_varlen_bwd (prep + Delta + main + dQ kernels, "
                                    "timed together)",
                          "peak_source": peaks["source"] + " bf16 burst"},
