@@ -232,9 +232,10 @@ __device__ __forceinline__ void flush_dq(float4 *dst, const float4 (&acc)[DH / 4
 //            s+1's copies); [P^T_h in TMEM, dS^T_h in shared memory, bar_p<h>]
 //            dV += P^T_h dO_h (A from TMEM), dK += dS^T_h Q_h; after half 1,
 //            dQ = dS K -> bar_m2;
-//   compute: lse, Delta -> shared (bar_ld); [bar_s<h>] P^T = exp(S^T scale -
-//            lse) into TMEM over the S^T columns it has read, dS^T = P^T (dP^T
-//            - Delta) into shared memory (bar_p); the previous step's dQ rows
+//   compute: lse, Delta -> shared (bar_ld); for h = 0, 1 in turn, all eight
+//            warps: [bar_s<h>] P^T = exp(S^T scale - lse) into TMEM over the
+//            S^T columns it has read, dS^T = P^T (dP^T - Delta) into shared
+//            memory (bar_p<h>); the previous step's dQ rows
 //            into the fp32 sum with vector atomics while the tensor core runs
 //            this step's products; [bar_m2] this step's dQ rows out of TMEM
 //            into registers (bar_dq).
@@ -282,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = (warp & 3) * 32 + lane;         // tile row (TMEM lane) of compute threads
     const int half = (warp >> 2) & 1;             // column half of compute threads
+    const int sub = half;                         // their 32-query slice within a query half
     const int j = j_lo + r;                       // key (local position) of row r
     __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(a.dk);
     __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(a.dv);
@@ -324,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
         mbar_init(bar_s1, 1);
         mbar_init(bar_m2, 1);
         mbar_init(bar_ld, kComputeThreads);
-        mbar_init(bar_p0, kComputeThreads / 2);
-        mbar_init(bar_p1, kComputeThreads / 2);
+        mbar_init(bar_p0, kComputeThreads);
+        mbar_init(bar_p1, kComputeThreads);
         mbar_init(bar_dq, kComputeThreads);
         mbar_init(bar_drain, 1);
         fence_barrier_init();
@@ -402,8 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
                 const int kk = h * 4 + k4;
-                // P^T of queries 16 kk .. +15: bf16 pairs at columns 64 h + 8 k4
-                const uint32_t p_col = h * 64 + k4 * 8;
+                // P^T of queries 16 kk .. +15: bf16 pairs at columns 64 h +
+                // 32 (k4 / 2) + 8 (k4 % 2), where the warps holding those queries put them
+                const uint32_t p_col = h * 64 + (k4 >> 1) * 32 + (k4 & 1) * 8;
                 const uint32_t ko = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
                 const uint32_t mo = (kk * 16 * 128) >> 4;
                 if (k4 == 0 && first) {
@@ -506,11 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
                     delta_s[c] = i < lq ? a.delta[row] : 0.f;
             }
             mbar_arrive(bar_ld);
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_ld, ph, abort) &&
-                                             mbar_wait(half ? bar_s1 : bar_s0, ph, abort));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_ld, ph, abort));
             if (!ok)
                 break;
-            tc_fence_after();
             // a tile every (key, query) pair of which is visible needs no mask
             BwdMask m;
             m.j = j;
@@ -523,33 +524,43 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
             const bool full = j_lo + kT <= lk && m.i_lo + kT <= lq &&
                               (!a.causal || j_lo + kT - 1 <= m.i_lo + off) &&
                               (wl < 0 || j_lo >= m.i_lo + kT - 1 + off - wl);
-            uint32_t pk[16];
+            // the query halves in turn, all eight warps on each: this warp takes
+            // queries 64 h + 32 g .. +31 of its 32 rows, so the tensor core runs
+            // half 1's S^T / dP^T and half 0's dV / dK while it works
+#pragma unroll 1
+            for (int h = 0; h < 2 && ok; ++h) {
+                ok = __all_sync(0xffffffffu, mbar_wait(h ? bar_s1 : bar_s0, ph, abort));
+                if (!ok)
+                    break;
+                tc_fence_after();
+                uint32_t pk[16];
 #pragma unroll
-            for (int h4 = 0; h4 < 4; ++h4) {
-                const int cb = half * 64 + h4 * 16;       // first query column of the chunk
-                uint32_t sr[16], dr[16];
-                tmem_ld16(tmem + lane_addr + C::COL_ST + cb, sr);
-                tmem_ld16(tmem + lane_addr + C::COL_DPT + cb, dr);
-                tmem_wait_ld();
-                uint32_t dk2[8];
-                if (full)
-                    bwd_chunk<true>(sr, dr, scale_log2, sLse, sDelta, cb, m, pk + (h4 & 1) * 8,
-                                    dk2);
-                else
-                    bwd_chunk<false>(sr, dr, scale_log2, sLse, sDelta, cb, m, pk + (h4 & 1) * 8,
-                                     dk2);
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int cb = h * 64 + sub * 32 + c2 * 16;   // first query column of the chunk
+                    uint32_t sr[16], dr[16];
+                    tmem_ld16(tmem + lane_addr + C::COL_ST + cb, sr);
+                    tmem_ld16(tmem + lane_addr + C::COL_DPT + cb, dr);
+                    tmem_wait_ld();
+                    uint32_t dk2[8];
+                    if (full)
+                        bwd_chunk<true>(sr, dr, scale_log2, sLse, sDelta, cb, m, pk + c2 * 8, dk2);
+                    else
+                        bwd_chunk<false>(sr, dr, scale_log2, sLse, sDelta, cb, m, pk + c2 * 8, dk2);
 #pragma unroll
-                for (int q8 = 0; q8 < 2; ++q8)
-                    st_shared_v4(sDS + sw_chunk(r, (cb >> 3) + q8), dk2[4 * q8], dk2[4 * q8 + 1],
-                                 dk2[4 * q8 + 2], dk2[4 * q8 + 3]);
-                // P^T (bf16 pairs) of 32 queries over S^T columns already read
-                if (h4 & 1)
-                    tmem_st16(tmem + lane_addr + C::COL_ST + half * 64 + (h4 >> 1) * 16, pk);
+                    for (int q8 = 0; q8 < 2; ++q8)
+                        st_shared_v4(sDS + sw_chunk(r, (cb >> 3) + q8), dk2[4 * q8],
+                                     dk2[4 * q8 + 1], dk2[4 * q8 + 2], dk2[4 * q8 + 3]);
+                }
+                // P^T (bf16 pairs) of these 32 queries over their own S^T columns,
+                // which only this warp reads
+                tmem_st16(tmem + lane_addr + C::COL_ST + h * 64 + sub * 32, pk);
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(h ? bar_p1 : bar_p0);
             }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(half ? bar_p1 : bar_p0);
+            if (!ok)
+                break;
             if (acc_dst != nullptr)
                 flush_dq<DH>(acc_dst, acc);
             ok = __all_sync(0xffffffffu, mbar_wait(bar_m2, ph, abort));
