@@ -69,6 +69,11 @@ def _load():
         lib.oracle_varlen_bwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f64, i32, i32, P,
                                           P, P, i32]
         lib.oracle_varlen_bwd.restype = i32
+        lib.oracle_varlen_fwd_fp8.argtypes = [P, P, P, P, P, i32, i32, i32, i32, f64, f64, f64,
+                                              i32, i32, P, P, i32]
+        lib.oracle_varlen_fwd_fp8.restype = i32
+        lib.oracle_fp8_e4m3_decode.argtypes = [P, i64, P]
+        lib.oracle_fp8_e4m3_decode.restype = None
         lib.oracle_decode_init.argtypes = [P, P, P, i32, i32, i32]
         lib.oracle_decode_init.restype = None
         lib.oracle_decode_step.argtypes = [P, P, P, i64, P, P, P, i32, i32, i32, i32, i32, i32,
@@ -157,6 +162,48 @@ def varlen_fwd_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_di
     return out, lse, int(n)
 
 
+def _u8(a) -> np.ndarray:
+    if isinstance(a, np.ndarray):
+        return np.ascontiguousarray(a.view(np.uint8))
+    import torch
+    return np.ascontiguousarray(a.detach().cpu().contiguous().view(torch.uint8).numpy())
+
+
+def fp8_e4m3_decode(codes) -> np.ndarray:
+    """Exact float64 values of FP8 E4M3 codes (uint8 array or a float8_e4m3fn tensor)."""
+    c = _u8(codes)
+    out = np.zeros(c.shape, dtype=np.float64)
+    _load().oracle_fp8_e4m3_decode(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def varlen_fwd_fp8(q8, k8, v, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_dim: int,
+                   softmax_scale: float, descale_q: float, descale_k: float, causal,
+                   nthreads: int = 0, num_kv_heads: int = 0, window_left: int = -1):
+    """Forward with FP8 E4M3 q and k (codes, one descale per tensor) and bf16 v.
+
+    Returns (out float64 [Tq,H,D], lse float64 [Tq,H], threads used)."""
+    lib = _load()
+    qb, kb, vb = _u8(q8), _u8(k8), _bits(v)
+    cq, ck = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    batch = len(cq) - 1
+    tq = int(cq[-1])
+    hkv = num_kv_heads or num_heads
+    if qb.size != tq * num_heads * head_dim:
+        raise ValueError("q size does not match cu_seqlens_q[-1] * H * D")
+    if kb.size != int(ck[-1]) * hkv * head_dim or vb.size != kb.size:
+        raise ValueError("k/v size does not match cu_seqlens_k[-1] * Hkv * D")
+    out = np.zeros((tq, num_heads, head_dim), dtype=np.float64)
+    lse = np.zeros((tq, num_heads), dtype=np.float64)
+    n = lib.oracle_varlen_fwd_fp8(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(cq), _ptr(ck), batch,
+                                  num_heads, hkv, head_dim, float(softmax_scale),
+                                  float(descale_q), float(descale_k), int(causal),
+                                  int(window_left), _ptr(out), _ptr(lse), int(nthreads))
+    if n <= 0:
+        raise ValueError(f"oracle_varlen_fwd_fp8 rejected its arguments ({n})")
+    return out, lse, int(n)
+
+
 def varlen_bwd(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, num_heads: int, head_dim: int,
                softmax_scale: float, causal, nthreads: int = 0, num_kv_heads: int = 0,
                window_left: int = -1):
@@ -240,5 +287,6 @@ def decode_finalize(state: DecodeState) -> np.ndarray:
 
 from .schedule import schedule, tile_cost  # noqa: E402  (integer rule, pure Python)
 
-__all__ = ["build", "default_threads", "varlen_fwd", "varlen_fwd_rows", "varlen_bwd", "DecodeState",
+__all__ = ["build", "default_threads", "varlen_fwd", "varlen_fwd_rows", "varlen_bwd",
+           "varlen_fwd_fp8", "fp8_e4m3_decode", "DecodeState",
            "decode_step", "decode_finalize", "schedule", "tile_cost", "FLT_MAX"]

@@ -12,6 +12,9 @@
  *     cu_seqlens prefix sums, scaled scores, causal and boundary masks,
  *     epilogue out = acc / l and lse = log(l) + m) and Task 2 Step 1
  *     (varlen_attention_cpu: per-sequence masked softmax times V).
+ *   - an FP8 variant of the forward (the plan names FP8 kernel configuration
+ *     types without content): q and k given as FP8 E4M3 codes with one
+ *     descale factor per tensor, read as descale * code exactly;
  *   - the backward is the derivative of that forward (the plan names a
  *     backward without giving one), written out per query row;
  *   - "attention_ref.rs" (spark_storage): AttnState::new, step_tile_ref,
@@ -63,6 +66,24 @@ static double bf16_to_double(uint16_t bits)
     return (double)f;
 }
 
+/*
+ * Exact value of an FP8 E4M3 code (the OCP 8-bit floating-point format's
+ * E4M3 encoding: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent 0 is subnormal, 2^-6 * m / 8; no infinities; S.1111.111 is NaN).
+ */
+static double fp8_e4m3_to_double(uint8_t b)
+{
+    const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    double mag;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
 /* Packed layout [tokens, heads, head_dim]: element (t, h, d). */
 static size_t packed_index(int64_t t, int h, int d, int num_heads, int head_dim)
 {
@@ -86,7 +107,20 @@ typedef struct {
     double scale;
     int causal;
     int window_left;                        /* < 0: none; else keys j >= i + off - window_left */
+    const uint8_t *q8, *k8;                 /* FP8 E4M3 q and k (then q, k unused), or NULL */
+    double descale_q, descale_k;            /* q = descale_q * code, k = descale_k * code */
 } varlen_problem;
+
+/* q and k elements as real numbers: bf16 widened, or FP8 code times its descale. */
+static double q_elem(const varlen_problem *p, size_t i)
+{
+    return p->q8 ? p->descale_q * fp8_e4m3_to_double(p->q8[i]) : bf16_to_double(p->q[i]);
+}
+
+static double k_elem(const varlen_problem *p, size_t i)
+{
+    return p->k8 ? p->descale_k * fp8_e4m3_to_double(p->k8[i]) : bf16_to_double(p->k[i]);
+}
 
 /*
  * One query row: local row i of sequence b, head h; its keys and values are
@@ -134,8 +168,8 @@ static void varlen_row(const varlen_problem *p, int b, int i, int h,
         const int64_t tk = k0 + kidx[a];
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
-            dot += bf16_to_double(p->q[packed_index(tq, h, d, H, D)]) *
-                   bf16_to_double(p->k[packed_index(tk, kh, d, Hkv, D)]);
+            dot += q_elem(p, packed_index(tq, h, d, H, D)) *
+                   k_elem(p, packed_index(tk, kh, d, Hkv, D));
         s[a] = p->scale * dot;
     }
     double M = s[0];
@@ -291,6 +325,43 @@ int oracle_varlen_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     job.out = out;
     job.lse = lse;
     return run_varlen_job(&job, nthreads);
+}
+
+/*
+ * The forward with FP8 E4M3 q and k: q8 [cu_q[B], H, D] and k8 [cu_k[B], Hkv, D]
+ * codes standing for descale_q * code and descale_k * code; v bf16.  Same
+ * definition, outputs and return value as oracle_varlen_fwd.
+ */
+int oracle_varlen_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint16_t *v,
+                          const int32_t *cu_q, const int32_t *cu_k, int batch, int num_heads,
+                          int num_kv_heads, int head_dim, double scale, double descale_q,
+                          double descale_k, int causal, int window_left, double *out,
+                          double *lse, int nthreads)
+{
+    if (batch < 1 || num_heads < 1 || num_kv_heads < 1 || num_heads % num_kv_heads != 0 ||
+        head_dim < 1 || causal < 0 || causal > 2 || (window_left >= 0 && causal == 0) ||
+        !q8 || !k8)
+        return -1;
+    if (check_cu(cu_q, batch) || check_cu(cu_k, batch))
+        return -2;
+    varlen_problem p = {NULL, NULL, v, cu_q, cu_k, batch, num_heads, num_kv_heads, head_dim,
+                        scale, causal, window_left, q8, k8, descale_q, descale_k};
+    varlen_job job;
+    memset(&job, 0, sizeof job);
+    job.p = &p;
+    job.rows = NULL;
+    job.n_units = (int64_t)batch * num_heads;
+    job.max_lk = max_len(cu_k, batch);
+    job.out = out;
+    job.lse = lse;
+    return run_varlen_job(&job, nthreads);
+}
+
+/* Exact values of n FP8 E4M3 codes (for the decoder's own pins). */
+void oracle_fp8_e4m3_decode(const uint8_t *codes, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = fp8_e4m3_to_double(codes[i]);
 }
 
 /*

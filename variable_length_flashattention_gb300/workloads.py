@@ -147,6 +147,23 @@ def tiny(causal: bool, seed: int = 0) -> VarlenCase:
                        value_seed=seed)
 
 
+@dataclass
+class Fp8Inputs:
+    """FP8 E4M3 q and k codes (uint8, shaped like the case's q and k) with one descale each."""
+    q8: torch.Tensor
+    k8: torch.Tensor
+    descale_q: float
+    descale_k: float
+
+
+def fp8_qk(case: VarlenCase, descale: float = 1.0 / 32.0) -> Fp8Inputs:
+    """The case's q and k rounded to FP8 E4M3 codes of x / descale (a power of two, so
+    descale * code is exact in bf16 too); seeded through the case's own values."""
+    def enc(t):
+        return (t.float() / descale).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+    return Fp8Inputs(enc(case.q), enc(case.k), descale, descale)
+
+
 def upstream_grad(case: VarlenCase, seed: int) -> torch.Tensor:
     """Seeded upstream gradient dL/dout for the backward: N(0, 1) in bf16, shaped like q."""
     g = torch.Generator().manual_seed(1_000_003 + seed)
