@@ -378,6 +378,39 @@ def run_ours(args):
     pre_mean = sum(pre_ms) / len(pre_ms)
     dec_mean = sum(dec_ms) / len(dec_ms)
 
+    # ---------------- FP8 q / k forward: its own timed loop (not part of the step)
+    fp8_mean = None
+    if case.head_dim == 128 and not args.no_fp8:
+        f8 = W.fp8_qk(case)
+        d_q8, d_k8 = f8.q8.to(dev), f8.k8.to(dev)
+        out8 = torch.empty_like(d_q)
+        lse8 = torch.empty_like(lse)
+
+        def forward_fp8():
+            vfa.varlen_fwd_fp8(d_q8, d_k8, d_v, d_cuq, d_cuk, case.max_seqlen_q,
+                               case.softmax_scale, f8.descale_q, f8.descale_k, case.causal,
+                               out=out8, lse=lse8, workspace=ws)
+
+        f_steps = max(5, min(args.steps, 500))
+        for _ in range(max(3, args.warmup)):
+            flush.fill_(4.0)
+            forward_fp8()
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(f_steps)]
+        torch.cuda.synchronize()
+        for i in range(f_steps):
+            flush.fill_(float(i))
+            fev[i][0].record(stream)
+            forward_fp8()
+            fev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if vfa.read_status(ws) != 0:
+            raise RuntimeError("fp8 forward device status not OK after timing")
+        fp8_mean = sum(e[0].elapsed_time(e[1]) for e in fev) / f_steps
+        if world > 1:
+            t = torch.tensor([fp8_mean], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            fp8_mean = float(t.item())
+
     # ---------------- backward: its own timed loop (not part of the step)
     bwd_mean = None
     if has_bwd:
@@ -552,6 +585,21 @@ def run_ours(args):
         "clocks": clocks,
         "wall_s": wall,
     }
+    if fp8_mean is not None:
+        ach_8 = flops / (fp8_mean * 1e-3) / 1e12
+        # half the FLOPs (S = Q K^T) at the FP8 rate (2x bf16, nominal), half (P V) at bf16
+        peak8 = 4.0 * peaks["bf16_tflops"] / 3.0
+        line["fp8"] = {
+            "value": world * ach_8, "unit": "TFLOP/s", "ms": fp8_mean, "steps": f_steps,
+            "gpu_launches": 2 * f_steps,
+            "how": "vfa_varlen_fwd_fp8 on the same batch (q, k as E4M3 codes with a power-of-"
+                   "two descale, v bf16); own timed loop with an L2 flush before each call",
+            "roofline": {"bound": "tensor", "achieved": ach_8, "peak": peak8, "unit": "TFLOP/s",
+                         "frac": ach_8 / peak8, "traffic": None,
+                         "kernel": "vfa_varlen_fwd_fp8 (scheduler + prefill kernel)",
+                         "peak_source": peaks["source"] + " bf16 burst x 4/3 (S at the nominal "
+                                        "FP8 rate of 2x bf16, P V at bf16)"},
+        }
     if bwd_mean is not None:
         bflops = A.varlen_bwd_flops(case)
         ach_b = bflops / (bwd_mean * 1e-3) / 1e12
@@ -592,6 +640,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward's timed loop")
+    ap.add_argument("--no-fp8", action="store_true",
+                    help="skip the FP8 q / k forward's timed loop")
     ap.add_argument("--profile", choices=["prefill", "decode", "backward"], default=None,
                     help="run only W + K passes of one part (for ncu captures); no JSON line")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -134,6 +134,29 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
                           size_t workspace_bytes, vfa_stream_t stream);
 
 /*
+ * vfa_varlen_fwd with q and k given as FP8 E4M3 codes (1 byte each: 1 sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits, no infinities), each tensor
+ * with one descale factor: element value = descale * code.  v stays bf16.
+ * The plan names FP8 kernel configuration types without content; this is
+ * the reading taken.  S = q.k is formed by the tensor core's FP8 product
+ * (exact products, fp32 accumulation) and scaled by softmax_scale *
+ * descale_q * descale_k; everything after S is as in vfa_varlen_fwd.
+ *
+ * q_fp8        device uint8 [total_q, num_heads, 128] E4M3 codes.
+ * k_fp8        device uint8 [total_k, num_kv_heads, 128] E4M3 codes.
+ * descale_q, descale_k  finite, > 0 (else VFA_ERR_INVALID_ARG).
+ * Other arguments, outputs, workspace and errors as in vfa_varlen_fwd;
+ * head_dim must be 128 (else VFA_ERR_UNSUPPORTED).
+ */
+vfa_status vfa_varlen_fwd_fp8(const void *q_fp8, const void *k_fp8, const void *v,
+                              const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                              int total_q, int total_k, int max_seqlen_q, int batch,
+                              int num_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                              float descale_q, float descale_k, int causal, int window_left,
+                              void *out, float *lse, void *workspace, size_t workspace_bytes,
+                              vfa_stream_t stream);
+
+/*
  * vfa_varlen_fwd without a caller workspace.  The pages have no counterpart:
  * this entry point exists for callers that cannot allocate device memory --
  * code on a real-time or callback thread that must not enter the allocator,

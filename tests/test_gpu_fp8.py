@@ -1,0 +1,101 @@
+"""GPU parity of vfa_varlen_fwd_fp8 (FP8 E4M3 q and k, bf16 v) against the fp64 oracle.
+
+The tensor core's FP8 products are exact and accumulate in fp32, as the
+bf16 products do, so the forward's tolerances apply unchanged (helpers.py).
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import BF16_NAN, assert_lse_close, assert_out_close
+from variable_length_flashattention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def vfa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from variable_length_flashattention_gb300 import build, vfa as binding
+    build.build()
+    return binding
+
+
+def _run(vfa, case, f8, causal, window_left=-1):
+    q8, k8, v = f8.q8.cuda(), f8.k8.cuda(), case.v.cuda()
+    cq = torch.from_numpy(case.cu_seqlens_q).cuda()
+    ck = torch.from_numpy(case.cu_seqlens_k).cuda()
+    out = torch.full(case.q.shape, 0, dtype=torch.int16, device="cuda").fill_(BF16_NAN)
+    out = out.view(torch.bfloat16)
+    lse = torch.full((case.total_q, case.num_heads), float("nan"), device="cuda")
+    ws = vfa.alloc_workspace(case.batch, case.total_q, case.total_k, case.num_heads,
+                             case.head_dim)
+    vfa.varlen_fwd_fp8(q8, k8, v, cq, ck, max(case.max_seqlen_q, 0), case.softmax_scale,
+                       f8.descale_q, f8.descale_k, causal, out=out, lse=lse, workspace=ws,
+                       window_left=window_left)
+    status = vfa.read_status(ws)
+    torch.cuda.synchronize()
+    return out.float().cpu().double().numpy(), lse.cpu().double().numpy(), status
+
+
+@pytest.mark.parametrize("causal,window_left", [(0, -1), (1, -1), (2, -1), (1, 200), (2, 37)])
+def test_mixes(vfa, oracle_mod, causal, window_left):
+    lq = [1, 7, 64, 129, 300, 0, 257, 1000]
+    lk = [1, 7, 64, 129, 300, 5, 90, 800]
+    case = W.make_varlen("fp8", lq, lk, 2, 128, bool(causal), 1.0, value_seed=20 + causal)
+    f8 = W.fp8_qk(case)
+    out, lse, status = _run(vfa, case, f8, causal, window_left)
+    assert status == 0
+    ref_out, ref_lse, _ = oracle_mod.varlen_fwd_fp8(f8.q8, f8.k8, case.v, case.cu_seqlens_q,
+                                                    case.cu_seqlens_k, 2, 128,
+                                                    case.softmax_scale, f8.descale_q,
+                                                    f8.descale_k, causal,
+                                                    window_left=window_left)
+    assert_out_close(out, ref_out, f"fp8 causal {causal} window {window_left}")
+    assert_lse_close(lse, ref_lse, f"fp8 causal {causal} window {window_left}")
+
+
+def test_grouped_kv_heads(vfa, oracle_mod):
+    lq, lk = [300, 7, 129, 64], [300, 40, 129, 200]
+    case = W.make_varlen("fp8-gqa", lq, lk, 8, 128, True, 1.0, value_seed=31)
+    case.k = case.k[:, :2].contiguous()
+    case.v = case.v[:, :2].contiguous()
+    f8 = W.fp8_qk(case)
+    out, lse, status = _run(vfa, case, f8, 1)
+    assert status == 0
+    ref_out, ref_lse, _ = oracle_mod.varlen_fwd_fp8(f8.q8, f8.k8, case.v, case.cu_seqlens_q,
+                                                    case.cu_seqlens_k, 8, 128,
+                                                    case.softmax_scale, f8.descale_q,
+                                                    f8.descale_k, 1, num_kv_heads=2)
+    assert_out_close(out, ref_out, "fp8 gqa")
+    assert_lse_close(lse, ref_lse, "fp8 gqa")
+
+
+def test_packed_batch_sampled(vfa, oracle_mod):
+    # the bench's packed batch with FP8 q and k; the oracle on three whole sequences
+    case = W.packed(0)
+    f8 = W.fp8_qk(case)
+    out, lse, status = _run(vfa, case, f8, 1)
+    assert status == 0
+    L = case.lengths_q
+    for b in (int(np.argmax(L)), int(np.argmin(L)), len(L) // 2):
+        q0, q1 = int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1])
+        cu = np.array([0, q1 - q0], dtype=np.int32)
+        ro, rl, _ = oracle_mod.varlen_fwd_fp8(f8.q8[q0:q1], f8.k8[q0:q1], case.v[q0:q1], cu, cu,
+                                              16, 128, case.softmax_scale, f8.descale_q,
+                                              f8.descale_k, 1)
+        assert_out_close(out[q0:q1], ro, f"fp8 packed seq {b}")
+        assert_lse_close(lse[q0:q1], rl, f"fp8 packed seq {b}")
+
+
+def test_rejects_other_head_dims_and_bad_descales(vfa):
+    case = W.make_varlen("fp8-d64", [8], [8], 1, 64, True, 1.0, value_seed=1)
+    f8 = W.fp8_qk(case)
+    with pytest.raises(vfa.VfaError):
+        _run(vfa, case, f8, 1)
+    case = W.make_varlen("fp8-bad", [8], [8], 1, 128, True, 1.0, value_seed=1)
+    f8 = W.fp8_qk(case)
+    f8.descale_q = 0.0
+    with pytest.raises(vfa.VfaError):
+        _run(vfa, case, f8, 1)

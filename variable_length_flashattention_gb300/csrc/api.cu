@@ -89,22 +89,28 @@ vfa_status get_encoder(EncodeTiledFn *fn)
     return VFA_OK;
 }
 
-// [rows, heads, head_dim] bf16 tensor as a 3-D TMA map (innermost first:
-// dim, head, row); box = 64 columns x 1 head x box_rows rows, 128-byte swizzle.
+// [rows, heads, head_dim] tensor of bf16 (elem_bytes 2) or 8-bit codes
+// (elem_bytes 1) as a 3-D TMA map (innermost first: dim, head, row); box =
+// 128 bytes of columns x 1 head x box_rows rows, 128-byte swizzle.
 vfa_status encode_packed_map(CUtensorMap *map, const void *base, int rows, int heads,
-                             int head_dim, int box_rows)
+                             int head_dim, int box_rows, int elem_bytes = 2)
 {
     EncodeTiledFn enc;
     vfa_status st = get_encoder(&enc);
     if (st)
         return st;
+    const cuuint64_t eb = static_cast<cuuint64_t>(elem_bytes);
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(heads),
                                 static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
-                                   static_cast<cuuint64_t>(heads) * head_dim * 2};
-    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * eb,
+                                   static_cast<cuuint64_t>(heads) * head_dim * eb};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), 1,
+                               static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+    CUresult r = enc(map,
+                     elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     3, const_cast<void *>(base), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -217,12 +223,16 @@ vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_se
     return VFA_OK;
 }
 
-vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
-                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int total_q,
-                          int total_k, int max_seqlen_q, int batch, int num_heads,
-                          int num_kv_heads, int head_dim, float softmax_scale, int causal,
-                          int window_left, void *out, float *lse, void *workspace,
-                          size_t workspace_bytes, vfa_stream_t stream)
+// The forward for bf16 q, k (qk_fp8 = 0) or FP8 E4M3 q, k codes with
+// per-tensor descales (qk_fp8 = 1, head_dim 128).
+static vfa_status varlen_fwd_impl(const void *q, const void *k, const void *v,
+                                  const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                  int total_q, int total_k, int max_seqlen_q, int batch,
+                                  int num_heads, int num_kv_heads, int head_dim,
+                                  float softmax_scale, int causal, int window_left, void *out,
+                                  float *lse, void *workspace, size_t workspace_bytes,
+                                  vfa_stream_t stream, int qk_fp8, float descale_q,
+                                  float descale_k)
 {
     if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !out || !lse || !workspace)
         return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
@@ -296,8 +306,9 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
 
     vfa::PrefillArgs pa;
     memset(&pa, 0, sizeof pa);
-    if ((st = encode_packed_map(&pa.tm_q, q, total_q, num_heads, head_dim, bq)) ||
-        (st = encode_packed_map(&pa.tm_k, k, total_k, num_kv_heads, head_dim, bk)) ||
+    const int qk_bytes = qk_fp8 ? 1 : 2;
+    if ((st = encode_packed_map(&pa.tm_q, q, total_q, num_heads, head_dim, bq, qk_bytes)) ||
+        (st = encode_packed_map(&pa.tm_k, k, total_k, num_kv_heads, head_dim, bk, qk_bytes)) ||
         (st = encode_packed_map(&pa.tm_v, v, total_k, num_kv_heads, head_dim, bk)))
         return st;
     pa.cu_q = cu_seqlens_q;
@@ -314,6 +325,13 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     // a zero scale (uniform weights) becomes the smallest normal float, which
     // gives the same weights for every finite score.
     pa.scale_log2 = softmax_scale > 0.f ? softmax_scale * 1.4426950408889634f : FLT_MIN;
+    if (qk_fp8) {
+        // S = descale_q * descale_k * (codes of q) . (codes of k)
+        const double sl = static_cast<double>(softmax_scale) * descale_q * descale_k *
+                          1.4426950408889634;
+        pa.scale_log2 = sl > 0.0 ? static_cast<float>(sl) : FLT_MIN;
+    }
+    pa.qk_fp8 = qk_fp8;
     pa.causal = causal;
     pa.window_left = sa.window_left;
     const int grid = wl.item_capacity < dev.sm_count ? wl.item_capacity : dev.sm_count;
@@ -321,6 +339,36 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
     if (e != cudaSuccess)
         return cuda_fail(e, "prefill launch");
     return VFA_OK;
+}
+
+vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
+                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int total_q,
+                          int total_k, int max_seqlen_q, int batch, int num_heads,
+                          int num_kv_heads, int head_dim, float softmax_scale, int causal,
+                          int window_left, void *out, float *lse, void *workspace,
+                          size_t workspace_bytes, vfa_stream_t stream)
+{
+    return varlen_fwd_impl(q, k, v, cu_seqlens_q, cu_seqlens_k, total_q, total_k, max_seqlen_q,
+                           batch, num_heads, num_kv_heads, head_dim, softmax_scale, causal,
+                           window_left, out, lse, workspace, workspace_bytes, stream, 0, 1.f, 1.f);
+}
+
+vfa_status vfa_varlen_fwd_fp8(const void *q_fp8, const void *k_fp8, const void *v,
+                              const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                              int total_q, int total_k, int max_seqlen_q, int batch,
+                              int num_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                              float descale_q, float descale_k, int causal, int window_left,
+                              void *out, float *lse, void *workspace, size_t workspace_bytes,
+                              vfa_stream_t stream)
+{
+    if (head_dim != 128)
+        return fail(VFA_ERR_UNSUPPORTED, "FP8 forward head_dim %d not supported (128)", head_dim);
+    if (!(descale_q > 0.f) || !(descale_k > 0.f) || descale_q > FLT_MAX || descale_k > FLT_MAX)
+        return fail(VFA_ERR_INVALID_ARG, "descale_q and descale_k must be finite and > 0");
+    return varlen_fwd_impl(q_fp8, k_fp8, v, cu_seqlens_q, cu_seqlens_k, total_q, total_k,
+                           max_seqlen_q, batch, num_heads, num_kv_heads, head_dim, softmax_scale,
+                           causal, window_left, out, lse, workspace, workspace_bytes, stream, 1,
+                           descale_q, descale_k);
 }
 
 size_t vfa_varlen_bwd_workspace_bytes(int batch, int total_q, int num_heads, int head_dim)

@@ -32,7 +32,10 @@
 //   * O / l leaves through a 2 KB shared-memory stage per warp (no cross-warp
 //     handshake, no TMA completion to wait for): every store instruction
 //     writes eight whole 64-byte row segments;
-//   * TMEM: O_a, O_b (D columns each), S/P_a, S/P_b (128 columns each).
+//   * TMEM: O_a, O_b (D columns each), S/P_a, S/P_b (128 columns each);
+//   * an FP8 instantiation (head_dim 128) takes Q and K as E4M3 codes: their
+//     tiles are half the bytes and S = Q K^T runs as kind::f8f6f4 in 32-byte
+//     k-steps; the per-tensor descales are folded into the score scale.
 // Everything else (item ring fed by an atomic counter, bounded waits with
 // drain-and-report on expiry) is as in prefill.cu.
 #include <cfloat>
@@ -46,21 +49,29 @@ namespace vfa {
 
 namespace {
 
-template <int D>
+// F8: Q and K are FP8 E4M3 codes (1 byte each) and S = Q K^T runs as
+// kind::f8f6f4; V, P and O stay as in the bf16 kernel.
+template <int D, bool F8 = false>
 struct PairCfg {
     static constexpr int BQ = kBlockQ;
     static constexpr int BK = 128;
     static constexpr int NS = D == 64 ? 4 : 2;            // K and V ring stages
-    static constexpr int DB = D / 64;                     // 128-byte column blocks per row
-    static constexpr uint32_t Q_BYTES = BQ * D * 2;
-    static constexpr uint32_t KV_BYTES = BK * D * 2;
+    static constexpr int DB = D / 64;                     // 128-byte column blocks per V / O row
+    static constexpr int QK_ELEM = F8 ? 1 : 2;            // bytes per Q / K element
+    static constexpr int QK_DB = D * QK_ELEM / 128;       // 128-byte column blocks per Q / K row
+    static constexpr int QK_BLOCK = 128 / QK_ELEM;        // elements per such block
+    static constexpr int QK_KSTEP = 32 / QK_ELEM;         // elements per MMA k-step (32 bytes)
+    static constexpr uint32_t Q_BYTES = BQ * D * QK_ELEM;
+    static constexpr uint32_t K_BYTES = BK * D * QK_ELEM;
+    static constexpr uint32_t KV_BYTES = BK * D * 2;      // one V stage
     static constexpr uint32_t WARP_STAGE = 32 * 64;       // one warp's 32 rows x 32 output columns
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL = 2 * D;              // S_x at S_COL + x * BK; O_x at x * D
     static constexpr int NUM_BARS = 4 + 4 * NS + 15;
-    static constexpr size_t SMEM = 1024 + 2 * Q_BYTES + 2 * NS * KV_BYTES + 8 * WARP_STAGE +
-                                   NUM_BARS * 8 + 64;
-    static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BQ, BK, false, false);
+    static constexpr size_t SMEM = 1024 + 2 * Q_BYTES + NS * (K_BYTES + KV_BYTES) +
+                                   8 * WARP_STAGE + NUM_BARS * 8 + 64;
+    static constexpr uint32_t IDESC_QK =
+        F8 ? idesc_e4m3_f32(BQ, BK) : idesc_bf16_f32(BQ, BK, false, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BQ, D, false, true);
     static_assert(S_COL + 2 * BK <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -195,11 +206,11 @@ __device__ __forceinline__ ItemSpan item_span(const int4 &it, const int4 &itb)
     return sp;
 }
 
-template <int D, bool WIN>
+template <int D, bool WIN, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ PrefillArgs p)
 {
-    using C = PairCfg<D>;
+    using C = PairCfg<D, F8>;
     constexpr int BQ = C::BQ, BK = C::BK, NS = C::NS, DB = C::DB;
 
     extern __shared__ uint8_t smem_raw[];
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t sQ = base;                           // Q_a, Q_b
     const uint32_t sK = sQ + 2 * C::Q_BYTES;
-    const uint32_t sV = sK + NS * C::KV_BYTES;
+    const uint32_t sV = sK + NS * C::K_BYTES;
     const uint32_t sO = sV + NS * C::KV_BYTES;          // output staging, 2 KB per softmax warp
     const uint32_t bars = sO + 8 * C::WARP_STAGE;
     auto q_full = [&](int x) { return bars + 8u * x; };
@@ -334,9 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(q_full(x), C::Q_BYTES);
-                    for (int db = 0; db < DB; ++db)
+                    for (int db = 0; db < C::QK_DB; ++db)
                         tma_load_3d(sQ + x * C::Q_BYTES + db * (BQ * 128), &p.tm_q, q_full(x),
-                                    db * 64, h, seq.x + i * BQ);
+                                    db * C::QK_BLOCK, h, seq.x + i * BQ);
                     ++qloads[x];
                 }
                 for (int j = sp.j0; j < sp.j1 && ok; ++j) {
@@ -345,10 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(k_full(st), C::KV_BYTES);
-                    for (int db = 0; db < DB; ++db)
-                        tma_load_3d(sK + st * C::KV_BYTES + db * (BK * 128), &p.tm_k, k_full(st),
-                                    db * 64, h / p.kv_group, seq.w + j * BK);
+                    mbar_arrive_expect_tx(k_full(st), C::K_BYTES);
+                    for (int db = 0; db < C::QK_DB; ++db)
+                        tma_load_3d(sK + st * C::K_BYTES + db * (BK * 128), &p.tm_k, k_full(st),
+                                    db * C::QK_BLOCK, h / p.kv_group, seq.w + j * BK);
                     ++kfills;
                 }
                 if (!ok)
@@ -408,13 +419,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             // previous O_x += P_x V protects P_x; see the file comment).
             auto issue_qk = [&](int x, int st) {
                 const uint64_t qd = q_desc0 + x * (C::Q_BYTES >> 4);
-                const uint64_t kd = k_desc0 + st * (C::KV_BYTES >> 4);
+                const uint64_t kd = k_desc0 + st * (C::K_BYTES >> 4);
                 const uint32_t s_tm = tmem + C::S_COL + x * BK;
-                mma_ss_w<0>(s_tm, qd, kd, C::IDESC_QK);
+                // k-steps of 32 bytes: 16 bf16 or 32 FP8 elements
 #pragma unroll
-                for (int kk = 1; kk < D / 16; ++kk)
-                    mma_ss_w<1>(s_tm, qd + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4),
-                                kd + (((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4), C::IDESC_QK);
+                for (int kk = 0; kk < D / C::QK_KSTEP; ++kk) {
+                    const uint64_t qo = qd + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4);
+                    const uint64_t ko = kd + (((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4);
+                    if constexpr (F8) {
+                        if (kk == 0)
+                            mma_ss_w8<0>(s_tm, qo, ko, C::IDESC_QK);
+                        else
+                            mma_ss_w8<1>(s_tm, qo, ko, C::IDESC_QK);
+                    } else {
+                        if (kk == 0)
+                            mma_ss_w<0>(s_tm, qo, ko, C::IDESC_QK);
+                        else
+                            mma_ss_w<1>(s_tm, qo, ko, C::IDESC_QK);
+                    }
+                }
                 mma_commit_w(s_full(x));
             };
             // O_x += P_x V for q slot x (its tile number gt[x]), V in ring slot st,
@@ -752,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool WIN>
+template <int D, bool WIN, bool F8>
 cudaError_t launch_pair_dw(const PrefillArgs &a, int grid, cudaStream_t stream)
 {
     static int attr_done[64] = {0};
@@ -761,9 +784,9 @@ cudaError_t launch_pair_dw(const PrefillArgs &a, int grid, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     if (dev < 64 && !attr_done[dev]) {
-        e = cudaFuncSetAttribute(prefill_pair_kernel<D, WIN>,
+        e = cudaFuncSetAttribute(prefill_pair_kernel<D, WIN, F8>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(PairCfg<D>::SMEM));
+                                 static_cast<int>(PairCfg<D, F8>::SMEM));
         if (e != cudaSuccess)
             return e;
         attr_done[dev] = 1;
@@ -771,25 +794,32 @@ cudaError_t launch_pair_dw(const PrefillArgs &a, int grid, cudaStream_t stream)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = PairCfg<D>::SMEM;
+    cfg.dynamicSmemBytes = PairCfg<D, F8>::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D, WIN>, a);
+    e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D, WIN, F8>, a);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
 }
 
-// The sliding-window mask has its own instantiation.
+// The sliding-window mask and FP8 Q / K (head_dim 128) have their own
+// instantiations.
 template <int D>
 cudaError_t launch_pair_d(const PrefillArgs &a, int grid, cudaStream_t stream)
 {
-    return a.window_left >= 0 ? launch_pair_dw<D, true>(a, grid, stream)
-                              : launch_pair_dw<D, false>(a, grid, stream);
+    if (a.qk_fp8) {
+        if constexpr (D == 128)
+            return a.window_left >= 0 ? launch_pair_dw<D, true, true>(a, grid, stream)
+                                      : launch_pair_dw<D, false, true>(a, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    return a.window_left >= 0 ? launch_pair_dw<D, true, false>(a, grid, stream)
+                              : launch_pair_dw<D, false, false>(a, grid, stream);
 }
 
 }  // namespace

@@ -285,6 +285,20 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint6
         : "memory");
 }
 
+// kind::f8f6f4 form of mma_ss_w (A and B 8-bit floating-point codes in smem).
+template <int ACC>
+__device__ __forceinline__ void mma_ss_w8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(ACC)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_w(uint32_t bar)
 {
     asm volatile(
@@ -420,6 +434,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
            | (1u << 10)                                // B format: bf16
            | ((a_mn_major ? 1u : 0u) << 15)            // A major-ness
            | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0),
+// both K-major, and f32 accumulate.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)
+{
+    return (1u << 4)                                   // D format: f32
+           | (0u << 7)                                 // A format: E4M3
+           | (0u << 10)                                // B format: E4M3
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }

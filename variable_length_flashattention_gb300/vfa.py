@@ -43,6 +43,8 @@ SIGNATURES = [
     ("vfa_varlen_fwd_tile_shape", _I, [_I, _P, _P, _P]),
     ("vfa_varlen_fwd", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P,
                             _S, _P]),
+    ("vfa_varlen_fwd_fp8", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F, _F, _I,
+                                _I, _P, _P, _P, _S, _P]),
     ("vfa_varlen_fwd_noalloc", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P,
                                     _P, _P, _P]),
     ("vfa_varlen_schedule", _I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P,
@@ -176,6 +178,41 @@ def varlen_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: 
                               _ptr(lse), _ptr(workspace),
                               workspace.numel() * workspace.element_size(),
                               _stream(stream))
+    _check(st)
+    return out, lse
+
+
+def varlen_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v: torch.Tensor,
+                   cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, max_seqlen_q: int,
+                   softmax_scale: float, descale_q: float, descale_k: float, causal,
+                   out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None, stream=None,
+                   window_left: int = -1):
+    """vfa_varlen_fwd_fp8: q8, k8 uint8 E4M3 codes [T, H(kv), 128], v bf16; returns (out, lse)."""
+    for t, n in ((q8, "q8"), (k8, "k8")):
+        _need(t, torch.uint8, n)
+    _need(v, torch.bfloat16, "v")
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _need(cu_seqlens_k, torch.int32, "cu_seqlens_k")
+    if (q8.dim() != 3 or k8.shape != v.shape or q8.shape[2] != k8.shape[2] or
+            q8.shape[1] % k8.shape[1] != 0):
+        raise ValueError("q8 [Tq, H, D], k8 and v [Tk, Hkv, D] with Hkv dividing H")
+    total_q, H, D = q8.shape
+    total_k, Hkv = k8.shape[0], k8.shape[1]
+    batch = cu_seqlens_q.numel() - 1
+    out = torch.empty(q8.shape, dtype=torch.bfloat16, device=q8.device) if out is None else out
+    if lse is None:
+        lse = torch.empty((total_q, H), dtype=torch.float32, device=q8.device)
+    _need(out, torch.bfloat16, "out")
+    _need(lse, torch.float32, "lse")
+    if workspace is None:
+        workspace = alloc_workspace(batch, total_q, total_k, H, D, device=q8.device)
+    st = lib().vfa_varlen_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v), _ptr(cu_seqlens_q),
+                                  _ptr(cu_seqlens_k), total_q, total_k, int(max_seqlen_q), batch,
+                                  H, Hkv, D, float(softmax_scale), float(descale_q),
+                                  float(descale_k), int(causal), int(window_left), _ptr(out),
+                                  _ptr(lse), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st)
     return out, lse
 
