@@ -323,10 +323,23 @@ def run_ours(args):
         if vfa.read_status(b_ws) != 0:
             raise RuntimeError("backward device status not OK in warm-up")
 
+    has_fp8 = case.head_dim == 128 and not args.no_fp8
+    if has_fp8:
+        f8 = W.fp8_qk(case)
+        d_q8, d_k8 = f8.q8.to(dev), f8.k8.to(dev)
+        out8 = torch.empty_like(d_q)
+        lse8 = torch.empty_like(lse)
+
+        def forward_fp8():
+            vfa.varlen_fwd_fp8(d_q8, d_k8, d_v, d_cuq, d_cuk, case.max_seqlen_q,
+                               case.softmax_scale, f8.descale_q, f8.descale_k, case.causal,
+                               out=out8, lse=lse8, workspace=ws)
+
     launches_per_step = 2 + (2 + len(tiles))
     if args.profile:
         part = {"prefill": prefill, "decode": graph.replay,
-                "backward": backward if has_bwd else None}[args.profile]
+                "backward": backward if has_bwd else None,
+                "fp8": forward_fp8 if has_fp8 else None}[args.profile]
         for i in range(args.warmup + args.steps):
             flush.fill_(float(i))
             part()
@@ -380,17 +393,7 @@ def run_ours(args):
 
     # ---------------- FP8 q / k forward: its own timed loop (not part of the step)
     fp8_mean = None
-    if case.head_dim == 128 and not args.no_fp8:
-        f8 = W.fp8_qk(case)
-        d_q8, d_k8 = f8.q8.to(dev), f8.k8.to(dev)
-        out8 = torch.empty_like(d_q)
-        lse8 = torch.empty_like(lse)
-
-        def forward_fp8():
-            vfa.varlen_fwd_fp8(d_q8, d_k8, d_v, d_cuq, d_cuk, case.max_seqlen_q,
-                               case.softmax_scale, f8.descale_q, f8.descale_k, case.causal,
-                               out=out8, lse=lse8, workspace=ws)
-
+    if has_fp8:
         f_steps = max(5, min(args.steps, 500))
         for _ in range(max(3, args.warmup)):
             flush.fill_(4.0)
@@ -595,7 +598,7 @@ def run_ours(args):
             "how": "vfa_varlen_fwd_fp8 on the same batch (q, k as E4M3 codes with a power-of-"
                    "two descale, v bf16); own timed loop with an L2 flush before each call",
             "roofline": {"bound": "tensor", "achieved": ach_8, "peak": peak8, "unit": "TFLOP/s",
-                         "frac": ach_8 / peak8, "traffic": None,
+                         "frac": ach_8 / peak8, "traffic": _traffic("prefill_fp8_d128"),
                          "kernel": "vfa_varlen_fwd_fp8 (scheduler + prefill kernel)",
                          "peak_source": peaks["source"] + " bf16 burst x 4/3 (S at the nominal "
                                         "FP8 rate of 2x bf16, P V at bf16)"},
@@ -642,7 +645,7 @@ def main():
                     help="skip the backward's timed loop")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the FP8 q / k forward's timed loop")
-    ap.add_argument("--profile", choices=["prefill", "decode", "backward"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "backward", "fp8"], default=None,
                     help="run only W + K passes of one part (for ncu captures); no JSON line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=4,
