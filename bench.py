@@ -145,6 +145,19 @@ def _dist():
     return world, rank, local
 
 
+def max_over_ranks(values, world: int, device):
+    """Per-rank timings -> their element-wise maximum over all ranks (the slowest rank
+    sets the job's time).  With world == 1 the values come back unchanged."""
+    vals = [float(v) for v in values]
+    if world <= 1:
+        return vals
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 def _oracle_rows_sample(case, n_rows, rng):
     import numpy as np
     H = case.num_heads
@@ -409,10 +422,7 @@ def run_ours(args):
         if vfa.read_status(ws) != 0:
             raise RuntimeError("fp8 forward device status not OK after timing")
         fp8_mean = sum(e[0].elapsed_time(e[1]) for e in fev) / f_steps
-        if world > 1:
-            t = torch.tensor([fp8_mean], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            fp8_mean = float(t.item())
+        fp8_mean = max_over_ranks([fp8_mean], world, dev)[0]
 
     # ---------------- backward: its own timed loop (not part of the step)
     bwd_mean = None
@@ -432,15 +442,9 @@ def run_ours(args):
         if vfa.read_status(b_ws) != 0:
             raise RuntimeError("backward device status not OK after timing")
         bwd_mean = sum(e[0].elapsed_time(e[1]) for e in bev) / b_steps
-        if world > 1:
-            t = torch.tensor([bwd_mean], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            bwd_mean = float(t.item())
+        bwd_mean = max_over_ranks([bwd_mean], world, dev)[0]
     step_ms = pre_mean + dec_mean
-    if world > 1:
-        t = torch.tensor([pre_mean, dec_mean, step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        pre_mean, dec_mean, step_ms = [float(x) for x in t.cpu()]
+    pre_mean, dec_mean, step_ms = max_over_ranks([pre_mean, dec_mean, step_ms], world, dev)
 
     # ---------------- end to end through the public API with host buffers
     # The batch goes through in chunks of whole sequences (each chunk a
@@ -526,10 +530,7 @@ def run_ours(args):
     for _ in range(e2e_steps):
         e2e_step()
     e2e_s = (time.perf_counter() - te) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks([e2e_s], world, dev)[0]
 
     if rank != 0:
         dist.destroy_process_group()
