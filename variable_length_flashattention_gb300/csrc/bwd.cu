@@ -15,13 +15,14 @@
 //     shared memory; for every query head of the group and every 128-row q
 //     tile that sees one of the tile's keys, TMA brings Q and dO (two
 //     buffers, so the next tile's copies overlap this one's work), and
-//     tcgen05.mma computes S^T = K Q^T and dP^T = V dO^T into TMEM; two
-//     threads per key row form P^T (bf16, back into TMEM over the S^T
-//     columns) and dS^T (bf16, 128-byte-swizzled shared memory), and three
-//     more MMAs accumulate dV += P^T dO and dK += dS^T Q in TMEM across the
-//     whole loop and compute this q tile's dQ = dS K, which the threads (now
-//     two per query row) add into an fp32 buffer with vector atomics.  At the
-//     end dK (scaled) and dV leave as bf16;
+//     tcgen05.mma computes S^T = K Q^T and dP^T = V dO^T into TMEM, one
+//     64-query half at a time; for each half in turn, two threads per key
+//     row form P^T (bf16, back into TMEM over the S^T columns) and dS^T (bf16,
+//     128-byte-swizzled shared memory), and more MMAs accumulate dV += P^T dO
+//     and dK += dS^T Q in TMEM across the whole loop; after both halves,
+//     dQ = dS K for this q tile, which the threads (now two per query row)
+//     add into an fp32 buffer with vector atomics.  At the end dK (scaled) and
+//     dV leave as bf16;
 //   * bwd_dq: dQ = bf16(scale * the fp32 sum).
 // TMEM: S^T 128 columns, dP^T 128 (dQ reuses them once dP is read), dV and
 // dK D each -- 512 for D = 128.  Every wait is bounded; on expiry the CTA
@@ -37,7 +38,7 @@ namespace vfa {
 namespace {
 
 constexpr int kT = 128;            // key rows and query rows per tile
-constexpr int kComputeWarps = 8;   // two threads per tile row, one per column half
+constexpr int kComputeWarps = 8;   // two threads per tile row
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kThreads = kComputeThreads + 32;   // + the TMA / MMA issuing warp
 constexpr int kPrepThreads = 1024;
@@ -222,8 +223,9 @@ __device__ __forceinline__ void flush_dq(float4 *dst, const float4 (&acc)[DH / 4
         atomicAdd(dst + c, acc[c]);
 }
 
-// Warps 0-7 compute (warp w: TMEM lanes / tile rows 32 (w % 4) .. +31,
-// column half w / 4); warp 8 lane 0 issues the TMA copies and the MMAs.
+// Warps 0-7 compute (warp w: TMEM lanes / tile rows 32 (w % 4) .. +31; of
+// each 64-query half the 32 queries 32 (w / 4) .. +31; of dQ, dK and dV the
+// column half w / 4); warp 8 issues the TMA copies and the MMAs.
 //
 // Per step s (one query head, one q tile):
 //   issuer:  per query half h (64 columns): S^T_h, dP^T_h -> bar_s<h> (S^T_0
