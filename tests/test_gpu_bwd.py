@@ -136,3 +136,13 @@ def test_bad_cu_seqlens_sets_status(vfa):
                                  case.softmax_scale, 1, dq=dq)
     assert vfa.read_status(ws) == vfa.VFA_ERR_BAD_SEQLENS
     assert torch.isnan(dq.float()).all()
+
+
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_edge_lengths(vfa, oracle_mod, causal):
+    # a query sequence with no keys (dq = 0), keys no query sees (dk = dv = 0),
+    # one-token sequences and an empty sequence between non-empty ones
+    lq = [10, 0, 1, 130, 3]
+    lk = [0, 7, 1, 130, 200]
+    case = W.make_varlen("bwd-edge", lq, lk, 2, 64, bool(causal), 1.0, value_seed=40 + causal)
+    _compare(vfa, oracle_mod, case, causal, seed=40)

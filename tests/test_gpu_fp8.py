@@ -99,3 +99,19 @@ def test_rejects_other_head_dims_and_bad_descales(vfa):
     f8.descale_q = 0.0
     with pytest.raises(vfa.VfaError):
         _run(vfa, case, f8, 1)
+
+
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_edge_lengths(vfa, oracle_mod, causal):
+    lq = [10, 0, 1, 130, 3]
+    lk = [0, 7, 1, 130, 200]
+    case = W.make_varlen("fp8-edge", lq, lk, 2, 128, bool(causal), 1.0, value_seed=50 + causal)
+    f8 = W.fp8_qk(case)
+    out, lse, status = _run(vfa, case, f8, causal)
+    assert status == 0
+    ref_out, ref_lse, _ = oracle_mod.varlen_fwd_fp8(f8.q8, f8.k8, case.v, case.cu_seqlens_q,
+                                                    case.cu_seqlens_k, 2, 128,
+                                                    case.softmax_scale, f8.descale_q,
+                                                    f8.descale_k, causal)
+    assert_out_close(out, ref_out, f"fp8 edge causal {causal}")
+    assert_lse_close(lse, ref_lse, f"fp8 edge causal {causal}")
