@@ -119,3 +119,28 @@ def test_product_path_does_not_import_the_oracle():
                     src = f.read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), fn
                 assert "vfa_oracle" not in src, fn
+
+
+def test_backward_and_fp8_host_checks(vfa):
+    # rejected on the host before any device work (no GPU needed)
+    L = vfa.lib()
+    fake = ctypes.c_void_p(0x100000)
+    nul = None
+    args = lambda D, scale, causal, wl, q=fake: (q, fake, fake, fake, fake, fake, fake, fake,
+                                                 4, 4, 1, 2, 2, D, scale, causal, wl, fake, fake,
+                                                 fake, fake, 1 << 30, nul)
+    assert L.vfa_varlen_bwd(*args(128, 0.1, 1, -1, q=nul)) == vfa.VFA_ERR_INVALID_ARG
+    assert b"null" in L.vfa_last_error()
+    assert L.vfa_varlen_bwd(*args(256, 0.1, 1, -1)) == vfa.VFA_ERR_UNSUPPORTED
+    assert L.vfa_varlen_bwd(*args(128, 0.0, 1, -1)) == vfa.VFA_ERR_INVALID_ARG
+    assert L.vfa_varlen_bwd(*args(128, 0.1, 0, 8)) == vfa.VFA_ERR_INVALID_ARG
+    assert b"window" in L.vfa_last_error()
+    assert L.vfa_varlen_bwd(*args(128, 0.1, 3, -1)) == vfa.VFA_ERR_INVALID_ARG
+    assert L.vfa_varlen_bwd_workspace_bytes(1, 10, 2, 256) == 0
+    assert L.vfa_varlen_bwd_workspace_bytes(2, 10, 2, 128) >= 256 + 10 * 2 * (4 + 128 * 4)
+    # FP8 forward: head_dim 128 only, descales finite and positive
+    f8 = lambda D, dq, dk: (fake, fake, fake, fake, fake, 4, 4, 4, 1, 2, 2, D, 0.1, dq, dk, 1, -1,
+                            fake, fake, fake, 1 << 30, nul)
+    assert L.vfa_varlen_fwd_fp8(*f8(64, 1.0, 1.0)) == vfa.VFA_ERR_UNSUPPORTED
+    assert L.vfa_varlen_fwd_fp8(*f8(128, 0.0, 1.0)) == vfa.VFA_ERR_INVALID_ARG
+    assert L.vfa_varlen_fwd_fp8(*f8(128, 1.0, float("inf"))) == vfa.VFA_ERR_INVALID_ARG
