@@ -14,6 +14,11 @@ Pages followed:
   * "attention_ref.rs" (spark_storage): ``AttnState::new``,
     ``step_tile_ref`` and ``finalize_ref``.
 
+Where the pages only name a variant, the oracle states the plainest reading:
+the backward is the exact derivative of the forward (``varlen_bwd``); the FP8
+forward reads E4M3 codes as descale * code exactly (``varlen_fwd_fp8``); the
+sliding window hides keys below row + off - window_left.
+
 ``vfa_oracle.c`` holds the floating-point definitions; ``schedule.py`` holds
 the integer tile-schedule rule.  Parity pins for every function are in
 ``tests/test_oracle_*.py``.
