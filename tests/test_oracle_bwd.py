@@ -10,7 +10,9 @@ things other than itself:
   * invariants of the softmax Jacobian: the rows of dS sum to zero, so the
     keys' dk sum to zero per (sequence, kv head); P's rows sum to one, so
     the keys' dv sum to the sum of dout over the rows that see a key;
-  * closed forms: a single visible key gives dq = dk = 0 and dv = dout.
+  * closed forms: a single visible key gives dq = dk = 0 and dv = dout;
+  * central finite differences of a separate numpy fp64 forward (the loss
+    sum(out * dout)) at sampled elements of q, k and v.
 """
 import numpy as np
 import pytest
@@ -117,3 +119,49 @@ def test_rejects_window_without_causal(oracle_mod):
     with pytest.raises(ValueError):
         oracle_mod.varlen_bwd(case.q, case.k, case.v, dout, case.cu_seqlens_q, case.cu_seqlens_k,
                               1, 8, case.softmax_scale, 0, window_left=3)
+
+
+def _np_loss(q, k, v, dout, cu_q, cu_k, scale, causal):
+    """L = sum(out * dout) of a plain numpy fp64 forward (whole masked score matrix)."""
+    total = 0.0
+    for b in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        lq, lk = q1 - q0, k1 - k0
+        if lq == 0 or lk == 0:
+            continue
+        off = lk - lq if causal == 2 else 0
+        for h in range(q.shape[1]):
+            s = scale * q[q0:q1, h] @ k[k0:k1, h].T
+            mask = np.ones((lq, lk), dtype=bool)
+            if causal:
+                mask = np.arange(lk)[None, :] <= np.arange(lq)[:, None] + off
+            s = np.where(mask, s, -np.inf)
+            live = mask.any(axis=1)
+            e = np.exp(s[live] - s[live].max(axis=1, keepdims=True))
+            p = e / e.sum(axis=1, keepdims=True)
+            total += float((p @ v[k0:k1, h] * dout[q0:q1, h][live]).sum())
+    return total
+
+
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_finite_differences(oracle_mod, causal):
+    # central differences of a separate numpy fp64 forward against the oracle's gradients
+    lq, lk = [3, 5], [4, 5]
+    case, dout = _case(lq, lk, 1, 4, seed=61 + causal)
+    dq, dk, dv, _ = oracle_mod.varlen_bwd(case.q, case.k, case.v, dout, case.cu_seqlens_q,
+                                          case.cu_seqlens_k, 1, 4, case.softmax_scale, causal)
+    base = [t.double().numpy().copy() for t in (case.q, case.k, case.v)]
+    g = dout.double().numpy()
+    cq, ck = [int(x) for x in case.cu_seqlens_q], [int(x) for x in case.cu_seqlens_k]
+    eps = 1e-6
+    rng = np.random.default_rng(causal)
+    for which, grad in enumerate((dq, dk, dv)):
+        for _ in range(6):
+            idx = tuple(int(rng.integers(0, n)) for n in base[which].shape)
+            plus = [x.copy() for x in base]
+            minus = [x.copy() for x in base]
+            plus[which][idx] += eps
+            minus[which][idx] -= eps
+            fd = (_np_loss(*plus, g, cq, ck, case.softmax_scale, causal) -
+                  _np_loss(*minus, g, cq, ck, case.softmax_scale, causal)) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (which, idx, fd, grad[idx])
