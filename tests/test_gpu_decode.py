@@ -66,8 +66,9 @@ def _compare(m, l, o, out, st, ref, what):
     assert_out_close(o[live] / l[live][:, None], ref[live], what + " o/l")
 
 
-def test_decode_workload(vfa, oracle_mod):
-    case = W.decode(0)
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_decode_workload(vfa, oracle_mod, seed):
+    case = W.decode(seed)
     assert case.num_steps <= 16 and case.num_seqs == 64
     m, l, o, out = _run_gpu(vfa, case)
     st, ref = _run_oracle(oracle_mod, case)
@@ -175,8 +176,9 @@ def test_bad_block_table_sets_status_and_skips_sequence(vfa, bad):
 # Contexts that end inside their last block, and an explicit scale: the step
 # absorbs only the first tile_token_counts[s] tokens of the listed blocks.
 
-def test_decode_workload_exact_context(vfa, oracle_mod):
-    case = W.decode(1)
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_decode_workload_exact_context(vfa, oracle_mod, seed):
+    case = W.decode(seed)
     assert any(c % case.block_size for c in case.context_lengths)
     m, l, o, out = _run_gpu(vfa, case, exact=True)
     st, ref = _run_oracle(oracle_mod, case, exact=True)

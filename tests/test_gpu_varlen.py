@@ -1,9 +1,11 @@
 """GPU parity of vfa_varlen_fwd against the fp64 oracle (through the C ABI).
 
-Full elementwise comparison where the oracle finishes in seconds (tiny,
-packed, cross-attention at D=64 and D=256, edge cases); sampled rows for the
-32768-token long-tail workload, in the same launch configuration the bench
-times.  Outputs start as NaN canaries, so a row the kernel never wrote fails.
+Every workload (tiny, packed, long-tail, cross-attention at D=64 and D=256)
+at seeds 0, 1 and 2, compared element by element over every output row, in
+the launch configuration the bench times; the long-tail workload (32768
+tokens, H=32, about a minute of oracle time per seed on 16 cores) too.
+Edge cases and variants on smaller shapes.  Outputs start as NaN canaries,
+so a row the kernel never wrote fails.
 """
 import numpy as np
 import pytest
@@ -45,41 +47,32 @@ def test_tiny(vfa, oracle_mod, causal, seed):
     _check_full(vfa, oracle_mod, W.tiny(causal, seed))
 
 
-@pytest.mark.parametrize("seed", [0, 1])
+@pytest.mark.parametrize("seed", [0, 1, 2])
 def test_packed_training_batch(vfa, oracle_mod, seed):
     _check_full(vfa, oracle_mod, W.packed(seed))
 
 
+@pytest.mark.parametrize("seed", [0, 1, 2])
 @pytest.mark.parametrize("head_dim", [64, 256])
-def test_cross_attention(vfa, oracle_mod, head_dim):
-    case = W.cross(head_dim, 0)
+def test_cross_attention(vfa, oracle_mod, head_dim, seed):
+    case = W.cross(head_dim, seed)
     assert sum(1 for x in case.lengths_k if x == 1) >= 4
     _check_full(vfa, oracle_mod, case)
 
 
-def test_longtail_sampled(vfa, oracle_mod):
-    case = W.longtail(0)
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_longtail_full(vfa, oracle_mod, seed):
+    # all 32768 x 32 (token, head) rows against the oracle, compared in slices
+    # of tokens to bound the host memory the comparison takes
+    case = W.longtail(seed)
     assert case.total_q == 32768 and max(case.lengths_q) == 8192
     out, lse, status = run_varlen(vfa, case)
     assert status == 0
-    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))     # every row written
-    rng = np.random.default_rng(123)
-    H = case.num_heads
-    rows = [np.stack([rng.integers(0, case.total_q, 1500), rng.integers(0, H, 1500)], 1)]
-    for b in range(case.batch):            # first and last row of every sequence, random head
-        q0, q1 = int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1])
-        if q1 > q0:
-            rows.append(np.array([[q0, rng.integers(0, H)], [q1 - 1, rng.integers(0, H)]]))
-    b8 = case.lengths_q.index(8192)        # the last q tile of the longest sequence, all heads 0/31
-    q1 = int(case.cu_seqlens_q[b8 + 1])
-    rows.append(np.stack([np.arange(q1 - 128, q1), np.zeros(128, int)], 1))
-    rows.append(np.stack([np.arange(q1 - 128, q1), np.full(128, H - 1)], 1))
-    rows = np.concatenate(rows).astype(np.int64)
-    ref_out, ref_lse, _ = oracle_mod.varlen_fwd_rows(case.q, case.k, case.v, case.cu_seqlens_q,
-                                                     case.cu_seqlens_k, H, case.head_dim,
-                                                     case.softmax_scale, True, rows)
-    assert_out_close(out[rows[:, 0], rows[:, 1]], ref_out, "longtail")
-    assert_lse_close(lse[rows[:, 0], rows[:, 1]], ref_lse, "longtail")
+    ref_out, ref_lse = _oracle_full(oracle_mod, case)
+    for t0 in range(0, case.total_q, 4096):
+        t1 = min(case.total_q, t0 + 4096)
+        assert_out_close(out[t0:t1], ref_out[t0:t1], f"longtail seed {seed} tokens {t0}..")
+        assert_lse_close(lse[t0:t1], ref_lse[t0:t1], f"longtail seed {seed} tokens {t0}..")
 
 
 EDGE = [
