@@ -173,11 +173,17 @@ vfa_status vfa_varlen_fwd_fp8(const void *q_fp8, const void *k_fp8, const void *
  *                (VFA_OK or VFA_ERR_BAD_SEQLENS ...), copied on `stream`.
  *
  * Limits and rules:
- *   - a problem whose vfa_varlen_fwd_workspace_bytes() exceeds 1 MiB
- *     (roughly num_heads * (total_q / 128 + batch) > 30000) returns
- *     VFA_ERR_UNSUPPORTED and enqueues nothing;
+ *   - a problem whose vfa_varlen_fwd_workspace_bytes() exceeds 1 MiB returns
+ *     VFA_ERR_UNSUPPORTED and enqueues nothing.  That size is exactly
+ *     round256(round256(256 + 32 * num_heads * (total_q / 128 + batch))
+ *     + 56 * (batch + 1)) bytes (integer division; round256 rounds up to a
+ *     multiple of 256): the status word and counters, 32 bytes per work
+ *     item, then 14 int32 of scheduler records per sequence;
  *   - the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture;
+ *     (cudaGetSymbolAddress) and remembers it together with the current CUDA
+ *     context; a call under another context (after cudaDeviceReset, or a
+ *     thread with a context of its own) looks it up again.  Make such first
+ *     calls before any stream capture;
  *   - all calls share the one array: calls whose work can overlap on the GPU
  *     (different streams without ordering) race and give undefined results.
  *     Each call rewrites every scratch word it reads, so stream-ordered calls

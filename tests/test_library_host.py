@@ -144,3 +144,34 @@ def test_backward_and_fp8_host_checks(vfa):
     assert L.vfa_varlen_fwd_fp8(*f8(64, 1.0, 1.0)) == vfa.VFA_ERR_UNSUPPORTED
     assert L.vfa_varlen_fwd_fp8(*f8(128, 0.0, 1.0)) == vfa.VFA_ERR_INVALID_ARG
     assert L.vfa_varlen_fwd_fp8(*f8(128, 1.0, float("inf"))) == vfa.VFA_ERR_INVALID_ARG
+
+
+def test_noalloc_rejects_problems_beyond_the_static_scratch(vfa):
+    # The static scratch of vfa_varlen_fwd_noalloc holds 1 MiB; a problem whose
+    # workspace is larger is refused on the host, before any device work.
+    L = vfa.lib()
+    nul = None
+    # 100k one-token sequences x 8 heads need far more than 1 MiB of work list
+    assert L.vfa_varlen_fwd_workspace_bytes(100000, 100000, 100000, 8, 128) > (1 << 20)
+    st = L.vfa_varlen_fwd_noalloc(nul, nul, nul, nul, nul, 100000, 100000, 1, 100000, 8, 8, 128,
+                                  0.1, 0, -1, nul, nul, nul, nul)
+    assert st == vfa.VFA_ERR_UNSUPPORTED
+    assert b"static scratch" in L.vfa_last_error()
+    # the limit is the exact size: one work item (32 bytes) past it is refused
+    r = lambda x: (x + 255) // 256 * 256
+    size = lambda B, tq, H: r(r(256 + 32 * H * (tq // 128 + B)) + 56 * (B + 1))
+    B, H = 1, 1
+    tq = 128 * ((1 << 20) - 1024) // 32         # just inside
+    while size(B, tq + 128, H) <= (1 << 20):
+        tq += 128
+    assert size(B, tq, H) <= (1 << 20) < size(B, tq + 128, H)
+    assert L.vfa_varlen_fwd_workspace_bytes(B, tq, tq, H, 128) == size(B, tq, H)
+    st = L.vfa_varlen_fwd_noalloc(nul, nul, nul, nul, nul, tq + 128, tq + 128, 1, B, H, H, 128,
+                                  0.1, 0, -1, nul, nul, nul, nul)
+    assert st == vfa.VFA_ERR_UNSUPPORTED
+    # within the limit the call gets past the size check (and then stops at the
+    # missing device or the null pointers)
+    st = L.vfa_varlen_fwd_noalloc(nul, nul, nul, nul, nul, tq, tq, 1, B, H, H, 128, 0.1, 0, -1,
+                                  nul, nul, nul, nul)
+    assert st in (vfa.VFA_ERR_INVALID_ARG, vfa.VFA_ERR_CUDA)
+    assert b"static scratch" not in L.vfa_last_error()

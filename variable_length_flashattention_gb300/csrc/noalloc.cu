@@ -24,23 +24,67 @@ namespace {
 constexpr size_t kStaticScratchBytes = 1u << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-// Device address of g_static_scratch on `dev` (the current device), looked
-// up once per device.  In host code the array's name only stands for the
-// symbol; the kernels must be given this address.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Identifier of the calling thread's current CUDA context (unique within the
+// process: a context created after cudaDeviceReset gets a new one).  False
+// when no context is current or the driver does not offer the query.
+bool current_context_id(unsigned long long *id)
+{
+    static std::once_flag once;
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+        return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_static_scratch on `dev` (the current device).  In host
+// code the array's name only stands for the symbol; the kernels must be given
+// this address.  It is looked up once per device and context: the cache
+// remembers which context the address belongs to, and a call made under
+// another context (after cudaDeviceReset, or from a thread with its own
+// context) looks the address up again instead of reusing a dead one.
 void *scratch_address(int dev, cudaError_t *err)
 {
     static std::mutex mu;
     static void *addr[64] = {nullptr};
+    static unsigned long long ctx_of[64] = {0};
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
     std::lock_guard<std::mutex> lk(mu);
-    if (addr[dev] == nullptr) {
-        void *p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (*err != cudaSuccess)
-            return nullptr;
-        addr[dev] = p;
+    if (addr[dev] != nullptr && have_id && ctx_of[dev] == id) {
+        *err = cudaSuccess;
+        return addr[dev];
     }
-    *err = cudaSuccess;
-    return addr[dev];
+    void *p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (*err != cudaSuccess)
+        return nullptr;
+    // the look-up makes the device's primary context current if none was
+    unsigned long long id_now = 0;
+    if (current_context_id(&id_now)) {
+        addr[dev] = p;
+        ctx_of[dev] = id_now;
+    } else {
+        addr[dev] = nullptr;      // no way to tell contexts apart: look up on every call
+    }
+    return p;
 }
 
 }  // namespace
