@@ -258,16 +258,17 @@ vfa_status vfa_varlen_schedule(const int32_t *cu_seqlens_q, const int32_t *cu_se
  * dk, dv        device bf16 [total_k, num_kv_heads, head_dim] (output; keys
  *               no query sees get 0).
  * workspace     device scratch of vfa_varlen_bwd_workspace_bytes() bytes,
- *               256-byte aligned (status word, per-sequence key-tile starts,
- *               Delta, an fp32 dq sum); calls sharing it must be
- *               stream-ordered.  Its first int32 is the device status word
+ *               256-byte aligned (status word, per-sequence key-tile and
+ *               q-tile starts, Delta = rowsum(dout * out)); calls sharing it
+ *               must be stream-ordered.  Its first int32 is the device status word
  *               (read with vfa_read_status): VFA_ERR_BAD_SEQLENS for invalid
  *               cu_seqlens (nothing written), VFA_ERR_TIMEOUT if a bounded
  *               wait expired.
  *
- * Supported: head_dim 64 or 128 (others: VFA_ERR_UNSUPPORTED); 16-byte
- * aligned tensors.  dq is accumulated with fp32 atomics, so its last bits
- * can vary between runs; dk and dv are deterministic.
+ * Supported: head_dim 64, 128 or 256 (others: VFA_ERR_UNSUPPORTED); 16-byte
+ * aligned tensors.  No gradient is accumulated with atomics: dk and dv are
+ * summed per key tile and dq per query tile in a fixed order, so the three
+ * are bit-identical from run to run.
  */
 size_t vfa_varlen_bwd_workspace_bytes(int batch, int total_q, int num_heads, int head_dim);
 
@@ -336,6 +337,56 @@ vfa_status vfa_paged_decode_step(const void *q, const void *k_pool, const void *
                                  int head_dim, int block_size, float softmax_scale, float *m,
                                  float *l, float *o, int32_t *device_status,
                                  vfa_stream_t stream);
+
+/*
+ * vfa_paged_decode_step with each (sequence, kv head) tile cut into
+ * num_splits contiguous runs of its blocks, one CTA per run, so a batch of
+ * few sequences with long tiles still spreads over every SM.  The result
+ * is the same state update: "attention_ref.rs" (file header) requires a
+ * tile's fragmentation to give the single-shot result, and the runs are
+ * merged with the same rule the step applies across tiles (m = max of the
+ * parts, l and o rescaled by exp(m_part - m) and summed).
+ *
+ * Each run's CTA writes its partial (m, l, o) to `workspace` and takes a
+ * ticket (one atomic add); the last CTA of a (sequence, kv head) merges
+ * every run with the incoming state, writes (m, l, o) and sets the ticket
+ * back to zero.  No CTA waits for another.
+ *
+ * Arguments, results and device checks as in vfa_paged_decode_step, plus:
+ * num_splits     runs per tile, 1 ..  1024 (1 = vfa_paged_decode_step;
+ *                vfa_paged_decode_split_count suggests one); runs past a
+ *                tile's last block are empty.
+ * workspace      device scratch of vfa_paged_decode_split_workspace_bytes()
+ *                bytes, 256-byte aligned, ignored when num_splits == 1.  It
+ *                must hold zeros before its first use (e.g. cleared when
+ *                allocated); every call leaves it that way.  Calls sharing
+ *                one workspace must be stream-ordered.
+ */
+vfa_status vfa_paged_decode_step_split(const void *q, const void *k_pool, const void *v_pool,
+                                       int num_blocks, const int32_t *tile_blocks,
+                                       const int32_t *tile_block_counts,
+                                       const int32_t *tile_token_counts, int tile_capacity,
+                                       int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, float softmax_scale,
+                                       float *m, float *l, float *o, int32_t *device_status,
+                                       int num_splits, void *workspace, size_t workspace_bytes,
+                                       vfa_stream_t stream);
+
+/*
+ * Workspace bytes of vfa_paged_decode_step_split: one ticket per (sequence,
+ * kv head) and (head_dim + 2) floats per (sequence, q head, run).  0 for
+ * unsupported sizes.
+ */
+size_t vfa_paged_decode_split_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                              int head_dim, int num_splits);
+
+/*
+ * A run count for vfa_paged_decode_step_split on the current device: about
+ * four CTAs per SM over num_seqs * num_kv_heads rows, with runs of at least
+ * eight blocks of a tile_capacity-block tile.
+ */
+vfa_status vfa_paged_decode_split_count(int num_seqs, int num_kv_heads, int tile_capacity,
+                                        int *num_splits);
 
 /*
  * finalize_ref of "attention_ref.rs": out = bf16(o * (l > 0 ? 1 / l : 0)),

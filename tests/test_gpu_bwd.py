@@ -70,7 +70,7 @@ def test_tiny(vfa, oracle_mod, causal, seed):
     _compare(vfa, oracle_mod, W.tiny(bool(causal), seed), causal, seed=seed)
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [0, 1, 2])
 def test_small_mixes(vfa, oracle_mod, D, causal):
     lq = [1, 7, 64, 129, 300, 0, 257]
@@ -79,15 +79,16 @@ def test_small_mixes(vfa, oracle_mod, D, causal):
     _compare(vfa, oracle_mod, case, causal, seed=causal)
 
 
+@pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("window_left", [0, 100, 300])
 @pytest.mark.parametrize("causal", [1, 2])
-def test_sliding_window(vfa, oracle_mod, window_left, causal):
+def test_sliding_window(vfa, oracle_mod, window_left, causal, D):
     lq, lk = [500, 64, 700, 1], [500, 300, 400, 50]
-    case = W.make_varlen("bwd-window", lq, lk, 2, 128, True, 1.0, value_seed=7 + window_left)
+    case = W.make_varlen("bwd-window", lq, lk, 2, D, True, 1.0, value_seed=7 + window_left)
     _compare(vfa, oracle_mod, case, causal, window_left=window_left, seed=window_left)
 
 
-@pytest.mark.parametrize("H,Hkv,D", [(8, 2, 128), (4, 1, 64)])
+@pytest.mark.parametrize("H,Hkv,D", [(8, 2, 128), (4, 1, 64), (4, 2, 256)])
 def test_grouped_kv_heads(vfa, oracle_mod, H, Hkv, D):
     lq, lk = [300, 7, 129, 64], [300, 40, 129, 200]
     case = W.make_varlen("bwd-gqa", lq, lk, H, D, True, 1.0, value_seed=H + Hkv)
@@ -118,11 +119,29 @@ def test_bad_cu_seqlens_sets_status(vfa):
     assert torch.isnan(dq.float()).all()
 
 
+@pytest.mark.parametrize("D", [64, 256])
 @pytest.mark.parametrize("causal", [0, 1, 2])
-def test_edge_lengths(vfa, oracle_mod, causal):
+def test_edge_lengths(vfa, oracle_mod, causal, D):
     # a query sequence with no keys (dq = 0), keys no query sees (dk = dv = 0),
     # one-token sequences and an empty sequence between non-empty ones
     lq = [10, 0, 1, 130, 3]
     lk = [0, 7, 1, 130, 200]
-    case = W.make_varlen("bwd-edge", lq, lk, 2, 64, bool(causal), 1.0, value_seed=40 + causal)
+    case = W.make_varlen("bwd-edge", lq, lk, 2, D, bool(causal), 1.0, value_seed=40 + causal)
     _compare(vfa, oracle_mod, case, causal, seed=40)
+
+
+def test_deterministic(vfa):
+    # no gradient is accumulated with atomics: two runs agree bit for bit
+    case = W.packed(2)
+    dout = W.upstream_grad(case, 2)
+    a = _run(vfa, case, dout, 1)
+    b = _run(vfa, case, dout, 1)
+    for x, y in zip(a[:3], b[:3]):
+        np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_cross_attention_d256(vfa, oracle_mod, seed):
+    # the cross-attention workload at head_dim 256 (32 sequences, q up to 512,
+    # k up to 4096 tokens, non-causal), every sequence and head
+    _compare(vfa, oracle_mod, W.cross(256, seed), 0, seed=seed)

@@ -131,13 +131,17 @@ def test_backward_and_fp8_host_checks(vfa):
                                                  fake, fake, 1 << 30, nul)
     assert L.vfa_varlen_bwd(*args(128, 0.1, 1, -1, q=nul)) == vfa.VFA_ERR_INVALID_ARG
     assert b"null" in L.vfa_last_error()
-    assert L.vfa_varlen_bwd(*args(256, 0.1, 1, -1)) == vfa.VFA_ERR_UNSUPPORTED
+    assert L.vfa_varlen_bwd(*args(96, 0.1, 1, -1)) == vfa.VFA_ERR_UNSUPPORTED
     assert L.vfa_varlen_bwd(*args(128, 0.0, 1, -1)) == vfa.VFA_ERR_INVALID_ARG
     assert L.vfa_varlen_bwd(*args(128, 0.1, 0, 8)) == vfa.VFA_ERR_INVALID_ARG
     assert b"window" in L.vfa_last_error()
     assert L.vfa_varlen_bwd(*args(128, 0.1, 3, -1)) == vfa.VFA_ERR_INVALID_ARG
-    assert L.vfa_varlen_bwd_workspace_bytes(1, 10, 2, 256) == 0
-    assert L.vfa_varlen_bwd_workspace_bytes(2, 10, 2, 128) >= 256 + 10 * 2 * (4 + 128 * 4)
+    assert L.vfa_varlen_bwd_workspace_bytes(1, 10, 2, 96) == 0
+    assert L.vfa_varlen_bwd_workspace_bytes(1, 10, 2, 256) > 0
+    # status word, key-tile and q-tile starts, Delta; no fp32 dq sum (dq is
+    # accumulated in TMEM per query tile)
+    assert L.vfa_varlen_bwd_workspace_bytes(2, 10, 2, 128) >= 256 + 2 * 3 * 4 + 10 * 2 * 4
+    assert L.vfa_varlen_bwd_workspace_bytes(2, 10, 2, 128) < 10 * 2 * 128 * 4
     # FP8 forward: head_dim 128 only, descales finite and positive
     f8 = lambda D, dq, dk: (fake, fake, fake, fake, fake, 4, 4, 4, 1, 2, 2, D, 0.1, dq, dk, 1, -1,
                             fake, fake, fake, 1 << 30, nul)

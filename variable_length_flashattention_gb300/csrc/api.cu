@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/vfa.h: argument checks, TMA tensor
 // map encoding, workspace carve-up and launches.  Nothing here allocates or
 // frees device memory.
+#include <algorithm>
 #include <cfloat>
 #include <cstdarg>
 #include <cmath>
@@ -130,6 +131,10 @@ vfa_status encode_pool_map(CUtensorMap *map, const void *base, int num_blocks, i
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
+
+// Most runs a split decode step cuts a tile into (the merge keeps one weight
+// per run and q head in the step kernel's 48 KB of shared memory).
+constexpr int kMaxDecodeSplits = 1024;
 
 }  // namespace
 
@@ -373,7 +378,7 @@ vfa_status vfa_varlen_fwd_fp8(const void *q_fp8, const void *k_fp8, const void *
 
 size_t vfa_varlen_bwd_workspace_bytes(int batch, int total_q, int num_heads, int head_dim)
 {
-    if (batch < 1 || total_q < 0 || num_heads < 1 || (head_dim != 64 && head_dim != 128))
+    if (batch < 1 || total_q < 0 || num_heads < 1 || !supported_head_dim(head_dim))
         return 0;
     return vfa::bwd_workspace_bytes(batch, total_q, num_heads, head_dim);
 }
@@ -398,8 +403,8 @@ vfa_status vfa_varlen_bwd(const void *q, const void *k, const void *v, const voi
         return fail(VFA_ERR_INVALID_ARG, "causal must be 0, 1 (top-left) or 2 (bottom-right)");
     if (window_left >= 0 && causal == 0)
         return fail(VFA_ERR_INVALID_ARG, "a sliding window needs a causal mode");
-    if (head_dim != 64 && head_dim != 128)
-        return fail(VFA_ERR_UNSUPPORTED, "backward head_dim %d not supported (64, 128)",
+    if (!supported_head_dim(head_dim))
+        return fail(VFA_ERR_UNSUPPORTED, "backward head_dim %d not supported (64, 128, 256)",
                     head_dim);
     if (!(softmax_scale > 0.f) || softmax_scale > FLT_MAX)
         return fail(VFA_ERR_INVALID_ARG, "softmax_scale must be finite and > 0 (got %g)",
@@ -422,10 +427,11 @@ vfa_status vfa_varlen_bwd(const void *q, const void *k, const void *v, const voi
         return st;
     vfa::BwdArgs a;
     memset(&a, 0, sizeof a);
-    if ((st = encode_packed_map(&a.tm_q, q, total_q, num_heads, head_dim, 128)) ||
-        (st = encode_packed_map(&a.tm_do, dout, total_q, num_heads, head_dim, 128)) ||
-        (st = encode_packed_map(&a.tm_k, k, total_k, num_kv_heads, head_dim, 128)) ||
-        (st = encode_packed_map(&a.tm_v, v, total_k, num_kv_heads, head_dim, 128)))
+    const int box = vfa::bwd_step_rows(head_dim);
+    if ((st = encode_packed_map(&a.tm_q, q, total_q, num_heads, head_dim, box)) ||
+        (st = encode_packed_map(&a.tm_do, dout, total_q, num_heads, head_dim, box)) ||
+        (st = encode_packed_map(&a.tm_k, k, total_k, num_kv_heads, head_dim, box)) ||
+        (st = encode_packed_map(&a.tm_v, v, total_k, num_kv_heads, head_dim, box)))
         return st;
     vfa::bwd_workspace_split(workspace, batch, total_q, num_heads, &a);
     a.cu_q = cu_seqlens_q;
@@ -446,12 +452,9 @@ vfa_status vfa_varlen_bwd(const void *q, const void *k, const void *v, const voi
     a.causal = causal;
     a.window_left = window_left < 0 ? -1 : window_left;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(a.dq_acc, 0,
-                                    static_cast<size_t>(total_q) * num_heads * head_dim * 4, s);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "dQ accumulator clear");
     const int key_tile_bound = total_k / 128 + batch;
-    e = vfa::launch_bwd(head_dim, a, key_tile_bound, dev.sm_count, s);
+    const int q_tile_bound = total_q / 128 + batch;
+    cudaError_t e = vfa::launch_bwd(head_dim, a, key_tile_bound, q_tile_bound, dev.sm_count, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "backward launch");
     return VFA_OK;
@@ -504,13 +507,14 @@ static vfa_status check_decode_args(const void *q, const void *k_pool, const voi
     return VFA_OK;
 }
 
-vfa_status vfa_paged_decode_step(const void *q, const void *k_pool, const void *v_pool,
-                                 int num_blocks, const int32_t *tile_blocks,
-                                 const int32_t *tile_block_counts,
-                                 const int32_t *tile_token_counts, int tile_capacity,
-                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                                 int block_size, float softmax_scale, float *m, float *l,
-                                 float *o, int32_t *device_status, vfa_stream_t stream)
+static vfa_status decode_step_impl(const void *q, const void *k_pool, const void *v_pool,
+                                   int num_blocks, const int32_t *tile_blocks,
+                                   const int32_t *tile_block_counts,
+                                   const int32_t *tile_token_counts, int tile_capacity,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, float softmax_scale, float *m, float *l,
+                                   float *o, int32_t *device_status, int num_splits,
+                                   void *workspace, size_t workspace_bytes, vfa_stream_t stream)
 {
     if (!q || !m || !l || !o)
         return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
@@ -546,6 +550,13 @@ vfa_status vfa_paged_decode_step(const void *q, const void *k_pool, const void *
     a.o = o;
     a.status = device_status;
     a.tile_token_counts = tile_token_counts;
+    a.num_splits = 1;
+    a.part = nullptr;
+    a.tickets = nullptr;
+    if (num_splits > 1) {
+        a.num_splits = num_splits;
+        vfa::decode_split_workspace_carve(workspace, num_seqs, num_kv_heads, &a);
+    }
     a.scale_log2 = static_cast<float>(
         (softmax_scale > 0.f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt(double(head_dim))) *
         1.4426950408889634);
@@ -559,6 +570,85 @@ vfa_status vfa_paged_decode_step(const void *q, const void *k_pool, const void *
     if (e != cudaSuccess)
         return cuda_fail(e, "decode step launch");
     return VFA_OK;
+}
+
+vfa_status vfa_paged_decode_step(const void *q, const void *k_pool, const void *v_pool,
+                                 int num_blocks, const int32_t *tile_blocks,
+                                 const int32_t *tile_block_counts,
+                                 const int32_t *tile_token_counts, int tile_capacity,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, float softmax_scale, float *m, float *l,
+                                 float *o, int32_t *device_status, vfa_stream_t stream)
+{
+    return decode_step_impl(q, k_pool, v_pool, num_blocks, tile_blocks, tile_block_counts,
+                            tile_token_counts, tile_capacity, num_seqs, num_q_heads,
+                            num_kv_heads, head_dim, block_size, softmax_scale, m, l, o,
+                            device_status, 1, nullptr, 0, stream);
+}
+
+size_t vfa_paged_decode_split_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                              int head_dim, int num_splits)
+{
+    if (num_seqs < 1 || num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads ||
+        !supported_head_dim(head_dim) || num_splits < 1 || num_splits > kMaxDecodeSplits)
+        return 0;
+    return vfa::decode_split_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                             num_splits);
+}
+
+vfa_status vfa_paged_decode_split_count(int num_seqs, int num_kv_heads, int tile_capacity,
+                                        int *num_splits)
+{
+    if (!num_splits)
+        return fail(VFA_ERR_INVALID_ARG, "null pointer argument");
+    if (num_seqs < 1 || num_kv_heads < 1 || tile_capacity < 0)
+        return fail(VFA_ERR_INVALID_ARG, "bad size argument");
+    DeviceInfo dev;
+    vfa_status st = current_device(&dev);
+    if (st)
+        return st;
+    // four step CTAs fit on an SM: aim for that many CTAs on every SM, with
+    // runs of at least eight blocks
+    const long long rows = static_cast<long long>(num_seqs) * num_kv_heads;
+    long long n = (4LL * dev.sm_count + rows - 1) / rows;
+    n = std::min<long long>(n, std::max(1, tile_capacity / 8));
+    n = std::max<long long>(1, std::min<long long>(n, kMaxDecodeSplits));
+    *num_splits = static_cast<int>(n);
+    return VFA_OK;
+}
+
+vfa_status vfa_paged_decode_step_split(const void *q, const void *k_pool, const void *v_pool,
+                                       int num_blocks, const int32_t *tile_blocks,
+                                       const int32_t *tile_block_counts,
+                                       const int32_t *tile_token_counts, int tile_capacity,
+                                       int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, float softmax_scale,
+                                       float *m, float *l, float *o, int32_t *device_status,
+                                       int num_splits, void *workspace, size_t workspace_bytes,
+                                       vfa_stream_t stream)
+{
+    if (num_splits < 1 || num_splits > kMaxDecodeSplits)
+        return fail(VFA_ERR_INVALID_ARG, "num_splits %d outside [1, %d]", num_splits,
+                    kMaxDecodeSplits);
+    if (num_splits > 1) {
+        if (!workspace || !aligned(workspace, 256))
+            return fail(VFA_ERR_INVALID_ARG, "workspace must be a non-null, 256-byte aligned "
+                                             "pointer");
+        if (num_seqs < 1 || num_kv_heads < 1 || num_q_heads < 1)
+            return fail(VFA_ERR_INVALID_ARG, "bad size argument");
+        const size_t need = vfa_paged_decode_split_workspace_bytes(num_seqs, num_q_heads,
+                                                                   num_kv_heads, head_dim,
+                                                                   num_splits);
+        if (need == 0)
+            return fail(VFA_ERR_UNSUPPORTED, "no split workspace for these sizes");
+        if (workspace_bytes < need)
+            return fail(VFA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes",
+                        workspace_bytes, need);
+    }
+    return decode_step_impl(q, k_pool, v_pool, num_blocks, tile_blocks, tile_block_counts,
+                            tile_token_counts, tile_capacity, num_seqs, num_q_heads,
+                            num_kv_heads, head_dim, block_size, softmax_scale, m, l, o,
+                            device_status, num_splits, workspace, workspace_bytes, stream);
 }
 
 vfa_status vfa_paged_decode_finalize(const float *l, const float *o, int num_seqs,

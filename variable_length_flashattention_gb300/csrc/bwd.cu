@@ -1,4 +1,5 @@
-// bwd.cu -- variable-length attention backward on sm_103a (head_dim 64, 128).
+// bwd.cu -- variable-length attention backward on sm_103a (head_dim 64, 128,
+// 256).
 //
 // Gradients of the forward (scaled scores, causal / bottom-right / sliding-
 // window masks on local positions, softmax over the visible keys) for an
@@ -7,26 +8,32 @@
 // dS = P * (dP - Delta):
 //   dV = P^T dO,   dK = scale * dS^T Q,   dQ = scale * dS K.
 //
-// Four kernels:
+// Four kernels, none of them with atomics, so every gradient is
+// deterministic:
 //   * bwd_prep: one CTA validates cu_seqlens and writes each sequence's first
-//     global key tile (a prefix sum of ceil(Lk_b / 128));
+//     global key tile and first global q tile (prefix sums of
+//     ceil(L / 128));
 //   * bwd_delta: Delta[t, h] = sum_d dO * out, one warp per (token, head);
-//   * bwd_kernel: one CTA per (128-key tile, kv head).  K and V stay in
-//     shared memory; for every query head of the group and every 128-row q
-//     tile that sees one of the tile's keys, TMA brings Q and dO (two
-//     buffers, so the next tile's copies overlap this one's work), and
-//     tcgen05.mma computes S^T = K Q^T and dP^T = V dO^T into TMEM, one
-//     64-query half at a time; for each half in turn, two threads per key
-//     row form P^T (bf16, back into TMEM over the S^T columns) and dS^T (bf16,
-//     128-byte-swizzled shared memory), and more MMAs accumulate dV += P^T dO
-//     and dK += dS^T Q in TMEM across the whole loop; after both halves,
-//     dQ = dS K for this q tile, which the threads (now two per query row)
-//     add into an fp32 buffer with vector atomics.  At the end dK (scaled) and
-//     dV leave as bf16;
-//   * bwd_dq: dQ = bf16(scale * the fp32 sum).
-// TMEM: S^T 128 columns, dP^T 128 (dQ reuses them once dP is read), dV and
-// dK D each -- 512 for D = 128.  Every wait is bounded; on expiry the CTA
-// records VFA_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
+//   * bwd_dkdv_kernel: one CTA per (128-key tile, kv head) -- at head_dim
+//     256 two, each owning one column half of dK and dV.  K and V stay in
+//     shared memory; the query rows that see a key of the tile stream past
+//     in steps of STEP rows (64; 32 at head_dim 256), every query head of the
+//     group, Q and dO through a TMA ring.  Per step the tensor core forms
+//     S^T = K Q^T and dP^T = V dO^T into one of two TMEM buffers; eight warps
+//     turn them into P^T and dS^T (bf16, written back over the columns they
+//     read), and the tensor core accumulates dV += P^T dO and dK += dS^T Q in
+//     TMEM with both A operands read from TMEM.  With two buffers the next
+//     step's S^T / dP^T run on the tensor core while this step's are being
+//     exponentiated;
+//   * bwd_dq_kernel: one CTA per (128-query tile, head), the same with the
+//     roles swapped: Q, dO stay, K and V stream past in blocks of STEP keys;
+//     S = Q K^T, dP = dO V^T into two TMEM buffers, dS (bf16, over dP) and
+//     dQ += dS K in TMEM.  dQ leaves as bf16 once, so no fp32 sum and no
+//     second pass exist.
+// The math warps evaluate masks only on steps that need them, as one
+// interval of visible columns per thread.  Every wait is bounded; on expiry
+// the CTA records VFA_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and
+// exits.
 #include <cfloat>
 #include <cuda_bf16.h>
 
@@ -37,57 +44,60 @@ namespace vfa {
 
 namespace {
 
-constexpr int kT = 128;            // key rows and query rows per tile
-constexpr int kComputeWarps = 8;   // two threads per tile row
-constexpr int kComputeThreads = kComputeWarps * 32;
-constexpr int kThreads = kComputeThreads + 32;   // + the TMA / MMA issuing warp
+constexpr int kOwn = 128;          // rows of a CTA's own tile (keys, resp. queries)
+constexpr int kMathWarps = 8;      // four TMEM lane quarters x two column halves
+constexpr int kFirstMathWarp = 4;
+constexpr int kMathThreads = kMathWarps * 32;
+constexpr int kThreads = (kFirstMathWarp + kMathWarps) * 32;   // + TMA, MMA, two idle warps
 constexpr int kPrepThreads = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Shapes per head_dim.  STEP rows (queries, resp. keys) stream past per step
+// (32 at head_dim 256, so that the own tiles and a two-stage ring fit shared
+// memory); the dK/dV kernel splits dK and dV into DSPLIT column halves, one
+// CTA each (at head_dim 256 the two accumulators would fill TMEM alone).
 template <int D>
 struct BwdCfg {
-    static constexpr int DB = D / 64;                       // 64-column blocks per row
-    static constexpr uint32_t TILE_BYTES = kT * D * 2;      // a 128-row tile of K, V, Q or dO
-    static constexpr uint32_t PS_BYTES = kT * kT * 2;       // dS^T, 128 x 128 bf16
-    static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + D;
-    static constexpr uint32_t COL_DQ = COL_DPT;             // dQ takes dP^T's columns
-    // P^T (bf16 pairs) goes over the S^T columns: queries 0-63 to columns
-    // 0-31, queries 64-127 to columns 64-95
+    static constexpr int DB = D / 64;                       // 128-byte column blocks per row
+    static constexpr int STEP = bwd_step_rows(D);           // also the TMA box height
+    static constexpr int NC = STEP / 2;                     // step columns per math thread
+    static constexpr int DSPLIT = D == 256 ? 2 : 1;
+    static constexpr int DKV = D / DSPLIT;                  // dK / dV columns per CTA
+    static constexpr uint32_t OWN_BYTES = kOwn * D * 2;     // a 128-row tile
+    static constexpr uint32_t STEP_BYTES = STEP * D * 2;    // a STEP-row tile
+    static constexpr int NSTAGE = D == 256 ? 2 : 4;         // streamed-tile ring stages
+    static constexpr uint32_t STAGE_BYTES = 2 * STEP_BYTES; // (Q, dO) or (K, V)
+    // TMEM.  dK/dV kernel: dV, dK (DKV columns each), then two buffers of S^T
+    // (STEP columns) + dP^T (STEP).  dQ kernel: dQ (D), then the two buffers.
+    static constexpr uint32_t COL_DV = 0, COL_DK = DKV, KV_BUF = 2 * DKV;
+    static constexpr uint32_t COL_DQ = 0, Q_BUF = D;
+    static constexpr uint32_t BUF_STRIDE = 2 * STEP;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int NUM_BARS = 11;
-    // K, V, two Q and two dO buffers, dS^T, lse, Delta, barriers
-    static constexpr size_t SMEM = 1024 + 6 * TILE_BYTES + PS_BYTES + 2 * kT * 4 +
-                                   NUM_BARS * 8 + 64;
-    static constexpr uint32_t IDESC_T = idesc_bf16_f32(kT, 64, false, false);   // S^T, dP^T halves
-    static constexpr uint32_t IDESC_KV = idesc_bf16_f32(kT, D, false, true);    // dV, dK
-    static constexpr uint32_t IDESC_Q = idesc_bf16_f32(kT, D, true, true);      // dQ
-    static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
+    static constexpr int NUM_BARS = 2 + 2 * NSTAGE + 2 + 2 + 2;
+    static constexpr size_t SMEM = 1024 + 2 * OWN_BYTES + NSTAGE * STAGE_BYTES +
+                                   kMathWarps * 256 + NUM_BARS * 8 + 64;
+    // S^T / dP^T (keys x STEP queries) and S / dP (queries x STEP keys): both K-major
+    static constexpr uint32_t IDESC_T = idesc_bf16_f32(kOwn, STEP, false, false);
+    // dV, dK (DKV columns) and dQ (D columns): A from TMEM, B (dO, Q or K rows) MN-major
+    static constexpr uint32_t IDESC_KV = idesc_bf16_f32(kOwn, DKV, false, true);
+    static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(kOwn, D, false, true);
+    static_assert(KV_BUF + 2 * BUF_STRIDE <= TMEM_COLS && Q_BUF + 2 * BUF_STRIDE <= TMEM_COLS,
+                  "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 // ------------------------------------------------------------ prep
 
-__global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const BwdArgs a)
+// Exclusive prefix sum over blockDim.x-wide chunks of per-sequence counts;
+// out[b] = sum of count(b') for b' < b, out[B] = the total.
+template <typename CountFn>
+__device__ void block_prefix(int B, int32_t *out, int *warp_sums, CountFn count)
 {
-    __shared__ int warp_sums[32];
-    __shared__ int s_bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int B = a.batch;
-    if (tid == 0)
-        s_bad = (a.cu_q[0] != 0 || a.cu_k[0] != 0 || a.cu_q[B] != a.total_q ||
-                 a.cu_k[B] != a.total_k);
-    __syncthreads();
     int carry = 0;
     for (int base = 0; base < B; base += kPrepThreads) {
         const int b = base + tid;
-        int nt = 0;
-        if (b < B) {
-            const int lq = a.cu_q[b + 1] - a.cu_q[b], lk = a.cu_k[b + 1] - a.cu_k[b];
-            if (lq < 0 || lk < 0)
-                s_bad = 1;
-            else
-                nt = (lk + kT - 1) / kT;
-        }
+        const int nt = b < B ? count(b) : 0;
         int x = nt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -111,14 +121,38 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const BwdArgs a)
         __syncthreads();
         const int excl = x - nt + (warp > 0 ? warp_sums[warp - 1] : 0);
         if (b < B)
-            a.ktile_start[b] = carry + excl;
+            out[b] = carry + excl;
         carry += warp_sums[31];
         __syncthreads();
     }
-    if (tid == 0) {
-        a.ktile_start[B] = carry;
+    if (tid == 0)
+        out[B] = carry;
+}
+
+__global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const BwdArgs a)
+{
+    __shared__ int warp_sums[32];
+    __shared__ int s_bad;
+    const int B = a.batch;
+    if (threadIdx.x == 0)
+        s_bad = (a.cu_q[0] != 0 || a.cu_k[0] != 0 || a.cu_q[B] != a.total_q ||
+                 a.cu_k[B] != a.total_k);
+    __syncthreads();
+    block_prefix(B, a.ktile_start, warp_sums, [&](int b) {
+        const int lq = a.cu_q[b + 1] - a.cu_q[b], lk = a.cu_k[b + 1] - a.cu_k[b];
+        if (lq < 0 || lk < 0) {
+            s_bad = 1;
+            return 0;
+        }
+        return (lk + kOwn - 1) / kOwn;
+    });
+    block_prefix(B, a.qtile_start, warp_sums, [&](int b) {
+        const int lq = a.cu_q[b + 1] - a.cu_q[b];
+        return lq > 0 ? (lq + kOwn - 1) / kOwn : 0;
+    });
+    __syncthreads();
+    if (threadIdx.x == 0)
         *a.status = s_bad ? VFA_ERR_BAD_SEQLENS : VFA_OK;
-    }
 }
 
 // ------------------------------------------------------------ Delta
@@ -151,102 +185,255 @@ __global__ void bwd_delta_kernel(const BwdArgs a)
     }
 }
 
-// ------------------------------------------------------------ main
+// ------------------------------------------------------------ shared pieces
 
-// Byte offset of the 16-byte chunk holding columns 8*c8 .. 8*c8+7 of row r in
-// a 128-row operand of 128 bf16 columns stored as two 64-column blocks with
-// the 128-byte swizzle (the layout TMA's SWIZZLE_128B gives).
-__device__ __forceinline__ uint32_t sw_chunk(int r, int c8)
+// Largest b with start[b] <= gt (start is a non-decreasing prefix sum).
+__device__ __forceinline__ int owner_of(const int32_t *start, int B, int gt)
 {
-    return static_cast<uint32_t>((c8 >> 3) * (kT * 128) + r * 128 + (((c8 & 7) ^ (r & 7)) << 4));
-}
-
-__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
-{
-    const uint4 v = ld_shared_v4(addr);
-    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
-                       __uint_as_float(v.w));
-}
-
-// Where the key row of this thread sees query column c of the tile (only
-// for tiles that are not fully visible).
-struct BwdMask {
-    int j, lk, lq, causal, wl;
-    long long i_lo, off;
-    __device__ __forceinline__ bool visible(int c) const
-    {
-        const long long i = i_lo + c;
-        bool v = j < lk && i < lq;
-        if (causal)
-            v = v && j <= i + off;
-        if (wl >= 0)
-            v = v && j >= i + off - wl;
-        return v;
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (start[mid] <= gt)
+            lo = mid;
+        else
+            hi = mid - 1;
     }
-};
+    return lo;
+}
 
-// P^T and dS^T of one 16-column chunk of this thread's key row: p = 2^(s *
-// scale_log2 - lse2) (masked entries 0), ds = p * (dp - Delta); lse2 and
-// Delta of the chunk's columns come from shared memory (nl = -lse2).  The
-// bf16 pairs land in pk[0..7] and dk2[0..7].
-template <bool FULL>
-__device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[16], const uint32_t (&dr)[16],
-                                          float scale_log2, uint32_t s_nl, uint32_t s_delta,
-                                          int cb, const BwdMask &m, uint32_t *pk, uint32_t *dk2)
+// The visible part of (at most 32) consecutive columns, [lo, hi) (empty when hi <= lo),
+// clamped to [-1, 33] so it fits an int.
+__device__ __forceinline__ int clamp_col(long long x)
 {
+    return static_cast<int>(x < -1 ? -1 : (x > 33 ? 33 : x));
+}
+
+// Key j's visible queries among i_base, i_base + 1, ... (the dK/dV kernel's
+// columns): i < Lq, and i >= j - off (causal), i <= j - off + window_left.
+__device__ __forceinline__ void key_row_span(long long j, long long i_base, int lk, int lq,
+                                             int causal, int wl, long long off, int *lo, int *hi)
+{
+    long long l = causal ? j - off - i_base : 0;
+    long long h = lq - i_base;
+    if (wl >= 0)
+        h = min(h, j - off + wl - i_base + 1);
+    if (j >= lk)
+        h = l;
+    *lo = clamp_col(l);
+    *hi = clamp_col(h);
+}
+
+// Query i's visible keys among j_base, j_base + 1, ... (the dQ kernel's
+// columns): j < Lk, and j <= i + off (causal), j >= i + off - window_left.
+__device__ __forceinline__ void query_row_span(long long i, long long j_base, int lk, int lq,
+                                               int causal, int wl, long long off, int *lo,
+                                               int *hi)
+{
+    long long l = (causal && wl >= 0) ? i + off - wl - j_base : 0;
+    long long h = lk - j_base;
+    if (causal)
+        h = min(h, i + off - j_base + 1);
+    if (i >= lq)
+        h = l;
+    *lo = clamp_col(l);
+    *hi = clamp_col(h);
+}
+
+// P^T and dS^T of this thread's key row over its NC query columns: p =
+// 2^(s scale_log2 + nl) (0 outside the visible columns [lo, hi) when MASK)
+// and ds = p (dp + nd), with nl = -lse log2(e) and nd = -Delta of each column
+// read from shared memory (NC floats each at wstat, wstat + 128).
+template <bool MASK, int NC>
+__device__ __forceinline__ void key_row_grads(const uint32_t (&sr)[NC], const uint32_t (&dr)[NC],
+                                              float scale_log2, uint32_t wstat, int lo, int hi,
+                                              uint32_t (&pk)[NC / 2], uint32_t (&dk2)[NC / 2])
+{
+    const float2 c2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
-    for (int e = 0; e < 16; e += 4) {
-        const float4 nl = ld_shared_f4(s_nl + (cb + e) * 4);
-        const float4 dl = ld_shared_f4(s_delta + (cb + e) * 4);
-        const float nls[4] = {nl.x, nl.y, nl.z, nl.w};
-        const float dls[4] = {dl.x, dl.y, dl.z, dl.w};
-        float p[4], d[4];
+    for (int e = 0; e < NC; e += 4) {
+        const uint4 nl4 = ld_shared_v4(wstat + e * 4);
+        const uint4 nd4 = ld_shared_v4(wstat + 128 + e * 4);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float x = ex2_approx(fmaf(__uint_as_float(sr[e + u]), scale_log2, nls[u]));
-            p[u] = FULL ? x : (m.visible(cb + e + u) ? x : 0.f);
-            d[u] = p[u] * (__uint_as_float(dr[e + u]) - dls[u]);
+        for (int u = 0; u < 4; u += 2) {
+            const uint32_t nla = u ? nl4.z : nl4.x, nlb = u ? nl4.w : nl4.y;
+            const uint32_t nda = u ? nd4.z : nd4.x, ndb = u ? nd4.w : nd4.y;
+            const float2 t = __ffma2_rn(make_float2(__uint_as_float(sr[e + u]),
+                                                    __uint_as_float(sr[e + u + 1])),
+                                        c2, make_float2(__uint_as_float(nla),
+                                                        __uint_as_float(nlb)));
+            float p0 = ex2_approx(t.x), p1 = ex2_approx(t.y);
+            if (MASK) {
+                p0 = (e + u >= lo && e + u < hi) ? p0 : 0.f;
+                p1 = (e + u + 1 >= lo && e + u + 1 < hi) ? p1 : 0.f;
+            }
+            const float2 g = __fadd2_rn(make_float2(__uint_as_float(dr[e + u]),
+                                                    __uint_as_float(dr[e + u + 1])),
+                                        make_float2(__uint_as_float(nda), __uint_as_float(ndb)));
+            const float2 ds = __fmul2_rn(make_float2(p0, p1), g);
+            pk[(e + u) >> 1] = pack_bf16x2(p0, p1);
+            dk2[(e + u) >> 1] = pack_bf16x2(ds.x, ds.y);
         }
-        pk[(e >> 1)] = pack_bf16x2(p[0], p[1]);
-        pk[(e >> 1) + 1] = pack_bf16x2(p[2], p[3]);
-        dk2[(e >> 1)] = pack_bf16x2(d[0], d[1]);
-        dk2[(e >> 1) + 1] = pack_bf16x2(d[2], d[3]);
     }
 }
 
-// Adds this thread's dQ row segment (DH floats) into the fp32 sum.
-template <int DH>
-__device__ __forceinline__ void flush_dq(float4 *dst, const float4 (&acc)[DH / 4])
+// dS of this thread's query row over its NC key columns: p = 2^(s
+// scale_log2 + nl) (0 outside [lo, hi) when MASK), ds = p (dp + nd) with the
+// row's nl = -lse log2(e) and nd = -Delta.
+template <bool MASK, int NC>
+__device__ __forceinline__ void query_row_grads(const uint32_t (&sr)[NC], const uint32_t (&dr)[NC],
+                                                float scale_log2, float nl, float nd, int lo,
+                                                int hi, uint32_t (&dk2)[NC / 2])
 {
+    const float2 c2 = make_float2(scale_log2, scale_log2);
+    const float2 nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
 #pragma unroll
-    for (int c = 0; c < DH / 4; ++c)
-        atomicAdd(dst + c, acc[c]);
+    for (int e = 0; e < NC; e += 2) {
+        const float2 t = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                    c2, nl2);
+        float p0 = ex2_approx(t.x), p1 = ex2_approx(t.y);
+        if (MASK) {
+            p0 = (e >= lo && e < hi) ? p0 : 0.f;
+            p1 = (e + 1 >= lo && e + 1 < hi) ? p1 : 0.f;
+        }
+        const float2 g = __fadd2_rn(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                    nd2);
+        const float2 ds = __fmul2_rn(make_float2(p0, p1), g);
+        dk2[e >> 1] = pack_bf16x2(ds.x, ds.y);
+    }
 }
 
-// Warps 0-7 compute (warp w: TMEM lanes / tile rows 32 (w % 4) .. +31; of
-// each 64-query half the 32 queries 32 (w / 4) .. +31; of dQ, dK and dV the
-// column half w / 4); warp 8 issues the TMA copies and the MMAs.
+// Loads a tile of `rows` rows (a multiple of the map's box height BOX) of
+// every 64-column block of row `row0`, head `head` into a 128-byte-swizzled
+// buffer holding `rows` rows per column block.
+template <int DB, int BOX>
+__device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                          int head, int row0, int rows)
+{
+    for (int db = 0; db < DB; ++db)
+        for (int r = 0; r < rows; r += BOX)
+            tma_load_3d(dst + db * (rows * 128) + r * 128, map, bar, db * 64, head, row0 + r);
+}
+
+// S (or S^T) = A B^T over K = D for A a 128-row operand and B a STEP-row
+// operand, both K-major in 128-byte-swizzled column blocks.
+template <int D, int STEP>
+__device__ __forceinline__ void issue_scores(uint32_t d_tmem, uint32_t a_buf, uint32_t b_buf,
+                                             uint32_t idesc)
+{
+    const uint64_t a0 = sdesc_sw128(a_buf, 16, 1024), b0 = sdesc_sw128(b_buf, 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t ao = ((kk >> 2) * (kOwn * 128) + (kk & 3) * 32) >> 4;
+        const uint64_t bo = ((kk >> 2) * (STEP * 128) + (kk & 3) * 32) >> 4;
+        if (kk == 0)
+            mma_ss_w<0>(d_tmem, a0 + ao, b0 + bo, idesc);
+        else
+            mma_ss_w<1>(d_tmem, a0 + ao, b0 + bo, idesc);
+    }
+}
+
+// D += A B over K = STEP streamed rows: A (128 x STEP, bf16 pairs) in TMEM at
+// a_tmem, written by the two column halves of the math warps (half g's STEP/2
+// columns packed into the first STEP/4 of its own STEP/2 columns); B the
+// STEP-row tile in shared memory from column block b_buf on, MN-major.
+template <int STEP>
+__device__ __forceinline__ void issue_accumulate(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_buf,
+                                                 uint32_t idesc, bool first)
+{
+    constexpr int HALF = STEP / 2;
+    const uint64_t b0 = sdesc_sw128(b_buf, STEP * 128, 1024);
+#pragma unroll
+    for (int kk = 0; kk < STEP / 16; ++kk) {
+        const uint32_t a = a_tmem + HALF * (kk * 16 / HALF) + ((kk * 16) % HALF) / 2;
+        const uint64_t bo = (kk * 16 * 128) >> 4;
+        if (kk == 0 && first)
+            mma_ts_w<0>(d_tmem, a, b0 + bo, idesc);
+        else
+            mma_ts_w<1>(d_tmem, a, b0 + bo, idesc);
+    }
+}
+
+// NC consecutive TMEM columns of this warp's lanes into r (warp-collective),
+// and NC / 2 packed columns back.
+template <int NC>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, uint32_t (&r)[NC])
+{
+    if constexpr (NC == 32)
+        tmem_ld32(taddr, r);
+    else
+        tmem_ld16(taddr, r);
+}
+
+template <int NC>
+__device__ __forceinline__ void wait_cols(uint32_t (&r)[NC], uint32_t (&q)[NC])
+{
+    if constexpr (NC == 32) {
+        tmem_wait_ld_r(r);
+        tmem_bind_r(q);
+    } else {
+        tmem_wait_ld_r16(r);
+        asm volatile(""
+                     : "+r"(q[0]), "+r"(q[1]), "+r"(q[2]), "+r"(q[3]), "+r"(q[4]), "+r"(q[5]),
+                       "+r"(q[6]), "+r"(q[7]), "+r"(q[8]), "+r"(q[9]), "+r"(q[10]), "+r"(q[11]),
+                       "+r"(q[12]), "+r"(q[13]), "+r"(q[14]), "+r"(q[15])
+                     :
+                     : "memory");
+    }
+}
+
+template <int NP>
+__device__ __forceinline__ void st_cols(uint32_t taddr, const uint32_t (&r)[NP])
+{
+    if constexpr (NP == 16) {
+        tmem_st16(taddr, r);
+    } else {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], "
+                     "{%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+                     "r"(r[6]), "r"(r[7])
+                     : "memory");
+    }
+}
+
+// 32 columns of D (fp32 in TMEM, this thread's lane) * f -> 64 bytes of bf16 at dst.
+__device__ __forceinline__ void store_row32(uint32_t taddr, float f, __nv_bfloat16 *dst, bool ok)
+{
+    uint32_t rr[32];
+    tmem_ld32(taddr, rr);
+    tmem_wait_ld_r(rr);
+    if (!ok)
+        return;
+#pragma unroll
+    for (int e = 0; e < 32; e += 8) {
+        uint4 v;
+        v.x = pack_bf16x2(__uint_as_float(rr[e]) * f, __uint_as_float(rr[e + 1]) * f);
+        v.y = pack_bf16x2(__uint_as_float(rr[e + 2]) * f, __uint_as_float(rr[e + 3]) * f);
+        v.z = pack_bf16x2(__uint_as_float(rr[e + 4]) * f, __uint_as_float(rr[e + 5]) * f);
+        v.w = pack_bf16x2(__uint_as_float(rr[e + 6]) * f, __uint_as_float(rr[e + 7]) * f);
+        *reinterpret_cast<uint4 *>(dst + e) = v;
+    }
+}
+
+// ------------------------------------------------------------ dK, dV
+
+// Warp 0 loads (K, V once; Q, dO per step), warp 1 issues the MMAs, warps
+// 4-11 form P^T and dS^T: warp w owns TMEM lanes (key rows) 32 (w % 4) .. +31
+// and, of each step's 64 queries, the 32 at 32 g, g = (w - 4) / 4.
 //
-// Per step s (one query head, one q tile):
-//   issuer:  per query half h (64 columns): S^T_h, dP^T_h -> bar_s<h> (S^T_0
-//            right away, dP^T once step s-1's dQ, which it overwrites, has
-//            been read; that also frees step s-1's Q / dO buffer for step
-//            s+1's copies); [P^T_h in TMEM, dS^T_h in shared memory, bar_p<h>]
-//            dV += P^T_h dO_h (A from TMEM), dK += dS^T_h Q_h; after half 1,
-//            dQ = dS K -> bar_m2;
-//   compute: lse, Delta -> shared (bar_ld); for h = 0, 1 in turn, all eight
-//            warps: [bar_s<h>] P^T = exp(S^T scale - lse) into TMEM over the
-//            S^T columns it has read, dS^T = P^T (dP^T - Delta) into shared
-//            memory (bar_p<h>); the previous step's dQ rows
-//            into the fp32 sum with vector atomics while the tensor core runs
-//            this step's products; [bar_m2] this step's dQ rows out of TMEM
-//            into registers (bar_dq).
+// Per step s (query head hq, query block qb), buffer x = s % 2, ring stage
+// st = s % NSTAGE:
+//   TMA:  [q_empty(st)] Q, dO rows -> stage st (q_full)
+//   MMA:  [q_full(st)] S^T_x = K Q^T, dP^T_x = V dO^T -> s_full(x);
+//         [p_full(x') of step s - 1] dV += P^T dO, dK += dS^T Q of step s - 1
+//         -> q_empty(st'), the buffer then free for step s + 1
+//   math: [s_full(x)] P^T = 2^(s scale log2e - lse log2e) (masked: 0),
+//         dS^T = P^T (dP^T - Delta) -> bf16 over S^T_x / dP^T_x -> p_full(x)
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant__ BwdArgs a)
+__global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdArgs a)
 {
     using C = BwdCfg<D>;
-    constexpr int DB = C::DB;
-    constexpr int DH = D / 2;                     // columns of dQ, dK, dV per thread
+    constexpr int DB = C::DB, NSTAGE = C::NSTAGE, STEP = C::STEP, NC = C::NC;
+    constexpr int DH = C::DKV / 2;                // dK, dV columns per math thread
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
@@ -254,46 +441,41 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     if (*a.status != VFA_OK)
         return;
     const int B = a.batch, H = a.num_heads, Hkv = a.num_kv_heads;
-    const int gt = blockIdx.x, kh = blockIdx.y;
+    // the column halves of a key tile are neighbours in launch order (their
+    // Q / dO reads meet in L2)
+    const int gt = blockIdx.x / C::DSPLIT, dh = blockIdx.x % C::DSPLIT, kh = blockIdx.y;
     if (gt >= a.ktile_start[B])
         return;
-    int lo = 0, hi = B - 1;                       // largest b with ktile_start[b] <= gt
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.ktile_start[mid] <= gt)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    const int b = lo, kt = gt - a.ktile_start[b];
+    const int b = owner_of(a.ktile_start, B, gt), kt = gt - a.ktile_start[b];
     const int q0 = a.cu_q[b], lq = a.cu_q[b + 1] - q0;
     const int k0 = a.cu_k[b], lk = a.cu_k[b + 1] - k0;
     const long long off = a.causal == 2 ? lk - lq : 0;
     const int wl = a.window_left;
-    const int j_lo = kt * kT, j_hi = min(lk, j_lo + kT);
+    const int j_lo = kt * kOwn, j_hi = min(lk, j_lo + kOwn);
     // query rows that see a key of this tile: i >= j - off (causal) and
     // i <= j - off + window_left (window)
     long long i_min = a.causal ? max(0ll, j_lo - off) : 0;
     long long i_max = lq - 1;
     if (wl >= 0)
         i_max = min(i_max, static_cast<long long>(j_hi) - 1 - off + wl);
-    const int it0 = i_min <= i_max ? static_cast<int>(i_min / kT) : 0;
-    const int n_it = i_min <= i_max ? static_cast<int>(i_max / kT) + 1 - it0 : 0;
+    const int qb0 = i_min <= i_max ? static_cast<int>(i_min / STEP) : 0;
+    const int n_qb = i_min <= i_max ? static_cast<int>(i_max / STEP) + 1 - qb0 : 0;
     const int group = H / Hkv;
-    const int n_steps = n_it * group;
+    const int n_steps = n_qb * group;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = (warp & 3) * 32 + lane;         // tile row (TMEM lane) of compute threads
-    const int half = (warp >> 2) & 1;             // column half of compute threads
-    const int sub = half;                         // their 32-query slice within a query half
-    const int j = j_lo + r;                       // key (local position) of row r
+    const int quarter = warp & 3;
+    const int half = warp >= kFirstMathWarp ? (warp - kFirstMathWarp) >> 2 : 0;
+    const int r = quarter * 32 + lane;            // key row of math threads
+    const int j = j_lo + r;
     __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(a.dk);
     __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(a.dv);
 
     if (n_steps == 0) {
         // no query sees these keys: zero gradients
-        if (warp < kComputeWarps && j < lk) {
-            const size_t row = (static_cast<size_t>(k0 + j) * Hkv + kh) * D + half * DH;
+        if (warp >= kFirstMathWarp && j < lk) {
+            const size_t row =
+                (static_cast<size_t>(k0 + j) * Hkv + kh) * D + dh * C::DKV + half * DH;
 #pragma unroll
             for (int d = 0; d < DH; d += 8) {
                 *reinterpret_cast<uint4 *>(dk + row + d) = make_uint4(0, 0, 0, 0);
@@ -305,36 +487,37 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t sK = base, sV = sK + C::TILE_BYTES;
-    const uint32_t sQ = sV + C::TILE_BYTES;           // two buffers
-    const uint32_t sDO = sQ + 2 * C::TILE_BYTES;      // two buffers
-    const uint32_t sDS = sDO + 2 * C::TILE_BYTES;
-    const uint32_t sLse = sDS + C::PS_BYTES, sDelta = sLse + kT * 4;
-    const uint32_t bars = sDelta + kT * 4;
-    const uint32_t bar_kv = bars, bar_s0 = bars + 8, bar_s1 = bars + 16, bar_m2 = bars + 24;
-    const uint32_t bar_ld = bars + 32, bar_p0 = bars + 40, bar_p1 = bars + 48;
-    const uint32_t bar_dq = bars + 56, bar_drain = bars + 64;
-    auto bar_q = [&](int x) { return bars + 72 + 8u * x; };
-    float *nl_s = reinterpret_cast<float *>(smem_raw + (sLse - raw));     // -lse * log2(e)
-    float *delta_s = reinterpret_cast<float *>(smem_raw + (sDelta - raw));
+    const uint32_t sK = base, sV = sK + C::OWN_BYTES;
+    const uint32_t sRing = sV + C::OWN_BYTES;                 // stage st: Q, then dO
+    const uint32_t sStat = sRing + NSTAGE * C::STAGE_BYTES;  // per math warp: -lse2, Delta
+    const uint32_t bars = sStat + kMathWarps * 256;
+    auto q_full = [&](int st) { return bars + 8u * st; };
+    auto q_empty = [&](int st) { return bars + 8u * (NSTAGE + st); };
+    auto s_full = [&](int x) { return bars + 8u * (2 * NSTAGE + x); };
+    auto p_full = [&](int x) { return bars + 8u * (2 * NSTAGE + 2 + x); };
+    const uint32_t bar_kv = bars + 8u * (2 * NSTAGE + 4);
+    const uint32_t bar_done = bars + 8u * (2 * NSTAGE + 5);
+    const uint32_t bar_drain = bars + 8u * (2 * NSTAGE + 6);
+    auto stage_q = [&](int st) { return sRing + st * C::STAGE_BYTES; };
+    auto stage_do = [&](int st) { return sRing + st * C::STAGE_BYTES + C::STEP_BYTES; };
     volatile int *abort = &s_abort;
 
     if (tid == 0) {
         s_abort = 0;
+        for (int st = 0; st < NSTAGE; ++st) {
+            mbar_init(q_full(st), 1);
+            mbar_init(q_empty(st), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(s_full(x), 1);
+            mbar_init(p_full(x), kMathThreads);
+        }
         mbar_init(bar_kv, 1);
-        mbar_init(bar_q(0), 1);
-        mbar_init(bar_q(1), 1);
-        mbar_init(bar_s0, 1);
-        mbar_init(bar_s1, 1);
-        mbar_init(bar_m2, 1);
-        mbar_init(bar_ld, kComputeThreads);
-        mbar_init(bar_p0, kComputeThreads);
-        mbar_init(bar_p1, kComputeThreads);
-        mbar_init(bar_dq, kComputeThreads);
+        mbar_init(bar_done, 1);
         mbar_init(bar_drain, 1);
         fence_barrier_init();
     }
-    if (warp == 0) {
+    if (warp == 1) {
         tmem_alloc(smem_u32(&s_tmem_base), C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -343,296 +526,156 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = s_tmem_base;
 
-    // step s -> (query head, q tile)
-    auto step_hq = [&](int s) { return kh * group + s / n_it; };
-    auto step_it = [&](int s) { return it0 + s % n_it; };
+    // step s -> (query head, query block)
+    auto step_hq = [&](int s) { return kh * group + s / n_qb; };
+    auto step_qb = [&](int s) { return qb0 + s % n_qb; };
 
-    if (warp == kComputeWarps) {
-        // ------------------------------------------------------------ issuer
-        // All 32 lanes run this loop on warp-uniform values; one elected lane
-        // issues each MMA and commit, lane 0 the copies.
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
         if (lane == 0) {
             tma_prefetch_map(&a.tm_q);
             tma_prefetch_map(&a.tm_k);
             tma_prefetch_map(&a.tm_v);
             tma_prefetch_map(&a.tm_do);
-        }
-        auto load_q = [&](int s) {
-            if (lane == 0) {
-                const int x = s & 1;
-                mbar_arrive_expect_tx(bar_q(x), 2 * C::TILE_BYTES);
-                const int row = q0 + step_it(s) * kT, hq = step_hq(s);
-                for (int db = 0; db < DB; ++db) {
-                    tma_load_3d(sQ + x * C::TILE_BYTES + db * (kT * 128), &a.tm_q, bar_q(x),
-                                db * 64, hq, row);
-                    tma_load_3d(sDO + x * C::TILE_BYTES + db * (kT * 128), &a.tm_do, bar_q(x),
-                                db * 64, hq, row);
+            mbar_arrive_expect_tx(bar_kv, 2 * C::OWN_BYTES);
+            load_rows<DB, STEP>(sK, &a.tm_k, bar_kv, kh, k0 + j_lo, kOwn);
+            load_rows<DB, STEP>(sV, &a.tm_v, bar_kv, kh, k0 + j_lo, kOwn);
+            int s = 0;
+            for (; s < n_steps; ++s) {
+                const int st = s % NSTAGE;
+                if (!mbar_wait(q_empty(st), ((s / NSTAGE) & 1u) ^ 1u, abort))
+                    break;
+                mbar_arrive_expect_tx(q_full(st), C::STAGE_BYTES);
+                const int row = q0 + step_qb(s) * STEP, hq = step_hq(s);
+                load_rows<DB, STEP>(stage_q(st), &a.tm_q, q_full(st), hq, row, STEP);
+                load_rows<DB, STEP>(stage_do(st), &a.tm_do, q_full(st), hq, row, STEP);
+            }
+            if (*abort) {
+                // the last fill of each stage may still be in flight
+                mbar_wait_drain(bar_kv, 0);
+                for (int st = 0; st < NSTAGE; ++st) {
+                    const int fills = s / NSTAGE + (st < s % NSTAGE ? 1 : 0);
+                    if (fills > 0)
+                        mbar_wait_drain(q_full(st), (fills - 1) & 1u);
                 }
             }
-            __syncwarp();
-        };
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar_kv, 2 * C::TILE_BYTES);
-            for (int db = 0; db < DB; ++db) {
-                tma_load_3d(sK + db * (kT * 128), &a.tm_k, bar_kv, db * 64, kh, k0 + j_lo);
-                tma_load_3d(sV + db * (kT * 128), &a.tm_v, bar_kv, db * 64, kh, k0 + j_lo);
-            }
         }
-        load_q(0);
-        int q_loads = 1;
-        if (n_steps > 1) {
-            load_q(1);
-            q_loads = 2;
-        }
-        const uint64_t k_d = sdesc_sw128(sK, 16, 1024), v_d = sdesc_sw128(sV, 16, 1024);
-        const uint64_t k_mn = sdesc_sw128(sK, kT * 128, 1024);
-        const uint64_t ds_d = sdesc_sw128(sDS, 16, 1024);
-        const uint64_t ds_mn = sdesc_sw128(sDS, kT * 128, 1024);
-        // S^T_h or dP^T_h = (K or V) (Q or dO)^T for query half h (N = 64):
-        // queries 64 h .. 64 h + 63 start 64 h rows into each 64-column block
-        auto issue_t = [&](uint32_t d_col, uint64_t a_d, uint32_t b_buf, int h) {
-            const uint64_t b_d = sdesc_sw128(b_buf + h * 64 * 128, 16, 1024);
-            mma_ss_w<0>(tmem + d_col + h * 64, a_d, b_d, C::IDESC_T);
-#pragma unroll
-            for (int kk = 1; kk < D / 16; ++kk) {
-                const uint32_t o16 = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
-                mma_ss_w<1>(tmem + d_col + h * 64, a_d + o16, b_d + o16, C::IDESC_T);
-            }
-        };
-        // dV += P^T dO and dK += dS^T Q over the queries of half h (K = 64)
-        auto issue_kv = [&](int h, uint32_t x, bool first) {
-            const uint64_t do_mn = sdesc_sw128(sDO + x * C::TILE_BYTES, kT * 128, 1024);
-            const uint64_t q_mn = sdesc_sw128(sQ + x * C::TILE_BYTES, kT * 128, 1024);
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const int kk = h * 4 + k4;
-                // P^T of queries 16 kk .. +15: bf16 pairs at columns 64 h +
-                // 32 (k4 / 2) + 8 (k4 % 2), where the warps holding those queries put them
-                const uint32_t p_col = h * 64 + (k4 >> 1) * 32 + (k4 & 1) * 8;
-                const uint32_t ko = ((kk >> 2) * (kT * 128) + (kk & 3) * 32) >> 4;
-                const uint32_t mo = (kk * 16 * 128) >> 4;
-                if (k4 == 0 && first) {
-                    mma_ts_w<0>(tmem + C::COL_DV, tmem + C::COL_ST + p_col, do_mn + mo,
-                                C::IDESC_KV);
-                    mma_ss_w<0>(tmem + C::COL_DK, ds_d + ko, q_mn + mo, C::IDESC_KV);
-                } else {
-                    mma_ts_w<1>(tmem + C::COL_DV, tmem + C::COL_ST + p_col, do_mn + mo,
-                                C::IDESC_KV);
-                    mma_ss_w<1>(tmem + C::COL_DK, ds_d + ko, q_mn + mo, C::IDESC_KV);
-                }
-            }
-        };
-        // a wait the whole warp agrees on (the elected issue needs all lanes)
-        auto wait_all = [&](uint32_t bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
-        };
-        bool ok = wait_all(bar_kv, 0);
-        for (int s = 0; s < n_steps && ok; ++s) {
-            const uint32_t x = static_cast<uint32_t>(s) & 1u;
-            const uint32_t ph = x;
-            if (!wait_all(bar_q(x), static_cast<uint32_t>(s >> 1) & 1u)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t q_buf = sQ + x * C::TILE_BYTES, o_buf = sDO + x * C::TILE_BYTES;
-            // S^T_0 needs no wait: it overwrites only P^T of the previous step,
-            // which that step's dV product (issued earlier) has read
-            issue_t(C::COL_ST, k_d, q_buf, 0);
-            if (s > 0) {
-                // dP^T goes over the previous step's dQ: wait until it is read;
-                // that step's products are then done, so its buffer takes the
-                // next step's Q and dO
-                if (!wait_all(bar_dq, ph ^ 1u)) {
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        // All 32 lanes run this loop on warp-uniform values; one elected lane
+        // issues each MMA and commit.
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar_kv, 0, abort));
+        for (int s = 0; s <= n_steps && ok; ++s) {
+            if (s < n_steps) {
+                const int st = s % NSTAGE, x = s & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(q_full(st), (s / NSTAGE) & 1u, abort))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (s + 1 < n_steps) {
-                    load_q(s + 1);
-                    ++q_loads;
+                // buffer x was last read by step s - 2's products, issued earlier
+                const uint32_t buf = tmem + C::KV_BUF + C::BUF_STRIDE * x;
+                issue_scores<D, STEP>(buf, sK, stage_q(st), C::IDESC_T);
+                issue_scores<D, STEP>(buf + STEP, sV, stage_do(st), C::IDESC_T);
+                mma_commit_w(s_full(x));
+            }
+            if (s >= 1) {
+                const int sp = s - 1, stp = sp % NSTAGE, xp = sp & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(p_full(xp), (sp >> 1) & 1u, abort))) {
+                    ok = false;
+                    break;
                 }
+                tc_fence_after();
+                const uint32_t buf = tmem + C::KV_BUF + C::BUF_STRIDE * xp;
+                // this CTA's column half of dO and Q: DKV / 64 column blocks on
+                const uint32_t col0 = dh * (C::DKV / 64) * (STEP * 128);
+                issue_accumulate<STEP>(tmem + C::COL_DV, buf, stage_do(stp) + col0, C::IDESC_KV,
+                                       sp == 0);
+                issue_accumulate<STEP>(tmem + C::COL_DK, buf + STEP, stage_q(stp) + col0,
+                                       C::IDESC_KV, sp == 0);
+                mma_commit_w(q_empty(stp));
             }
-            issue_t(C::COL_DPT, v_d, o_buf, 0);
-            mma_commit_w(bar_s0);
-            issue_t(C::COL_ST, k_d, q_buf, 1);
-            issue_t(C::COL_DPT, v_d, o_buf, 1);
-            mma_commit_w(bar_s1);
-            if (!wait_all(bar_p0, ph)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            issue_kv(0, x, s == 0);
-            if (!wait_all(bar_p1, ph)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            issue_kv(1, x, false);
-            // dQ = dS K over all 128 keys
-            mma_ss_w<0>(tmem + C::COL_DQ, ds_mn, k_mn, C::IDESC_Q);
-#pragma unroll
-            for (int kk = 1; kk < kT / 16; ++kk) {
-                const uint32_t mo = (kk * 16 * 128) >> 4;
-                mma_ss_w<1>(tmem + C::COL_DQ, ds_mn + mo, k_mn + mo, C::IDESC_Q);
-            }
-            mma_commit_w(bar_m2);
         }
-        if (!ok || *abort) {
+        if (ok)
+            mma_commit_w(bar_done);
+        else {
             mma_commit_w(bar_drain);
             mbar_wait_drain(bar_drain, 0);
-            mbar_wait_drain(bar_kv, 0);
-            for (int xb = 0; xb < 2; ++xb) {
-                const int n = q_loads / 2 + (xb < q_loads % 2 ? 1 : 0);   // copies into buffer xb
-                if (n > 0)
-                    mbar_wait_drain(bar_q(xb), static_cast<uint32_t>(n - 1) & 1u);
-            }
         }
-    } else {
-        // ------------------------------------------------------------ compute
-        const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    } else if (warp >= kFirstMathWarp) {
+        // ------------------------------------------------------------ P^T, dS^T
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t wstat = sStat + (warp - kFirstMathWarp) * 256;   // 32 nl, 32 -Delta
+        float *stat = reinterpret_cast<float *>(smem_raw + (wstat - raw));
         const float scale_log2 = a.scale_log2;
-        float4 acc[DH / 4];                       // dQ row segment of the previous step
-        float4 *acc_dst = nullptr;                // where it goes (null: nothing pending)
         bool ok = true;
         for (int s = 0; s < n_steps && ok; ++s) {
-            const uint32_t ph = static_cast<uint32_t>(s) & 1u;
-            const int hq = step_hq(s), it = step_it(s);
+            const int x = s & 1, hq = step_hq(s), qb = step_qb(s);
+            const int i_base = qb * STEP + half * NC;   // this thread's first query column
             {
-                // -lse (log2 units) and Delta of the tile's query rows; the
-                // previous step's readers are past bar_m2, which needed them all
-                const int c = tid & (kT - 1);
-                const int i = it * kT + c;
+                const int i = i_base + lane;
+                const bool in = lane < NC && i < lq;
                 const size_t row = static_cast<size_t>(q0 + i) * H + hq;
-                if (tid < kT)
-                    nl_s[c] = i < lq ? -a.lse[row] * kLog2e : 0.f;
-                else
-                    delta_s[c] = i < lq ? a.delta[row] : 0.f;
+                const float nl = in ? -a.lse[row] * kLog2e : 0.f;
+                const float nd = in ? -a.delta[row] : 0.f;
+                __syncwarp();
+                stat[lane] = nl;
+                stat[32 + lane] = nd;
+                __syncwarp();
             }
-            mbar_arrive(bar_ld);
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_ld, ph, abort));
-            if (!ok)
-                break;
-            // a tile every (key, query) pair of which is visible needs no mask
-            BwdMask m;
-            m.j = j;
-            m.lk = lk;
-            m.lq = lq;
-            m.causal = a.causal;
-            m.wl = wl;
-            m.i_lo = static_cast<long long>(it) * kT;
-            m.off = off;
-            const bool full = j_lo + kT <= lk && m.i_lo + kT <= lq &&
-                              (!a.causal || j_lo + kT - 1 <= m.i_lo + off) &&
-                              (wl < 0 || j_lo >= m.i_lo + kT - 1 + off - wl);
-            // the query halves in turn, all eight warps on each: this warp takes
-            // queries 64 h + 32 g .. +31 of its 32 rows, so the tensor core runs
-            // half 1's S^T / dP^T and half 0's dV / dK while it works
-#pragma unroll 1
-            for (int h = 0; h < 2 && ok; ++h) {
-                ok = __all_sync(0xffffffffu, mbar_wait(h ? bar_s1 : bar_s0, ph, abort));
-                if (!ok)
-                    break;
-                tc_fence_after();
-                uint32_t pk[16];
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    const int cb = h * 64 + sub * 32 + c2 * 16;   // first query column of the chunk
-                    uint32_t sr[16], dr[16];
-                    tmem_ld16(tmem + lane_addr + C::COL_ST + cb, sr);
-                    tmem_ld16(tmem + lane_addr + C::COL_DPT + cb, dr);
-                    tmem_wait_ld();
-                    uint32_t dk2[8];
-                    if (full)
-                        bwd_chunk<true>(sr, dr, scale_log2, sLse, sDelta, cb, m, pk + c2 * 8, dk2);
-                    else
-                        bwd_chunk<false>(sr, dr, scale_log2, sLse, sDelta, cb, m, pk + c2 * 8, dk2);
-#pragma unroll
-                    for (int q8 = 0; q8 < 2; ++q8)
-                        st_shared_v4(sDS + sw_chunk(r, (cb >> 3) + q8), dk2[4 * q8],
-                                     dk2[4 * q8 + 1], dk2[4 * q8 + 2], dk2[4 * q8 + 3]);
-                }
-                // P^T (bf16 pairs) of these 32 queries over their own S^T columns,
-                // which only this warp reads
-                tmem_st16(tmem + lane_addr + C::COL_ST + h * 64 + sub * 32, pk);
-                tmem_wait_st();
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(h ? bar_p1 : bar_p0);
-            }
-            if (!ok)
-                break;
-            if (acc_dst != nullptr)
-                flush_dq<DH>(acc_dst, acc);
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_m2, ph, abort));
+            // a step every (key, query) pair of which is visible needs no mask
+            const long long qlo = static_cast<long long>(qb) * STEP;
+            const bool full = j_lo + kOwn <= lk && qlo + STEP <= lq &&
+                              (!a.causal || j_lo + kOwn - 1 <= qlo + off) &&
+                              (wl < 0 || j_lo >= qlo + STEP - 1 + off - wl);
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full(x), (s >> 1) & 1u, abort));
             if (!ok)
                 break;
             tc_fence_after();
-            // this half of the q tile's dQ rows (TMEM lane = query row)
-#pragma unroll
-            for (int cb = 0; cb < DH; cb += 32) {
-                uint32_t qr[32];
-                tmem_ld32(tmem + lane_addr + C::COL_DQ + half * DH + cb, qr);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    acc[(cb + e) >> 2] =
-                        make_float4(__uint_as_float(qr[e]), __uint_as_float(qr[e + 1]),
-                                    __uint_as_float(qr[e + 2]), __uint_as_float(qr[e + 3]));
+            const uint32_t st_addr =
+                tmem + lane_addr + C::KV_BUF + C::BUF_STRIDE * x + half * NC;
+            uint32_t sr[NC], dr[NC];
+            ld_cols<NC>(st_addr, sr);
+            ld_cols<NC>(st_addr + STEP, dr);
+            wait_cols<NC>(sr, dr);
+            uint32_t pk[NC / 2], dk2[NC / 2];
+            if (full) {
+                key_row_grads<false, NC>(sr, dr, scale_log2, wstat, 0, NC, pk, dk2);
+            } else {
+                int lo, hi;
+                key_row_span(j, i_base, lk, lq, a.causal, wl, off, &lo, &hi);
+                key_row_grads<true, NC>(sr, dr, scale_log2, wstat, lo, hi, pk, dk2);
             }
+            // P^T, dS^T (bf16 pairs) over the first half of this thread's own
+            // S^T / dP^T columns, which only this warp reads
+            st_cols<NC / 2>(st_addr, pk);
+            st_cols<NC / 2>(st_addr + STEP, dk2);
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar_dq);
-            const int i = it * kT + r;
-            acc_dst = i < lq ? reinterpret_cast<float4 *>(
-                                   a.dq_acc + (static_cast<size_t>(q0 + i) * H + hq) * D +
-                                   half * DH)
-                             : nullptr;
+            mbar_arrive(p_full(x));
         }
-        if (ok && acc_dst != nullptr)
-            flush_dq<DH>(acc_dst, acc);
+        if (ok)
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, abort));
+        if (ok) {
+            // dV and dK (scaled) rows of this key tile, this thread's column half
+            tc_fence_after();
+            const size_t row =
+                (static_cast<size_t>(k0 + j) * Hkv + kh) * D + dh * C::DKV + half * DH;
+#pragma unroll 1
+            for (int cb = 0; cb < DH; cb += 32) {
+                store_row32(tmem + lane_addr + C::COL_DV + half * DH + cb, 1.f, dv + row + cb,
+                            j < lk);
+                store_row32(tmem + lane_addr + C::COL_DK + half * DH + cb, a.scale,
+                            dk + row + cb, j < lk);
+            }
+        }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (*abort == 0 && warp < kComputeWarps) {
-        // dK (scaled) and dV rows of this key tile, this thread's column half
-        tc_fence_after();
-        const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const float sc = a.scale;
-        const size_t row = (static_cast<size_t>(k0 + j) * Hkv + kh) * D + half * DH;
-#pragma unroll 1
-        for (int which = 0; which < 2; ++which) {
-            const uint32_t col = (which == 0 ? C::COL_DV : C::COL_DK) + half * DH;
-            const float f = which == 0 ? 1.f : sc;
-            __nv_bfloat16 *dst = which == 0 ? dv : dk;
-#pragma unroll
-            for (int cb = 0; cb < DH; cb += 32) {
-                uint32_t rr[32];
-                tmem_ld32(tmem + lane_addr + col + cb, rr);
-                tmem_wait_ld();
-                if (j < lk) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(rr[e]) * f, __uint_as_float(rr[e + 1]) * f);
-                        v.y = pack_bf16x2(__uint_as_float(rr[e + 2]) * f,
-                                          __uint_as_float(rr[e + 3]) * f);
-                        v.z = pack_bf16x2(__uint_as_float(rr[e + 4]) * f,
-                                          __uint_as_float(rr[e + 5]) * f);
-                        v.w = pack_bf16x2(__uint_as_float(rr[e + 6]) * f,
-                                          __uint_as_float(rr[e + 7]) * f);
-                        *reinterpret_cast<uint4 *>(dst + row + cb + e) = v;
-                    }
-                }
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
     if (*abort && tid == 0)
         atomicCAS(a.status, VFA_OK, VFA_ERR_TIMEOUT);
-    if (warp == 0) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
@@ -640,24 +683,236 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_kernel(const __grid_constant_
 
 // ------------------------------------------------------------ dQ
 
+// Warp 0 loads (Q, dO once; K, V per step), warp 1 issues the MMAs, warps
+// 4-11 form dS: warp w owns TMEM lanes (query rows) 32 (w % 4) .. +31 and, of
+// each step's 64 keys, the 32 at 32 g, g = (w - 4) / 4.
+//
+// Per step s (key block kb), buffer x = s % 2, ring stage st = s % NSTAGE:
+//   TMA:  [kv_empty(st)] K, V rows -> stage st (kv_full)
+//   MMA:  [kv_full(st)] S_x = Q K^T, dP_x = dO V^T -> s_full(x);
+//         [p_full(x') of step s - 1] dQ += dS K of step s - 1 -> kv_empty(st')
+//   math: [s_full(x)] dS = 2^(s scale log2e - lse log2e) (dP - Delta)
+//         (masked: 0) -> bf16 over dP_x -> p_full(x)
 template <int D>
-__global__ void bwd_dq_kernel(const BwdArgs a)
+__global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdArgs a)
 {
+    using C = BwdCfg<D>;
+    constexpr int DB = C::DB, NSTAGE = C::NSTAGE, STEP = C::STEP, NC = C::NC;
+    constexpr int DH = D / 2;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem_base;
+    __shared__ int s_abort;
+
     if (*a.status != VFA_OK)
         return;
-    const long long n4 = static_cast<long long>(a.total_q) * a.num_heads * D / 4;
-    const float sc = a.scale;
-    const float4 *src = reinterpret_cast<const float4 *>(a.dq_acc);
-    uint2 *dst = reinterpret_cast<uint2 *>(a.dq);
-    for (long long x = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; x < n4;
-         x += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const float4 v = src[x];
-        dst[x] = make_uint2(pack_bf16x2(v.x * sc, v.y * sc), pack_bf16x2(v.z * sc, v.w * sc));
+    const int B = a.batch, H = a.num_heads, Hkv = a.num_kv_heads;
+    const int n_tiles = a.qtile_start[B];
+    // the grid runs the tiles of each sequence last-first (the longest key
+    // ranges of a causal sequence first)
+    const int gt = n_tiles - 1 - static_cast<int>(blockIdx.x);
+    if (gt < 0)
+        return;
+    const int h = blockIdx.y, kh = h / (H / Hkv);
+    const int b = owner_of(a.qtile_start, B, gt), qt = gt - a.qtile_start[b];
+    const int q0 = a.cu_q[b], lq = a.cu_q[b + 1] - q0;
+    const int k0 = a.cu_k[b], lk = a.cu_k[b + 1] - k0;
+    const long long off = a.causal == 2 ? lk - lq : 0;
+    const int wl = a.window_left;
+    const int i_lo = qt * kOwn, i_hi = min(lq, i_lo + kOwn);
+    // keys some row of this tile sees: j <= i + off (causal), j >= i + off -
+    // window_left (window)
+    long long j_min = (a.causal && wl >= 0) ? max(0ll, i_lo + off - wl) : 0;
+    long long j_max = lk - 1;
+    if (a.causal)
+        j_max = min(j_max, static_cast<long long>(i_hi) - 1 + off);
+    const int kb0 = j_min <= j_max ? static_cast<int>(j_min / STEP) : 0;
+    const int n_steps = j_min <= j_max ? static_cast<int>(j_max / STEP) + 1 - kb0 : 0;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3;
+    const int half = warp >= kFirstMathWarp ? (warp - kFirstMathWarp) >> 2 : 0;
+    const int r = quarter * 32 + lane;            // query row of math threads
+    const int i = i_lo + r;
+    __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(a.dq);
+    const size_t out_row = (static_cast<size_t>(q0 + i) * H + h) * D + half * DH;
+
+    if (n_steps == 0) {
+        // these rows see no key: zero gradient
+        if (warp >= kFirstMathWarp && i < lq) {
+#pragma unroll
+            for (int d = 0; d < DH; d += 8)
+                *reinterpret_cast<uint4 *>(dq + out_row + d) = make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t sQ = base, sDO = sQ + C::OWN_BYTES;
+    const uint32_t sRing = sDO + C::OWN_BYTES;                 // stage st: K, then V
+    const uint32_t bars = sRing + NSTAGE * C::STAGE_BYTES + kMathWarps * 256;
+    auto kv_full = [&](int st) { return bars + 8u * st; };
+    auto kv_empty = [&](int st) { return bars + 8u * (NSTAGE + st); };
+    auto s_full = [&](int x) { return bars + 8u * (2 * NSTAGE + x); };
+    auto p_full = [&](int x) { return bars + 8u * (2 * NSTAGE + 2 + x); };
+    const uint32_t bar_q = bars + 8u * (2 * NSTAGE + 4);
+    const uint32_t bar_done = bars + 8u * (2 * NSTAGE + 5);
+    const uint32_t bar_drain = bars + 8u * (2 * NSTAGE + 6);
+    auto stage_k = [&](int st) { return sRing + st * C::STAGE_BYTES; };
+    auto stage_v = [&](int st) { return sRing + st * C::STAGE_BYTES + C::STEP_BYTES; };
+    volatile int *abort = &s_abort;
+
+    if (tid == 0) {
+        s_abort = 0;
+        for (int st = 0; st < NSTAGE; ++st) {
+            mbar_init(kv_full(st), 1);
+            mbar_init(kv_empty(st), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(s_full(x), 1);
+            mbar_init(p_full(x), kMathThreads);
+        }
+        mbar_init(bar_q, 1);
+        mbar_init(bar_done, 1);
+        mbar_init(bar_drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&s_tmem_base), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            tma_prefetch_map(&a.tm_q);
+            tma_prefetch_map(&a.tm_k);
+            tma_prefetch_map(&a.tm_v);
+            tma_prefetch_map(&a.tm_do);
+            mbar_arrive_expect_tx(bar_q, 2 * C::OWN_BYTES);
+            load_rows<DB, STEP>(sQ, &a.tm_q, bar_q, h, q0 + i_lo, kOwn);
+            load_rows<DB, STEP>(sDO, &a.tm_do, bar_q, h, q0 + i_lo, kOwn);
+            int s = 0;
+            for (; s < n_steps; ++s) {
+                const int st = s % NSTAGE;
+                if (!mbar_wait(kv_empty(st), ((s / NSTAGE) & 1u) ^ 1u, abort))
+                    break;
+                mbar_arrive_expect_tx(kv_full(st), C::STAGE_BYTES);
+                const int row = k0 + (kb0 + s) * STEP;
+                load_rows<DB, STEP>(stage_k(st), &a.tm_k, kv_full(st), kh, row, STEP);
+                load_rows<DB, STEP>(stage_v(st), &a.tm_v, kv_full(st), kh, row, STEP);
+            }
+            if (*abort) {
+                mbar_wait_drain(bar_q, 0);
+                for (int st = 0; st < NSTAGE; ++st) {
+                    const int fills = s / NSTAGE + (st < s % NSTAGE ? 1 : 0);
+                    if (fills > 0)
+                        mbar_wait_drain(kv_full(st), (fills - 1) & 1u);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort));
+        for (int s = 0; s <= n_steps && ok; ++s) {
+            if (s < n_steps) {
+                const int st = s % NSTAGE, x = s & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(kv_full(st), (s / NSTAGE) & 1u, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t buf = tmem + C::Q_BUF + C::BUF_STRIDE * x;
+                issue_scores<D, STEP>(buf, sQ, stage_k(st), C::IDESC_T);
+                issue_scores<D, STEP>(buf + STEP, sDO, stage_v(st), C::IDESC_T);
+                mma_commit_w(s_full(x));
+            }
+            if (s >= 1) {
+                const int sp = s - 1, stp = sp % NSTAGE, xp = sp & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(p_full(xp), (sp >> 1) & 1u, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issue_accumulate<STEP>(tmem + C::COL_DQ,
+                                       tmem + C::Q_BUF + C::BUF_STRIDE * xp + STEP, stage_k(stp),
+                                       C::IDESC_DQ, sp == 0);
+                mma_commit_w(kv_empty(stp));
+            }
+        }
+        if (ok)
+            mma_commit_w(bar_done);
+        else {
+            mma_commit_w(bar_drain);
+            mbar_wait_drain(bar_drain, 0);
+        }
+    } else if (warp >= kFirstMathWarp) {
+        // ------------------------------------------------------------ dS
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const float scale_log2 = a.scale_log2;
+        const size_t srow = static_cast<size_t>(q0 + i) * H + h;
+        const float nl = i < lq ? -a.lse[srow] * kLog2e : 0.f;
+        const float nd = i < lq ? -a.delta[srow] : 0.f;
+        bool ok = true;
+        for (int s = 0; s < n_steps && ok; ++s) {
+            const int x = s & 1;
+            const int j_base = (kb0 + s) * STEP + half * NC;   // this thread's first key column
+            const long long klo = static_cast<long long>(kb0 + s) * STEP;
+            const bool full = klo + STEP <= lk && i_lo + kOwn <= lq &&
+                              (!a.causal || klo + STEP - 1 <= i_lo + off) &&
+                              (wl < 0 || klo >= i_lo + kOwn - 1 + off - wl);
+            ok = __all_sync(0xffffffffu, mbar_wait(s_full(x), (s >> 1) & 1u, abort));
+            if (!ok)
+                break;
+            tc_fence_after();
+            const uint32_t st_addr =
+                tmem + lane_addr + C::Q_BUF + C::BUF_STRIDE * x + half * NC;
+            uint32_t sr[NC], dr[NC];
+            ld_cols<NC>(st_addr, sr);
+            ld_cols<NC>(st_addr + STEP, dr);
+            wait_cols<NC>(sr, dr);
+            uint32_t dk2[NC / 2];
+            if (full) {
+                query_row_grads<false, NC>(sr, dr, scale_log2, nl, nd, 0, NC, dk2);
+            } else {
+                int lo, hi;
+                query_row_span(i, j_base, lk, lq, a.causal, wl, off, &lo, &hi);
+                query_row_grads<true, NC>(sr, dr, scale_log2, nl, nd, lo, hi, dk2);
+            }
+            // dS (bf16 pairs) over the first half of this thread's own dP columns
+            st_cols<NC / 2>(st_addr + STEP, dk2);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(p_full(x));
+        }
+        if (ok)
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, abort));
+        if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int cb = 0; cb < DH; cb += 32)
+                store_row32(tmem + lane_addr + C::COL_DQ + half * DH + cb, a.scale,
+                            dq + out_row + cb, i < lq);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort && tid == 0)
+        atomicCAS(a.status, VFA_OK, VFA_ERR_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 
 template <int D>
-cudaError_t launch_bwd_d(const BwdArgs &a, int key_tile_bound, int sm_count, cudaStream_t s)
+cudaError_t launch_bwd_d(const BwdArgs &a, int key_tile_bound, int q_tile_bound, int sm_count,
+                         cudaStream_t s)
 {
     static int attr_done[64] = {0};
     int dev = 0;
@@ -665,61 +920,72 @@ cudaError_t launch_bwd_d(const BwdArgs &a, int key_tile_bound, int sm_count, cud
     if (e != cudaSuccess)
         return e;
     if (dev < 64 && !attr_done[dev]) {
-        e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(BwdCfg<D>::SMEM));
-        if (e != cudaSuccess)
+        if ((e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(BwdCfg<D>::SMEM))) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(bwd_dq_kernel<D>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(BwdCfg<D>::SMEM))) != cudaSuccess)
             return e;
         attr_done[dev] = 1;
     }
     bwd_prep_kernel<<<1, kPrepThreads, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
-    const int grid_rows = sm_count * 8;
-    bwd_delta_kernel<D><<<grid_rows, 256, 0, s>>>(a);
+    bwd_delta_kernel<D><<<sm_count * 8, 256, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
     if (key_tile_bound > 0) {
-        bwd_kernel<D><<<dim3(key_tile_bound, a.num_kv_heads), kThreads, BwdCfg<D>::SMEM, s>>>(a);
+        bwd_dkdv_kernel<D><<<dim3(key_tile_bound * BwdCfg<D>::DSPLIT, a.num_kv_heads), kThreads,
+                             BwdCfg<D>::SMEM, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
-    bwd_dq_kernel<D><<<grid_rows, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    if (q_tile_bound > 0) {
+        bwd_dq_kernel<D><<<dim3(q_tile_bound, a.num_heads), kThreads, BwdCfg<D>::SMEM, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace
 
 size_t bwd_workspace_bytes(int batch, int total_q, int num_heads, int head_dim)
 {
+    (void)head_dim;
     size_t n = 256;                                                   // status word
     n += (static_cast<size_t>(batch) + 1) * sizeof(int32_t);          // key tile starts
     n = (n + 255) & ~static_cast<size_t>(255);
-    n += static_cast<size_t>(total_q) * num_heads * sizeof(float);    // Delta
+    n += (static_cast<size_t>(batch) + 1) * sizeof(int32_t);          // q tile starts
     n = (n + 255) & ~static_cast<size_t>(255);
-    n += static_cast<size_t>(total_q) * num_heads * head_dim * sizeof(float);   // dQ sum
+    n += static_cast<size_t>(total_q) * num_heads * sizeof(float);    // Delta
     return (n + 255) & ~static_cast<size_t>(255);
 }
 
 void bwd_workspace_split(void *ws, int batch, int total_q, int num_heads, BwdArgs *a)
 {
+    (void)total_q;
+    (void)num_heads;
     uint8_t *p = static_cast<uint8_t *>(ws);
     a->status = reinterpret_cast<int32_t *>(p);
     size_t n = 256;
     a->ktile_start = reinterpret_cast<int32_t *>(p + n);
     n += (static_cast<size_t>(batch) + 1) * sizeof(int32_t);
     n = (n + 255) & ~static_cast<size_t>(255);
-    a->delta = reinterpret_cast<float *>(p + n);
-    n += static_cast<size_t>(total_q) * num_heads * sizeof(float);
+    a->qtile_start = reinterpret_cast<int32_t *>(p + n);
+    n += (static_cast<size_t>(batch) + 1) * sizeof(int32_t);
     n = (n + 255) & ~static_cast<size_t>(255);
-    a->dq_acc = reinterpret_cast<float *>(p + n);
+    a->delta = reinterpret_cast<float *>(p + n);
 }
 
-cudaError_t launch_bwd(int head_dim, const BwdArgs &a, int key_tile_bound, int sm_count,
-                       cudaStream_t stream)
+cudaError_t launch_bwd(int head_dim, const BwdArgs &a, int key_tile_bound, int q_tile_bound,
+                       int sm_count, cudaStream_t stream)
 {
     switch (head_dim) {
-    case 64: return launch_bwd_d<64>(a, key_tile_bound, sm_count, stream);
-    case 128: return launch_bwd_d<128>(a, key_tile_bound, sm_count, stream);
+    case 64: return launch_bwd_d<64>(a, key_tile_bound, q_tile_bound, sm_count, stream);
+    case 128: return launch_bwd_d<128>(a, key_tile_bound, q_tile_bound, sm_count, stream);
+    case 256: return launch_bwd_d<256>(a, key_tile_bound, q_tile_bound, sm_count, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -109,7 +109,19 @@ struct DecodeStepArgs {
     int num_blocks, tile_capacity, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
     float *m, *l, *o;
     int32_t *status;      // nullable
+    // Split step (num_splits > 1): each (kv head, sequence) tile is cut into
+    // num_splits contiguous runs of blocks, one CTA each; a CTA writes its
+    // partial state to `part` and the last of a row's CTAs (atomic ticket)
+    // merges them into (m, l, o).
+    int num_splits;
+    float *part;          // [num_seqs, num_kv_heads, num_splits, G, D + 2]
+    int32_t *tickets;     // [num_seqs, num_kv_heads], zero between calls
 };
+
+// Bytes of the split step's workspace: tickets, then the partial states.
+size_t decode_split_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int num_splits);
+void decode_split_workspace_carve(void *ws, int num_seqs, int num_kv_heads, DecodeStepArgs *a);
 
 cudaError_t launch_decode_init(float *m, float *l, float *o, int num_seqs, int num_q_heads,
                                int head_dim, int32_t *status, cudaStream_t stream);
@@ -131,27 +143,36 @@ cudaError_t launch_decode_gather(const DecodeStepArgs &a, void *k_out, void *v_o
 // ------------------------------------------------------------ backward
 
 struct BwdArgs {
-    CUtensorMap tm_q, tm_k, tm_v, tm_do;   // boxes of 64 x 1 x 128 rows, 128-byte swizzle
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;   // boxes of 64 columns x 1 head x bwd_step_rows() rows,
+                                            // 128-byte swizzle
     const int32_t *cu_q;
     const int32_t *cu_k;
     const void *out, *dout;                 // bf16 [total_q, H, D]
     const float *lse;                       // f32 [total_q, H], natural log
     void *dq, *dk, *dv;                     // bf16 outputs
     int32_t *status;                        // workspace: status word
-    int32_t *ktile_start;                   // workspace: [batch + 1] first key tile per sequence
+    int32_t *ktile_start;                   // workspace: [batch + 1] first 128-key tile per sequence
+    int32_t *qtile_start;                   // workspace: [batch + 1] first 128-query tile per sequence
     float *delta;                           // workspace: [total_q, H]
-    float *dq_acc;                          // workspace: [total_q, H, D] fp32 dQ / scale
     int batch, total_q, total_k, num_heads, num_kv_heads;
     float scale, scale_log2;
     int causal, window_left;
 };
 
+// Rows the backward streams per step (queries past a key tile, keys past a
+// query tile); its TMA maps use boxes of this many rows.
+__host__ __device__ constexpr int bwd_step_rows(int head_dim)
+{
+    return head_dim == 256 ? 32 : 64;
+}
+
 // Workspace bytes of the backward and its split into the BwdArgs pointers.
 size_t bwd_workspace_bytes(int batch, int total_q, int num_heads, int head_dim);
 void bwd_workspace_split(void *ws, int batch, int total_q, int num_heads, BwdArgs *a);
-// prep, Delta, main (grid: key_tile_bound x num_kv_heads) and dQ kernels.
-cudaError_t launch_bwd(int head_dim, const BwdArgs &a, int key_tile_bound, int sm_count,
-                       cudaStream_t stream);
+// prep, Delta, dK/dV (grid: key_tile_bound x column halves, num_kv_heads) and
+// dQ (grid: q_tile_bound x num_heads) kernels.
+cudaError_t launch_bwd(int head_dim, const BwdArgs &a, int key_tile_bound, int q_tile_bound,
+                       int sm_count, cudaStream_t stream);
 
 // ------------------------------------------------------------ test hooks
 
