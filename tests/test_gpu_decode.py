@@ -214,3 +214,88 @@ def test_bad_token_count_sets_status_and_skips_sequence(vfa):
     assert int(status.item()) == vfa.VFA_ERR_BAD_BLOCK
     assert torch.all(torch.isneginf(m[0])) and torch.all(l[0] == 0)      # left as it was
     assert torch.all(torch.isfinite(m[1])) and torch.all(l[1] > 0)       # the valid one ran
+
+
+# Split step: each (sequence, kv head) tile cut into runs of blocks, one CTA
+# each, merged by the last CTA of the row.  The result is the step's state
+# update whatever the cut ("attention_ref.rs": tile fragmentation must give
+# the single-shot result), checked against the oracle's single-shot state.
+
+def _run_gpu_split(vfa, case, num_splits, exact=False, status=None, ws=None):
+    m, l, o = _gpu_state(case)
+    q, kp, vp = case.q.cuda(), case.k_pool.cuda(), case.v_pool.cuda()
+    S, Hq, Hkv, D = case.num_seqs, case.num_q_heads, case.num_kv_heads, case.head_dim
+    if ws is None:
+        ws = vfa.alloc_decode_split_workspace(S, Hq, Hkv, D, num_splits)
+    vfa.decode_init(m, l, o, status)
+    for t in range(case.num_steps):
+        tb, tc = case.tile(t)
+        tt = torch.from_numpy(case.tile_tokens(t)).cuda() if exact else None
+        vfa.decode_step_split(q, kp, vp, torch.from_numpy(tb).cuda(),
+                              torch.from_numpy(tc).cuda(), m, l, o, num_splits, ws, status,
+                              tile_token_counts=tt)
+    out = vfa.decode_finalize(l, o)
+    torch.cuda.synchronize()
+    return (m.cpu().double().numpy(), l.cpu().double().numpy(), o.cpu().double().numpy(),
+            out.float().cpu().double().numpy(), ws)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_split_decode_long_contexts(vfa, oracle_mod, seed):
+    # four contexts of 49k-64k tokens, each in one tile of up to 4096 blocks:
+    # without the split the step has only 32 CTAs for 152 SMs
+    case = W.decode_long(seed)
+    assert case.num_steps == 1 and max(case.context_lengths) == 65536
+    n = vfa.decode_split_count(case.num_seqs, case.num_kv_heads, case.tile_capacity)
+    assert n > 1
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    m, l, o, out, ws = _run_gpu_split(vfa, case, n, exact=True, status=status)
+    assert int(status.item()) == 0
+    st, ref = _run_oracle(oracle_mod, case, exact=True)
+    _compare(m, l, o, out, st, ref, f"split decode long x{n}")
+    tickets = ws[:4 * case.num_seqs * case.num_kv_heads].view(torch.int32)
+    assert torch.all(tickets == 0)                   # left ready for the next call
+
+
+@pytest.mark.parametrize("num_splits", [2, 7, 40])
+def test_split_decode_workload_steps(vfa, oracle_mod, num_splits):
+    # the 64-sequence workload, every 32-block step split (40 runs: most of them
+    # empty), chained on one workspace through all steps
+    case = W.decode(0)
+    m, l, o, out, _ = _run_gpu_split(vfa, case, num_splits)
+    st, ref = _run_oracle(oracle_mod, case)
+    _compare(m, l, o, out, st, ref, f"split decode x{num_splits}")
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 8, 64), (8, 1, 128), (16, 2, 256), (4, 2, 64)])
+def test_split_decode_shapes_exact_context(vfa, oracle_mod, Hq, Hkv, D):
+    rng = np.random.default_rng(Hq + D + 1)
+    n_blocks = [50, 0, 1, 130, 7, 3]
+    ctx = [50 * 16 - 3, 0, 1, 130 * 16, 7 * 16 - 15, 33]
+    perm = rng.permutation(sum(n_blocks)).astype(np.int32)
+    case = W.make_decode("split-exact", n_blocks, Hq, Hkv, D, 16, 64, perm, value_seed=D + Hq,
+                         context_lengths=ctx)
+    m, l, o, out, _ = _run_gpu_split(vfa, case, 5, exact=True)
+    st, ref = _run_oracle(oracle_mod, case, exact=True)
+    _compare(m, l, o, out, st, ref, f"split exact {Hq}/{Hkv}/{D}")
+
+
+def test_split_decode_bad_block_skips_row_and_keeps_tickets(vfa):
+    n_blocks = [20, 20]
+    rng = np.random.default_rng(4)
+    case = W.make_decode("bad-split", n_blocks, 8, 2, 128, 16, 20,
+                         rng.permutation(40).astype(np.int32), value_seed=3)
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    m, l, o = _gpu_state(case)
+    ws = vfa.alloc_decode_split_workspace(2, 8, 2, 128, 4)
+    vfa.decode_init(m, l, o, status)
+    tb, tc = case.tile(0)
+    tb[1, 13] = case.num_blocks                      # out of the pool
+    vfa.decode_step_split(case.q.cuda(), case.k_pool.cuda(), case.v_pool.cuda(),
+                          torch.from_numpy(tb).cuda(), torch.from_numpy(tc).cuda(), m, l, o, 4,
+                          ws, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == vfa.VFA_ERR_BAD_BLOCK
+    assert torch.all(torch.isneginf(m[1])) and torch.all(l[1] == 0) and torch.all(o[1] == 0)
+    assert torch.all(l[0] > 0)
+    assert torch.all(ws[:16].view(torch.int32) == 0)

@@ -175,7 +175,9 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t base, int row, int chunk)
     return base + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
-template <int D, int G>
+// SPLIT: the CTA takes run blockIdx.z of the tile's blocks (the split step)
+// and merges through the workspace instead of into the state directly.
+template <int D, int G, bool SPLIT>
 __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
     const DecodeStepArgs a, const __grid_constant__ DecodeMaps t)
 {
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
     __shared__ float s_min[G], s_lin[G];
     __shared__ int s_abort;
     __shared__ int s_fills[NS], s_used[NS];   // per stage: fills issued, fills consumed
+    __shared__ int s_last;
 
     const int kh = blockIdx.x;
     const int s = blockIdx.y;
@@ -216,7 +219,15 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
     }
     if (count == 0 || n_tok == 0)
         return;                                 // an empty tile leaves the state as it was
-    const int nb = (n_tok + kBlockSize - 1) / kBlockSize;   // blocks holding those tokens
+    const int nb_all = (n_tok + kBlockSize - 1) / kBlockSize;   // blocks holding those tokens
+    // This CTA's run of blocks [kb0, kb0 + nb): the whole tile, or run
+    // blockIdx.z of num_splits equal runs (possibly empty).
+    int kb0 = 0, nb = nb_all;
+    if (SPLIT) {
+        const int per = (nb_all + a.num_splits - 1) / a.num_splits;
+        kb0 = min(nb_all, static_cast<int>(blockIdx.z) * per);
+        nb = min(nb_all, kb0 + per) - kb0;
+    }
 
     const uint32_t ring = smem_u32(dsm);
     auto stage_k = [&](int st) { return ring + st * C::STAGE; };
@@ -233,8 +244,8 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
     __syncthreads();
     volatile int *abort = &s_abort;
 
-    const int32_t *row_ids = a.tile_blocks + static_cast<long long>(s) * a.tile_capacity;
-    // Block k of the tile into stage k % NS (one thread issues a fill).
+    const int32_t *row_ids = a.tile_blocks + static_cast<long long>(s) * a.tile_capacity + kb0;
+    // Block k of the run into stage k % NS (one thread issues a fill).
     auto issue = [&](int k) {
         const int blk = row_ids[k];
         const int st = k % NS;
@@ -304,7 +315,7 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
         // sacc: tokens lane/4 (0, 1) and lane/4 + 8 (2, 3); heads 2*t4 (0, 2), 2*t4+1 (1, 3).
         // Tokens past n_tok (only in the last block) get weight zero; every
         // block read holds at least one token that counts.
-        const int valid = n_tok - k * kBlockSize;
+        const int valid = n_tok - (kb0 + k) * kBlockSize;
         if (valid < kBlockSize) {
             const int t0 = lane >> 2;
             if (t0 >= valid) {
@@ -375,9 +386,10 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
         l_part[h] = x;
     }
     __syncthreads();                                    // every warp is out of the ring
-    // The previous step (or the init) must be complete before its state is read.
+    // The previous step (or the init) must be complete before its state is
+    // read, and (split step) before the shared workspace is written.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (*abort) {
+    if (!SPLIT && *abort) {
         // A stage's last fill may still be in flight if nobody consumed it:
         // wait for it (bounded) before the CTA exits; the state is left as it was.
         if (threadIdx.x == 0) {
@@ -388,6 +400,26 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
                 atomicCAS(a.status, 0, VFA_ERR_TIMEOUT);
         }
         return;
+    }
+    if (SPLIT && *abort) {
+        // the partial is not usable: contribute an empty one, keep the tickets whole
+        if (threadIdx.x == 0)
+            for (int st = 0; st < NS; ++st)
+                if (s_fills[st] > s_used[st])
+                    mbar_wait_drain(full(st), (s_fills[st] - 1) & 1u);
+        __syncthreads();
+        if (lane < 4)
+            for (int h = 0; h < 2; ++h) {
+                m_run[h] = -INFINITY;
+                l_part[h] = 0.f;
+            }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                o[mt][e] = 0.f;
+        if (threadIdx.x == 0 && a.status)
+            atomicCAS(a.status, 0, VFA_ERR_TIMEOUT);
     }
     float *s_o = reinterpret_cast<float *>(dsm);        // [warps][G][D], over the ring
     if (lane < 4) {
@@ -407,6 +439,84 @@ __global__ void __launch_bounds__(kStepWarps * 32) decode_step_kernel(
             if (h < G)
                 s_o[(warp * G + h) * D + col] = o[mt][e];
         }
+    if (SPLIT) {
+        // This CTA's partial state, its warps merged relative to one max
+        // (log2 units): [g][0] = m, [g][1] = l, [g][2 ..] = o.
+        __syncthreads();
+        const int row = s * a.num_kv_heads + kh;
+        float *part = a.part + (static_cast<long long>(row) * a.num_splits + blockIdx.z) * G *
+                                   (D + 2);
+        for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+            const int g = e / D, d = e % D;
+            float mt = s_m[0][g];
+#pragma unroll
+            for (int w = 1; w < kStepWarps; ++w)
+                mt = fmaxf(mt, s_m[w][g]);
+            float acc_o = 0.f, acc_l = 0.f;
+            if (mt != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kStepWarps; ++w) {
+                    const float fw = ex2_approx(s_m[w][g] - mt);
+                    acc_o = fmaf(s_o[(w * G + g) * D + d], fw, acc_o);
+                    acc_l = fmaf(s_l[w][g], fw, acc_l);
+                }
+            }
+            part[g * (D + 2) + 2 + d] = acc_o;
+            if (d == 0) {
+                part[g * (D + 2)] = mt;
+                part[g * (D + 2) + 1] = acc_l;
+            }
+        }
+        // Publish the partial, then take a ticket; the last CTA of the row merges.
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0)
+            s_last = atomicAdd(a.tickets + row, 1) == a.num_splits - 1;
+        __syncthreads();
+        if (!s_last)
+            return;
+        __threadfence();
+        const float *parts = a.part + static_cast<long long>(row) * a.num_splits * G * (D + 2);
+        // per head: the merged max and the weights of the incoming state (w[0])
+        // and of each run (w[1 + c]), over the ring, which is free now
+        const int NW = a.num_splits + 1;
+        float *s_w = reinterpret_cast<float *>(dsm);          // [G][NW]
+        __syncthreads();
+        if (threadIdx.x < G) {
+            const int g = threadIdx.x;
+            const long long sh = static_cast<long long>(s) * Hq + kh * G + g;
+            const float m_in = a.m[sh] * kLog2e;
+            float mt = m_in;
+            for (int c = 0; c < a.num_splits; ++c)
+                mt = fmaxf(mt, __ldcg(parts + (c * G + g) * (D + 2)));
+            const bool live = mt != -INFINITY;
+            s_w[g * NW] = live ? ex2_approx(m_in - mt) : 0.f;   // 0 for a fresh state
+            for (int c = 0; c < a.num_splits; ++c)
+                s_w[g * NW + 1 + c] =
+                    live ? ex2_approx(__ldcg(parts + (c * G + g) * (D + 2)) - mt) : 0.f;
+            s_min[g] = mt;
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+            const int g = e / D, d = e % D;
+            const long long sh = static_cast<long long>(s) * Hq + kh * G + g;
+            const float *w = s_w + g * NW;
+            float acc_o = a.o[sh * D + d] * w[0];
+            for (int c = 0; c < a.num_splits; ++c)
+                acc_o = fmaf(__ldcg(parts + (c * G + g) * (D + 2) + 2 + d), w[1 + c], acc_o);
+            a.o[sh * D + d] = acc_o;
+            if (d == 0) {
+                float acc_l = a.l[sh] * w[0];
+                for (int c = 0; c < a.num_splits; ++c)
+                    acc_l = fmaf(__ldcg(parts + (c * G + g) * (D + 2) + 1), w[1 + c], acc_l);
+                a.l[sh] = acc_l;
+                a.m[sh] = s_min[g] == -INFINITY ? -INFINITY : s_min[g] * kLn2;
+            }
+        }
+        if (threadIdx.x == 0)
+            a.tickets[row] = 0;                          // ready for the next call
+        return;
+    }
     if (threadIdx.x < G) {
         const long long sh = static_cast<long long>(s) * Hq + kh * G + threadIdx.x;
         s_min[threadIdx.x] = a.m[sh] * kLog2e;
@@ -527,8 +637,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_gather_kernel(const Decode
     }
 }
 
-template <int D, int G>
-cudaError_t step_dg(const DecodeStepArgs &a, const DecodeMaps &maps, cudaStream_t stream)
+template <int D, int G, bool SPLIT>
+cudaError_t step_dgs(const DecodeStepArgs &a, const DecodeMaps &maps, cudaStream_t stream)
 {
     static int attr_done[64] = {0};
     int dev = 0;
@@ -537,7 +647,7 @@ cudaError_t step_dg(const DecodeStepArgs &a, const DecodeMaps &maps, cudaStream_
         return e;
     const size_t smem = step_smem_bytes<D, G>();
     if (dev < 64 && !attr_done[dev]) {
-        e = cudaFuncSetAttribute(decode_step_kernel<D, G>,
+        e = cudaFuncSetAttribute(decode_step_kernel<D, G, SPLIT>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
         if (e != cudaSuccess)
@@ -545,7 +655,7 @@ cudaError_t step_dg(const DecodeStepArgs &a, const DecodeMaps &maps, cudaStream_
         attr_done[dev] = 1;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.num_kv_heads, a.num_seqs);
+    cfg.gridDim = dim3(a.num_kv_heads, a.num_seqs, SPLIT ? a.num_splits : 1);
     cfg.blockDim = dim3(kStepWarps * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -554,10 +664,17 @@ cudaError_t step_dg(const DecodeStepArgs &a, const DecodeMaps &maps, cudaStream_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_step_kernel<D, G>, a, maps);
+    e = cudaLaunchKernelEx(&cfg, decode_step_kernel<D, G, SPLIT>, a, maps);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t step_dg(const DecodeStepArgs &a, const DecodeMaps &maps, cudaStream_t stream)
+{
+    return a.num_splits > 1 ? step_dgs<D, G, true>(a, maps, stream)
+                            : step_dgs<D, G, false>(a, maps, stream);
 }
 
 template <int D>
@@ -583,6 +700,25 @@ int grid_for(long long n, int threads)
 }
 
 }  // namespace
+
+size_t decode_split_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int num_splits)
+{
+    size_t n = static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(int32_t);   // tickets
+    n = (n + 255) & ~static_cast<size_t>(255);
+    n += static_cast<size_t>(num_seqs) * num_q_heads * num_splits * (head_dim + 2) *
+         sizeof(float);
+    return (n + 255) & ~static_cast<size_t>(255);
+}
+
+void decode_split_workspace_carve(void *ws, int num_seqs, int num_kv_heads, DecodeStepArgs *a)
+{
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    a->tickets = reinterpret_cast<int32_t *>(p);
+    size_t n = static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(int32_t);
+    n = (n + 255) & ~static_cast<size_t>(255);
+    a->part = reinterpret_cast<float *>(p + n);
+}
 
 cudaError_t launch_decode_init(float *m, float *l, float *o, int num_seqs, int num_q_heads,
                                int head_dim, int32_t *status, cudaStream_t stream)

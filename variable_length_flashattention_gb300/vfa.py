@@ -55,6 +55,10 @@ SIGNATURES = [
     ("vfa_paged_decode_init", _I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     ("vfa_paged_decode_step", _I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                                    _P, _P, _P, _P]),
+    ("vfa_paged_decode_step_split", _I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
+                                         _P, _P, _P, _P, _I, _P, _S, _P]),
+    ("vfa_paged_decode_split_workspace_bytes", _S, [_I, _I, _I, _I, _I]),
+    ("vfa_paged_decode_split_count", _I, [_I, _I, _I, _P]),
     ("vfa_paged_decode_finalize", _I, [_P, _P, _I, _I, _I, _P, _P]),
     ("vfa_debug_paged_gather", _I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     ("vfa_debug_bounded_wait", _I, [_P, _P]),
@@ -352,6 +356,50 @@ def decode_step(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                                        tile_blocks.shape[1], S, Hq, Hkv, D, bs,
                                        float(softmax_scale), _ptr(m), _ptr(l), _ptr(o),
                                        _ptr(status), _stream(stream)))
+
+
+def decode_split_count(num_seqs: int, num_kv_heads: int, tile_capacity: int) -> int:
+    """vfa_paged_decode_split_count: a run count for the current device."""
+    n = ctypes.c_int()
+    _check(lib().vfa_paged_decode_split_count(num_seqs, num_kv_heads, tile_capacity,
+                                              ctypes.byref(n)))
+    return n.value
+
+
+def alloc_decode_split_workspace(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                 head_dim: int, num_splits: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace for vfa_paged_decode_step_split (the tickets start at zero)."""
+    n = lib().vfa_paged_decode_split_workspace_bytes(num_seqs, num_q_heads, num_kv_heads,
+                                                     head_dim, num_splits)
+    if n == 0:
+        raise VfaError(VFA_ERR_UNSUPPORTED, "no split workspace for these sizes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode_step_split(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                      tile_blocks: torch.Tensor, tile_block_counts: torch.Tensor,
+                      m: torch.Tensor, l: torch.Tensor, o: torch.Tensor, num_splits: int,
+                      workspace: torch.Tensor, status: Optional[torch.Tensor] = None,
+                      stream=None, tile_token_counts: Optional[torch.Tensor] = None,
+                      softmax_scale: float = 0.0):
+    """vfa_paged_decode_step_split: the step with each tile cut into num_splits runs."""
+    _need(q, torch.bfloat16, "q")
+    if tile_token_counts is not None:
+        _need(tile_token_counts, torch.int32, "tile_token_counts")
+    _need(k_pool, torch.bfloat16, "k_pool")
+    _need(v_pool, torch.bfloat16, "v_pool")
+    _need(tile_blocks, torch.int32, "tile_blocks")
+    _need(tile_block_counts, torch.int32, "tile_block_counts")
+    _need(workspace, torch.uint8, "workspace")
+    S, Hq, D = q.shape
+    nb, bs, Hkv, D2 = k_pool.shape
+    if D2 != D or v_pool.shape != k_pool.shape or tile_blocks.shape[0] != S:
+        raise ValueError("inconsistent decode shapes")
+    _check(lib().vfa_paged_decode_step_split(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), nb, _ptr(tile_blocks), _ptr(tile_block_counts),
+        _ptr(tile_token_counts), tile_blocks.shape[1], S, Hq, Hkv, D, bs, float(softmax_scale),
+        _ptr(m), _ptr(l), _ptr(o), _ptr(status), int(num_splits), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
 
 
 def decode_finalize(l: torch.Tensor, o: torch.Tensor, out: Optional[torch.Tensor] = None,

@@ -23,7 +23,11 @@ Workloads (lengths per the plan's packed layout and cu_seqlens semantics):
                Hq=32, Hkv=8, D=128, block_size=16; the pool holds exactly
                sum(n_blocks) blocks and logical block j of sequence s sits at
                physical id perm[offset_s + j] for a seeded permutation perm;
-               step t covers logical blocks [32 t, 32 t + 32).
+               step t covers logical blocks [32 t, 32 t + 32);
+  * decode-long: a few long contexts (the first 65536 tokens, the others
+               U{49152..65536}), the decode workload's heads, dims, block
+               size and block-id permutation, and one tile holding every
+               block of a context (4096 blocks), so one step covers it.
 """
 from __future__ import annotations
 
@@ -281,3 +285,16 @@ def decode(seed: int = 0, num_seqs: int = 64, ctx_lo: int = 128, ctx_hi: int = 8
     perm = rng.permutation(sum(n_blocks)).astype(np.int32)
     return make_decode("decode", n_blocks, num_q_heads, num_kv_heads, head_dim, block_size,
                        tile_capacity, perm, value_seed=seed, context_lengths=[int(c) for c in ctx])
+
+
+def decode_long(seed: int = 0, num_seqs: int = 4, longest: int = 65536, shortest: int = 49152,
+                num_q_heads: int = 32, num_kv_heads: int = 8, head_dim: int = 128,
+                block_size: int = 16) -> DecodeCase:
+    """A few long contexts decoded in one tile step each (tile capacity = the
+    longest context's blocks)."""
+    rng = np.random.default_rng(seed)
+    ctx = [longest] + [int(c) for c in rng.integers(shortest, longest + 1, num_seqs - 1)]
+    n_blocks = [int(-(-c // block_size)) for c in ctx]
+    perm = rng.permutation(sum(n_blocks)).astype(np.int32)
+    return make_decode("decode-long", n_blocks, num_q_heads, num_kv_heads, head_dim, block_size,
+                       max(n_blocks), perm, value_seed=seed + 500, context_lengths=ctx)
