@@ -39,54 +39,67 @@ def _run(vfa, case, f8, causal, window_left=-1):
     return out.float().cpu().double().numpy(), lse.cpu().double().numpy(), status
 
 
+@pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("causal,window_left", [(0, -1), (1, -1), (2, -1), (1, 200), (2, 37)])
-def test_mixes(vfa, oracle_mod, causal, window_left):
+def test_mixes(vfa, oracle_mod, causal, window_left, D):
     lq = [1, 7, 64, 129, 300, 0, 257, 1000]
     lk = [1, 7, 64, 129, 300, 5, 90, 800]
-    case = W.make_varlen("fp8", lq, lk, 2, 128, bool(causal), 1.0, value_seed=20 + causal)
+    case = W.make_varlen("fp8", lq, lk, 2, D, bool(causal), 1.0, value_seed=20 + causal + D)
     f8 = W.fp8_qk(case)
     out, lse, status = _run(vfa, case, f8, causal, window_left)
     assert status == 0
     ref_out, ref_lse, _ = oracle_mod.varlen_fwd_fp8(f8.q8, f8.k8, case.v, case.cu_seqlens_q,
-                                                    case.cu_seqlens_k, 2, 128,
+                                                    case.cu_seqlens_k, 2, D,
                                                     case.softmax_scale, f8.descale_q,
                                                     f8.descale_k, causal,
                                                     window_left=window_left)
-    assert_out_close(out, ref_out, f"fp8 causal {causal} window {window_left}")
-    assert_lse_close(lse, ref_lse, f"fp8 causal {causal} window {window_left}")
+    assert_out_close(out, ref_out, f"fp8 D={D} causal {causal} window {window_left}")
+    assert_lse_close(lse, ref_lse, f"fp8 D={D} causal {causal} window {window_left}")
 
 
-def test_grouped_kv_heads(vfa, oracle_mod):
+@pytest.mark.parametrize("D", [128, 256])
+def test_grouped_kv_heads(vfa, oracle_mod, D):
     lq, lk = [300, 7, 129, 64], [300, 40, 129, 200]
-    case = W.make_varlen("fp8-gqa", lq, lk, 8, 128, True, 1.0, value_seed=31)
+    case = W.make_varlen("fp8-gqa", lq, lk, 8, D, True, 1.0, value_seed=31 + D)
     case.k = case.k[:, :2].contiguous()
     case.v = case.v[:, :2].contiguous()
     f8 = W.fp8_qk(case)
     out, lse, status = _run(vfa, case, f8, 1)
     assert status == 0
     ref_out, ref_lse, _ = oracle_mod.varlen_fwd_fp8(f8.q8, f8.k8, case.v, case.cu_seqlens_q,
-                                                    case.cu_seqlens_k, 8, 128,
+                                                    case.cu_seqlens_k, 8, D,
                                                     case.softmax_scale, f8.descale_q,
                                                     f8.descale_k, 1, num_kv_heads=2)
     assert_out_close(out, ref_out, "fp8 gqa")
     assert_lse_close(lse, ref_lse, "fp8 gqa")
 
 
-def test_packed_batch_sampled(vfa, oracle_mod):
-    # the bench's packed batch with FP8 q and k; the oracle on three whole sequences
-    case = W.packed(0)
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_packed_batch(vfa, oracle_mod, seed):
+    # the bench's packed batch with FP8 q and k, every sequence and head
+    case = W.packed(seed)
     f8 = W.fp8_qk(case)
     out, lse, status = _run(vfa, case, f8, 1)
     assert status == 0
-    L = case.lengths_q
-    for b in (int(np.argmax(L)), int(np.argmin(L)), len(L) // 2):
-        q0, q1 = int(case.cu_seqlens_q[b]), int(case.cu_seqlens_q[b + 1])
-        cu = np.array([0, q1 - q0], dtype=np.int32)
-        ro, rl, _ = oracle_mod.varlen_fwd_fp8(f8.q8[q0:q1], f8.k8[q0:q1], case.v[q0:q1], cu, cu,
-                                              16, 128, case.softmax_scale, f8.descale_q,
-                                              f8.descale_k, 1)
-        assert_out_close(out[q0:q1], ro, f"fp8 packed seq {b}")
-        assert_lse_close(lse[q0:q1], rl, f"fp8 packed seq {b}")
+    ro, rl, _ = oracle_mod.varlen_fwd_fp8(f8.q8, f8.k8, case.v, case.cu_seqlens_q,
+                                          case.cu_seqlens_k, 16, 128, case.softmax_scale,
+                                          f8.descale_q, f8.descale_k, 1)
+    assert_out_close(out, ro, f"fp8 packed seed {seed}")
+    assert_lse_close(lse, rl, f"fp8 packed seed {seed}")
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_cross_attention_d256(vfa, oracle_mod, seed):
+    # the cross-attention workload at head_dim 256 with FP8 q and k
+    case = W.cross(256, seed)
+    f8 = W.fp8_qk(case)
+    out, lse, status = _run(vfa, case, f8, 0)
+    assert status == 0
+    ro, rl, _ = oracle_mod.varlen_fwd_fp8(f8.q8, f8.k8, case.v, case.cu_seqlens_q,
+                                          case.cu_seqlens_k, 8, 256, case.softmax_scale,
+                                          f8.descale_q, f8.descale_k, 0)
+    assert_out_close(out, ro, f"fp8 cross-d256 seed {seed}")
+    assert_lse_close(lse, rl, f"fp8 cross-d256 seed {seed}")
 
 
 def test_rejects_other_head_dims_and_bad_descales(vfa):

@@ -366,8 +366,9 @@ vfa_status vfa_varlen_fwd_fp8(const void *q_fp8, const void *k_fp8, const void *
                               void *out, float *lse, void *workspace, size_t workspace_bytes,
                               vfa_stream_t stream)
 {
-    if (head_dim != 128)
-        return fail(VFA_ERR_UNSUPPORTED, "FP8 forward head_dim %d not supported (128)", head_dim);
+    if (head_dim != 128 && head_dim != 256)
+        return fail(VFA_ERR_UNSUPPORTED, "FP8 forward head_dim %d not supported (128, 256)",
+                    head_dim);
     if (!(descale_q > 0.f) || !(descale_k > 0.f) || descale_q > FLT_MAX || descale_k > FLT_MAX)
         return fail(VFA_ERR_INVALID_ARG, "descale_q and descale_k must be finite and > 0");
     return varlen_fwd_impl(q_fp8, k_fp8, v, cu_seqlens_q, cu_seqlens_k, total_q, total_k,

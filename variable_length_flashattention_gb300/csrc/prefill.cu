@@ -1,6 +1,9 @@
 // prefill.cu -- variable-length attention forward on sm_103a, one q tile per
 // CTA work item (used for head_dim 256, whose O accumulator alone fills half
-// of TMEM; head_dim 64 and 128 use prefill_pair.cu).
+// of TMEM; head_dim 64 and 128 use prefill_pair.cu).  An FP8 instantiation
+// takes Q and K as E4M3 codes: their tiles are half the bytes and S = Q K^T
+// runs as kind::f8f6f4 in 32-byte k-steps (the per-tensor descales are
+// folded into the score scale); P, V and O are the bf16 kernel's.
 //
 // Computes, per packed query row, softmax(scale * q K^T, masks) V and the
 // natural-log log-sum-exp, by the tiled online-softmax recurrence of
@@ -37,23 +40,31 @@ namespace vfa {
 
 namespace {
 
-template <int D>
+// F8: Q and K are FP8 E4M3 codes (1 byte each) and S = Q K^T runs as
+// kind::f8f6f4 in 32-byte k-steps; V, P and O stay as in the bf16 kernel.
+template <int D, bool F8 = false>
 struct Cfg {
     static constexpr int BQ = kBlockQ;
     static constexpr int BK = block_k_for(D);
     static constexpr int NS = 2;                          // K/V ring stages
     static constexpr int NQ = D == 256 ? 1 : 2;           // Q buffers
-    static constexpr int DB = D / 64;                     // 128-byte column blocks per row
-    static constexpr uint32_t Q_BYTES = BQ * D * 2;
-    static constexpr uint32_t KV_BYTES = BK * D * 2;
+    static constexpr int DB = D / 64;                     // 128-byte column blocks per V / O row
+    static constexpr int QK_ELEM = F8 ? 1 : 2;            // bytes per Q / K element
+    static constexpr int QK_DB = D * QK_ELEM / 128;       // 128-byte column blocks per Q / K row
+    static constexpr int QK_BLOCK = 128 / QK_ELEM;        // elements per such block
+    static constexpr int KSTEPS = D * QK_ELEM / 32;       // 32-byte MMA k-steps of S = Q K^T
+    static constexpr uint32_t Q_BYTES = BQ * D * QK_ELEM;
+    static constexpr uint32_t K_BYTES = BK * D * QK_ELEM;
+    static constexpr uint32_t KV_BYTES = BK * D * 2;      // one V stage
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int NSB = 3;                         // S/P buffers in TMEM
     static constexpr uint32_t O_COL = 0;                  // O: columns [0, D)
     static constexpr uint32_t S_COL = D;                  // S buffer x: [D + x*BK, D + (x+1)*BK)
     static constexpr int NUM_BARS = 2 * NQ + 4 * NS + 3 * NSB + 1 + 4;
-    static constexpr size_t SMEM = 1024 /*alignment slack*/ + NQ * Q_BYTES + 2 * NS * KV_BYTES +
-                                   NUM_BARS * 8 + 64;
-    static constexpr uint32_t IDESC_QK = idesc_bf16_f32(BQ, BK, false, false);
+    static constexpr size_t SMEM = 1024 /*alignment slack*/ + NQ * Q_BYTES +
+                                   NS * (K_BYTES + KV_BYTES) + NUM_BARS * 8 + 64;
+    static constexpr uint32_t IDESC_QK =
+        F8 ? idesc_e4m3_f32(BQ, BK) : idesc_bf16_f32(BQ, BK, false, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BQ, D, false, true);
     static_assert(S_COL + NSB * BK <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -67,10 +78,10 @@ __device__ __forceinline__ void record_error(int32_t *status, int code)
     atomicCAS(status, 0, code);
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs p)
 {
-    using C = Cfg<D>;
+    using C = Cfg<D, F8>;
     constexpr int BQ = C::BQ, BK = C::BK, NS = C::NS, NQ = C::NQ, DB = C::DB;
 
     extern __shared__ uint8_t smem_raw[];
@@ -87,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t sQ = base;
     const uint32_t sK = sQ + NQ * C::Q_BYTES;
-    const uint32_t sV = sK + NS * C::KV_BYTES;
+    const uint32_t sV = sK + NS * C::K_BYTES;
     const uint32_t bars = sV + NS * C::KV_BYTES;
     auto q_full = [&](int i) { return bars + 8u * i; };
     auto q_empty = [&](int i) { return bars + 8u * (NQ + i); };
@@ -195,9 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     break;
                 }
                 mbar_arrive_expect_tx(q_full(qb), C::Q_BYTES);
-                for (int db = 0; db < DB; ++db)
+                for (int db = 0; db < C::QK_DB; ++db)
                     tma_load_3d(sQ + qb * C::Q_BYTES + db * (BQ * 128), &p.tm_q, q_full(qb),
-                                db * 64, h, q_row0);
+                                db * C::QK_BLOCK, h, q_row0);
                 ++qit;
                 for (int j = first; j < j_end; ++j) {
                     const int st = kfills % NS;
@@ -205,10 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(k_full(st), C::KV_BYTES);
-                    for (int db = 0; db < DB; ++db)
-                        tma_load_3d(sK + st * C::KV_BYTES + db * (BK * 128), &p.tm_k, k_full(st),
-                                    db * 64, h / p.kv_group, k_row0 + j * BK);
+                    mbar_arrive_expect_tx(k_full(st), C::K_BYTES);
+                    for (int db = 0; db < C::QK_DB; ++db)
+                        tma_load_3d(sK + st * C::K_BYTES + db * (BK * 128), &p.tm_k, k_full(st),
+                                    db * C::QK_BLOCK, h / p.kv_group, k_row0 + j * BK);
                     ++kfills;
                     if (!mbar_wait(v_empty(st), ((vfills / NS) & 1u) ^ 1u, abort)) {
                         ok = false;
@@ -298,14 +309,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t kd = k_desc0 + st * (C::KV_BYTES >> 4);
+                    const uint64_t kd = k_desc0 + st * (C::K_BYTES >> 4);
                     const uint32_t s_tm = tmem + C::S_COL + x * BK;
-                    mma_ss_c<0>(s_tm, qd, kd, C::IDESC_QK);
+                    // k-steps of 32 bytes: 16 bf16 or 32 FP8 elements
 #pragma unroll
-                    for (int kk = 1; kk < D / 16; ++kk)
-                        mma_ss_c<1>(s_tm, qd + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4),
-                                    kd + (((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4),
-                                    C::IDESC_QK);
+                    for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                        const uint64_t qo = qd + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4);
+                        const uint64_t ko = kd + (((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4);
+                        if constexpr (F8) {
+                            if (kk == 0)
+                                mma_ss_c8<0>(s_tm, qo, ko, C::IDESC_QK);
+                            else
+                                mma_ss_c8<1>(s_tm, qo, ko, C::IDESC_QK);
+                        } else {
+                            if (kk == 0)
+                                mma_ss_c<0>(s_tm, qo, ko, C::IDESC_QK);
+                            else
+                                mma_ss_c<1>(s_tm, qo, ko, C::IDESC_QK);
+                        }
+                    }
                     mma_commit(s_full(x));
                     mma_commit(k_empty(st));
                     if (j == j_end - 1)
@@ -529,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_d(const PrefillArgs &a, int grid, cudaStream_t stream)
 {
     static int attr_done[64] = {0};
@@ -538,8 +560,8 @@ cudaError_t launch_d(const PrefillArgs &a, int grid, cudaStream_t stream)
     if (e != cudaSuccess)
         return e;
     if (dev < 64 && !attr_done[dev]) {
-        e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(Cfg<D>::SMEM));
+        e = cudaFuncSetAttribute(prefill_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(Cfg<D, F8>::SMEM));
         if (e != cudaSuccess)
             return e;
         attr_done[dev] = 1;
@@ -548,14 +570,14 @@ cudaError_t launch_d(const PrefillArgs &a, int grid, cudaStream_t stream)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+    cfg.dynamicSmemBytes = Cfg<D, F8>::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_kernel<D>, a);
+    e = cudaLaunchKernelEx(&cfg, prefill_kernel<D, F8>, a);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
@@ -568,7 +590,8 @@ cudaError_t launch_prefill(int head_dim, const PrefillArgs &a, int grid, cudaStr
     if (pairs_for(head_dim))
         return launch_prefill_pair(head_dim, a, grid, stream);
     if (head_dim == 256)
-        return launch_d<256>(a, grid, stream);
+        return a.qk_fp8 ? launch_d<256, true>(a, grid, stream)
+                        : launch_d<256, false>(a, grid, stream);
     return cudaErrorInvalidValue;
 }
 

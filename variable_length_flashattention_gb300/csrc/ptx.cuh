@@ -224,6 +224,19 @@ __device__ __forceinline__ void mma_ts_c(uint32_t d_tmem, uint32_t a_tmem, uint6
         : "memory");
 }
 
+// kind::f8f6f4 form of mma_ss_c (A and B 8-bit floating-point codes in smem).
+template <int ACC>
+__device__ __forceinline__ void mma_ss_c8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(ACC)
+        : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, both operands described by descriptors.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate)
