@@ -14,26 +14,30 @@
 //     global key tile and first global q tile (prefix sums of
 //     ceil(L / 128));
 //   * bwd_delta: Delta[t, h] = sum_d dO * out, one warp per (token, head);
-//   * bwd_dkdv_kernel: one CTA per (128-key tile, kv head) -- at head_dim
-//     256 two, each owning one column half of dK and dV.  K and V stay in
-//     shared memory; the query rows that see a key of the tile stream past
-//     in steps of STEP rows (64; 32 at head_dim 256), every query head of the
-//     group, Q and dO through a TMA ring.  Per step the tensor core forms
+//   * the dK/dV kernel (bwd_main_kernel<D, false>): for each 128-key tile and
+//     kv head -- at head_dim 256 each column half of dK and dV -- K and V
+//     stay in shared memory; the query rows that see a key of the tile stream
+//     past in steps of STEP rows (64; 32 at head_dim 256), every query head of
+//     the group, Q and dO through a TMA ring.  Per step the tensor core forms
 //     S^T = K Q^T and dP^T = V dO^T into one of two TMEM buffers; eight warps
 //     turn them into P^T and dS^T (bf16, written back over the columns they
 //     read), and the tensor core accumulates dV += P^T dO and dK += dS^T Q in
 //     TMEM with both A operands read from TMEM.  With two buffers the next
 //     step's S^T / dP^T run on the tensor core while this step's are being
 //     exponentiated;
-//   * bwd_dq_kernel: one CTA per (128-query tile, head), the same with the
-//     roles swapped: Q, dO stay, K and V stream past in blocks of STEP keys;
-//     S = Q K^T, dP = dO V^T into two TMEM buffers, dS (bf16, over dP) and
-//     dQ += dS K in TMEM.  dQ leaves as bf16 once, so no fp32 sum and no
-//     second pass exist.
+//   * the dQ kernel (bwd_main_kernel<D, true>): for each 128-query tile and
+//     head, the same with the roles swapped: Q, dO stay, K and V stream past
+//     in blocks of STEP keys; S = Q K^T, dP = dO V^T into two TMEM buffers,
+//     dS (bf16, over dP) and dQ += dS K in TMEM.  dQ leaves as bf16 once, so
+//     no fp32 sum and no second pass exist.
+// Both are persistent: one CTA per SM takes (tile, head) units from an atomic
+// counter, and consecutive units overlap (the next unit's own tiles load and
+// its first score products run while the current one finishes).
 // The math warps evaluate masks only on steps that need them, as one
 // interval of visible columns per thread.  Every wait is bounded; on expiry
 // the CTA records VFA_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and
 // exits.
+#include <algorithm>
 #include <cfloat>
 #include <cuda_bf16.h>
 
@@ -73,7 +77,9 @@ struct BwdCfg {
     static constexpr uint32_t COL_DQ = 0, Q_BUF = D;
     static constexpr uint32_t BUF_STRIDE = 2 * STEP;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int NUM_BARS = 2 + 2 * NSTAGE + 2 + 2 + 2;
+    // ring full / empty per stage; s_full, p_full, unit_full, unit_empty per
+    // buffer; own_full, own_empty, acc_done, epi_done, drain
+    static constexpr int NUM_BARS = 2 * NSTAGE + 8 + 5;
     static constexpr size_t SMEM = 1024 + 2 * OWN_BYTES + NSTAGE * STAGE_BYTES +
                                    kMathWarps * 256 + NUM_BARS * 8 + 64;
     // S^T / dP^T (keys x STEP queries) and S / dP (queries x STEP keys): both K-major
@@ -151,8 +157,11 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const BwdArgs a)
         return lq > 0 ? (lq + kOwn - 1) / kOwn : 0;
     });
     __syncthreads();
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
+        a.status[1] = 0;                 // unit counters of the two main kernels
+        a.status[2] = 0;
         *a.status = s_bad ? VFA_ERR_BAD_SEQLENS : VFA_OK;
+    }
 }
 
 // ------------------------------------------------------------ Delta
@@ -414,107 +423,157 @@ __device__ __forceinline__ void store_row32(uint32_t taddr, float f, __nv_bfloat
     }
 }
 
-// ------------------------------------------------------------ dK, dV
+// ------------------------------------------------------------ the two main kernels
 
-// Warp 0 loads (K, V once; Q, dO per step), warp 1 issues the MMAs, warps
-// 4-11 form P^T and dS^T: warp w owns TMEM lanes (key rows) 32 (w % 4) .. +31
-// and, of each step's 64 queries, the 32 at 32 g, g = (w - 4) / 4.
+// One unit of work, decoded by the loading warp and handed to the others
+// through a two-slot shared-memory ring.  dK/dV kernel: (kv head, 128-key
+// tile, column half); dQ kernel: (head, 128-query tile).
+struct BwdUnit {
+    int b, t, head, dh;          // sequence, tile in it, (kv) head, column half
+    int q0, lq, k0, lk;          // the sequence's rows and lengths
+    int first, n_blk, n_steps;   // streamed blocks [first, first + n_blk); steps (x group)
+    int valid;                   // 0: no more units
+};
+
+// Unit u of the dK/dV kernel (DQ false) or the dQ kernel (DQ true); `tiles`
+// is the number of 128-row tiles of all sequences.
+template <int D, bool DQ>
+__device__ BwdUnit decode_unit(const BwdArgs &a, int u, int tiles)
+{
+    using C = BwdCfg<D>;
+    constexpr int STEP = C::STEP;
+    constexpr int SPLIT = DQ ? 1 : C::DSPLIT;
+    BwdUnit w;
+    const int per_head = tiles * SPLIT;
+    const int n_heads = DQ ? a.num_heads : a.num_kv_heads;
+    w.valid = u < per_head * n_heads;
+    if (!w.valid)
+        return w;
+    w.head = u / per_head;
+    const int r = u % per_head;
+    // dQ: each head's tiles run last-first (a causal sequence's longest key
+    // ranges first); dK/dV: in order (a sequence's first key tiles see the
+    // most queries); a key tile's column halves are neighbours
+    int gt = r / SPLIT;
+    w.dh = r % SPLIT;
+    if (DQ)
+        gt = tiles - 1 - gt;
+    const int32_t *start = DQ ? a.qtile_start : a.ktile_start;
+    w.b = owner_of(start, a.batch, gt);
+    w.t = gt - start[w.b];
+    w.q0 = a.cu_q[w.b];
+    w.lq = a.cu_q[w.b + 1] - w.q0;
+    w.k0 = a.cu_k[w.b];
+    w.lk = a.cu_k[w.b + 1] - w.k0;
+    const long long off = a.causal == 2 ? w.lk - w.lq : 0;
+    const int wl = a.window_left;
+    long long lo, hi;
+    if (!DQ) {
+        // queries that see a key of this tile: i >= j - off (causal),
+        // i <= j - off + window_left (window)
+        const int j_lo = w.t * kOwn, j_hi = min(w.lk, j_lo + kOwn);
+        lo = a.causal ? max(0ll, j_lo - off) : 0;
+        hi = w.lq - 1;
+        if (wl >= 0)
+            hi = min(hi, static_cast<long long>(j_hi) - 1 - off + wl);
+    } else {
+        // keys some row of this tile sees: j <= i + off (causal), j >= i + off
+        // - window_left (window)
+        const int i_lo = w.t * kOwn, i_hi = min(w.lq, i_lo + kOwn);
+        lo = (a.causal && wl >= 0) ? max(0ll, i_lo + off - wl) : 0;
+        hi = w.lk - 1;
+        if (a.causal)
+            hi = min(hi, static_cast<long long>(i_hi) - 1 + off);
+    }
+    w.first = lo <= hi ? static_cast<int>(lo / STEP) : 0;
+    w.n_blk = lo <= hi ? static_cast<int>(hi / STEP) + 1 - w.first : 0;
+    w.n_steps = DQ ? w.n_blk : w.n_blk * (a.num_heads / a.num_kv_heads);
+    return w;
+}
+
+// Persistent CTAs, one per SM, take units from an atomic counter.  Warp 0
+// loads (the unit's own 128-row tiles once, the streamed tiles per step),
+// warp 1 issues the MMAs, warps 4-11 do the elementwise work: warp w owns
+// TMEM lanes (own rows) 32 (w % 4) .. +31 and, of each step's STEP streamed
+// rows, the half g = (w - 4) / 4.
 //
-// Per step s (query head hq, query block qb), buffer x = s % 2, ring stage
-// st = s % NSTAGE:
-//   TMA:  [q_empty(st)] Q, dO rows -> stage st (q_full)
-//   MMA:  [q_full(st)] S^T_x = K Q^T, dP^T_x = V dO^T -> s_full(x);
-//         [p_full(x') of step s - 1] dV += P^T dO, dK += dS^T Q of step s - 1
-//         -> q_empty(st'), the buffer then free for step s + 1
-//   math: [s_full(x)] P^T = 2^(s scale log2e - lse log2e) (masked: 0),
-//         dS^T = P^T (dP^T - Delta) -> bf16 over S^T_x / dP^T_x -> p_full(x)
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdArgs a)
+// dK/dV kernel (DQ false): own = K, V of a key tile; a step is a block of
+// STEP queries of one query head of the group; per step
+//   MMA:  S^T = K Q^T, dP^T = V dO^T -> buffer x (s_full(x));
+//         then, for the previous step: dV += P^T dO, dK += dS^T Q
+//   math: P^T = 2^(s scale log2e - lse log2e) (masked: 0), dS^T = P^T (dP^T -
+//         Delta) -> bf16 over S^T / dP^T (p_full(x))
+// dQ kernel (DQ true): own = Q, dO of a query tile; a step is a block of
+// STEP keys; S = Q K^T, dP = dO V^T; dS (over dP); dQ += dS K.
+//
+// Across units nothing restarts: the step counter (ring stage, TMEM buffer
+// and their barrier phases) runs on, the next unit's own tiles load as soon
+// as the last score products of the current one have read the old ones, and
+// the next unit's first scores run during the current unit's epilogue; only
+// its first accumulating product waits for the epilogue (epi_done) to have
+// read the accumulators.
+template <int D, bool DQ>
+__global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a)
 {
     using C = BwdCfg<D>;
     constexpr int DB = C::DB, NSTAGE = C::NSTAGE, STEP = C::STEP, NC = C::NC;
-    constexpr int DH = C::DKV / 2;                // dK, dV columns per math thread
+    constexpr int NACC = DQ ? D : C::DKV;        // accumulator columns (each)
+    constexpr int DH = NACC / 2;                  // accumulator columns per math thread
+    constexpr uint32_t BUF = DQ ? C::Q_BUF : C::KV_BUF;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
+    __shared__ BwdUnit s_unit[2];
 
     if (*a.status != VFA_OK)
         return;
     const int B = a.batch, H = a.num_heads, Hkv = a.num_kv_heads;
-    // the column halves of a key tile are neighbours in launch order (their
-    // Q / dO reads meet in L2)
-    const int gt = blockIdx.x / C::DSPLIT, dh = blockIdx.x % C::DSPLIT, kh = blockIdx.y;
-    if (gt >= a.ktile_start[B])
-        return;
-    const int b = owner_of(a.ktile_start, B, gt), kt = gt - a.ktile_start[b];
-    const int q0 = a.cu_q[b], lq = a.cu_q[b + 1] - q0;
-    const int k0 = a.cu_k[b], lk = a.cu_k[b + 1] - k0;
-    const long long off = a.causal == 2 ? lk - lq : 0;
-    const int wl = a.window_left;
-    const int j_lo = kt * kOwn, j_hi = min(lk, j_lo + kOwn);
-    // query rows that see a key of this tile: i >= j - off (causal) and
-    // i <= j - off + window_left (window)
-    long long i_min = a.causal ? max(0ll, j_lo - off) : 0;
-    long long i_max = lq - 1;
-    if (wl >= 0)
-        i_max = min(i_max, static_cast<long long>(j_hi) - 1 - off + wl);
-    const int qb0 = i_min <= i_max ? static_cast<int>(i_min / STEP) : 0;
-    const int n_qb = i_min <= i_max ? static_cast<int>(i_max / STEP) + 1 - qb0 : 0;
-    const int group = H / Hkv;
-    const int n_steps = n_qb * group;
+    const int tiles = DQ ? a.qtile_start[B] : a.ktile_start[B];
+    int32_t *counter = a.status + (DQ ? 2 : 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;
     const int half = warp >= kFirstMathWarp ? (warp - kFirstMathWarp) >> 2 : 0;
-    const int r = quarter * 32 + lane;            // key row of math threads
-    const int j = j_lo + r;
-    __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(a.dk);
-    __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(a.dv);
-
-    if (n_steps == 0) {
-        // no query sees these keys: zero gradients
-        if (warp >= kFirstMathWarp && j < lk) {
-            const size_t row =
-                (static_cast<size_t>(k0 + j) * Hkv + kh) * D + dh * C::DKV + half * DH;
-#pragma unroll
-            for (int d = 0; d < DH; d += 8) {
-                *reinterpret_cast<uint4 *>(dk + row + d) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(dv + row + d) = make_uint4(0, 0, 0, 0);
-            }
-        }
-        return;
-    }
+    const int r = quarter * 32 + lane;            // own row of math threads
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t sK = base, sV = sK + C::OWN_BYTES;
-    const uint32_t sRing = sV + C::OWN_BYTES;                 // stage st: Q, then dO
-    const uint32_t sStat = sRing + NSTAGE * C::STAGE_BYTES;  // per math warp: -lse2, Delta
+    const uint32_t sOwn0 = base, sOwn1 = sOwn0 + C::OWN_BYTES;     // K, V  /  Q, dO
+    const uint32_t sRing = sOwn1 + C::OWN_BYTES;                    // stage: Q, dO  /  K, V
+    const uint32_t sStat = sRing + NSTAGE * C::STAGE_BYTES;         // per math warp: nl, -Delta
     const uint32_t bars = sStat + kMathWarps * 256;
-    auto q_full = [&](int st) { return bars + 8u * st; };
-    auto q_empty = [&](int st) { return bars + 8u * (NSTAGE + st); };
+    auto ring_full = [&](int st) { return bars + 8u * st; };
+    auto ring_empty = [&](int st) { return bars + 8u * (NSTAGE + st); };
     auto s_full = [&](int x) { return bars + 8u * (2 * NSTAGE + x); };
     auto p_full = [&](int x) { return bars + 8u * (2 * NSTAGE + 2 + x); };
-    const uint32_t bar_kv = bars + 8u * (2 * NSTAGE + 4);
-    const uint32_t bar_done = bars + 8u * (2 * NSTAGE + 5);
-    const uint32_t bar_drain = bars + 8u * (2 * NSTAGE + 6);
-    auto stage_q = [&](int st) { return sRing + st * C::STAGE_BYTES; };
-    auto stage_do = [&](int st) { return sRing + st * C::STAGE_BYTES + C::STEP_BYTES; };
+    auto unit_full = [&](int x) { return bars + 8u * (2 * NSTAGE + 4 + x); };
+    auto unit_empty = [&](int x) { return bars + 8u * (2 * NSTAGE + 6 + x); };
+    const uint32_t own_full = bars + 8u * (2 * NSTAGE + 8);
+    const uint32_t own_empty = bars + 8u * (2 * NSTAGE + 9);
+    const uint32_t acc_done = bars + 8u * (2 * NSTAGE + 10);
+    const uint32_t epi_done = bars + 8u * (2 * NSTAGE + 11);
+    const uint32_t drain_bar = bars + 8u * (2 * NSTAGE + 12);
+    auto stage0 = [&](int st) { return sRing + st * C::STAGE_BYTES; };
+    auto stage1 = [&](int st) { return sRing + st * C::STAGE_BYTES + C::STEP_BYTES; };
     volatile int *abort = &s_abort;
 
     if (tid == 0) {
         s_abort = 0;
         for (int st = 0; st < NSTAGE; ++st) {
-            mbar_init(q_full(st), 1);
-            mbar_init(q_empty(st), 1);
+            mbar_init(ring_full(st), 1);
+            mbar_init(ring_empty(st), 1);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(s_full(x), 1);
             mbar_init(p_full(x), kMathThreads);
+            mbar_init(unit_full(x), 1);
+            mbar_init(unit_empty(x), 1 + kMathWarps);
         }
-        mbar_init(bar_kv, 1);
-        mbar_init(bar_done, 1);
-        mbar_init(bar_drain, 1);
+        mbar_init(own_full, 1);
+        mbar_init(own_empty, 1);
+        mbar_init(acc_done, 1);
+        mbar_init(epi_done, kMathThreads);
+        mbar_init(drain_bar, 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -526,9 +585,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = s_tmem_base;
 
-    // step s -> (query head, query block)
-    auto step_hq = [&](int s) { return kh * group + s / n_qb; };
-    auto step_qb = [&](int s) { return qb0 + s % n_qb; };
+    // Consumers take unit n from the ring; false at the end (or on abort).
+    auto take_unit = [&](uint32_t n, BwdUnit &w) -> bool {
+        if (!mbar_wait(unit_full(n & 1), (n >> 1) & 1u, abort))
+            return false;
+        w = s_unit[n & 1];
+        return w.valid;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
@@ -537,26 +600,53 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             tma_prefetch_map(&a.tm_k);
             tma_prefetch_map(&a.tm_v);
             tma_prefetch_map(&a.tm_do);
-            mbar_arrive_expect_tx(bar_kv, 2 * C::OWN_BYTES);
-            load_rows<DB, STEP>(sK, &a.tm_k, bar_kv, kh, k0 + j_lo, kOwn);
-            load_rows<DB, STEP>(sV, &a.tm_v, bar_kv, kh, k0 + j_lo, kOwn);
-            int s = 0;
-            for (; s < n_steps; ++s) {
-                const int st = s % NSTAGE;
-                if (!mbar_wait(q_empty(st), ((s / NSTAGE) & 1u) ^ 1u, abort))
+            const CUtensorMap *own0 = DQ ? &a.tm_q : &a.tm_k, *own1 = DQ ? &a.tm_do : &a.tm_v;
+            const CUtensorMap *str0 = DQ ? &a.tm_k : &a.tm_q, *str1 = DQ ? &a.tm_v : &a.tm_do;
+            uint32_t g = 0, owns = 0;
+            bool ok = true;
+            for (uint32_t n = 0; ok; ++n) {
+                if (!mbar_wait(unit_empty(n & 1), ((n >> 1) & 1u) ^ 1u, abort))
                     break;
-                mbar_arrive_expect_tx(q_full(st), C::STAGE_BYTES);
-                const int row = q0 + step_qb(s) * STEP, hq = step_hq(s);
-                load_rows<DB, STEP>(stage_q(st), &a.tm_q, q_full(st), hq, row, STEP);
-                load_rows<DB, STEP>(stage_do(st), &a.tm_do, q_full(st), hq, row, STEP);
+                const BwdUnit w = decode_unit<D, DQ>(a, atomicAdd(counter, 1), tiles);
+                s_unit[n & 1] = w;
+                mbar_arrive(unit_full(n & 1));
+                if (!w.valid)
+                    break;
+                if (w.n_steps == 0)
+                    continue;
+                // the previous unit's score products have read the own tiles
+                if (!mbar_wait(own_empty, (owns & 1u) ^ 1u, abort))
+                    break;
+                mbar_arrive_expect_tx(own_full, 2 * C::OWN_BYTES);
+                const int own_row = (DQ ? w.q0 : w.k0) + w.t * kOwn;
+                load_rows<DB, STEP>(sOwn0, own0, own_full, w.head, own_row, kOwn);
+                load_rows<DB, STEP>(sOwn1, own1, own_full, w.head, own_row, kOwn);
+                ++owns;
+                const int group = H / Hkv;
+                for (int s = 0; s < w.n_steps; ++s, ++g) {
+                    const int st = g % NSTAGE;
+                    if (!mbar_wait(ring_empty(st), ((g / NSTAGE) & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(ring_full(st), C::STAGE_BYTES);
+                    // dK/dV: step s = (query head of the group, query block);
+                    // dQ: key block of the head's kv head
+                    const int blk = w.first + (DQ ? s : s % w.n_blk);
+                    const int row = (DQ ? w.k0 : w.q0) + blk * STEP;
+                    const int head = DQ ? w.head / group : w.head * group + s / w.n_blk;
+                    load_rows<DB, STEP>(stage0(st), str0, ring_full(st), head, row, STEP);
+                    load_rows<DB, STEP>(stage1(st), str1, ring_full(st), head, row, STEP);
+                }
             }
             if (*abort) {
-                // the last fill of each stage may still be in flight
-                mbar_wait_drain(bar_kv, 0);
+                // the last fill of each stage and of the own tiles may be in flight
+                if (owns > 0)
+                    mbar_wait_drain(own_full, (owns - 1) & 1u);
                 for (int st = 0; st < NSTAGE; ++st) {
-                    const int fills = s / NSTAGE + (st < s % NSTAGE ? 1 : 0);
+                    const uint32_t fills = g / NSTAGE + (static_cast<uint32_t>(st) < g % NSTAGE ? 1u : 0u);
                     if (fills > 0)
-                        mbar_wait_drain(q_full(st), (fills - 1) & 1u);
+                        mbar_wait_drain(ring_full(st), (fills - 1) & 1u);
                 }
             }
         }
@@ -564,339 +654,219 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         // ------------------------------------------------------------ MMA
         // All 32 lanes run this loop on warp-uniform values; one elected lane
         // issues each MMA and commit.
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar_kv, 0, abort));
-        for (int s = 0; s <= n_steps && ok; ++s) {
-            if (s < n_steps) {
-                const int st = s % NSTAGE, x = s & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(q_full(st), (s / NSTAGE) & 1u, abort))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // buffer x was last read by step s - 2's products, issued earlier
-                const uint32_t buf = tmem + C::KV_BUF + C::BUF_STRIDE * x;
-                issue_scores<D, STEP>(buf, sK, stage_q(st), C::IDESC_T);
-                issue_scores<D, STEP>(buf + STEP, sV, stage_do(st), C::IDESC_T);
-                mma_commit_w(s_full(x));
+        uint32_t g = 0, owns = 0, units = 0;
+        bool ok = true;
+        for (uint32_t n = 0; ok; ++n) {
+            BwdUnit w;
+            const bool more = take_unit(n, w);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(unit_empty(n & 1));
+            if (!more)
+                break;
+            if (w.n_steps == 0)
+                continue;
+            if (!__all_sync(0xffffffffu, mbar_wait(own_full, owns & 1u, abort))) {
+                ok = false;
+                break;
             }
-            if (s >= 1) {
-                const int sp = s - 1, stp = sp % NSTAGE, xp = sp & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(p_full(xp), (sp >> 1) & 1u, abort))) {
-                    ok = false;
-                    break;
+            ++owns;
+            // this unit's column half of the streamed tiles' columns (dK/dV at
+            // head_dim 256): DKV / 64 column blocks on
+            const uint32_t col0 = DQ ? 0u : w.dh * (C::DKV / 64) * (STEP * 128);
+            for (int s = 0; s <= w.n_steps && ok; ++s) {
+                if (s < w.n_steps) {
+                    const uint32_t gs = g + s;
+                    const int st = gs % NSTAGE, x = gs & 1;
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(ring_full(st), (gs / NSTAGE) & 1u, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // buffer x was last read by step gs - 2's products, issued earlier
+                    const uint32_t buf = tmem + BUF + C::BUF_STRIDE * x;
+                    issue_scores<D, STEP>(buf, sOwn0, stage0(st), C::IDESC_T);
+                    issue_scores<D, STEP>(buf + STEP, sOwn1, stage1(st), C::IDESC_T);
+                    mma_commit_w(s_full(x));
+                    if (s == w.n_steps - 1)
+                        mma_commit_w(own_empty);        // own tiles free once these complete
                 }
-                tc_fence_after();
-                const uint32_t buf = tmem + C::KV_BUF + C::BUF_STRIDE * xp;
-                // this CTA's column half of dO and Q: DKV / 64 column blocks on
-                const uint32_t col0 = dh * (C::DKV / 64) * (STEP * 128);
-                issue_accumulate<STEP>(tmem + C::COL_DV, buf, stage_do(stp) + col0, C::IDESC_KV,
-                                       sp == 0);
-                issue_accumulate<STEP>(tmem + C::COL_DK, buf + STEP, stage_q(stp) + col0,
-                                       C::IDESC_KV, sp == 0);
-                mma_commit_w(q_empty(stp));
+                if (s >= 1) {
+                    const uint32_t gp = g + s - 1;
+                    const int stp = gp % NSTAGE, xp = gp & 1;
+                    if (!__all_sync(0xffffffffu, mbar_wait(p_full(xp), (gp >> 1) & 1u, abort)) ||
+                        (s == 1 && !__all_sync(0xffffffffu,
+                                               mbar_wait(epi_done, (units & 1u) ^ 1u, abort)))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t buf = tmem + BUF + C::BUF_STRIDE * xp;
+                    if (DQ) {
+                        issue_accumulate<STEP>(tmem + C::COL_DQ, buf + STEP, stage0(stp),
+                                               C::IDESC_DQ, s == 1);
+                    } else {
+                        issue_accumulate<STEP>(tmem + C::COL_DV, buf, stage1(stp) + col0,
+                                               C::IDESC_KV, s == 1);
+                        issue_accumulate<STEP>(tmem + C::COL_DK, buf + STEP, stage0(stp) + col0,
+                                               C::IDESC_KV, s == 1);
+                    }
+                    mma_commit_w(ring_empty(stp));
+                }
             }
+            if (!ok)
+                break;
+            mma_commit_w(acc_done);
+            g += w.n_steps;
+            ++units;
         }
-        if (ok)
-            mma_commit_w(bar_done);
-        else {
-            mma_commit_w(bar_drain);
-            mbar_wait_drain(bar_drain, 0);
+        if (!ok || *abort) {
+            mma_commit_w(drain_bar);
+            mbar_wait_drain(drain_bar, 0);
         }
     } else if (warp >= kFirstMathWarp) {
-        // ------------------------------------------------------------ P^T, dS^T
+        // ------------------------------------------------------------ elementwise, epilogue
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t wstat = sStat + (warp - kFirstMathWarp) * 256;   // 32 nl, 32 -Delta
+        const uint32_t wstat = sStat + (warp - kFirstMathWarp) * 256;   // NC nl, NC -Delta
         float *stat = reinterpret_cast<float *>(smem_raw + (wstat - raw));
         const float scale_log2 = a.scale_log2;
+        uint32_t g = 0, units = 0;
         bool ok = true;
-        for (int s = 0; s < n_steps && ok; ++s) {
-            const int x = s & 1, hq = step_hq(s), qb = step_qb(s);
-            const int i_base = qb * STEP + half * NC;   // this thread's first query column
-            {
-                const int i = i_base + lane;
-                const bool in = lane < NC && i < lq;
-                const size_t row = static_cast<size_t>(q0 + i) * H + hq;
-                const float nl = in ? -a.lse[row] * kLog2e : 0.f;
-                const float nd = in ? -a.delta[row] : 0.f;
-                __syncwarp();
-                stat[lane] = nl;
-                stat[32 + lane] = nd;
-                __syncwarp();
+        __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(a.dq);
+        __nv_bfloat16 *dk = static_cast<__nv_bfloat16 *>(a.dk);
+        __nv_bfloat16 *dv = static_cast<__nv_bfloat16 *>(a.dv);
+        for (uint32_t n = 0; ok; ++n) {
+            BwdUnit w;
+            const bool more = take_unit(n, w);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(unit_empty(n & 1));
+            if (!more)
+                break;
+            const long long off = a.causal == 2 ? w.lk - w.lq : 0;
+            const int wl = a.window_left;
+            const int own = w.t * kOwn + r;       // this thread's own row (key or query)
+            // where this thread's accumulator columns go
+            size_t row_out;
+            if (DQ)
+                row_out = (static_cast<size_t>(w.q0 + own) * H + w.head) * D + half * DH;
+            else
+                row_out = (static_cast<size_t>(w.k0 + own) * Hkv + w.head) * D + w.dh * C::DKV +
+                          half * DH;
+            const bool own_valid = DQ ? own < w.lq : own < w.lk;
+            if (w.n_steps == 0) {
+                // no key / query pairs: zero gradients
+                if (own_valid) {
+#pragma unroll
+                    for (int d = 0; d < DH; d += 8) {
+                        if (DQ) {
+                            *reinterpret_cast<uint4 *>(dq + row_out + d) = make_uint4(0, 0, 0, 0);
+                        } else {
+                            *reinterpret_cast<uint4 *>(dk + row_out + d) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(dv + row_out + d) = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
+                continue;
             }
-            // a step every (key, query) pair of which is visible needs no mask
-            const long long qlo = static_cast<long long>(qb) * STEP;
-            const bool full = j_lo + kOwn <= lk && qlo + STEP <= lq &&
-                              (!a.causal || j_lo + kOwn - 1 <= qlo + off) &&
-                              (wl < 0 || j_lo >= qlo + STEP - 1 + off - wl);
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full(x), (s >> 1) & 1u, abort));
+            // dQ: this thread's row constants
+            float nl_row = 0.f, nd_row = 0.f;
+            if (DQ && own_valid) {
+                const size_t srow = static_cast<size_t>(w.q0 + own) * H + w.head;
+                nl_row = -a.lse[srow] * kLog2e;
+                nd_row = -a.delta[srow];
+            }
+            const int group = H / Hkv;
+            for (int s = 0; s < w.n_steps && ok; ++s) {
+                const uint32_t gs = g + s;
+                const int x = gs & 1;
+                const int blk = w.first + (DQ ? s : s % w.n_blk);
+                const int c_base = blk * STEP + half * NC;   // this thread's first streamed column
+                if (!DQ) {
+                    // -lse log2(e) and -Delta of this thread's query columns
+                    const int hq = w.head * group + s / w.n_blk;
+                    const int i = c_base + lane;
+                    const bool in = lane < NC && i < w.lq;
+                    const size_t srow = static_cast<size_t>(w.q0 + i) * H + hq;
+                    const float nl = in ? -a.lse[srow] * kLog2e : 0.f;
+                    const float nd = in ? -a.delta[srow] : 0.f;
+                    __syncwarp();
+                    stat[lane] = nl;
+                    stat[32 + lane] = nd;
+                    __syncwarp();
+                }
+                // a step every (own, streamed) pair of which is visible needs no mask
+                const long long slo = static_cast<long long>(blk) * STEP;
+                const long long olo = static_cast<long long>(w.t) * kOwn;
+                bool full;
+                if (DQ)
+                    full = slo + STEP <= w.lk && olo + kOwn <= w.lq &&
+                           (!a.causal || slo + STEP - 1 <= olo + off) &&
+                           (wl < 0 || slo >= olo + kOwn - 1 + off - wl);
+                else
+                    full = olo + kOwn <= w.lk && slo + STEP <= w.lq &&
+                           (!a.causal || olo + kOwn - 1 <= slo + off) &&
+                           (wl < 0 || olo >= slo + STEP - 1 + off - wl);
+                ok = __all_sync(0xffffffffu, mbar_wait(s_full(x), (gs >> 1) & 1u, abort));
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint32_t st_addr = tmem + lane_addr + BUF + C::BUF_STRIDE * x + half * NC;
+                uint32_t sr[NC], dr[NC];
+                ld_cols<NC>(st_addr, sr);
+                ld_cols<NC>(st_addr + STEP, dr);
+                wait_cols<NC>(sr, dr);
+                uint32_t dk2[NC / 2];
+                if (DQ) {
+                    if (full) {
+                        query_row_grads<false, NC>(sr, dr, scale_log2, nl_row, nd_row, 0, NC, dk2);
+                    } else {
+                        int lo, hi;
+                        query_row_span(own, c_base, w.lk, w.lq, a.causal, wl, off, &lo, &hi);
+                        query_row_grads<true, NC>(sr, dr, scale_log2, nl_row, nd_row, lo, hi, dk2);
+                    }
+                } else {
+                    uint32_t pk[NC / 2];
+                    if (full) {
+                        key_row_grads<false, NC>(sr, dr, scale_log2, wstat, 0, NC, pk, dk2);
+                    } else {
+                        int lo, hi;
+                        key_row_span(own, c_base, w.lk, w.lq, a.causal, wl, off, &lo, &hi);
+                        key_row_grads<true, NC>(sr, dr, scale_log2, wstat, lo, hi, pk, dk2);
+                    }
+                    // P^T (bf16 pairs) over the first half of this thread's own S^T columns
+                    st_cols<NC / 2>(st_addr, pk);
+                }
+                // dS (bf16 pairs) over the first half of this thread's own dP columns
+                st_cols<NC / 2>(st_addr + STEP, dk2);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(p_full(x));
+            }
+            if (!ok)
+                break;
+            ok = __all_sync(0xffffffffu, mbar_wait(acc_done, units & 1u, abort));
             if (!ok)
                 break;
             tc_fence_after();
-            const uint32_t st_addr =
-                tmem + lane_addr + C::KV_BUF + C::BUF_STRIDE * x + half * NC;
-            uint32_t sr[NC], dr[NC];
-            ld_cols<NC>(st_addr, sr);
-            ld_cols<NC>(st_addr + STEP, dr);
-            wait_cols<NC>(sr, dr);
-            uint32_t pk[NC / 2], dk2[NC / 2];
-            if (full) {
-                key_row_grads<false, NC>(sr, dr, scale_log2, wstat, 0, NC, pk, dk2);
-            } else {
-                int lo, hi;
-                key_row_span(j, i_base, lk, lq, a.causal, wl, off, &lo, &hi);
-                key_row_grads<true, NC>(sr, dr, scale_log2, wstat, lo, hi, pk, dk2);
-            }
-            // P^T, dS^T (bf16 pairs) over the first half of this thread's own
-            // S^T / dP^T columns, which only this warp reads
-            st_cols<NC / 2>(st_addr, pk);
-            st_cols<NC / 2>(st_addr + STEP, dk2);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(p_full(x));
-        }
-        if (ok)
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, abort));
-        if (ok) {
-            // dV and dK (scaled) rows of this key tile, this thread's column half
-            tc_fence_after();
-            const size_t row =
-                (static_cast<size_t>(k0 + j) * Hkv + kh) * D + dh * C::DKV + half * DH;
 #pragma unroll 1
             for (int cb = 0; cb < DH; cb += 32) {
-                store_row32(tmem + lane_addr + C::COL_DV + half * DH + cb, 1.f, dv + row + cb,
-                            j < lk);
-                store_row32(tmem + lane_addr + C::COL_DK + half * DH + cb, a.scale,
-                            dk + row + cb, j < lk);
-            }
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (*abort && tid == 0)
-        atomicCAS(a.status, VFA_OK, VFA_ERR_TIMEOUT);
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
-    }
-}
-
-// ------------------------------------------------------------ dQ
-
-// Warp 0 loads (Q, dO once; K, V per step), warp 1 issues the MMAs, warps
-// 4-11 form dS: warp w owns TMEM lanes (query rows) 32 (w % 4) .. +31 and, of
-// each step's 64 keys, the 32 at 32 g, g = (w - 4) / 4.
-//
-// Per step s (key block kb), buffer x = s % 2, ring stage st = s % NSTAGE:
-//   TMA:  [kv_empty(st)] K, V rows -> stage st (kv_full)
-//   MMA:  [kv_full(st)] S_x = Q K^T, dP_x = dO V^T -> s_full(x);
-//         [p_full(x') of step s - 1] dQ += dS K of step s - 1 -> kv_empty(st')
-//   math: [s_full(x)] dS = 2^(s scale log2e - lse log2e) (dP - Delta)
-//         (masked: 0) -> bf16 over dP_x -> p_full(x)
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdArgs a)
-{
-    using C = BwdCfg<D>;
-    constexpr int DB = C::DB, NSTAGE = C::NSTAGE, STEP = C::STEP, NC = C::NC;
-    constexpr int DH = D / 2;
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ uint32_t s_tmem_base;
-    __shared__ int s_abort;
-
-    if (*a.status != VFA_OK)
-        return;
-    const int B = a.batch, H = a.num_heads, Hkv = a.num_kv_heads;
-    const int n_tiles = a.qtile_start[B];
-    // the grid runs the tiles of each sequence last-first (the longest key
-    // ranges of a causal sequence first)
-    const int gt = n_tiles - 1 - static_cast<int>(blockIdx.x);
-    if (gt < 0)
-        return;
-    const int h = blockIdx.y, kh = h / (H / Hkv);
-    const int b = owner_of(a.qtile_start, B, gt), qt = gt - a.qtile_start[b];
-    const int q0 = a.cu_q[b], lq = a.cu_q[b + 1] - q0;
-    const int k0 = a.cu_k[b], lk = a.cu_k[b + 1] - k0;
-    const long long off = a.causal == 2 ? lk - lq : 0;
-    const int wl = a.window_left;
-    const int i_lo = qt * kOwn, i_hi = min(lq, i_lo + kOwn);
-    // keys some row of this tile sees: j <= i + off (causal), j >= i + off -
-    // window_left (window)
-    long long j_min = (a.causal && wl >= 0) ? max(0ll, i_lo + off - wl) : 0;
-    long long j_max = lk - 1;
-    if (a.causal)
-        j_max = min(j_max, static_cast<long long>(i_hi) - 1 + off);
-    const int kb0 = j_min <= j_max ? static_cast<int>(j_min / STEP) : 0;
-    const int n_steps = j_min <= j_max ? static_cast<int>(j_max / STEP) + 1 - kb0 : 0;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3;
-    const int half = warp >= kFirstMathWarp ? (warp - kFirstMathWarp) >> 2 : 0;
-    const int r = quarter * 32 + lane;            // query row of math threads
-    const int i = i_lo + r;
-    __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(a.dq);
-    const size_t out_row = (static_cast<size_t>(q0 + i) * H + h) * D + half * DH;
-
-    if (n_steps == 0) {
-        // these rows see no key: zero gradient
-        if (warp >= kFirstMathWarp && i < lq) {
-#pragma unroll
-            for (int d = 0; d < DH; d += 8)
-                *reinterpret_cast<uint4 *>(dq + out_row + d) = make_uint4(0, 0, 0, 0);
-        }
-        return;
-    }
-
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t sQ = base, sDO = sQ + C::OWN_BYTES;
-    const uint32_t sRing = sDO + C::OWN_BYTES;                 // stage st: K, then V
-    const uint32_t bars = sRing + NSTAGE * C::STAGE_BYTES + kMathWarps * 256;
-    auto kv_full = [&](int st) { return bars + 8u * st; };
-    auto kv_empty = [&](int st) { return bars + 8u * (NSTAGE + st); };
-    auto s_full = [&](int x) { return bars + 8u * (2 * NSTAGE + x); };
-    auto p_full = [&](int x) { return bars + 8u * (2 * NSTAGE + 2 + x); };
-    const uint32_t bar_q = bars + 8u * (2 * NSTAGE + 4);
-    const uint32_t bar_done = bars + 8u * (2 * NSTAGE + 5);
-    const uint32_t bar_drain = bars + 8u * (2 * NSTAGE + 6);
-    auto stage_k = [&](int st) { return sRing + st * C::STAGE_BYTES; };
-    auto stage_v = [&](int st) { return sRing + st * C::STAGE_BYTES + C::STEP_BYTES; };
-    volatile int *abort = &s_abort;
-
-    if (tid == 0) {
-        s_abort = 0;
-        for (int st = 0; st < NSTAGE; ++st) {
-            mbar_init(kv_full(st), 1);
-            mbar_init(kv_empty(st), 1);
-        }
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(s_full(x), 1);
-            mbar_init(p_full(x), kMathThreads);
-        }
-        mbar_init(bar_q, 1);
-        mbar_init(bar_done, 1);
-        mbar_init(bar_drain, 1);
-        fence_barrier_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(&s_tmem_base), C::TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = s_tmem_base;
-
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA
-        if (lane == 0) {
-            tma_prefetch_map(&a.tm_q);
-            tma_prefetch_map(&a.tm_k);
-            tma_prefetch_map(&a.tm_v);
-            tma_prefetch_map(&a.tm_do);
-            mbar_arrive_expect_tx(bar_q, 2 * C::OWN_BYTES);
-            load_rows<DB, STEP>(sQ, &a.tm_q, bar_q, h, q0 + i_lo, kOwn);
-            load_rows<DB, STEP>(sDO, &a.tm_do, bar_q, h, q0 + i_lo, kOwn);
-            int s = 0;
-            for (; s < n_steps; ++s) {
-                const int st = s % NSTAGE;
-                if (!mbar_wait(kv_empty(st), ((s / NSTAGE) & 1u) ^ 1u, abort))
-                    break;
-                mbar_arrive_expect_tx(kv_full(st), C::STAGE_BYTES);
-                const int row = k0 + (kb0 + s) * STEP;
-                load_rows<DB, STEP>(stage_k(st), &a.tm_k, kv_full(st), kh, row, STEP);
-                load_rows<DB, STEP>(stage_v(st), &a.tm_v, kv_full(st), kh, row, STEP);
-            }
-            if (*abort) {
-                mbar_wait_drain(bar_q, 0);
-                for (int st = 0; st < NSTAGE; ++st) {
-                    const int fills = s / NSTAGE + (st < s % NSTAGE ? 1 : 0);
-                    if (fills > 0)
-                        mbar_wait_drain(kv_full(st), (fills - 1) & 1u);
+                if (DQ) {
+                    store_row32(tmem + lane_addr + C::COL_DQ + half * DH + cb, a.scale,
+                                dq + row_out + cb, own_valid);
+                } else {
+                    store_row32(tmem + lane_addr + C::COL_DV + half * DH + cb, 1.f,
+                                dv + row_out + cb, own_valid);
+                    store_row32(tmem + lane_addr + C::COL_DK + half * DH + cb, a.scale,
+                                dk + row_out + cb, own_valid);
                 }
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, abort));
-        for (int s = 0; s <= n_steps && ok; ++s) {
-            if (s < n_steps) {
-                const int st = s % NSTAGE, x = s & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(kv_full(st), (s / NSTAGE) & 1u, abort))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t buf = tmem + C::Q_BUF + C::BUF_STRIDE * x;
-                issue_scores<D, STEP>(buf, sQ, stage_k(st), C::IDESC_T);
-                issue_scores<D, STEP>(buf + STEP, sDO, stage_v(st), C::IDESC_T);
-                mma_commit_w(s_full(x));
-            }
-            if (s >= 1) {
-                const int sp = s - 1, stp = sp % NSTAGE, xp = sp & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(p_full(xp), (sp >> 1) & 1u, abort))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                issue_accumulate<STEP>(tmem + C::COL_DQ,
-                                       tmem + C::Q_BUF + C::BUF_STRIDE * xp + STEP, stage_k(stp),
-                                       C::IDESC_DQ, sp == 0);
-                mma_commit_w(kv_empty(stp));
-            }
-        }
-        if (ok)
-            mma_commit_w(bar_done);
-        else {
-            mma_commit_w(bar_drain);
-            mbar_wait_drain(bar_drain, 0);
-        }
-    } else if (warp >= kFirstMathWarp) {
-        // ------------------------------------------------------------ dS
-        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        const float scale_log2 = a.scale_log2;
-        const size_t srow = static_cast<size_t>(q0 + i) * H + h;
-        const float nl = i < lq ? -a.lse[srow] * kLog2e : 0.f;
-        const float nd = i < lq ? -a.delta[srow] : 0.f;
-        bool ok = true;
-        for (int s = 0; s < n_steps && ok; ++s) {
-            const int x = s & 1;
-            const int j_base = (kb0 + s) * STEP + half * NC;   // this thread's first key column
-            const long long klo = static_cast<long long>(kb0 + s) * STEP;
-            const bool full = klo + STEP <= lk && i_lo + kOwn <= lq &&
-                              (!a.causal || klo + STEP - 1 <= i_lo + off) &&
-                              (wl < 0 || klo >= i_lo + kOwn - 1 + off - wl);
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full(x), (s >> 1) & 1u, abort));
-            if (!ok)
-                break;
-            tc_fence_after();
-            const uint32_t st_addr =
-                tmem + lane_addr + C::Q_BUF + C::BUF_STRIDE * x + half * NC;
-            uint32_t sr[NC], dr[NC];
-            ld_cols<NC>(st_addr, sr);
-            ld_cols<NC>(st_addr + STEP, dr);
-            wait_cols<NC>(sr, dr);
-            uint32_t dk2[NC / 2];
-            if (full) {
-                query_row_grads<false, NC>(sr, dr, scale_log2, nl, nd, 0, NC, dk2);
-            } else {
-                int lo, hi;
-                query_row_span(i, j_base, lk, lq, a.causal, wl, off, &lo, &hi);
-                query_row_grads<true, NC>(sr, dr, scale_log2, nl, nd, lo, hi, dk2);
-            }
-            // dS (bf16 pairs) over the first half of this thread's own dP columns
-            st_cols<NC / 2>(st_addr + STEP, dk2);
-            tmem_wait_st();
+            // the accumulators may be overwritten by the next unit's products
             tc_fence_before();
-            mbar_arrive(p_full(x));
-        }
-        if (ok)
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, abort));
-        if (ok) {
-            tc_fence_after();
-#pragma unroll 1
-            for (int cb = 0; cb < DH; cb += 32)
-                store_row32(tmem + lane_addr + C::COL_DQ + half * DH + cb, a.scale,
-                            dq + out_row + cb, i < lq);
+            mbar_arrive(epi_done);
+            g += w.n_steps;
+            ++units;
         }
     }
 
@@ -920,10 +890,10 @@ cudaError_t launch_bwd_d(const BwdArgs &a, int key_tile_bound, int q_tile_bound,
     if (e != cudaSuccess)
         return e;
     if (dev < 64 && !attr_done[dev]) {
-        if ((e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>,
+        if ((e = cudaFuncSetAttribute(bwd_main_kernel<D, false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(BwdCfg<D>::SMEM))) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(bwd_dq_kernel<D>,
+            (e = cudaFuncSetAttribute(bwd_main_kernel<D, true>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(BwdCfg<D>::SMEM))) != cudaSuccess)
             return e;
@@ -935,14 +905,19 @@ cudaError_t launch_bwd_d(const BwdArgs &a, int key_tile_bound, int q_tile_bound,
     bwd_delta_kernel<D><<<sm_count * 8, 256, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
-    if (key_tile_bound > 0) {
-        bwd_dkdv_kernel<D><<<dim3(key_tile_bound * BwdCfg<D>::DSPLIT, a.num_kv_heads), kThreads,
-                             BwdCfg<D>::SMEM, s>>>(a);
+    // persistent grids: one CTA per SM (fewer when there are fewer units)
+    const long long kv_units =
+        static_cast<long long>(key_tile_bound) * BwdCfg<D>::DSPLIT * a.num_kv_heads;
+    const long long q_units = static_cast<long long>(q_tile_bound) * a.num_heads;
+    if (kv_units > 0) {
+        bwd_main_kernel<D, false><<<static_cast<int>(std::min<long long>(kv_units, sm_count)),
+                                    kThreads, BwdCfg<D>::SMEM, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
-    if (q_tile_bound > 0) {
-        bwd_dq_kernel<D><<<dim3(q_tile_bound, a.num_heads), kThreads, BwdCfg<D>::SMEM, s>>>(a);
+    if (q_units > 0) {
+        bwd_main_kernel<D, true><<<static_cast<int>(std::min<long long>(q_units, sm_count)),
+                                   kThreads, BwdCfg<D>::SMEM, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
