@@ -64,7 +64,7 @@ template <int D>
 struct BwdCfg {
     static constexpr int DB = D / 64;                       // 128-byte column blocks per row
     static constexpr int STEP = bwd_step_rows(D);           // also the TMA box height
-    static constexpr int NC = STEP / 2;                     // step columns per math thread
+    static constexpr int NCH = STEP / 32;                   // 32-column chunks per step
     static constexpr int DSPLIT = D == 256 ? 2 : 1;
     static constexpr int DKV = D / DSPLIT;                  // dK / dV columns per CTA
     static constexpr uint32_t OWN_BYTES = kOwn * D * 2;     // a 128-row tile
@@ -81,7 +81,7 @@ struct BwdCfg {
     // buffer; own_full, own_empty, acc_done, epi_done, drain
     static constexpr int NUM_BARS = 2 * NSTAGE + 8 + 5;
     static constexpr size_t SMEM = 1024 + 2 * OWN_BYTES + NSTAGE * STAGE_BYTES +
-                                   kMathWarps * 256 + NUM_BARS * 8 + 64;
+                                   kMathWarps * 512 + NUM_BARS * 8 + 64;
     // S^T / dP^T (keys x STEP queries) and S / dP (queries x STEP keys): both K-major
     static constexpr uint32_t IDESC_T = idesc_bf16_f32(kOwn, STEP, false, false);
     // dV, dK (DKV columns) and dQ (D columns): A from TMEM, B (dO, Q or K rows) MN-major
@@ -342,18 +342,17 @@ __device__ __forceinline__ void issue_scores(uint32_t d_tmem, uint32_t a_buf, ui
 }
 
 // D += A B over K = STEP streamed rows: A (128 x STEP, bf16 pairs) in TMEM at
-// a_tmem, written by the two column halves of the math warps (half g's STEP/2
-// columns packed into the first STEP/4 of its own STEP/2 columns); B the
-// STEP-row tile in shared memory from column block b_buf on, MN-major.
+// a_tmem, written by the math warps in chunks of 32 columns (chunk c's 32
+// values packed into the first 16 of its own 32 columns); B the STEP-row tile
+// in shared memory from column block b_buf on, MN-major.
 template <int STEP>
 __device__ __forceinline__ void issue_accumulate(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_buf,
                                                  uint32_t idesc, bool first)
 {
-    constexpr int HALF = STEP / 2;
     const uint64_t b0 = sdesc_sw128(b_buf, STEP * 128, 1024);
 #pragma unroll
     for (int kk = 0; kk < STEP / 16; ++kk) {
-        const uint32_t a = a_tmem + HALF * (kk * 16 / HALF) + ((kk * 16) % HALF) / 2;
+        const uint32_t a = a_tmem + 32 * (kk >> 1) + 8 * (kk & 1);
         const uint64_t bo = (kk * 16 * 128) >> 4;
         if (kk == 0 && first)
             mma_ts_w<0>(d_tmem, a, b0 + bo, idesc);
@@ -494,8 +493,8 @@ __device__ BwdUnit decode_unit(const BwdArgs &a, int u, int tiles)
 // Persistent CTAs, one per SM, take units from an atomic counter.  Warp 0
 // loads (the unit's own 128-row tiles once, the streamed tiles per step),
 // warp 1 issues the MMAs, warps 4-11 do the elementwise work: warp w owns
-// TMEM lanes (own rows) 32 (w % 4) .. +31 and, of each step's STEP streamed
-// rows, the half g = (w - 4) / 4.
+// TMEM lanes (own rows) 32 (w % 4) .. +31; warpgroup g = (w - 4) / 4 takes
+// the steps held in TMEM buffer g, all STEP columns of each.
 //
 // dK/dV kernel (DQ false): own = K, V of a key tile; a step is a block of
 // STEP queries of one query head of the group; per step
@@ -516,7 +515,7 @@ template <int D, bool DQ>
 __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a)
 {
     using C = BwdCfg<D>;
-    constexpr int DB = C::DB, NSTAGE = C::NSTAGE, STEP = C::STEP, NC = C::NC;
+    constexpr int DB = C::DB, NSTAGE = C::NSTAGE, STEP = C::STEP, NCH = C::NCH;
     constexpr int NACC = DQ ? D : C::DKV;        // accumulator columns (each)
     constexpr int DH = NACC / 2;                  // accumulator columns per math thread
     constexpr uint32_t BUF = DQ ? C::Q_BUF : C::KV_BUF;
@@ -541,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     const uint32_t sOwn0 = base, sOwn1 = sOwn0 + C::OWN_BYTES;     // K, V  /  Q, dO
     const uint32_t sRing = sOwn1 + C::OWN_BYTES;                    // stage: Q, dO  /  K, V
     const uint32_t sStat = sRing + NSTAGE * C::STAGE_BYTES;         // per math warp: nl, -Delta
-    const uint32_t bars = sStat + kMathWarps * 256;
+    const uint32_t bars = sStat + kMathWarps * 512;
     auto ring_full = [&](int st) { return bars + 8u * st; };
     auto ring_empty = [&](int st) { return bars + 8u * (NSTAGE + st); };
     auto s_full = [&](int x) { return bars + 8u * (2 * NSTAGE + x); };
@@ -565,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(s_full(x), 1);
-            mbar_init(p_full(x), kMathThreads);
+            mbar_init(p_full(x), kMathThreads / 2);    // buffer x's warpgroup
             mbar_init(unit_full(x), 1);
             mbar_init(unit_empty(x), 1 + kMathWarps);
         }
@@ -728,7 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     } else if (warp >= kFirstMathWarp) {
         // ------------------------------------------------------------ elementwise, epilogue
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t wstat = sStat + (warp - kFirstMathWarp) * 256;   // NC nl, NC -Delta
+        // per warp and 32-column chunk: 32 nl, then 32 -Delta
+        const uint32_t wstat = sStat + (warp - kFirstMathWarp) * 512;
         float *stat = reinterpret_cast<float *>(smem_raw + (wstat - raw));
         const float scale_log2 = a.scale_log2;
         uint32_t g = 0, units = 0;
@@ -778,26 +778,29 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
                 nd_row = -a.delta[srow];
             }
             const int group = H / Hkv;
-            for (int s = 0; s < w.n_steps && ok; ++s) {
+            // The two warpgroups take the steps in turn (warpgroup x the steps
+            // in TMEM buffer x), each doing all STEP columns of its rows in
+            // chunks of 32, so two steps are in the works at once.
+            for (int s = (half - static_cast<int>(g & 1u)) & 1; s < w.n_steps && ok; s += 2) {
                 const uint32_t gs = g + s;
                 const int x = gs & 1;
                 const int blk = w.first + (DQ ? s : s % w.n_blk);
-                const int c_base = blk * STEP + half * NC;   // this thread's first streamed column
+                const int c0 = blk * STEP;                 // the step's first streamed column
                 if (!DQ) {
-                    // -lse log2(e) and -Delta of this thread's query columns
+                    // -lse log2(e) and -Delta of the step's query columns
                     const int hq = w.head * group + s / w.n_blk;
-                    const int i = c_base + lane;
-                    const bool in = lane < NC && i < w.lq;
-                    const size_t srow = static_cast<size_t>(w.q0 + i) * H + hq;
-                    const float nl = in ? -a.lse[srow] * kLog2e : 0.f;
-                    const float nd = in ? -a.delta[srow] : 0.f;
                     __syncwarp();
-                    stat[lane] = nl;
-                    stat[32 + lane] = nd;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        const int i = c0 + 32 * c + lane;
+                        const size_t srow = static_cast<size_t>(w.q0 + i) * H + hq;
+                        stat[64 * c + lane] = i < w.lq ? -a.lse[srow] * kLog2e : 0.f;
+                        stat[64 * c + 32 + lane] = i < w.lq ? -a.delta[srow] : 0.f;
+                    }
                     __syncwarp();
                 }
                 // a step every (own, streamed) pair of which is visible needs no mask
-                const long long slo = static_cast<long long>(blk) * STEP;
+                const long long slo = static_cast<long long>(c0);
                 const long long olo = static_cast<long long>(w.t) * kOwn;
                 bool full;
                 if (DQ)
@@ -812,34 +815,41 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
                 if (!ok)
                     break;
                 tc_fence_after();
-                const uint32_t st_addr = tmem + lane_addr + BUF + C::BUF_STRIDE * x + half * NC;
-                uint32_t sr[NC], dr[NC];
-                ld_cols<NC>(st_addr, sr);
-                ld_cols<NC>(st_addr + STEP, dr);
-                wait_cols<NC>(sr, dr);
-                uint32_t dk2[NC / 2];
-                if (DQ) {
-                    if (full) {
-                        query_row_grads<false, NC>(sr, dr, scale_log2, nl_row, nd_row, 0, NC, dk2);
+#pragma unroll 1
+                for (int c = 0; c < NCH; ++c) {
+                    const uint32_t st_addr = tmem + lane_addr + BUF + C::BUF_STRIDE * x + 32 * c;
+                    uint32_t sr[32], dr[32];
+                    ld_cols<32>(st_addr, sr);
+                    ld_cols<32>(st_addr + STEP, dr);
+                    wait_cols<32>(sr, dr);
+                    uint32_t dk2[16];
+                    const int cb = c0 + 32 * c;            // the chunk's first streamed column
+                    if (DQ) {
+                        if (full) {
+                            query_row_grads<false, 32>(sr, dr, scale_log2, nl_row, nd_row, 0, 32,
+                                                       dk2);
+                        } else {
+                            int lo, hi;
+                            query_row_span(own, cb, w.lk, w.lq, a.causal, wl, off, &lo, &hi);
+                            query_row_grads<true, 32>(sr, dr, scale_log2, nl_row, nd_row, lo, hi,
+                                                      dk2);
+                        }
                     } else {
-                        int lo, hi;
-                        query_row_span(own, c_base, w.lk, w.lq, a.causal, wl, off, &lo, &hi);
-                        query_row_grads<true, NC>(sr, dr, scale_log2, nl_row, nd_row, lo, hi, dk2);
+                        uint32_t pk[16];
+                        const uint32_t cstat = wstat + 256 * c;
+                        if (full) {
+                            key_row_grads<false, 32>(sr, dr, scale_log2, cstat, 0, 32, pk, dk2);
+                        } else {
+                            int lo, hi;
+                            key_row_span(own, cb, w.lk, w.lq, a.causal, wl, off, &lo, &hi);
+                            key_row_grads<true, 32>(sr, dr, scale_log2, cstat, lo, hi, pk, dk2);
+                        }
+                        // P^T (bf16 pairs) over the first half of the chunk's S^T columns
+                        st_cols<16>(st_addr, pk);
                     }
-                } else {
-                    uint32_t pk[NC / 2];
-                    if (full) {
-                        key_row_grads<false, NC>(sr, dr, scale_log2, wstat, 0, NC, pk, dk2);
-                    } else {
-                        int lo, hi;
-                        key_row_span(own, c_base, w.lk, w.lq, a.causal, wl, off, &lo, &hi);
-                        key_row_grads<true, NC>(sr, dr, scale_log2, wstat, lo, hi, pk, dk2);
-                    }
-                    // P^T (bf16 pairs) over the first half of this thread's own S^T columns
-                    st_cols<NC / 2>(st_addr, pk);
+                    // dS (bf16 pairs) over the first half of the chunk's dP columns
+                    st_cols<16>(st_addr + STEP, dk2);
                 }
-                // dS (bf16 pairs) over the first half of this thread's own dP columns
-                st_cols<NC / 2>(st_addr + STEP, dk2);
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(p_full(x));
