@@ -146,7 +146,7 @@ vfa_status vfa_varlen_fwd(const void *q, const void *k, const void *v,
  * k_fp8        device uint8 [total_k, num_kv_heads, head_dim] E4M3 codes.
  * descale_q, descale_k  finite, > 0 (else VFA_ERR_INVALID_ARG).
  * Other arguments, outputs, workspace and errors as in vfa_varlen_fwd;
- * head_dim must be 128 or 256 (else VFA_ERR_UNSUPPORTED).
+ * head_dim 64, 128 or 256 (else VFA_ERR_UNSUPPORTED).
  */
 vfa_status vfa_varlen_fwd_fp8(const void *q_fp8, const void *k_fp8, const void *v,
                               const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,

@@ -39,7 +39,7 @@ def _run(vfa, case, f8, causal, window_left=-1):
     return out.float().cpu().double().numpy(), lse.cpu().double().numpy(), status
 
 
-@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal,window_left", [(0, -1), (1, -1), (2, -1), (1, 200), (2, 37)])
 def test_mixes(vfa, oracle_mod, causal, window_left, D):
     lq = [1, 7, 64, 129, 300, 0, 257, 1000]
@@ -57,7 +57,7 @@ def test_mixes(vfa, oracle_mod, causal, window_left, D):
     assert_lse_close(lse, ref_lse, f"fp8 D={D} causal {causal} window {window_left}")
 
 
-@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("D", [64, 128, 256])
 def test_grouped_kv_heads(vfa, oracle_mod, D):
     lq, lk = [300, 7, 129, 64], [300, 40, 129, 200]
     case = W.make_varlen("fp8-gqa", lq, lk, 8, D, True, 1.0, value_seed=31 + D)
@@ -103,7 +103,7 @@ def test_cross_attention_d256(vfa, oracle_mod, seed):
 
 
 def test_rejects_other_head_dims_and_bad_descales(vfa):
-    case = W.make_varlen("fp8-d64", [8], [8], 1, 64, True, 1.0, value_seed=1)
+    case = W.make_varlen("fp8-d96", [8], [8], 1, 96, True, 1.0, value_seed=1)
     f8 = W.fp8_qk(case)
     with pytest.raises(vfa.VfaError):
         _run(vfa, case, f8, 1)
@@ -128,3 +128,17 @@ def test_edge_lengths(vfa, oracle_mod, causal):
                                                     f8.descale_k, causal)
     assert_out_close(out, ref_out, f"fp8 edge causal {causal}")
     assert_lse_close(lse, ref_lse, f"fp8 edge causal {causal}")
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_cross_attention_d64(vfa, oracle_mod, seed):
+    # the cross-attention workload at head_dim 64 with FP8 q and k (64-byte rows)
+    case = W.cross(64, seed)
+    f8 = W.fp8_qk(case)
+    out, lse, status = _run(vfa, case, f8, 0)
+    assert status == 0
+    ro, rl, _ = oracle_mod.varlen_fwd_fp8(f8.q8, f8.k8, case.v, case.cu_seqlens_q,
+                                          case.cu_seqlens_k, 8, 64, case.softmax_scale,
+                                          f8.descale_q, f8.descale_k, 0)
+    assert_out_close(out, ro, f"fp8 cross-d64 seed {seed}")
+    assert_lse_close(lse, rl, f"fp8 cross-d64 seed {seed}")

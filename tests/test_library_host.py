@@ -145,7 +145,7 @@ def test_backward_and_fp8_host_checks(vfa):
     # FP8 forward: head_dim 128 only, descales finite and positive
     f8 = lambda D, dq, dk: (fake, fake, fake, fake, fake, 4, 4, 4, 1, 2, 2, D, 0.1, dq, dk, 1, -1,
                             fake, fake, fake, 1 << 30, nul)
-    assert L.vfa_varlen_fwd_fp8(*f8(64, 1.0, 1.0)) == vfa.VFA_ERR_UNSUPPORTED
+    assert L.vfa_varlen_fwd_fp8(*f8(96, 1.0, 1.0)) == vfa.VFA_ERR_UNSUPPORTED
     assert L.vfa_varlen_fwd_fp8(*f8(128, 0.0, 1.0)) == vfa.VFA_ERR_INVALID_ARG
     assert L.vfa_varlen_fwd_fp8(*f8(128, 1.0, float("inf"))) == vfa.VFA_ERR_INVALID_ARG
 

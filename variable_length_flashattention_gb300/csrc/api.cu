@@ -92,7 +92,9 @@ vfa_status get_encoder(EncodeTiledFn *fn)
 
 // [rows, heads, head_dim] tensor of bf16 (elem_bytes 2) or 8-bit codes
 // (elem_bytes 1) as a 3-D TMA map (innermost first: dim, head, row); box =
-// 128 bytes of columns x 1 head x box_rows rows, 128-byte swizzle.
+// 128 bytes of columns x 1 head x box_rows rows, 128-byte swizzle -- or, for
+// rows of only 64 bytes (8-bit codes at head_dim 64), 64 bytes with the
+// 64-byte swizzle.
 vfa_status encode_packed_map(CUtensorMap *map, const void *base, int rows, int heads,
                              int head_dim, int box_rows, int elem_bytes = 2)
 {
@@ -105,14 +107,16 @@ vfa_status encode_packed_map(CUtensorMap *map, const void *base, int rows, int h
                                 static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * eb,
                                    static_cast<cuuint64_t>(heads) * head_dim * eb};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), 1,
+    const int box_bytes = head_dim * elem_bytes >= 128 ? 128 : 64;
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_bytes / elem_bytes), 1,
                                static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map,
                      elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                      3, const_cast<void *>(base), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(VFA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
@@ -366,8 +370,8 @@ vfa_status vfa_varlen_fwd_fp8(const void *q_fp8, const void *k_fp8, const void *
                               void *out, float *lse, void *workspace, size_t workspace_bytes,
                               vfa_stream_t stream)
 {
-    if (head_dim != 128 && head_dim != 256)
-        return fail(VFA_ERR_UNSUPPORTED, "FP8 forward head_dim %d not supported (128, 256)",
+    if (!supported_head_dim(head_dim))
+        return fail(VFA_ERR_UNSUPPORTED, "FP8 forward head_dim %d not supported (64, 128, 256)",
                     head_dim);
     if (!(descale_q > 0.f) || !(descale_k > 0.f) || descale_q > FLT_MAX || descale_k > FLT_MAX)
         return fail(VFA_ERR_INVALID_ARG, "descale_q and descale_k must be finite and > 0");

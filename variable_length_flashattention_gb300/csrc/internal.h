@@ -84,7 +84,7 @@ struct PrefillArgs {
     float scale_log2;     // softmax_scale * log2(e), > 0
     int causal;           // 0 none, 1 top-left, 2 bottom-right
     int window_left;      // < 0 none; else keys j >= row + off - window_left only
-    int qk_fp8;           // non-zero: tm_q / tm_k map FP8 E4M3 codes (head_dim 128 or 256)
+    int qk_fp8;           // non-zero: tm_q / tm_k map FP8 E4M3 codes (any supported head_dim)
 };
 
 // Whether the forward for `head_dim` runs two q tiles per work item.

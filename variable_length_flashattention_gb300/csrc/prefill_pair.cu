@@ -33,9 +33,10 @@
 //     handshake, no TMA completion to wait for): every store instruction
 //     writes eight whole 64-byte row segments;
 //   * TMEM: O_a, O_b (D columns each), S/P_a, S/P_b (128 columns each);
-//   * an FP8 instantiation (head_dim 128) takes Q and K as E4M3 codes: their
-//     tiles are half the bytes and S = Q K^T runs as kind::f8f6f4 in 32-byte
-//     k-steps; the per-tensor descales are folded into the score scale.
+//   * an FP8 instantiation takes Q and K as E4M3 codes: their tiles are half
+//     the bytes (at head_dim 64 rows of 64 bytes, stored with the 64-byte
+//     swizzle) and S = Q K^T runs as kind::f8f6f4 in 32-byte k-steps; the
+//     per-tensor descales are folded into the score scale.
 // Everything else (item ring fed by an atomic counter, bounded waits with
 // drain-and-report on expiry) is as in prefill.cu.
 #include <cfloat>
@@ -58,8 +59,12 @@ struct PairCfg {
     static constexpr int NS = D == 64 ? 4 : 2;            // K and V ring stages
     static constexpr int DB = D / 64;                     // 128-byte column blocks per V / O row
     static constexpr int QK_ELEM = F8 ? 1 : 2;            // bytes per Q / K element
-    static constexpr int QK_DB = D * QK_ELEM / 128;       // 128-byte column blocks per Q / K row
-    static constexpr int QK_BLOCK = 128 / QK_ELEM;        // elements per such block
+    // Q / K rows are stored in swizzled column blocks of QK_ROW bytes: 128
+    // (128-byte swizzle), or 64 for FP8 at head_dim 64, whose rows are only 64
+    // bytes (64-byte swizzle)
+    static constexpr int QK_ROW = D * QK_ELEM >= 128 ? 128 : 64;
+    static constexpr int QK_DB = D * QK_ELEM / QK_ROW;    // column blocks per Q / K row
+    static constexpr int QK_BLOCK = QK_ROW / QK_ELEM;     // elements per such block
     static constexpr int QK_KSTEP = 32 / QK_ELEM;         // elements per MMA k-step (32 bytes)
     static constexpr uint32_t Q_BYTES = BQ * D * QK_ELEM;
     static constexpr uint32_t K_BYTES = BK * D * QK_ELEM;
@@ -346,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mbar_arrive_expect_tx(q_full(x), C::Q_BYTES);
                     for (int db = 0; db < C::QK_DB; ++db)
-                        tma_load_3d(sQ + x * C::Q_BYTES + db * (BQ * 128), &p.tm_q, q_full(x),
+                        tma_load_3d(sQ + x * C::Q_BYTES + db * (BQ * C::QK_ROW), &p.tm_q, q_full(x),
                                     db * C::QK_BLOCK, h, seq.x + i * BQ);
                     ++qloads[x];
                 }
@@ -358,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mbar_arrive_expect_tx(k_full(st), C::K_BYTES);
                     for (int db = 0; db < C::QK_DB; ++db)
-                        tma_load_3d(sK + st * C::K_BYTES + db * (BK * 128), &p.tm_k, k_full(st),
+                        tma_load_3d(sK + st * C::K_BYTES + db * (BK * C::QK_ROW), &p.tm_k, k_full(st),
                                     db * C::QK_BLOCK, h / p.kv_group, seq.w + j * BK);
                     ++kfills;
                 }
@@ -410,8 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // All 32 lanes run this loop on warp-uniform values; one elected lane
         // issues each MMA and commit.
         {
-            const uint64_t q_desc0 = sdesc_sw128(sQ, 16, 1024);
-            const uint64_t k_desc0 = sdesc_sw128(sK, 16, 1024);
+            const uint64_t q_desc0 = C::QK_ROW == 128 ? sdesc_sw128(sQ, 16, 1024)
+                                                      : sdesc_sw64(sQ, 16, 512);
+            const uint64_t k_desc0 = C::QK_ROW == 128 ? sdesc_sw128(sK, 16, 1024)
+                                                      : sdesc_sw64(sK, 16, 512);
             const uint64_t v_desc0 = sdesc_sw128(sV, BK * 128, 1024);
             uint32_t n = 0, kv = 0, qloads[2] = {0, 0}, gt[2] = {0, 0};   // tiles per q slot
             bool ok = true;
@@ -422,10 +429,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t kd = k_desc0 + st * (C::K_BYTES >> 4);
                 const uint32_t s_tm = tmem + C::S_COL + x * BK;
                 // k-steps of 32 bytes: 16 bf16 or 32 FP8 elements
+                // (KPB k-steps per swizzled row of QK_ROW bytes)
+                constexpr int KPB = C::QK_ROW / 32;
 #pragma unroll
                 for (int kk = 0; kk < D / C::QK_KSTEP; ++kk) {
-                    const uint64_t qo = qd + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4);
-                    const uint64_t ko = kd + (((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4);
+                    const uint64_t qo =
+                        qd + (((kk / KPB) * (BQ * C::QK_ROW) + (kk % KPB) * 32) >> 4);
+                    const uint64_t ko =
+                        kd + (((kk / KPB) * (BK * C::QK_ROW) + (kk % KPB) * 32) >> 4);
                     if constexpr (F8) {
                         if (kk == 0)
                             mma_ss_w8<0>(s_tm, qo, ko, C::IDESC_QK);
@@ -807,17 +818,13 @@ cudaError_t launch_pair_dw(const PrefillArgs &a, int grid, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-// The sliding-window mask and FP8 Q / K (head_dim 128) have their own
-// instantiations.
+// The sliding-window mask and FP8 Q / K have their own instantiations.
 template <int D>
 cudaError_t launch_pair_d(const PrefillArgs &a, int grid, cudaStream_t stream)
 {
-    if (a.qk_fp8) {
-        if constexpr (D == 128)
-            return a.window_left >= 0 ? launch_pair_dw<D, true, true>(a, grid, stream)
-                                      : launch_pair_dw<D, false, true>(a, grid, stream);
-        return cudaErrorInvalidValue;
-    }
+    if (a.qk_fp8)
+        return a.window_left >= 0 ? launch_pair_dw<D, true, true>(a, grid, stream)
+                                  : launch_pair_dw<D, false, true>(a, grid, stream);
     return a.window_left >= 0 ? launch_pair_dw<D, true, false>(a, grid, stream)
                               : launch_pair_dw<D, false, false>(a, grid, stream);
 }

@@ -438,6 +438,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
            (2ull << 61);           // swizzle mode: 128-byte
 }
 
+// The same for the 64-byte swizzle (CU_TENSOR_MAP_SWIZZLE_64B into a 512-byte
+// aligned buffer): K-major rows of 64 bytes, 8-row atoms of 512 bytes (sbo).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+           (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
+           (1ull << 46) |          // descriptor version for tcgen05
+           (4ull << 61);           // swizzle mode: 64-byte
+}
+
 // Instruction descriptor for kind::f16 with bf16 inputs and f32 accumulate.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
                                                       bool b_mn_major)
