@@ -145,3 +145,24 @@ def test_cross_attention_d256(vfa, oracle_mod, seed):
     # the cross-attention workload at head_dim 256 (32 sequences, q up to 512,
     # k up to 4096 tokens, non-causal), every sequence and head
     _compare(vfa, oracle_mod, W.cross(256, seed), 0, seed=seed)
+
+
+def test_longtail_longest_sequences(vfa, oracle_mod):
+    # the long-tail workload's 8192-token sequence (H=32, sigma 0.5) with two
+    # of its short sequences: long units of the persistent kernels, many
+    # query blocks per key tile, every element against the oracle
+    full = W.longtail(0)
+    L = full.lengths_q
+    picks = [L.index(8192)] + [i for i in range(len(L)) if L[i] < 300][:2]
+    lens = [L[i] for i in picks]
+    case = W.make_varlen("longtail-sub", lens, lens, 32, 128, True, 0.5, value_seed=0)
+    parts_q, parts_k, parts_v = [], [], []
+    for i in picks:
+        r0, r1 = int(full.cu_seqlens_q[i]), int(full.cu_seqlens_q[i + 1])
+        parts_q.append(full.q[r0:r1])
+        parts_k.append(full.k[r0:r1])
+        parts_v.append(full.v[r0:r1])
+    case.q = torch.cat(parts_q).contiguous()
+    case.k = torch.cat(parts_k).contiguous()
+    case.v = torch.cat(parts_v).contiguous()
+    _compare(vfa, oracle_mod, case, 1, seed=0)

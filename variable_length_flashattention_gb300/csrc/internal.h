@@ -169,8 +169,8 @@ __host__ __device__ constexpr int bwd_step_rows(int head_dim)
 // Workspace bytes of the backward and its split into the BwdArgs pointers.
 size_t bwd_workspace_bytes(int batch, int total_q, int num_heads, int head_dim);
 void bwd_workspace_split(void *ws, int batch, int total_q, int num_heads, BwdArgs *a);
-// prep, Delta, dK/dV (grid: key_tile_bound x column halves, num_kv_heads) and
-// dQ (grid: q_tile_bound x num_heads) kernels.
+// prep, Delta, then the persistent dK/dV and dQ kernels (one CTA per SM each,
+// taking (key tile, kv head) and (q tile, head) units from atomic counters).
 cudaError_t launch_bwd(int head_dim, const BwdArgs &a, int key_tile_bound, int q_tile_bound,
                        int sm_count, cudaStream_t stream);
 
