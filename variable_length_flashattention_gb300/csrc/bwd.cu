@@ -54,6 +54,7 @@ constexpr int kFirstMathWarp = 4;
 constexpr int kMathThreads = kMathWarps * 32;
 constexpr int kThreads = (kFirstMathWarp + kMathWarps) * 32;   // + TMA, MMA, two idle warps
 constexpr int kPrepThreads = 1024;
+constexpr uint32_t kEpiStage = 32 * 64;    // per math warp: 32 rows x 32 bf16 columns of output
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shapes per head_dim.  STEP rows (queries, resp. keys) stream past per step
@@ -81,7 +82,7 @@ struct BwdCfg {
     // buffer; own_full, own_empty, acc_done, epi_done, drain
     static constexpr int NUM_BARS = 2 * NSTAGE + 8 + 5;
     static constexpr size_t SMEM = 1024 + 2 * OWN_BYTES + NSTAGE * STAGE_BYTES +
-                                   kMathWarps * 512 + NUM_BARS * 8 + 64;
+                                   kMathWarps * (512 + kEpiStage) + NUM_BARS * 8 + 64;
     // S^T / dP^T (keys x STEP queries) and S / dP (queries x STEP keys): both K-major
     static constexpr uint32_t IDESC_T = idesc_bf16_f32(kOwn, STEP, false, false);
     // dV, dK (DKV columns) and dQ (D columns): A from TMEM, B (dO, Q or K rows) MN-major
@@ -403,23 +404,35 @@ __device__ __forceinline__ void st_cols(uint32_t taddr, const uint32_t (&r)[NP])
     }
 }
 
-// 32 columns of D (fp32 in TMEM, this thread's lane) * f -> 64 bytes of bf16 at dst.
-__device__ __forceinline__ void store_row32(uint32_t taddr, float f, __nv_bfloat16 *dst, bool ok)
+// 32 accumulator columns of this warp's 32 rows (fp32 in TMEM at taddr; the
+// thread's lane is its row) * f -> bf16 at dst0 (the warp's first row, the
+// chunk's first column; rows row_stride elements apart).  The values pass
+// through the warp's 2 KB stage (row segments swizzled by row, so the writes
+// are conflict-free) so that every global store instruction writes eight
+// whole 64-byte row segments; rows n_valid and later are not written.
+__device__ __forceinline__ void store_tile32(uint32_t taddr, float f, uint32_t stage, int lane,
+                                             __nv_bfloat16 *dst0, size_t row_stride, int n_valid)
 {
     uint32_t rr[32];
     tmem_ld32(taddr, rr);
     tmem_wait_ld_r(rr);
-    if (!ok)
-        return;
+    const uint32_t row = stage + lane * 64;
 #pragma unroll
-    for (int e = 0; e < 32; e += 8) {
-        uint4 v;
-        v.x = pack_bf16x2(__uint_as_float(rr[e]) * f, __uint_as_float(rr[e + 1]) * f);
-        v.y = pack_bf16x2(__uint_as_float(rr[e + 2]) * f, __uint_as_float(rr[e + 3]) * f);
-        v.z = pack_bf16x2(__uint_as_float(rr[e + 4]) * f, __uint_as_float(rr[e + 5]) * f);
-        v.w = pack_bf16x2(__uint_as_float(rr[e + 6]) * f, __uint_as_float(rr[e + 7]) * f);
-        *reinterpret_cast<uint4 *>(dst + e) = v;
+    for (int c = 0; c < 4; ++c)
+        st_shared_v4(row + ((c ^ ((lane >> 1) & 3)) << 4),
+                     pack_bf16x2(__uint_as_float(rr[8 * c + 0]) * f, __uint_as_float(rr[8 * c + 1]) * f),
+                     pack_bf16x2(__uint_as_float(rr[8 * c + 2]) * f, __uint_as_float(rr[8 * c + 3]) * f),
+                     pack_bf16x2(__uint_as_float(rr[8 * c + 4]) * f, __uint_as_float(rr[8 * c + 5]) * f),
+                     pack_bf16x2(__uint_as_float(rr[8 * c + 6]) * f, __uint_as_float(rr[8 * c + 7]) * f));
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int rw = 8 * k + (lane >> 2), ch = lane & 3;
+        const uint4 v = ld_shared_v4(stage + rw * 64 + ((ch ^ ((rw >> 1) & 3)) << 4));
+        if (rw < n_valid)
+            *reinterpret_cast<uint4 *>(dst0 + rw * row_stride + ch * 8) = v;
     }
+    __syncwarp();
 }
 
 // ------------------------------------------------------------ the two main kernels
@@ -540,7 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     const uint32_t sOwn0 = base, sOwn1 = sOwn0 + C::OWN_BYTES;     // K, V  /  Q, dO
     const uint32_t sRing = sOwn1 + C::OWN_BYTES;                    // stage: Q, dO  /  K, V
     const uint32_t sStat = sRing + NSTAGE * C::STAGE_BYTES;         // per math warp: nl, -Delta
-    const uint32_t bars = sStat + kMathWarps * 512;
+    const uint32_t sEpi = sStat + kMathWarps * 512;                 // per math warp: output stage
+    const uint32_t bars = sEpi + kMathWarps * kEpiStage;
     auto ring_full = [&](int st) { return bars + 8u * st; };
     auto ring_empty = [&](int st) { return bars + 8u * (NSTAGE + st); };
     auto s_full = [&](int x) { return bars + 8u * (2 * NSTAGE + x); };
@@ -860,16 +874,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             if (!ok)
                 break;
             tc_fence_after();
+            {
+                // this warp's 32 rows start at own row w.t * 128 + 32 * quarter
+                const int wrow = w.t * kOwn + quarter * 32;
+                const int n_valid = (DQ ? w.lq : w.lk) - wrow;
+                const uint32_t stage = sEpi + (warp - kFirstMathWarp) * kEpiStage;
+                const size_t stride = static_cast<size_t>(DQ ? H : Hkv) * D;
+                const size_t base_out = row_out - static_cast<size_t>(lane) * stride;
 #pragma unroll 1
-            for (int cb = 0; cb < DH; cb += 32) {
-                if (DQ) {
-                    store_row32(tmem + lane_addr + C::COL_DQ + half * DH + cb, a.scale,
-                                dq + row_out + cb, own_valid);
-                } else {
-                    store_row32(tmem + lane_addr + C::COL_DV + half * DH + cb, 1.f,
-                                dv + row_out + cb, own_valid);
-                    store_row32(tmem + lane_addr + C::COL_DK + half * DH + cb, a.scale,
-                                dk + row_out + cb, own_valid);
+                for (int cb = 0; cb < DH; cb += 32) {
+                    if (DQ) {
+                        store_tile32(tmem + lane_addr + C::COL_DQ + half * DH + cb, a.scale, stage,
+                                     lane, dq + base_out + cb, stride, n_valid);
+                    } else {
+                        store_tile32(tmem + lane_addr + C::COL_DV + half * DH + cb, 1.f, stage,
+                                     lane, dv + base_out + cb, stride, n_valid);
+                        store_tile32(tmem + lane_addr + C::COL_DK + half * DH + cb, a.scale, stage,
+                                     lane, dk + base_out + cb, stride, n_valid);
+                    }
                 }
             }
             // the accumulators may be overwritten by the next unit's products
