@@ -105,11 +105,12 @@ def test_large_logits_rescale_path(vfa, oracle_mod):
 
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-def test_rising_scores_rescale_every_half(vfa, oracle_mod, D, causal):
+def test_rising_scores_rescale_every_tile(vfa, oracle_mod, D, causal):
     # q . k grows by more than 2^8 (in log2 units) every 64 keys along each
-    # sequence: every half-tile after the first moves the reference max, so the
-    # kernel takes its rescale-and-redo path in both halves of every key tile
-    # (including the rescale that must wait for the first half's O += P V).
+    # sequence: every key tile after the first moves the reference max, so the
+    # kernel rescales O and l at every tile (after waiting for the previous
+    # tile's O += P V) and the D = 256 kernel, whose tiles are 64 keys, at
+    # every tile too.
     lengths = [700, 300, 64, 129]
     case = W.make_varlen("rising", lengths, lengths, 2, D, causal, 0.3, value_seed=D + 7)
     q = case.q.float()

@@ -19,16 +19,18 @@
 //     in issue order, so the product has read P_x before S_x is rewritten
 //     (and waiting for its completion instead would idle the tensor core);
 //   * warps 4-7 own tile a's 128 rows, warps 8-11 tile b's, one row per
-//     thread (TMEM lane = row).  A key tile's scores are taken in two halves
-//     of 64 columns held in registers; p is computed against the reference
-//     max in the same pass that finds the half's max, and only if the max
-//     grew by more than 2^8 does the reference move (O, l rescaled) and the
-//     half get redone (its scores reloaded from TMEM, still intact).  Each half of P is published on
-//     its own and O_x += P_x V runs per half, so the tensor core starts on
-//     the first 64 keys while the second half is still being exponentiated;
+//     thread (TMEM lane = row).  A key tile's 128 scores of a row come into
+//     registers with one TMEM wait (tcgen05.wait::ld waits for all of a
+//     thread's loads, so loading in pieces would expose the load latency once
+//     per piece); the row max is taken from the registers, the reference max
+//     moves (O, l rescaled) only if the tile's max exceeds it by more than
+//     2^8, and p is then computed once per score.  Each half of P (64 keys)
+//     is published on its own and O_x += P_x V runs per half, so the tensor
+//     core starts on the first 64 keys while the second half is still being
+//     exponentiated;
 //   * in a masked tile (causal diagonal, ragged key tail) a 32-column chunk
 //     that is valid for all 32 rows of a warp skips the mask, and one that
-//     is masked for all of them skips its TMEM load and its exponentials;
+//     is masked for all of them skips its exponentials;
 //   * O / l leaves through a 2 KB shared-memory stage per warp (no cross-warp
 //     handshake, no TMA completion to wait for): every store instruction
 //     writes eight whole 64-byte row segments;
@@ -109,58 +111,6 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int cb, int lim, 
 #pragma unroll
     for (int e = 0; e < 32; ++e)
         sr[e] = (cb + e < lim && (!LO || cb + e >= lo)) ? sr[e] : __float_as_uint(-INFINITY);
-}
-
-// Folds the (masked) scores of the 32-column chunk at TMEM address taddr into
-// the running maxima mx.  An all-masked chunk is skipped.
-template <int MK>
-__device__ __forceinline__ void chunk_max(uint32_t taddr, int cb, int lim, int lim_lo, int lo,
-                                          int lo_hi, bool empty, float (&mx)[4])
-{
-    if (empty)
-        return;
-    uint32_t sr[32];
-    tmem_ld32(taddr, sr);
-    tmem_wait_ld_r(sr);
-    if (MK > 0)
-        mask_chunk<MK == 2>(sr, cb, lim, lim_lo, lo, lo_hi);
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-        mx[e & 3] = fmax3(mx[e & 3], __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
-}
-
-// p = 2^(s * scale_log2 - m) for the 32-column chunk at TMEM address taddr,
-// packed to bf16 pairs in pk[pb .. pb + 15], with the row sums accumulated in
-// ls (fp32) and, if WITH_MAX, the scores folded into mx.  An all-masked chunk
-// gives zeros without loads or exponentials.  MK: 0 no mask, 1 upper bound
-// only, 2 both bounds.
-template <int MK, bool WITH_MAX>
-__device__ __forceinline__ void chunk_exp(uint32_t taddr, int cb, int lim, int lim_lo, int lo,
-                                          int lo_hi, bool empty,
-                                          float2 scale2, float2 negm2, float2 (&ls)[4],
-                                          float (&mx)[4], uint32_t (&pk)[32], int pb)
-{
-    if (empty) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-            pk[pb + e] = 0u;
-        return;
-    }
-    uint32_t sr[32];
-    tmem_ld32(taddr, sr);
-    tmem_wait_ld_r(sr);
-    if (MK > 0)
-        mask_chunk<MK == 2>(sr, cb, lim, lim_lo, lo, lo_hi);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-        const float s0 = __uint_as_float(sr[2 * e]), s1 = __uint_as_float(sr[2 * e + 1]);
-        if (WITH_MAX)
-            mx[e & 3] = fmax3(mx[e & 3], s0, s1);
-        const float2 t = __ffma2_rn(make_float2(s0, s1), scale2, negm2);
-        const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-        ls[e & 3] = __fadd2_rn(ls[e & 3], pp);
-        pk[pb + e] = pack_bf16x2(pp.x, pp.y);
-    }
 }
 
 // O rows *= f for this warp's 32 lanes, 16 columns at a time (rare path).
@@ -641,10 +591,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int lim_lo = need_mask ? __reduce_min_sync(0xffffffffu, lim) : BK;
                 const int lim_hi = need_mask ? __reduce_max_sync(0xffffffffu, lim) : BK;
 
-                // One half of the key tile: 64 scores as two 32-column chunks.
-                auto half = [&](auto masked, int hh) -> bool {
+                // The whole key tile's 128 scores of this row are loaded with one
+                // wait.  The row max comes from the registers first; the reference
+                // max moves (O, l rescaled) only if it grew by more than 2^8; then
+                // p = 2^(s * scale_log2 - m) per 32-column chunk, stored as bf16
+                // pairs over the chunk's first 16 S columns (all scores are in
+                // registers by then), each half of P published on its own so that
+                // O_x += P_x V starts on the first 64 keys while the second half is
+                // being exponentiated.
+                auto tile = [&](auto masked) -> bool {
                     constexpr int MK = decltype(masked)::value;
-                    const int c0 = hh * 64;
                     // banded tiles: this row's visible columns start at lo
                     int lo = 0, lo_lo = 0, lo_hi = 0;
                     if (MK == 2) {
@@ -656,46 +612,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                         lo_lo = __reduce_min_sync(0xffffffffu, lo);
                         lo_hi = __reduce_max_sync(0xffffffffu, lo);
                     }
+                    uint32_t sc[4][32];
+                    tmem_ld32(s_addr, sc[0]);
+                    tmem_ld32(s_addr + 32, sc[1]);
+                    tmem_ld32(s_addr + 64, sc[2]);
+                    tmem_ld32(s_addr + 96, sc[3]);
+                    tmem_wait_ld_r(sc[0]);
+                    tmem_bind_r(sc[1]);
+                    tmem_bind_r(sc[2]);
+                    tmem_bind_r(sc[3]);
                     // a chunk every row of the warp masks entirely
-                    const bool empty0 = MK > 0 && (c0 >= lim_hi || (MK == 2 && c0 + 32 <= lo_lo));
-                    const bool empty1 =
-                        MK > 0 && (c0 + 32 >= lim_hi || (MK == 2 && c0 + 64 <= lo_lo));
-                    const uint32_t sa = s_addr + c0;
-                    // p is computed against the reference max in the pass that
-                    // finds the half's max; if the max grew by more than 2^8 the
-                    // half is redone at the new max from TMEM, where its scores
-                    // are still intact.  A warp with a row that has no reference
-                    // yet finds the max first.
-                    const bool fresh = __any_sync(0xffffffffu, m_used == -INFINITY);
-                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                    float2 ls[4];
-                    uint32_t pk[32];
-                    if (fresh) {
-                        chunk_max<MK>(sa, c0, lim, lim_lo, lo, lo_hi, empty0, mx);
-                        chunk_max<MK>(sa + 32, c0 + 32, lim, lim_lo, lo, lo_hi, empty1, mx);
-                    } else {
-                        const float2 negm2 = make_float2(-m_used, -m_used);
+                    bool empty[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            ls[e] = make_float2(0.f, 0.f);
-                        chunk_exp<MK, true>(sa, c0, lim, lim_lo, lo, lo_hi, empty0, scale2, negm2,
-                                            ls, mx, pk, 0);
-                        chunk_exp<MK, true>(sa + 32, c0 + 32, lim, lim_lo, lo, lo_hi, empty1, scale2,
-                                            negm2, ls, mx, pk, 16);
+                    for (int c = 0; c < 4; ++c)
+                        empty[c] = MK > 0 && (32 * c >= lim_hi || (MK == 2 && 32 * c + 32 <= lo_lo));
+                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (empty[c])
+                            continue;
+                        if (MK > 0)
+                            mask_chunk<MK == 2>(sc[c], 32 * c, lim, lim_lo, lo, lo_hi);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            mx[e & 3] = fmax3(mx[e & 3], __uint_as_float(sc[c][2 * e]),
+                                              __uint_as_float(sc[c][2 * e + 1]));
                     }
                     const float mraw = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
-                    const float m_half = mraw == -INFINITY ? -INFINITY : mraw * scale_log2;
-                    const float m_new = fmaxf(m_used, m_half);
+                    const float m_tile = mraw == -INFINITY ? -INFINITY : mraw * scale_log2;
+                    const float m_new = fmaxf(m_used, m_tile);
                     const bool grow = m_new > m_used + kRescaleThreshold;   // true for m_used = -inf
-                    const bool redo = __any_sync(0xffffffffu, grow);
-                    if (redo) {
-                        if (j > j_first || hh > 0) {
-                            // O_x must hold every product issued so far before it
-                            // is rescaled: the previous tile's second half, or this
-                            // tile's first.
-                            const bool waited = hh == 0 ? mbar_wait(o_h2(x), (g - 1) & 1u, abort)
-                                                        : mbar_wait(o_h1(x), g & 1u, abort);
-                            if (!waited)
+                    if (__any_sync(0xffffffffu, grow)) {
+                        if (j > j_first) {
+                            // O_x holds every product issued so far (the previous
+                            // tile's, complete once S_x of this one is)
+                            if (!mbar_wait(o_h2(x), (g - 1) & 1u, abort))
                                 return false;
                             tc_fence_after();
                             const float f = grow ? ex2_approx(m_used - m_new) : 1.f;
@@ -705,28 +656,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (grow)
                             m_used = m_new;
                     }
-                    if (fresh || redo) {
-                        const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-                        const float2 negm2 = make_float2(neg_m, neg_m);
+                    const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+                    const float2 negm2 = make_float2(neg_m, neg_m);
+                    float2 ls[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            ls[e] = make_float2(0.f, 0.f);
-                        chunk_exp<MK, false>(sa, c0, lim, lim_lo, lo, lo_hi, empty0, scale2, negm2,
-                                             ls, mx, pk, 0);
-                        chunk_exp<MK, false>(sa + 32, c0 + 32, lim, lim_lo, lo, lo_hi, empty1,
-                                             scale2, negm2, ls, mx, pk, 16);
+                    for (int e = 0; e < 4; ++e)
+                        ls[e] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t pk[16];
+                        if (empty[c]) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                pk[e] = 0u;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const float2 t = __ffma2_rn(
+                                    make_float2(__uint_as_float(sc[c][2 * e]),
+                                                __uint_as_float(sc[c][2 * e + 1])),
+                                    scale2, negm2);
+                                const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+                                ls[e & 3] = __fadd2_rn(ls[e & 3], pp);
+                                pk[e] = pack_bf16x2(pp.x, pp.y);
+                            }
+                        }
+                        tmem_st16(s_addr + 16 * c, pk);
+                        if (c & 1) {
+                            tmem_wait_st();
+                            tc_fence_before();
+                            mbar_arrive(p_half(x, c >> 1));
+                        }
                     }
                     const float2 l2 = __fadd2_rn(__fadd2_rn(ls[0], ls[1]), __fadd2_rn(ls[2], ls[3]));
                     l += l2.x + l2.y;
-                    // P (bf16 pairs) over this half's S columns, already read.
-                    tmem_st32(s_addr + hh * 32, pk);
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(p_half(x, hh));
                     return true;
                 };
-                for (int hh = 0; hh < 2 && ok; ++hh)
-                    ok = need_mask ? half(Masked{}, hh) : half(Plain{}, hh);
+                ok = need_mask ? tile(Masked{}) : tile(Plain{});
                 ++g;
             }
             if (!ok)
