@@ -251,7 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // All 32 lanes run this loop on warp-uniform values (operands in
+        // uniform registers); one elected lane issues each MMA and commit.
+        {
             // Descriptors of every buffer, built once; a k-step only adds a
             // compile-time offset (in 16-byte units) to the start-address field.
             // (The start-address field is the low 14 bits, address / 16; shared
@@ -273,22 +275,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 const uint64_t vd = v_desc0 + stp * (C::KV_BYTES >> 4);
                 const uint32_t a_tm = tmem + C::S_COL + xp * BK;
                 if (acc)
-                    mma_ts_c<1>(tmem + C::O_COL, a_tm, vd, C::IDESC_PV);
+                    mma_ts_w<1>(tmem + C::O_COL, a_tm, vd, C::IDESC_PV);
                 else
-                    mma_ts_c<0>(tmem + C::O_COL, a_tm, vd, C::IDESC_PV);
+                    mma_ts_w<0>(tmem + C::O_COL, a_tm, vd, C::IDESC_PV);
 #pragma unroll
                 for (int kk = 1; kk < BK / 16; ++kk)
-                    mma_ts_c<1>(tmem + C::O_COL, a_tm + kk * 8, vd + kk * (16 * 128 / 16),
+                    mma_ts_w<1>(tmem + C::O_COL, a_tm + kk * 8, vd + kk * (16 * 128 / 16),
                                 C::IDESC_PV);
-                mma_commit(s_free(xp));
-                mma_commit(v_empty(stp));
+                mma_commit_w(s_free(xp));
+                mma_commit_w(v_empty(stp));
                 return true;
             };
             for (;; ++n) {
                 int4 it, seq;
                 int first;
                 const bool more = next_item(n, it, seq, first);
-                mbar_arrive(item_empty(n & 1));
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(item_empty(n & 1));
                 if (!more)
                     break;
                 const int j_end = it.w;
@@ -318,20 +322,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         const uint64_t ko = kd + (((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4);
                         if constexpr (F8) {
                             if (kk == 0)
-                                mma_ss_c8<0>(s_tm, qo, ko, C::IDESC_QK);
+                                mma_ss_w8<0>(s_tm, qo, ko, C::IDESC_QK);
                             else
-                                mma_ss_c8<1>(s_tm, qo, ko, C::IDESC_QK);
+                                mma_ss_w8<1>(s_tm, qo, ko, C::IDESC_QK);
                         } else {
                             if (kk == 0)
-                                mma_ss_c<0>(s_tm, qo, ko, C::IDESC_QK);
+                                mma_ss_w<0>(s_tm, qo, ko, C::IDESC_QK);
                             else
-                                mma_ss_c<1>(s_tm, qo, ko, C::IDESC_QK);
+                                mma_ss_w<1>(s_tm, qo, ko, C::IDESC_QK);
                         }
                     }
-                    mma_commit(s_full(x));
-                    mma_commit(k_empty(st));
+                    mma_commit_w(s_full(x));
+                    mma_commit_w(k_empty(st));
                     if (j == j_end - 1)
-                        mma_commit(q_empty(qb));
+                        mma_commit_w(q_empty(qb));
                     if (j > first && !issue_pv(g - 1, kv - 1, j - 1 > first)) {
                         ok = false;
                         break;
@@ -348,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 ++qit;
             }
             if (!ok || *abort) {
-                // Every MMA this thread issued must finish before TMEM is freed.
-                mma_commit(drain_bar);
+                // Every MMA this warp issued must finish before TMEM is freed.
+                mma_commit_w(drain_bar);
                 mbar_wait_drain(drain_bar, 0);
             }
         }
@@ -515,24 +519,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             const uint32_t o_addr = tmem + lane_addr + C::O_COL;
             uint4 *dst = reinterpret_cast<uint4 *>(out + (tok * H + h) * D);
+            // 128 columns of O per TMEM wait (the wait covers all of a thread's
+            // loads in flight, so smaller pieces would each expose its latency)
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t rr[32];
-                tmem_ld32(o_addr + c * 32, rr);
-                tmem_wait_ld();
+            for (int c0 = 0; c0 < D / 32; c0 += 4) {
+                uint32_t rr[4][32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    tmem_ld32(o_addr + (c0 + q) * 32, rr[q]);
+                tmem_wait_ld_r(rr[0]);
+                tmem_bind_r(rr[1]);
+                tmem_bind_r(rr[2]);
+                tmem_bind_r(rr[3]);
                 if (row_valid) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(rr[8 * e + 0]) * inv_l,
-                                          __uint_as_float(rr[8 * e + 1]) * inv_l);
-                        v.y = pack_bf16x2(__uint_as_float(rr[8 * e + 2]) * inv_l,
-                                          __uint_as_float(rr[8 * e + 3]) * inv_l);
-                        v.z = pack_bf16x2(__uint_as_float(rr[8 * e + 4]) * inv_l,
-                                          __uint_as_float(rr[8 * e + 5]) * inv_l);
-                        v.w = pack_bf16x2(__uint_as_float(rr[8 * e + 6]) * inv_l,
-                                          __uint_as_float(rr[8 * e + 7]) * inv_l);
-                        dst[c * 4 + e] = v;
+                    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(rr[q][8 * e + 0]) * inv_l,
+                                              __uint_as_float(rr[q][8 * e + 1]) * inv_l);
+                            v.y = pack_bf16x2(__uint_as_float(rr[q][8 * e + 2]) * inv_l,
+                                              __uint_as_float(rr[q][8 * e + 3]) * inv_l);
+                            v.z = pack_bf16x2(__uint_as_float(rr[q][8 * e + 4]) * inv_l,
+                                              __uint_as_float(rr[q][8 * e + 5]) * inv_l);
+                            v.w = pack_bf16x2(__uint_as_float(rr[q][8 * e + 6]) * inv_l,
+                                              __uint_as_float(rr[q][8 * e + 7]) * inv_l);
+                            dst[(c0 + q) * 4 + e] = v;
+                        }
                     }
                 }
             }
