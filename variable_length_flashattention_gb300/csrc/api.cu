@@ -432,11 +432,13 @@ vfa_status vfa_varlen_bwd(const void *q, const void *k, const void *v, const voi
         return st;
     vfa::BwdArgs a;
     memset(&a, 0, sizeof a);
-    const int box = vfa::bwd_step_rows(head_dim);
+    const int box = vfa::bwd_step_rows(head_dim), box_kv = vfa::bwd_dq_step_rows(head_dim);
     if ((st = encode_packed_map(&a.tm_q, q, total_q, num_heads, head_dim, box)) ||
         (st = encode_packed_map(&a.tm_do, dout, total_q, num_heads, head_dim, box)) ||
         (st = encode_packed_map(&a.tm_k, k, total_k, num_kv_heads, head_dim, box)) ||
-        (st = encode_packed_map(&a.tm_v, v, total_k, num_kv_heads, head_dim, box)))
+        (st = encode_packed_map(&a.tm_v, v, total_k, num_kv_heads, head_dim, box)) ||
+        (st = encode_packed_map(&a.tm_ks, k, total_k, num_kv_heads, head_dim, box_kv)) ||
+        (st = encode_packed_map(&a.tm_vs, v, total_k, num_kv_heads, head_dim, box_kv)))
         return st;
     vfa::bwd_workspace_split(workspace, batch, total_q, num_heads, &a);
     a.cu_q = cu_seqlens_q;

@@ -27,7 +27,8 @@
 //     exponentiated;
 //   * the dQ kernel (bwd_main_kernel<D, true>): for each 128-query tile and
 //     head, the same with the roles swapped: Q, dO stay, K and V stream past
-//     in blocks of STEP keys; S = Q K^T, dP = dO V^T into two TMEM buffers,
+//     in blocks of STEP keys (96; 32 at head_dim 256, through their own TMA
+//     maps with boxes of that height); S = Q K^T, dP = dO V^T into two TMEM buffers,
 //     dS (bf16, over dP) and dQ += dS K in TMEM.  dQ leaves as bf16 once, so
 //     no fp32 sum and no second pass exist.
 // Both are persistent: one CTA per SM takes (tile, head) units from an atomic
@@ -57,21 +58,32 @@ constexpr int kPrepThreads = 1024;
 constexpr uint32_t kEpiStage = 32 * 64;    // per math warp: 32 rows x 32 bf16 columns of output
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Shapes per head_dim.  STEP rows (queries, resp. keys) stream past per step
-// (32 at head_dim 256, so that the own tiles and a two-stage ring fit shared
-// memory); the dK/dV kernel splits dK and dV into DSPLIT column halves, one
-// CTA each (at head_dim 256 the two accumulators would fill TMEM alone).
-template <int D>
+// Shapes per head_dim and kernel (DQ: the dQ kernel).  STEP rows (queries,
+// resp. keys) stream past per step: 64 queries past a key tile; 96 keys past
+// a query tile, which the dQ kernel's TMEM (dQ + two buffers of 2 x 96
+// columns at head_dim 128) just holds and which runs its score products at
+// N = 96 (56.9 cycles per product against 48.9 at N = 64 for 1.5x the work);
+// 32 either way at head_dim 256, so that the own tiles and a two-stage ring
+// fit shared memory.  The dK/dV kernel splits dK and dV into DSPLIT column
+// halves, one CTA each (at head_dim 256 the two accumulators would fill TMEM
+// alone).
+template <int D, bool DQ>
 struct BwdCfg {
     static constexpr int DB = D / 64;                       // 128-byte column blocks per row
-    static constexpr int STEP = bwd_step_rows(D);           // also the TMA box height
+    static constexpr int STEP = DQ ? bwd_dq_step_rows(D) : bwd_step_rows(D);   // TMA box height
+    static constexpr int OWN_BOX = bwd_step_rows(D);        // box height of the own-tile maps
     static constexpr int NCH = STEP / 32;                   // 32-column chunks per step
     static constexpr int DSPLIT = D == 256 ? 2 : 1;
     static constexpr int DKV = D / DSPLIT;                  // dK / dV columns per CTA
     static constexpr uint32_t OWN_BYTES = kOwn * D * 2;     // a 128-row tile
     static constexpr uint32_t STEP_BYTES = STEP * D * 2;    // a STEP-row tile
-    static constexpr int NSTAGE = D == 256 ? 2 : 4;         // streamed-tile ring stages
+    // streamed-tile ring stages (three 96-key stages at head_dim 128 fill
+    // shared memory)
+    static constexpr int NSTAGE = D == 256 ? 2 : (DQ && STEP == 96 && D == 128 ? 3 : 4);
     static constexpr uint32_t STAGE_BYTES = 2 * STEP_BYTES; // (Q, dO) or (K, V)
+    // per math warp: -lse log2(e) and -Delta of a step's query columns (the
+    // dK/dV kernel only; the dQ kernel keeps its rows' in registers)
+    static constexpr uint32_t STAT_BYTES = DQ ? 0 : 512;
     // TMEM.  dK/dV kernel: dV, dK (DKV columns each), then two buffers of S^T
     // (STEP columns) + dP^T (STEP).  dQ kernel: dQ (D), then the two buffers.
     static constexpr uint32_t COL_DV = 0, COL_DK = DKV, KV_BUF = 2 * DKV;
@@ -82,15 +94,15 @@ struct BwdCfg {
     // buffer; own_full, own_empty, acc_done, epi_done, drain
     static constexpr int NUM_BARS = 2 * NSTAGE + 8 + 5;
     static constexpr size_t SMEM = 1024 + 2 * OWN_BYTES + NSTAGE * STAGE_BYTES +
-                                   kMathWarps * (512 + kEpiStage) + NUM_BARS * 8 + 64;
+                                   kMathWarps * (STAT_BYTES + kEpiStage) + NUM_BARS * 8 + 64;
     // S^T / dP^T (keys x STEP queries) and S / dP (queries x STEP keys): both K-major
     static constexpr uint32_t IDESC_T = idesc_bf16_f32(kOwn, STEP, false, false);
     // dV, dK (DKV columns) and dQ (D columns): A from TMEM, B (dO, Q or K rows) MN-major
     static constexpr uint32_t IDESC_KV = idesc_bf16_f32(kOwn, DKV, false, true);
     static constexpr uint32_t IDESC_DQ = idesc_bf16_f32(kOwn, D, false, true);
-    static_assert(KV_BUF + 2 * BUF_STRIDE <= TMEM_COLS && Q_BUF + 2 * BUF_STRIDE <= TMEM_COLS,
-                  "TMEM budget");
+    static_assert((DQ ? Q_BUF : KV_BUF) + 2 * BUF_STRIDE <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(STEP % 32 == 0 && STEP <= 256 && kOwn % OWN_BOX == 0, "step shape");
 };
 
 // ------------------------------------------------------------ prep
@@ -452,7 +464,7 @@ struct BwdUnit {
 template <int D, bool DQ>
 __device__ BwdUnit decode_unit(const BwdArgs &a, int u, int tiles)
 {
-    using C = BwdCfg<D>;
+    using C = BwdCfg<D, DQ>;
     constexpr int STEP = C::STEP;
     constexpr int SPLIT = DQ ? 1 : C::DSPLIT;
     BwdUnit w;
@@ -527,7 +539,7 @@ __device__ BwdUnit decode_unit(const BwdArgs &a, int u, int tiles)
 template <int D, bool DQ>
 __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a)
 {
-    using C = BwdCfg<D>;
+    using C = BwdCfg<D, DQ>;
     constexpr int DB = C::DB, NSTAGE = C::NSTAGE, STEP = C::STEP, NCH = C::NCH;
     constexpr int NACC = DQ ? D : C::DKV;        // accumulator columns (each)
     constexpr int DH = NACC / 2;                  // accumulator columns per math thread
@@ -553,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     const uint32_t sOwn0 = base, sOwn1 = sOwn0 + C::OWN_BYTES;     // K, V  /  Q, dO
     const uint32_t sRing = sOwn1 + C::OWN_BYTES;                    // stage: Q, dO  /  K, V
     const uint32_t sStat = sRing + NSTAGE * C::STAGE_BYTES;         // per math warp: nl, -Delta
-    const uint32_t sEpi = sStat + kMathWarps * 512;                 // per math warp: output stage
+    const uint32_t sEpi = sStat + kMathWarps * C::STAT_BYTES;       // per math warp: output stage
     const uint32_t bars = sEpi + kMathWarps * kEpiStage;
     auto ring_full = [&](int st) { return bars + 8u * st; };
     auto ring_empty = [&](int st) { return bars + 8u * (NSTAGE + st); };
@@ -613,8 +625,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             tma_prefetch_map(&a.tm_k);
             tma_prefetch_map(&a.tm_v);
             tma_prefetch_map(&a.tm_do);
+            if (DQ) {
+                tma_prefetch_map(&a.tm_ks);
+                tma_prefetch_map(&a.tm_vs);
+            }
             const CUtensorMap *own0 = DQ ? &a.tm_q : &a.tm_k, *own1 = DQ ? &a.tm_do : &a.tm_v;
-            const CUtensorMap *str0 = DQ ? &a.tm_k : &a.tm_q, *str1 = DQ ? &a.tm_v : &a.tm_do;
+            const CUtensorMap *str0 = DQ ? &a.tm_ks : &a.tm_q, *str1 = DQ ? &a.tm_vs : &a.tm_do;
             uint32_t g = 0, owns = 0;
             bool ok = true;
             for (uint32_t n = 0; ok; ++n) {
@@ -632,8 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
                     break;
                 mbar_arrive_expect_tx(own_full, 2 * C::OWN_BYTES);
                 const int own_row = (DQ ? w.q0 : w.k0) + w.t * kOwn;
-                load_rows<DB, STEP>(sOwn0, own0, own_full, w.head, own_row, kOwn);
-                load_rows<DB, STEP>(sOwn1, own1, own_full, w.head, own_row, kOwn);
+                load_rows<DB, C::OWN_BOX>(sOwn0, own0, own_full, w.head, own_row, kOwn);
+                load_rows<DB, C::OWN_BOX>(sOwn1, own1, own_full, w.head, own_row, kOwn);
                 ++owns;
                 const int group = H / Hkv;
                 for (int s = 0; s < w.n_steps; ++s, ++g) {
@@ -924,10 +940,10 @@ cudaError_t launch_bwd_d(const BwdArgs &a, int key_tile_bound, int q_tile_bound,
     if (dev < 64 && !attr_done[dev]) {
         if ((e = cudaFuncSetAttribute(bwd_main_kernel<D, false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(BwdCfg<D>::SMEM))) != cudaSuccess ||
+                                      static_cast<int>(BwdCfg<D, false>::SMEM))) != cudaSuccess ||
             (e = cudaFuncSetAttribute(bwd_main_kernel<D, true>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(BwdCfg<D>::SMEM))) != cudaSuccess)
+                                      static_cast<int>(BwdCfg<D, true>::SMEM))) != cudaSuccess)
             return e;
         attr_done[dev] = 1;
     }
@@ -939,17 +955,17 @@ cudaError_t launch_bwd_d(const BwdArgs &a, int key_tile_bound, int q_tile_bound,
         return e;
     // persistent grids: one CTA per SM (fewer when there are fewer units)
     const long long kv_units =
-        static_cast<long long>(key_tile_bound) * BwdCfg<D>::DSPLIT * a.num_kv_heads;
+        static_cast<long long>(key_tile_bound) * BwdCfg<D, false>::DSPLIT * a.num_kv_heads;
     const long long q_units = static_cast<long long>(q_tile_bound) * a.num_heads;
     if (kv_units > 0) {
         bwd_main_kernel<D, false><<<static_cast<int>(std::min<long long>(kv_units, sm_count)),
-                                    kThreads, BwdCfg<D>::SMEM, s>>>(a);
+                                    kThreads, BwdCfg<D, false>::SMEM, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
     if (q_units > 0) {
         bwd_main_kernel<D, true><<<static_cast<int>(std::min<long long>(q_units, sm_count)),
-                                   kThreads, BwdCfg<D>::SMEM, s>>>(a);
+                                   kThreads, BwdCfg<D, true>::SMEM, s>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }

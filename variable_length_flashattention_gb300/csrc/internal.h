@@ -145,6 +145,8 @@ cudaError_t launch_decode_gather(const DecodeStepArgs &a, void *k_out, void *v_o
 struct BwdArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;   // boxes of 64 columns x 1 head x bwd_step_rows() rows,
                                             // 128-byte swizzle
+    CUtensorMap tm_ks, tm_vs;               // K, V with boxes of bwd_dq_step_rows() rows (the
+                                            // dQ kernel's streamed tiles)
     const int32_t *cu_q;
     const int32_t *cu_k;
     const void *out, *dout;                 // bf16 [total_q, H, D]
@@ -164,6 +166,13 @@ struct BwdArgs {
 __host__ __device__ constexpr int bwd_step_rows(int head_dim)
 {
     return head_dim == 256 ? 32 : 64;
+}
+
+// Keys the dQ kernel streams per step past a query tile; the tm_ks / tm_vs
+// maps use boxes of this many rows.
+__host__ __device__ constexpr int bwd_dq_step_rows(int head_dim)
+{
+    return head_dim == 256 ? 32 : 96;
 }
 
 // Workspace bytes of the backward and its split into the BwdArgs pointers.
