@@ -549,6 +549,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     __shared__ int s_abort;
     __shared__ BwdUnit s_unit[2];
 
+    // The dQ kernel, launched next with programmatic dependent launch, reads
+    // nothing this kernel writes: let it take each SM this kernel's CTAs leave.
+    if (!DQ)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (*a.status != VFA_OK)
         return;
     const int B = a.batch, H = a.num_heads, Hkv = a.num_kv_heads;
@@ -964,8 +968,24 @@ cudaError_t launch_bwd_d(const BwdArgs &a, int key_tile_bound, int q_tile_bound,
             return e;
     }
     if (q_units > 0) {
-        bwd_main_kernel<D, true><<<static_cast<int>(std::min<long long>(q_units, sm_count)),
-                                   kThreads, BwdCfg<D, true>::SMEM, s>>>(a);
+        // Programmatic dependent launch: the dQ kernel's CTAs start on the SMs
+        // the dK/dV kernel's CTAs leave, without waiting for the whole grid.  It
+        // reads only the prep and Delta kernels' output, complete before the
+        // dK/dV kernel started (a plain launch after them), so it needs no
+        // griddepcontrol.wait; its atomic unit counter balances CTAs that start
+        // late.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(std::min<long long>(q_units, sm_count)));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = BwdCfg<D, true>::SMEM;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = kv_units > 0 ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, bwd_main_kernel<D, true>, a)) != cudaSuccess)
+            return e;
         if ((e = cudaGetLastError()) != cudaSuccess)
             return e;
     }
