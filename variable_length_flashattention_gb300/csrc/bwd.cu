@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 
     // Consumers take unit n from the ring; false at the end (or on abort).
     auto take_unit = [&](uint32_t n, BwdUnit &w) -> bool {
-        if (!mbar_wait(unit_full(n & 1), (n >> 1) & 1u, abort))
+        if (!mbar_wait_warp(unit_full(n & 1), (n >> 1) & 1u, abort))
             return false;
         w = s_unit[n & 1];
         return w.valid;
@@ -699,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
                 break;
             if (w.n_steps == 0)
                 continue;
-            if (!__all_sync(0xffffffffu, mbar_wait(own_full, owns & 1u, abort))) {
+            if (!mbar_wait_warp(own_full, owns & 1u, abort)) {
                 ok = false;
                 break;
             }
@@ -711,8 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
                 if (s < w.n_steps) {
                     const uint32_t gs = g + s;
                     const int st = gs % NSTAGE, x = gs & 1;
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait(ring_full(st), (gs / NSTAGE) & 1u, abort))) {
+                    if (!mbar_wait_warp(ring_full(st), (gs / NSTAGE) & 1u, abort)) {
                         ok = false;
                         break;
                     }
@@ -728,9 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
                 if (s >= 1) {
                     const uint32_t gp = g + s - 1;
                     const int stp = gp % NSTAGE, xp = gp & 1;
-                    if (!__all_sync(0xffffffffu, mbar_wait(p_full(xp), (gp >> 1) & 1u, abort)) ||
-                        (s == 1 && !__all_sync(0xffffffffu,
-                                               mbar_wait(epi_done, (units & 1u) ^ 1u, abort)))) {
+                    if (!mbar_wait_warp(p_full(xp), (gp >> 1) & 1u, abort) ||
+                        (s == 1 && !mbar_wait_warp(epi_done, (units & 1u) ^ 1u, abort))) {
                         ok = false;
                         break;
                     }
@@ -845,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
                     full = olo + kOwn <= w.lk && slo + STEP <= w.lq &&
                            (!a.causal || olo + kOwn - 1 <= slo + off) &&
                            (wl < 0 || olo >= slo + STEP - 1 + off - wl);
-                ok = __all_sync(0xffffffffu, mbar_wait(s_full(x), (gs >> 1) & 1u, abort));
+                ok = mbar_wait_warp(s_full(x), (gs >> 1) & 1u, abort);
                 if (!ok)
                     break;
                 tc_fence_after();
@@ -890,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             }
             if (!ok)
                 break;
-            ok = __all_sync(0xffffffffu, mbar_wait(acc_done, units & 1u, abort));
+            ok = mbar_wait_warp(acc_done, units & 1u, abort);
             if (!ok)
                 break;
             tc_fence_after();

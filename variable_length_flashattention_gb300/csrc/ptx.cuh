@@ -85,6 +85,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// mbar_wait for a whole warp (every lane calls it, converged, with the same
+// arguments; all get the same result): a warp-wide first test, then the
+// bounded per-lane wait.  A phase that has already completed then costs one
+// test and one vote (measured between two batches of tcgen05.mma: about 50
+// cycles of tensor-pipe idle against about 95 for the per-lane wait and a
+// vote).  The backward's warps use it; in the forward, whose waits mostly
+// meet phases that have not completed yet, it measured slower.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort)
+{
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity)))
+        return true;
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
 // Same, for the drain path after an abort: ignores *abort, keeps the limit.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity)
 {
