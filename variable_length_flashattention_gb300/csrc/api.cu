@@ -123,6 +123,29 @@ vfa_status encode_packed_map(CUtensorMap *map, const void *base, int rows, int h
     return VFA_OK;
 }
 
+// The bf16 output [rows, heads, head_dim] as a 3-D TMA map for tile stores:
+// boxes of 32 columns (64 bytes) x 1 head x 32 rows, 64-byte swizzle -- one
+// prefill warp's 32 rows of a 32-column chunk, as it stages them.
+vfa_status encode_out_map(CUtensorMap *map, void *base, int rows, int heads, int head_dim)
+{
+    EncodeTiledFn enc;
+    vfa_status st = get_encoder(&enc);
+    if (st)
+        return st;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(heads),
+                                static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                   static_cast<cuuint64_t>(heads) * head_dim * 2};
+    const cuuint32_t box[3] = {32, 1, 32};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(VFA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return VFA_OK;
+}
+
 // [num_blocks * block_size tokens, kv_heads, head_dim] bf16 pool as the same
 // kind of 3-D TMA map as the packed tensors: one box is 64 columns of one
 // block's block_size token rows for one kv head.
@@ -318,7 +341,8 @@ static vfa_status varlen_fwd_impl(const void *q, const void *k, const void *v,
     const int qk_bytes = qk_fp8 ? 1 : 2;
     if ((st = encode_packed_map(&pa.tm_q, q, total_q, num_heads, head_dim, bq, qk_bytes)) ||
         (st = encode_packed_map(&pa.tm_k, k, total_k, num_kv_heads, head_dim, bk, qk_bytes)) ||
-        (st = encode_packed_map(&pa.tm_v, v, total_k, num_kv_heads, head_dim, bk)))
+        (st = encode_packed_map(&pa.tm_v, v, total_k, num_kv_heads, head_dim, bk)) ||
+        (st = encode_out_map(&pa.tm_o, out, total_q, num_heads, head_dim)))
         return st;
     pa.cu_q = cu_seqlens_q;
     pa.cu_k = cu_seqlens_k;

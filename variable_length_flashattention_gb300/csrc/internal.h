@@ -71,6 +71,7 @@ int schedule_scratch_ints(int batch, int total_q, int total_k, int block_q, int 
 
 struct PrefillArgs {
     CUtensorMap tm_q, tm_k, tm_v;
+    CUtensorMap tm_o;     // out: boxes of 32 columns x 1 head x 32 rows, 64-byte swizzle
     const int32_t *cu_q;
     const int32_t *cu_k;
     const int4 *items;    // two int4 per item

@@ -32,8 +32,9 @@
 //     that is valid for all 32 rows of a warp skips the mask, and one that
 //     is masked for all of them skips its exponentials;
 //   * O / l leaves through a 2 KB shared-memory stage per warp (no cross-warp
-//     handshake, no TMA completion to wait for): every store instruction
-//     writes eight whole 64-byte row segments;
+//     handshake): a warp whose 32 rows all lie in the sequence hands each
+//     32-column chunk to a TMA tile store; in a sequence's last tile, plain
+//     stores write eight whole 64-byte row segments per instruction;
 //   * TMEM: O_a, O_b (D columns each), S/P_a, S/P_b (128 columns each);
 //   * an FP8 instantiation takes Q and K as E4M3 codes: their tiles are half
 //     the bytes (at head_dim 64 rows of 64 bytes, stored with the 64-byte
@@ -706,15 +707,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_valid)
                 p.lse[tok * H + h] = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -FLT_MAX;
             // O / l -> bf16, 32 columns at a time through this warp's stage: each
-            // thread writes its row segment (swizzled, conflict-free), then every
-            // store instruction writes eight whole 64-byte row segments.
+            // thread writes its row segment (swizzled as the 64-byte TMA swizzle
+            // lays it out, conflict-free).  A warp whose 32 rows all belong to the
+            // sequence then hands the chunk to a TMA tile store; otherwise (the
+            // sequence's last tile: rows past it belong to the next sequence)
+            // every store instruction writes eight whole 64-byte row segments of
+            // the rows that exist.
             const int tile_rows = min(BQ, lq - i * BQ);
+            const bool warp_rows = quarter * 32 + 32 <= tile_rows;   // warp-uniform
             __nv_bfloat16 *out_tile = out + ((static_cast<long long>(q0) + i * BQ) * H + h) * D;
 #pragma unroll
             for (int cb = 0; cb < D / 32; ++cb) {
                 uint32_t rr[32];
                 tmem_ld32(o_addr + cb * 32, rr);
                 tmem_wait_ld_r(rr);
+                // the stage's previous tile store has read it
+                if (lane == 0)
+                    bulk_wait_group_read0();
+                __syncwarp();
                 const uint32_t row = wstage + lane * 64;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
@@ -727,19 +737,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              __uint_as_float(rr[8 * c + 5]) * inv_l),
                                  pack_bf16x2(__uint_as_float(rr[8 * c + 6]) * inv_l,
                                              __uint_as_float(rr[8 * c + 7]) * inv_l));
-                __syncwarp();
+                if (warp_rows) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&p.tm_o, wstage, cb * 32, h, q0 + i * BQ + quarter * 32);
+                        bulk_commit_group();
+                    }
+                } else {
+                    __syncwarp();
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int rw = 8 * k + (lane >> 2), ch = lane & 3;
-                    const int rt = quarter * 32 + rw;          // row within the tile
-                    const uint4 v = ld_shared_v4(wstage + rw * 64 + ((ch ^ ((rw >> 1) & 3)) << 4));
-                    if (rt < tile_rows)
-                        *reinterpret_cast<uint4 *>(out_tile + static_cast<long long>(rt) * H * D +
-                                                   cb * 32 + ch * 8) = v;
+                    for (int k = 0; k < 4; ++k) {
+                        const int rw = 8 * k + (lane >> 2), ch = lane & 3;
+                        const int rt = quarter * 32 + rw;          // row within the tile
+                        const uint4 v =
+                            ld_shared_v4(wstage + rw * 64 + ((ch ^ ((rw >> 1) & 3)) << 4));
+                        if (rt < tile_rows)
+                            *reinterpret_cast<uint4 *>(out_tile + static_cast<long long>(rt) * H * D +
+                                                       cb * 32 + ch * 8) = v;
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
         }
+        // every tile store of this warp has completed before the CTA exits
+        if (lane == 0)
+            bulk_wait_group0();
+        __syncwarp();
     }
 
     tc_fence_before();
