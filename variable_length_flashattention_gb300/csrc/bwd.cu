@@ -28,12 +28,15 @@
 //   * the dQ kernel (bwd_main_kernel<D, true>): for each 128-query tile and
 //     head, the same with the roles swapped: Q, dO stay, K and V stream past
 //     in blocks of STEP keys (96; 32 at head_dim 256, through their own TMA
-//     maps with boxes of that height); S = Q K^T, dP = dO V^T into two TMEM buffers,
-//     dS (bf16, over dP) and dQ += dS K in TMEM.  dQ leaves as bf16 once, so
-//     no fp32 sum and no second pass exist.
+//     maps with boxes of that height); S = Q K^T, dP = dO V^T into two TMEM
+//     buffers, dS (bf16, over dP) and dQ += dS K in TMEM.  dQ leaves as bf16
+//     once, so no fp32 sum and no second pass exist.  It is launched with
+//     programmatic dependent launch and starts on the SMs the dK/dV kernel's
+//     CTAs leave (it reads nothing that kernel writes).
 // Both are persistent: one CTA per SM takes (tile, head) units from an atomic
 // counter, and consecutive units overlap (the next unit's own tiles load and
-// its first score products run while the current one finishes).
+// its first score products run while the current one finishes).  dK, dV and
+// dQ leave through a per-warp shared-memory stage.
 // The math warps evaluate masks only on steps that need them, as one
 // interval of visible columns per thread.  Every wait is bounded; on expiry
 // the CTA records VFA_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and
