@@ -457,12 +457,15 @@ vfa_status vfa_varlen_bwd(const void *q, const void *k, const void *v, const voi
     vfa::BwdArgs a;
     memset(&a, 0, sizeof a);
     const int box = vfa::bwd_step_rows(head_dim), box_kv = vfa::bwd_dq_step_rows(head_dim);
+    const int box_q = vfa::bwd_kv_step_rows(head_dim);
     if ((st = encode_packed_map(&a.tm_q, q, total_q, num_heads, head_dim, box)) ||
         (st = encode_packed_map(&a.tm_do, dout, total_q, num_heads, head_dim, box)) ||
         (st = encode_packed_map(&a.tm_k, k, total_k, num_kv_heads, head_dim, box)) ||
         (st = encode_packed_map(&a.tm_v, v, total_k, num_kv_heads, head_dim, box)) ||
         (st = encode_packed_map(&a.tm_ks, k, total_k, num_kv_heads, head_dim, box_kv)) ||
-        (st = encode_packed_map(&a.tm_vs, v, total_k, num_kv_heads, head_dim, box_kv)))
+        (st = encode_packed_map(&a.tm_vs, v, total_k, num_kv_heads, head_dim, box_kv)) ||
+        (st = encode_packed_map(&a.tm_qs, q, total_q, num_heads, head_dim, box_q)) ||
+        (st = encode_packed_map(&a.tm_dos, dout, total_q, num_heads, head_dim, box_q)))
         return st;
     vfa::bwd_workspace_split(workspace, batch, total_q, num_heads, &a);
     a.cu_q = cu_seqlens_q;

@@ -62,18 +62,18 @@ constexpr uint32_t kEpiStage = 32 * 64;    // per math warp: 32 rows x 32 bf16 c
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shapes per head_dim and kernel (DQ: the dQ kernel).  STEP rows (queries,
-// resp. keys) stream past per step: 64 queries past a key tile; 96 keys past
-// a query tile, which the dQ kernel's TMEM (dQ + two buffers of 2 x 96
-// columns at head_dim 128) just holds and which runs its score products at
-// N = 96 (56.9 cycles per product against 48.9 at N = 64 for 1.5x the work);
-// 32 either way at head_dim 256, so that the own tiles and a two-stage ring
-// fit shared memory.  The dK/dV kernel splits dK and dV into DSPLIT column
+// resp. keys) stream past per step, as many as TMEM holds two buffers of:
+// 96 keys past a query tile (dQ + 2 x (2 x 96) columns at head_dim 128), 64
+// queries past a key tile at head_dim 128 (dK, dV and 2 x (2 x 64)) and 96
+// at head_dim 64; N = 96 score products run at 56.9 cycles against 48.9 at
+// N = 64 for 1.5x the work.  32 either way at head_dim 256, so that the own
+// tiles and a two-stage ring fit shared memory.  The dK/dV kernel splits dK and dV into DSPLIT column
 // halves, one CTA each (at head_dim 256 the two accumulators would fill TMEM
 // alone).
 template <int D, bool DQ>
 struct BwdCfg {
     static constexpr int DB = D / 64;                       // 128-byte column blocks per row
-    static constexpr int STEP = DQ ? bwd_dq_step_rows(D) : bwd_step_rows(D);   // TMA box height
+    static constexpr int STEP = DQ ? bwd_dq_step_rows(D) : bwd_kv_step_rows(D);   // TMA box height
     static constexpr int OWN_BOX = bwd_step_rows(D);        // box height of the own-tile maps
     static constexpr int NCH = STEP / 32;                   // 32-column chunks per step
     static constexpr int DSPLIT = D == 256 ? 2 : 1;
@@ -86,7 +86,7 @@ struct BwdCfg {
     static constexpr uint32_t STAGE_BYTES = 2 * STEP_BYTES; // (Q, dO) or (K, V)
     // per math warp: -lse log2(e) and -Delta of a step's query columns (the
     // dK/dV kernel only; the dQ kernel keeps its rows' in registers)
-    static constexpr uint32_t STAT_BYTES = DQ ? 0 : 512;
+    static constexpr uint32_t STAT_BYTES = DQ ? 0 : 256 * NCH;
     // TMEM.  dK/dV kernel: dV, dK (DKV columns each), then two buffers of S^T
     // (STEP columns) + dP^T (STEP).  dQ kernel: dQ (D), then the two buffers.
     static constexpr uint32_t COL_DV = 0, COL_DK = DKV, KV_BUF = 2 * DKV;
@@ -632,12 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             tma_prefetch_map(&a.tm_k);
             tma_prefetch_map(&a.tm_v);
             tma_prefetch_map(&a.tm_do);
-            if (DQ) {
-                tma_prefetch_map(&a.tm_ks);
-                tma_prefetch_map(&a.tm_vs);
-            }
             const CUtensorMap *own0 = DQ ? &a.tm_q : &a.tm_k, *own1 = DQ ? &a.tm_do : &a.tm_v;
-            const CUtensorMap *str0 = DQ ? &a.tm_ks : &a.tm_q, *str1 = DQ ? &a.tm_vs : &a.tm_do;
+            const CUtensorMap *str0 = DQ ? &a.tm_ks : &a.tm_qs, *str1 = DQ ? &a.tm_vs : &a.tm_dos;
+            tma_prefetch_map(str0);
+            tma_prefetch_map(str1);
             uint32_t g = 0, owns = 0;
             bool ok = true;
             for (uint32_t n = 0; ok; ++n) {
@@ -763,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         // ------------------------------------------------------------ elementwise, epilogue
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         // per warp and 32-column chunk: 32 nl, then 32 -Delta
-        const uint32_t wstat = sStat + (warp - kFirstMathWarp) * 512;
+        const uint32_t wstat = sStat + (warp - kFirstMathWarp) * C::STAT_BYTES;
         float *stat = reinterpret_cast<float *>(smem_raw + (wstat - raw));
         const float scale_log2 = a.scale_log2;
         uint32_t g = 0, units = 0;

@@ -148,6 +148,8 @@ struct BwdArgs {
                                             // 128-byte swizzle
     CUtensorMap tm_ks, tm_vs;               // K, V with boxes of bwd_dq_step_rows() rows (the
                                             // dQ kernel's streamed tiles)
+    CUtensorMap tm_qs, tm_dos;              // Q, dO with boxes of bwd_kv_step_rows() rows (the
+                                            // dK/dV kernel's streamed tiles)
     const int32_t *cu_q;
     const int32_t *cu_k;
     const void *out, *dout;                 // bf16 [total_q, H, D]
@@ -167,6 +169,14 @@ struct BwdArgs {
 __host__ __device__ constexpr int bwd_step_rows(int head_dim)
 {
     return head_dim == 256 ? 32 : 64;
+}
+
+// Queries the dK/dV kernel streams per step past a key tile (its TMEM holds
+// dK, dV and two buffers of 2 x this many columns); the tm_qs / tm_dos maps
+// use boxes of this many rows.
+__host__ __device__ constexpr int bwd_kv_step_rows(int head_dim)
+{
+    return head_dim == 64 ? 96 : bwd_step_rows(head_dim);
 }
 
 // Keys the dQ kernel streams per step past a query tile; the tm_ks / tm_vs
