@@ -47,6 +47,21 @@ def test_tiny(vfa, oracle_mod, causal, seed):
     _check_full(vfa, oracle_mod, W.tiny(causal, seed))
 
 
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_counts_at_warp_boundaries(vfa, oracle_mod, head_dim, causal):
+    # The pair kernel writes a tile's output 32 rows (one warp) at a time: by a
+    # tile store when all 32 rows belong to the sequence, by plain stores of
+    # the existing rows otherwise (rows past the sequence are the next
+    # sequence's).  Lengths at, just below and just above multiples of 32 and
+    # of the 128-row tile put every warp of a tile on both sides of that
+    # boundary, with the next sequence's rows right behind.
+    lengths = [31, 32, 33, 63, 64, 65, 96, 127, 128, 129, 160, 191, 224, 255, 256, 257]
+    case = W.make_varlen("warp-rows", lengths, lengths, 2, head_dim, causal, 1.0,
+                         value_seed=head_dim + 3 * causal)
+    _check_full(vfa, oracle_mod, case)
+
+
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_packed_training_batch(vfa, oracle_mod, seed):
     _check_full(vfa, oracle_mod, W.packed(seed))
