@@ -119,6 +119,19 @@ def test_bad_cu_seqlens_sets_status(vfa):
     assert torch.isnan(dq.float()).all()
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [0, 1, 2])
+def test_step_boundaries(vfa, oracle_mod, causal, D):
+    # The dQ kernel streams keys in steps of 96, the dK/dV kernel queries in
+    # steps of 96 at head_dim 64 (64 at 128): lengths at, just below and just
+    # above multiples of 96 (and of the 128-row tiles) end steps at every
+    # offset, with the next sequence's rows right behind the last step.
+    lq = [95, 96, 97, 191, 192, 193, 288, 64]
+    lk = [95, 96, 97, 191, 192, 193, 288, 300] if causal == 2 else lq
+    case = W.make_varlen("bwd-steps", lq, lk, 2, D, bool(causal), 1.0, value_seed=60 + D + causal)
+    _compare(vfa, oracle_mod, case, causal, seed=60 + causal)
+
+
 @pytest.mark.parametrize("D", [64, 256])
 @pytest.mark.parametrize("causal", [0, 1, 2])
 def test_edge_lengths(vfa, oracle_mod, causal, D):
