@@ -222,7 +222,10 @@ def run_reference(args):
     budget = 120.0 / max(1, args.steps + args.warmup)          # seconds of CPU per step
     rng = np.random.default_rng(args.seed)
     rate, threads, _, _ = cpu_oracle_rate(case, min(2.0, budget), args.seed)
-    rows_per_step = max(1, int(budget * rate * 1e12 / max(1, 4 * case.head_dim * 1024)))
+    # rows a step's budget covers at that rate, at the workload's average work per row
+    from variable_length_flashattention_gb300 import accounting as A
+    flops_per_row = A.varlen_flops(case) / max(1, case.total_q * case.num_heads)
+    rows_per_step = max(1, int(budget * rate * 1e12 / max(1.0, flops_per_row)))
     rows_per_step = min(rows_per_step, case.total_q * case.num_heads)
     flops_total, t_total = 0, 0.0
     for step in range(args.warmup + args.steps):
