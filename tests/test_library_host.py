@@ -142,7 +142,7 @@ def test_backward_and_fp8_host_checks(vfa):
     # accumulated in TMEM per query tile)
     assert L.vfa_varlen_bwd_workspace_bytes(2, 10, 2, 128) >= 256 + 2 * 3 * 4 + 10 * 2 * 4
     assert L.vfa_varlen_bwd_workspace_bytes(2, 10, 2, 128) < 10 * 2 * 128 * 4
-    # FP8 forward: head_dim 128 only, descales finite and positive
+    # FP8 forward: head_dim 64, 128 or 256, descales finite and positive
     f8 = lambda D, dq, dk: (fake, fake, fake, fake, fake, 4, 4, 4, 1, 2, 2, D, 0.1, dq, dk, 1, -1,
                             fake, fake, fake, 1 << 30, nul)
     assert L.vfa_varlen_fwd_fp8(*f8(96, 1.0, 1.0)) == vfa.VFA_ERR_UNSUPPORTED
@@ -179,3 +179,39 @@ def test_noalloc_rejects_problems_beyond_the_static_scratch(vfa):
                                   nul, nul, nul, nul)
     assert st in (vfa.VFA_ERR_INVALID_ARG, vfa.VFA_ERR_CUDA)
     assert b"static scratch" not in L.vfa_last_error()
+
+
+def test_split_decode_host_checks(vfa):
+    # the split step's workspace size is exact and its arguments are checked
+    # on the host before any device work (no GPU needed)
+    L = vfa.lib()
+    r = lambda x: (x + 255) // 256 * 256
+    for S, Hq, Hkv, D, n in ((4, 32, 8, 128, 19), (1, 8, 8, 64, 1), (64, 32, 8, 256, 1024)):
+        want = r(r(S * Hkv * 4) + S * Hq * n * (D + 2) * 4)
+        assert L.vfa_paged_decode_split_workspace_bytes(S, Hq, Hkv, D, n) == want
+    # unsupported sizes give 0
+    assert L.vfa_paged_decode_split_workspace_bytes(4, 32, 8, 96, 4) == 0       # head_dim
+    assert L.vfa_paged_decode_split_workspace_bytes(4, 30, 8, 128, 4) == 0      # Hq % Hkv
+    assert L.vfa_paged_decode_split_workspace_bytes(4, 32, 8, 128, 0) == 0      # runs
+    assert L.vfa_paged_decode_split_workspace_bytes(4, 32, 8, 128, 1025) == 0
+    assert L.vfa_paged_decode_split_workspace_bytes(0, 32, 8, 128, 4) == 0
+    # run count: null result pointer and bad sizes
+    n = ctypes.c_int(0)
+    assert L.vfa_paged_decode_split_count(4, 8, 32, None) == vfa.VFA_ERR_INVALID_ARG
+    assert L.vfa_paged_decode_split_count(0, 8, 32, ctypes.byref(n)) == vfa.VFA_ERR_INVALID_ARG
+    assert L.vfa_paged_decode_split_count(4, 0, 32, ctypes.byref(n)) == vfa.VFA_ERR_INVALID_ARG
+    # split step: run count outside [1, 1024], missing or misaligned workspace,
+    # too small a workspace
+    fake = ctypes.c_void_p(0x100000)
+    ws = ctypes.c_void_p(0x200000)
+    step = lambda splits, w, wbytes: L.vfa_paged_decode_step_split(
+        fake, fake, fake, 64, fake, fake, None, 32, 4, 32, 8, 128, 16, 0.1, fake, fake, fake,
+        None, splits, w, wbytes, None)
+    assert step(0, ws, 1 << 30) == vfa.VFA_ERR_INVALID_ARG
+    assert step(1025, ws, 1 << 30) == vfa.VFA_ERR_INVALID_ARG
+    assert b"num_splits" in L.vfa_last_error()
+    assert step(4, None, 1 << 30) == vfa.VFA_ERR_INVALID_ARG
+    assert step(4, ctypes.c_void_p(0x200010), 1 << 30) == vfa.VFA_ERR_INVALID_ARG
+    need = L.vfa_paged_decode_split_workspace_bytes(4, 32, 8, 128, 4)
+    assert step(4, ws, need - 1) == vfa.VFA_ERR_INVALID_ARG
+    assert b"too small" in L.vfa_last_error()
